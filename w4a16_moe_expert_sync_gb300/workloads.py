@@ -1,0 +1,114 @@
+"""Seeded synthetic workloads for the W4A16 routed-MoE layer.
+
+This module is shared by the CUDA path's tests and benchmark and by the
+oracle's tests, so it holds none of the layer's arithmetic: no quantisation,
+no routing, no alignment, no matmul.  It only defines the workload shapes and
+draws the random tensors they start from:
+
+* activations x ~ N(0, 1), stored as bfloat16;
+* expert weights W ~ N(0, 0.02^2), fp32, drawn expert by expert so that any
+  subset of experts can be regenerated on its own;
+* router logits ~ N(0, 1), fp32, plus (skewed workload only) a per-expert
+  bias b_e = -1.2 * ln(r_e), with r a seeded permutation of 1..E, so that
+  expert popularity follows a Zipf law with exponent 1.2.
+
+The shapes follow the pages' layer: a 256-token canvas, hidden size 2816,
+expert intermediate size 704, 128 experts, top-8 routing ("Inference: Making
+every denoising pass fast" -- Quantisation alone leaves a sparse execution
+problem; "diffusiongemma-26B-A4B-w4a16" -- What the model is, Checkpoint
+format).  Random streams are numpy PCG64 keyed by (seed, tensor tag[, expert]).
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+# tensor tags in the seed sequence
+_TAG_X, _TAG_WGU, _TAG_WDN, _TAG_LOGITS, _TAG_ZIPF = 1, 2, 3, 4, 5
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerShape:
+    name: str
+    M: int          # tokens (canvas rows)
+    d: int          # hidden size (gate_up contraction dim)
+    m: int          # expert intermediate size (down contraction dim)
+    E: int          # experts
+    k: int          # experts per token
+    seed: int
+    routing: str = "gaussian"   # or "zipf"
+    gu_group: int = 128
+    dn_group: int = 64
+    weight_std: float = 0.02
+
+    @property
+    def A(self) -> int:
+        return self.M * self.k
+
+
+def _sweep():
+    return {f"sweep_M{M}": LayerShape(f"sweep_M{M}", M, 2816, 704, 128, 8, seed=10 + i)
+            for i, M in enumerate((1, 8, 32, 64, 128, 256))}
+
+
+CONFIGS = {
+    # small case the oracle finishes in well under a second
+    "tiny": LayerShape("tiny", 16, 256, 128, 8, 2, seed=0),
+    # several tiles in every dimension and a ragged contraction tail
+    "ragged": LayerShape("ragged", 37, 384, 192, 12, 3, seed=6),
+    # one 256-token canvas at the pages' layer shape
+    "layer256": LayerShape("layer256", 256, 2816, 704, 128, 8, seed=1),
+    # skewed routing: a few experts with >100 rows, many with none
+    "zipf256": LayerShape("zipf256", 256, 2816, 704, 128, 8, seed=4, routing="zipf"),
+    # eight overlapping canvases
+    "canvas2048": LayerShape("canvas2048", 2048, 2816, 704, 128, 8, seed=5),
+    **_sweep(),
+}
+
+
+def _rng(*key: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(list(key))))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Store fp32 samples as bfloat16 (round to nearest even); returns uint16 bits."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def activations(cfg: LayerShape) -> np.ndarray:
+    """x [M, d] as bfloat16 bits (uint16)."""
+    x = _rng(cfg.seed, _TAG_X).standard_normal((cfg.M, cfg.d), dtype=np.float32)
+    return f32_to_bf16_bits(x)
+
+
+def gate_up_weight(cfg: LayerShape, e: int) -> np.ndarray:
+    """W_gu[e] [2m, d] fp32 ~ N(0, std^2)."""
+    w = _rng(cfg.seed, _TAG_WGU, e).standard_normal((2 * cfg.m, cfg.d), dtype=np.float32)
+    return w * np.float32(cfg.weight_std)
+
+
+def down_weight(cfg: LayerShape, e: int) -> np.ndarray:
+    """W_dn[e] [d, m] fp32 ~ N(0, std^2)."""
+    w = _rng(cfg.seed, _TAG_WDN, e).standard_normal((cfg.d, cfg.m), dtype=np.float32)
+    return w * np.float32(cfg.weight_std)
+
+
+def router_logits(cfg: LayerShape) -> np.ndarray:
+    """Router logits [M, E] fp32: N(0, 1), plus the Zipf bias when skewed."""
+    l = _rng(cfg.seed, _TAG_LOGITS).standard_normal((cfg.M, cfg.E), dtype=np.float32)
+    if cfg.routing == "zipf":
+        r = _rng(cfg.seed, _TAG_ZIPF).permutation(cfg.E).astype(np.float64) + 1.0
+        bias = (-1.2 * np.log(r)).astype(np.float32)
+        l = l + bias[None, :]
+    return l
+
+
+def all_gate_up_weights(cfg: LayerShape) -> np.ndarray:
+    return np.stack([gate_up_weight(cfg, e) for e in range(cfg.E)])
+
+
+def all_down_weights(cfg: LayerShape) -> np.ndarray:
+    return np.stack([down_weight(cfg, e) for e in range(cfg.E)])
