@@ -1,0 +1,225 @@
+/*
+ * w4moe.h -- C ABI of libw4moe.so, a GB300 (sm_103a) library for the W4A16
+ * routed mixture-of-experts layer of a block-diffusion LM's denoising forward.
+ *
+ * The layer (per token t with routed experts e_j and weights w_j, j < k):
+ *     g, u  = x_t . deq(Wgu[e_j])^T        gate rows [0, m), up rows [m, 2m)
+ *     h     = gelu_tanh(g) * u
+ *     y_j   = h . deq(Wdn[e_j])^T
+ *     out_t = sum_{j = 0..k-1, in order} w_j * y_j
+ * with deq(W)[r, c] = s[r, c/group] * (q[r, c] - z[r, c/group]), q a uint4
+ * code, s and z fp16 ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format;
+ * "Inference: Making every denoising pass fast" -- The first constraint was
+ * capacity, Quantisation alone leaves a sparse execution problem;
+ * "dg-w4-kernels" -- Grouped MoE).  The gated activation is not named on the
+ * pages; this library uses gelu_tanh(gate) * up.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *     where stated.  The library never allocates device memory, never
+ *     synchronises the device and never reads device data on the host, so a
+ *     sequence of calls can be captured in a CUDA graph.
+ *   - Every call is asynchronous on `stream` (0 = the legacy default stream).
+ *   - The return value reports argument and launch errors only (w4_status).
+ *     On a nonzero return nothing was launched.  w4_last_error_detail() gives
+ *     a one-line description of the last failure on the calling thread.
+ *   - Errors found on the device (an expert id outside [0, E), a pipeline
+ *     wait that ran past its time limit) are OR-ed into *dev_status as the
+ *     W4_DEV_* bits below; the kernels never trap.  dev_status may be NULL
+ *     where the signature allows it, in which case such errors are dropped.
+ *   - Dtypes: bf16 and fp16 values travel as uint16_t bit patterns.
+ *   - Pointers to data read with 16-byte vector loads or TMA must be 16-byte
+ *     aligned (W4_ERR_MISALIGNED otherwise); allocations from cudaMalloc or
+ *     PyTorch always are.
+ *   - Shapes are int; products that exceed 2^31 are not supported.
+ */
+#ifndef W4MOE_H
+#define W4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4MOE_ABI_VERSION 1
+
+/* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st *w4_stream_t;
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, bad option   */
+    W4_ERR_UNSUPPORTED_SHAPE = 2, /* a shape the kernels do not handle         */
+    W4_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned          */
+    W4_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed      */
+    W4_ERR_NO_DEVICE = 5,         /* no sm_103 device, or a driver entry point
+                                     the library needs is missing              */
+    W4_ERR_WORKSPACE = 6          /* workspace NULL or smaller than required   */
+} w4_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define W4_DEV_BAD_EXPERT_ID 0x1      /* an id outside [0, E); it was skipped   */
+#define W4_DEV_PIPELINE_TIMEOUT 0x2   /* a pipeline wait exceeded ~1 s; the
+                                         kernel stopped and its outputs are
+                                         incomplete                              */
+#define W4_DEV_TOO_MANY_JOBS 0x4      /* internal job list overflow (cannot
+                                         happen for shapes the host accepted)   */
+
+/* Human-readable name of a w4_status value (static string). */
+const char *w4_status_string(int status);
+
+/* Description of the last failure on the calling thread (static per thread). */
+const char *w4_last_error_detail(void);
+
+/* W4MOE_ABI_VERSION of the loaded library. */
+int w4_abi_version(void);
+
+/* --------------------------------------------------------------------------
+ * w4_quantize -- quantize_w4, the checkpoint packer
+ * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: asymmetric uint4,
+ *  fp16 scale and zero-point per group, two nibbles per byte,
+ *  byte j = q[2j] | q[2j+1] << 4; -- Benchmarks: round-to-nearest min/max;
+ *  "dg-w4-kernels" -- W4A16: qw, scale, zero = quantize_w4(W, group_size)).
+ *
+ *   W   [E, N, K] fp32, row-major (contraction dim K innermost)
+ *   q   [E, N, K/2] uint8 out, two codes per byte, low nibble first
+ *   s,z [E, N, K/group] fp16 out
+ * Per group of `group` consecutive elements of a row, in fp32:
+ *   s = (max - min) / 15, stored fp16 (a zero fp16 scale becomes 1.0);
+ *   z = -min / s16, stored fp16 (fractional zero point);
+ *   q = clamp(round_half_even(w / s16 + z16), 0, 15), no fused multiply-add.
+ * group must be 64, 128 or 256 and divide K.  W must be 16-byte aligned.
+ * Offline, one-time; not part of the timed layer.
+ * ------------------------------------------------------------------------ */
+int w4_quantize(const float *W, int E, int N, int K, int group,
+                uint8_t *q, uint16_t *s, uint16_t *z, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_route -- router: softmax over E logits, top-k, renormalise
+ * ("Inference: Making every denoising pass fast" -- Quantisation alone leaves
+ *  a sparse execution problem: a router scores the experts per token and the
+ *  token runs through the 8 best of 128).
+ *
+ *   logits        [M, E] fp32
+ *   topk_ids      [M, k] int32 out: the k largest logits, ties to the lower
+ *                 index, in descending order
+ *   topk_weights  [M, k] fp32 out: exp(l_j - l_max) / sum_i exp(l_i - l_max)
+ *                 over the k selected (= softmax renormalised over the k)
+ * Requires 1 <= k <= 32, k <= E <= 1024.
+ * ------------------------------------------------------------------------ */
+int w4_moe_route(const float *logits, int M, int E, int k,
+                 int32_t *topk_ids, float *topk_weights, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_align -- sync-free token-to-expert alignment
+ * ("Inference: Making every denoising pass fast" -- Quantisation alone leaves
+ *  a sparse execution problem: sort assignments by expert, pad into regular
+ *  blocks; "dg-w4-kernels" -- Grouped MoE: sync-free, CUDA-graph safe).
+ *
+ * Flat assignment index a = t*k + j (A = M*k).  With c_e the number of
+ * assignments to expert e and bm = block_m:
+ *   expert_offsets [E+1] out: o_0 = 0, o_{e+1} = o_e + ceil(c_e/bm)*bm
+ *   sorted_ids     [cap] out: slot o_e + r holds the r-th smallest a routed
+ *                  to e (stable); padding slots and slots >= o_E hold A
+ *   block_expert   [cap/bm] out: owning expert of block b, -1 past o_E
+ *   num_padded     [1] out: o_E (stays on the device)
+ * where cap = w4_moe_align_capacity(M, k, E, block_m).  ids outside [0, E)
+ * are skipped and set W4_DEV_BAD_EXPERT_ID in *dev_status (may be NULL).
+ * block_m must be 16, 32, 64, 128 or 256; E <= 1024.  One CTA, no atomics
+ * on global memory, no host synchronisation.
+ * ------------------------------------------------------------------------ */
+int64_t w4_moe_align_capacity(int M, int k, int E, int block_m);
+int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m,
+                 int32_t *sorted_ids, int32_t *block_expert, int32_t *expert_offsets,
+                 int32_t *num_padded, int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_grouped_gemm_gate_up -- grouped W4A16 gate_up GEMM with the gated
+ * activation in its epilogue
+ * ("dg-w4-kernels" -- Grouped MoE: one launch for all experts, activation
+ *  folded into the first GEMM's epilogue; "diffusiongemma-26B-A4B-w4a16" --
+ *  Checkpoint format: gate_up groups of 128 along the contraction dim).
+ *
+ *   x              [M, d] bf16
+ *   gu_q           [E, 2m, d/2] uint8 (w4_quantize layout), gu_s/gu_z
+ *                  [E, 2m, d/group] fp16; rows [0, m) gate, [m, 2m) up
+ *   sorted_ids, expert_offsets   from w4_moe_align with the same block_m
+ *   h              [cap, m] fp16 out, row = alignment slot:
+ *                  h[slot] = gelu_tanh(g) * u for the token of sorted_ids[slot],
+ *                  zero rows for padding slots inside an expert's range;
+ *                  rows at slots >= num_padded are not written
+ * Weights are dequantised in registers to fp16 (s*q + (-z*s), one rounding)
+ * and multiplied on the tensor cores (tcgen05, fp16 x fp16 -> fp32); x is
+ * converted to fp16 (exact within fp16 range); h is rounded to fp16 with
+ * saturation at +-65504.
+ * Requires d % 128 == 0, m % 64 == 0, group == 128.
+ * dev_status may be NULL.
+ * ------------------------------------------------------------------------ */
+int w4_grouped_gemm_gate_up(const uint16_t *x, int M, int d, int m, int E, int k, int block_m,
+                            const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                            int group, const int32_t *sorted_ids,
+                            const int32_t *expert_offsets, uint16_t *h,
+                            int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_grouped_gemm_down -- grouped W4A16 down GEMM, contraction dim m (704 on
+ * the pages) with groups of 64
+ * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: down_proj groups of
+ *  64 because 128 does not divide 704).
+ *
+ *   h              [cap, m] fp16 (from w4_grouped_gemm_gate_up)
+ *   dn_q           [E, d, m/2] uint8, dn_s/dn_z [E, d, m/group] fp16
+ *   y              [M*k, d] fp32 out, row a = flat assignment index
+ *                  (y[a] = h[slot of a] . deq(Wdn[e])^T); rows of skipped
+ *                  (invalid-id) assignments are not written
+ * Requires d % 128 == 0, m % 64 == 0, group == 64.  dev_status may be NULL.
+ * ------------------------------------------------------------------------ */
+int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
+                         const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z,
+                         int group, const int32_t *sorted_ids,
+                         const int32_t *expert_offsets, float *y,
+                         int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_combine_fixed_order -- atomics-free weighted combine
+ * ("Inference: Making every denoising pass fast" -- Quantisation alone leaves
+ *  a sparse execution problem: a token's eight outputs are reduced in a fixed
+ *  order, never with index_add_ atomics, so reruns are bit-identical).
+ *
+ *   out[t, c] = bf16_rn( fma-chain over j = 0..k-1 in order, starting at 0,
+ *                        of topk_weights[t, j] * y[t*k + j, c] )  in fp32;
+ *   slots whose id is outside [0, E) contribute nothing.
+ *   y [M*k, d] fp32, topk_ids/topk_weights [M, k], out [M, d] bf16.
+ * Requires d % 4 == 0.
+ * ------------------------------------------------------------------------ */
+int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids,
+                               const float *topk_weights, int M, int k, int d, int E,
+                               uint16_t *out, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_layer -- the whole routed-expert layer: align, gate_up + activation,
+ * down, fixed-order combine, as four launches on one stream
+ * ("dg-w4-kernels" -- Grouped MoE: out = fused_moe_w4_v2(hidden, experts,
+ *  topk_ids, topk_weights)).
+ *
+ * workspace: caller-owned device buffer of at least
+ * w4_moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds the
+ * alignment outputs, h and y.  Its contents on return are the intermediates
+ * of this call (layout: see the implementation; not part of the ABI).
+ * Same shape rules as the individual calls; dev_status may be NULL.
+ * ------------------------------------------------------------------------ */
+size_t w4_moe_layer_workspace_size(int M, int d, int m, int E, int k, int block_m);
+int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                 int M, int d, int m, int E, int k, int block_m,
+                 const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z, int gu_group,
+                 const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
+                 void *workspace, size_t workspace_bytes, uint16_t *out,
+                 int32_t *dev_status, w4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4MOE_H */

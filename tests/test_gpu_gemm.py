@@ -1,0 +1,111 @@
+"""The two grouped W4A16 GEMMs against the oracle's float64 intermediates
+("dg-w4-kernels" -- Grouped MoE; "diffusiongemma-26B-A4B-w4a16" -- Checkpoint
+format).
+
+h is compared slot by slot with the oracle's h of the assignment in that slot;
+y row by row.  Tolerance: max|gpu - oracle| / rms(oracle) <= 1e-2 per step
+(the layer's bound is 2e-2 on the bf16 output).  The weights are rounded to
+fp16 after dequantisation (relative error <= 2^-11) and h to fp16, so the
+expected error is a few 1e-4.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import gpu_weights, oracle_weights, rel_max_err
+from w4a16_moe_expert_sync_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+STEP_TOL = 1e-2
+
+
+def _cuda(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _run_steps(lib, cfg, gu, dn, x_bits, ids, block_m):
+    import torch
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = _cuda(x_bits.view(np.int16)).view(torch.bfloat16)
+    al = lib.w4_moe_align(_cuda(ids), cfg.E, block_m, dev_status=status)
+    h = lib.w4_grouped_gemm_gate_up(x, *gu, al, dev_status=status)
+    y = lib.w4_grouped_gemm_down(h, *dn, al, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return (al["sorted_ids"].cpu().numpy(), int(al["num_padded"].item()),
+            h.float().cpu().numpy(), y.cpu().numpy())
+
+
+def _compare(cfg, sorted_ids, npad, h, y, h_ref, y_ref, rows=None):
+    A = cfg.A
+    real = [(s, a) for s, a in enumerate(sorted_ids[:npad]) if a < A]
+    if rows is not None:
+        real = [(s, a) for s, a in real if a in rows]
+    slots = np.array([s for s, _ in real])
+    assign = np.array([a for _, a in real])
+    eh = rel_max_err(h[slots], h_ref[assign])
+    ey = rel_max_err(y[assign], y_ref[assign])
+    print(f"{cfg.name}: h err {eh:.3e}  y err {ey:.3e}")
+    assert eh <= STEP_TOL and ey <= STEP_TOL
+    if rows is None:
+        pads = [s for s, a in enumerate(sorted_ids[:npad]) if a == A]
+        assert np.all(h[pads] == 0.0)
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64])
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_gemm_steps_match_oracle(lib, name, block_m):
+    cfg = wl.CONFIGS[name]
+    gu, dn = gpu_weights(name)
+    ogu, odn = oracle_weights(cfg, range(cfg.E))
+    # the packed weights the GPU made are the oracle's, bit for bit
+    assert np.array_equal(gu[0].cpu().numpy(), ogu[0])
+    assert np.array_equal(dn[0].cpu().numpy(), odn[0])
+    x_bits = wl.activations(cfg)
+    ids, w = oracle.route(wl.router_logits(cfg), cfg.k)
+    sorted_ids, npad, h, y = _run_steps(lib, cfg, gu, dn, x_bits, ids, block_m)
+    _, h_ref, y_ref = oracle.moe_layer(x_bits, ogu, odn, ids, w, want_intermediates=True)
+    _compare(cfg, sorted_ids, npad, h, y, h_ref, y_ref)
+
+
+def test_gemm_expert_with_more_than_256_tokens(lib):
+    """One expert receives 300 tokens: its range splits into two jobs (256 + 48)."""
+    import torch
+    cfg = wl.LayerShape("hot", 300, 256, 128, 4, 2, seed=21)
+    rng = np.random.default_rng(21)
+    ids = np.stack([np.zeros(300, np.int64), rng.integers(1, 4, 300)], axis=1).astype(np.int32)
+    w = np.full((300, 2), 0.5, np.float32)
+    x_bits = wl.activations(cfg)
+    ogu, odn = oracle_weights(cfg, range(cfg.E))
+    gu = tuple(_cuda(a) for a in ogu)
+    dn = tuple(_cuda(a) for a in odn)
+    gu = (gu[0], gu[1].view(torch.float16), gu[2].view(torch.float16))
+    dn = (dn[0], dn[1].view(torch.float16), dn[2].view(torch.float16))
+    sorted_ids, npad, h, y = _run_steps(lib, cfg, gu, dn, x_bits, ids, 16)
+    _, h_ref, y_ref = oracle.moe_layer(x_bits, ogu, odn, ids, w, want_intermediates=True)
+    _compare(cfg, sorted_ids, npad, h, y, h_ref, y_ref)
+
+
+@pytest.mark.parametrize("name", ["layer256", "canvas2048"])
+def test_gemm_steps_full_size_sampled(lib, name):
+    """Pages' layer shape: check the rows of a few sampled tokens."""
+    cfg = wl.CONFIGS[name]
+    gu, dn = gpu_weights(name)
+    x_bits = wl.activations(cfg)
+    ids, w = oracle.route(wl.router_logits(cfg), cfg.k)
+    sorted_ids, npad, h, y = _run_steps(lib, cfg, gu, dn, x_bits, ids, 16)
+    toks = np.random.default_rng(0).choice(cfg.M, size=4, replace=False)
+    experts = ids[toks].ravel()
+    ogu, odn = oracle_weights(cfg, experts)
+    _, h_ref, y_ref = oracle.moe_layer(x_bits[toks], ogu, odn, ids[toks], w[toks],
+                                       want_intermediates=True)
+    # map the sampled tokens' assignments back to full flat indices
+    rows = {int(t) * cfg.k + j for t in toks for j in range(cfg.k)}
+    full_h = np.zeros((cfg.A, cfg.m))
+    full_y = np.zeros((cfg.A, cfg.d))
+    for i, t in enumerate(toks):
+        for j in range(cfg.k):
+            full_h[t * cfg.k + j] = h_ref[i * cfg.k + j]
+            full_y[t * cfg.k + j] = y_ref[i * cfg.k + j]
+    _compare(cfg, sorted_ids, npad, h, y, full_h, full_y, rows=rows)

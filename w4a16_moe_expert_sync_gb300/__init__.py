@@ -1,1 +1,24 @@
-"""GB300-native W4A16 routed mixture-of-experts layer (placeholder, filled in below)."""
+"""GB300-native W4A16 routed mixture-of-experts layer.
+
+The compute lives in libw4moe.so (hand-written CUDA for sm_103a, C ABI in
+include/w4moe.h).  This package is its thin Python binding plus the seeded
+synthetic workloads (``workloads``) used by the tests and the benchmark.
+
+    import w4a16_moe_expert_sync_gb300 as w4
+    q, s, z = w4.w4_quantize(W_fp32_cuda, group=128)
+    ids, w = w4.w4_moe_route(logits, k=8)
+    out = w4.w4_moe_layer(x_bf16, ids, w, (gu_q, gu_s, gu_z), (dn_q, dn_s, dn_z))
+"""
+from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_PIPELINE_TIMEOUT, W4_DEV_TOO_MANY_JOBS,
+                   W4Error, header_functions, load_library, w4_grouped_gemm_down,
+                   w4_grouped_gemm_gate_up, w4_moe_align, w4_moe_align_capacity,
+                   w4_moe_combine_fixed_order, w4_moe_layer, w4_moe_layer_workspace_size,
+                   w4_moe_route, w4_quantize)
+
+__all__ = [
+    "W4Error", "load_library", "header_functions",
+    "w4_quantize", "w4_moe_route", "w4_moe_align", "w4_moe_align_capacity",
+    "w4_grouped_gemm_gate_up", "w4_grouped_gemm_down", "w4_moe_combine_fixed_order",
+    "w4_moe_layer", "w4_moe_layer_workspace_size",
+    "W4_DEV_BAD_EXPERT_ID", "W4_DEV_PIPELINE_TIMEOUT", "W4_DEV_TOO_MANY_JOBS",
+]

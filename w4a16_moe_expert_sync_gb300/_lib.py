@@ -1,0 +1,239 @@
+"""ctypes binding of libw4moe.so: the C entry points of include/w4moe.h under
+the same names, taking torch tensors.  Argument marshalling only: shapes are
+read from the tensors, outputs are allocated with torch (device memory), the
+pointers and the current CUDA stream are passed through, and a nonzero status
+raises W4Error.  Every step of the layer runs in the library's CUDA kernels;
+there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from .build import LIB as _LIB_PATH
+
+_lock = threading.Lock()
+_lib = None
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "w4moe.h")
+
+# device status bits (include/w4moe.h)
+W4_DEV_BAD_EXPERT_ID = 0x1
+W4_DEV_PIPELINE_TIMEOUT = 0x2
+W4_DEV_TOO_MANY_JOBS = 0x4
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name} ({status}): {detail}")
+        self.status = status
+        self.name = name
+        self.detail = detail
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/w4moe.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(w4_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def load_library(path: str | None = None):
+    """Load libw4moe.so (built by __graft_entry__.build()); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        V, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "w4_status_string": ([I], ctypes.c_char_p),
+            "w4_last_error_detail": ([], ctypes.c_char_p),
+            "w4_abi_version": ([], I),
+            "w4_quantize": ([V, I, I, I, I, V, V, V, V], I),
+            "w4_moe_route": ([V, I, I, I, V, V, V], I),
+            "w4_moe_align_capacity": ([I, I, I, I], I64),
+            "w4_moe_align": ([V, I, I, I, I, V, V, V, V, V, V], I),
+            "w4_grouped_gemm_gate_up": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
+            "w4_grouped_gemm_down": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
+            "w4_moe_combine_fixed_order": ([V, V, V, I, I, I, I, V, V], I),
+            "w4_moe_layer_workspace_size": ([I, I, I, I, I, I], SZ),
+            "w4_moe_layer": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V, SZ, V, V,
+                              V], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        lib = load_library()
+        raise W4Error(rc, lib.w4_status_string(rc).decode(),
+                      f"{what}: {lib.w4_last_error_detail().decode()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors passed to the CUDA library must live on the GPU")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors passed to the CUDA library must be contiguous")
+
+
+# --------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# --------------------------------------------------------------------------
+def w4_quantize(W, group: int, out=None, stream=None):
+    """quantize_w4: W [E, N, K] fp32 -> (q [E,N,K/2] u8, s, z [E,N,K/group] fp16)."""
+    import torch
+    _require_cuda(W)
+    if W.dim() == 2:
+        W = W.unsqueeze(0)
+    E, N, K = W.shape
+    if out is None:
+        out = (torch.empty((E, N, K // 2), dtype=torch.uint8, device=W.device),
+               torch.empty((E, N, K // group), dtype=torch.float16, device=W.device),
+               torch.empty((E, N, K // group), dtype=torch.float16, device=W.device))
+    q, s, z = out
+    _check(load_library().w4_quantize(_ptr(W), E, N, K, group, _ptr(q), _ptr(s), _ptr(z),
+                                      _stream(stream)), "w4_quantize")
+    return q, s, z
+
+
+def w4_moe_route(logits, k: int, stream=None):
+    """Router: logits [M, E] fp32 -> (topk_ids [M,k] int32, topk_weights [M,k] fp32)."""
+    import torch
+    _require_cuda(logits)
+    M, E = logits.shape
+    ids = torch.empty((M, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((M, k), dtype=torch.float32, device=logits.device)
+    _check(load_library().w4_moe_route(_ptr(logits), M, E, k, _ptr(ids), _ptr(w),
+                                       _stream(stream)), "w4_moe_route")
+    return ids, w
+
+
+def w4_moe_align_capacity(M: int, k: int, E: int, block_m: int) -> int:
+    cap = load_library().w4_moe_align_capacity(M, k, E, block_m)
+    if cap < 0:
+        raise W4Error(1, "W4_ERR_INVALID_ARG", "w4_moe_align_capacity: bad arguments")
+    return int(cap)
+
+
+def w4_moe_align(topk_ids, E: int, block_m: int = 16, dev_status=None, stream=None):
+    """Alignment: topk_ids [M, k] int32 -> dict of device tensors."""
+    import torch
+    _require_cuda(topk_ids, dev_status)
+    M, k = topk_ids.shape
+    cap = w4_moe_align_capacity(M, k, E, block_m)
+    dev = topk_ids.device
+    r = dict(sorted_ids=torch.empty(cap, dtype=torch.int32, device=dev),
+             block_expert=torch.empty(cap // block_m, dtype=torch.int32, device=dev),
+             expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+             num_padded=torch.empty(1, dtype=torch.int32, device=dev),
+             M=M, k=k, E=E, block_m=block_m)
+    _check(load_library().w4_moe_align(_ptr(topk_ids), M, k, E, block_m, _ptr(r["sorted_ids"]),
+                                       _ptr(r["block_expert"]), _ptr(r["expert_offsets"]),
+                                       _ptr(r["num_padded"]), _ptr(dev_status),
+                                       _stream(stream)), "w4_moe_align")
+    return r
+
+
+def w4_grouped_gemm_gate_up(x, gu_q, gu_s, gu_z, align: dict, group: int = 128, h=None,
+                            dev_status=None, stream=None):
+    """x [M, d] bf16 -> h [cap, m] fp16 = gelu_tanh(gate) * up per alignment slot."""
+    import torch
+    _require_cuda(x, gu_q, gu_s, gu_z, h, dev_status)
+    M, d = x.shape
+    E, two_m, _ = gu_q.shape
+    m = two_m // 2
+    cap = align["sorted_ids"].numel()
+    if h is None:
+        h = torch.empty((cap, m), dtype=torch.float16, device=x.device)
+    _check(load_library().w4_grouped_gemm_gate_up(
+        _ptr(x), M, d, m, E, align["k"], align["block_m"], _ptr(gu_q), _ptr(gu_s), _ptr(gu_z),
+        group, _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(h),
+        _ptr(dev_status), _stream(stream)), "w4_grouped_gemm_gate_up")
+    return h
+
+
+def w4_grouped_gemm_down(h, dn_q, dn_s, dn_z, align: dict, group: int = 64, y=None,
+                         dev_status=None, stream=None):
+    """h [cap, m] fp16 -> y [M*k, d] fp32 (row = flat assignment index)."""
+    import torch
+    _require_cuda(h, dn_q, dn_s, dn_z, y, dev_status)
+    E, d, half_m = dn_q.shape
+    m = half_m * 2
+    M, k = align["M"], align["k"]
+    if y is None:
+        y = torch.empty((M * k, d), dtype=torch.float32, device=h.device)
+    _check(load_library().w4_grouped_gemm_down(
+        _ptr(h), M, d, m, E, k, align["block_m"], _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), group,
+        _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(y), _ptr(dev_status),
+        _stream(stream)), "w4_grouped_gemm_down")
+    return y
+
+
+def w4_moe_combine_fixed_order(y, topk_ids, topk_weights, E: int, out=None, stream=None):
+    """out [M, d] bf16 = fixed-order sum_j w[t,j] * y[t*k+j]."""
+    import torch
+    _require_cuda(y, topk_ids, topk_weights, out)
+    M, k = topk_ids.shape
+    d = y.shape[1]
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=y.device)
+    _check(load_library().w4_moe_combine_fixed_order(
+        _ptr(y), _ptr(topk_ids), _ptr(topk_weights), M, k, d, E, _ptr(out), _stream(stream)),
+        "w4_moe_combine_fixed_order")
+    return out
+
+
+def w4_moe_layer_workspace_size(M, d, m, E, k, block_m=16) -> int:
+    return int(load_library().w4_moe_layer_workspace_size(M, d, m, E, k, block_m))
+
+
+def w4_moe_layer(x, topk_ids, topk_weights, gu, dn, block_m: int = 16, gu_group: int = 128,
+                 dn_group: int = 64, workspace=None, out=None, dev_status=None, stream=None):
+    """The whole routed-expert layer (align, gate_up + activation, down,
+    fixed-order combine) as four launches on the current stream."""
+    import torch
+    gu_q, gu_s, gu_z = gu
+    dn_q, dn_s, dn_z = dn
+    _require_cuda(x, topk_ids, topk_weights, gu_q, gu_s, gu_z, dn_q, dn_s, dn_z, workspace,
+                  out, dev_status)
+    M, d = x.shape
+    E, two_m, _ = gu_q.shape
+    m = two_m // 2
+    k = topk_ids.shape[1]
+    need = w4_moe_layer_workspace_size(M, d, m, E, k, block_m)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
+    _check(load_library().w4_moe_layer(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, d, m, E, k, block_m, _ptr(gu_q),
+        _ptr(gu_s), _ptr(gu_z), gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), dn_group,
+        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(dev_status), _stream(stream)),
+        "w4_moe_layer")
+    return out

@@ -1,0 +1,340 @@
+// api.cu -- the extern "C" entry points declared in include/w4moe.h: argument
+// validation on the host, then kernel launches on the caller's stream.  No
+// device allocation, no synchronisation, no device-to-host reads.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/w4moe.h"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_detail[512] = "";
+
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t err, const char *what)
+{
+    return fail(W4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+cudaStream_t as_stream(w4_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// The cubin targets sm_103a only; refuse anything else up front.
+int check_device()
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "cudaGetDevice");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(W4_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
+                    dev, major, minor);
+    return W4_OK;
+}
+
+bool valid_block_m(int bm) { return bm == 16 || bm == 32 || bm == 64 || bm == 128 || bm == 256; }
+
+int64_t align_capacity(int M, int k, int E, int bm)
+{
+    const int64_t A = static_cast<int64_t>(M) * k;
+    const int64_t cap = A + static_cast<int64_t>(E) * (bm - 1);
+    return (cap + bm - 1) / bm * bm;
+}
+
+// Shared checks for the two grouped GEMMs.
+int check_gemm_common(int M, int d, int m, int E, int k, int block_m, const void *act,
+                      const void *q, const void *s, const void *z, const void *sorted_ids,
+                      const void *offsets, const void *out)
+{
+    if (!act || !q || !s || !z || !sorted_ids || !offsets || !out)
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || d <= 0 || m <= 0 || E <= 0 || k <= 0)
+        return fail(W4_ERR_INVALID_ARG, "sizes must be positive (M >= 0)");
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (d % 128 || m % 64)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need d %% 128 == 0 and m %% 64 == 0 (d=%d, m=%d)", d,
+                    m);
+    if (E > 1024 || k > E)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need k <= E <= 1024");
+    const int64_t A = static_cast<int64_t>(M) * k;
+    if (A > (1ll << 30) || static_cast<int64_t>(E) * 2 * m > (1ll << 30) ||
+        static_cast<int64_t>(E) * d > (1ll << 30))
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "problem too large for 32-bit indexing");
+    if (!aligned16(act) || !aligned16(q) || !aligned16(s) || !aligned16(z) || !aligned16(out))
+        return fail(W4_ERR_MISALIGNED, "activation, weight, scale, zero and output pointers "
+                                       "must be 16-byte aligned");
+    if (!aligned4(sorted_ids) || !aligned4(offsets))
+        return fail(W4_ERR_MISALIGNED, "index arrays must be 4-byte aligned");
+    return W4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *w4_status_string(int status)
+{
+    switch (status) {
+    case W4_OK: return "W4_OK";
+    case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG";
+    case W4_ERR_UNSUPPORTED_SHAPE: return "W4_ERR_UNSUPPORTED_SHAPE";
+    case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED";
+    case W4_ERR_CUDA: return "W4_ERR_CUDA";
+    case W4_ERR_NO_DEVICE: return "W4_ERR_NO_DEVICE";
+    case W4_ERR_WORKSPACE: return "W4_ERR_WORKSPACE";
+    default: return "W4_ERR_UNKNOWN";
+    }
+}
+
+const char *w4_last_error_detail(void) { return g_detail; }
+
+int w4_abi_version(void) { return W4MOE_ABI_VERSION; }
+
+int w4_quantize(const float *W, int E, int N, int K, int group, uint8_t *q, uint16_t *s,
+                uint16_t *z, w4_stream_t stream)
+{
+    if (!W || !q || !s || !z)
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (E < 0 || N < 0 || K <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes E=%d N=%d K=%d", E, N, K);
+    if (group != 64 && group != 128 && group != 256)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "group must be 64, 128 or 256 (got %d)", group);
+    if (K % group)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "group %d does not divide K=%d", group, K);
+    if (!aligned16(W) || !aligned4(q) || !aligned4(s) || !aligned4(z))
+        return fail(W4_ERR_MISALIGNED, "W must be 16-byte aligned, outputs 4-byte aligned");
+    if (int rc = check_device())
+        return rc;
+    const int64_t rows = static_cast<int64_t>(E) * N;
+    cudaError_t err = w4::launch_quantize(W, rows, K, group, q, s, z, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "quantize launch");
+}
+
+int w4_moe_route(const float *logits, int M, int E, int k, int32_t *topk_ids, float *topk_weights,
+                 w4_stream_t stream)
+{
+    if (!logits || !topk_ids || !topk_weights)
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || E <= 0 || k <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d E=%d k=%d", M, E, k);
+    if (k > 32 || k > E || E > 1024)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need 1 <= k <= 32, k <= E <= 1024");
+    if (!aligned4(logits) || !aligned4(topk_ids) || !aligned4(topk_weights))
+        return fail(W4_ERR_MISALIGNED, "pointers must be 4-byte aligned");
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err = w4::launch_route(logits, M, E, k, topk_ids, topk_weights, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "route launch");
+}
+
+int64_t w4_moe_align_capacity(int M, int k, int E, int block_m)
+{
+    if (M < 0 || k <= 0 || E <= 0 || !valid_block_m(block_m))
+        return -1;
+    return align_capacity(M, k, E, block_m);
+}
+
+int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m, int32_t *sorted_ids,
+                 int32_t *block_expert, int32_t *expert_offsets, int32_t *num_padded,
+                 int32_t *dev_status, w4_stream_t stream)
+{
+    if (!sorted_ids || !block_expert || !expert_offsets || !num_padded || (M > 0 && !topk_ids))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || k <= 0 || E <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d k=%d E=%d", M, k, E);
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (E > 1024)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "E must be <= 1024");
+    const int64_t cap = align_capacity(M, k, E, block_m);
+    if (cap > (1ll << 30))
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "too many assignments");
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err = w4::launch_align(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
+                                       expert_offsets, num_padded, dev_status, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "align launch");
+}
+
+int w4_grouped_gemm_gate_up(const uint16_t *x, int M, int d, int m, int E, int k, int block_m,
+                            const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                            int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
+                            uint16_t *h, int32_t *dev_status, w4_stream_t stream)
+{
+    if (int rc = check_gemm_common(M, d, m, E, k, block_m, x, gu_q, gu_s, gu_z, sorted_ids,
+                                   expert_offsets, h))
+        return rc;
+    if (group != 128)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "gate_up group must be 128 (got %d)", group);
+    if (int rc = check_device())
+        return rc;
+    w4::GroupedGemmProblem p{};
+    p.gate_up = true;
+    p.act = x;
+    p.wq = gu_q;
+    p.ws = gu_s;
+    p.wz = gu_z;
+    p.sorted_ids = sorted_ids;
+    p.expert_offsets = expert_offsets;
+    p.out = h;
+    p.dev_status = dev_status;
+    p.M = M;
+    p.k = k;
+    p.E = E;
+    p.K = d;
+    p.R = 2 * m;
+    p.group = group;
+    p.out_cols = m;
+    p.cap = align_capacity(M, k, E, block_m);
+    if (M == 0)
+        return W4_OK;
+    const char *why = nullptr;
+    cudaError_t err = w4::launch_grouped_gemm(p, as_stream(stream), &why);
+    if (why)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "%s", why);
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "gate_up launch");
+}
+
+int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
+                         const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
+                         const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
+                         int32_t *dev_status, w4_stream_t stream)
+{
+    if (int rc = check_gemm_common(M, d, m, E, k, block_m, h, dn_q, dn_s, dn_z, sorted_ids,
+                                   expert_offsets, y))
+        return rc;
+    if (group != 64)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "down group must be 64 (got %d)", group);
+    if (int rc = check_device())
+        return rc;
+    w4::GroupedGemmProblem p{};
+    p.gate_up = false;
+    p.act = h;
+    p.wq = dn_q;
+    p.ws = dn_s;
+    p.wz = dn_z;
+    p.sorted_ids = sorted_ids;
+    p.expert_offsets = expert_offsets;
+    p.out = y;
+    p.dev_status = dev_status;
+    p.M = M;
+    p.k = k;
+    p.E = E;
+    p.K = m;
+    p.R = d;
+    p.group = group;
+    p.out_cols = d;
+    p.cap = align_capacity(M, k, E, block_m);
+    if (M == 0)
+        return W4_OK;
+    const char *why = nullptr;
+    cudaError_t err = w4::launch_grouped_gemm(p, as_stream(stream), &why);
+    if (why)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "%s", why);
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "down launch");
+}
+
+int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const float *topk_weights,
+                               int M, int k, int d, int E, uint16_t *out, w4_stream_t stream)
+{
+    if (!out || (M > 0 && (!y || !topk_ids || !topk_weights)))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || k <= 0 || d <= 0 || E <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d k=%d d=%d E=%d", M, k, d, E);
+    if (d % 4)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "d must be a multiple of 4");
+    if (!aligned16(y) || (reinterpret_cast<uintptr_t>(out) & 7u))
+        return fail(W4_ERR_MISALIGNED, "y must be 16-byte and out 8-byte aligned");
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err =
+        w4::launch_combine(y, topk_ids, topk_weights, M, k, d, E, out, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "combine launch");
+}
+
+// Workspace layout of w4_moe_layer (each piece 256-byte aligned):
+//   sorted_ids [cap] i32 | block_expert [cap/bm] i32 | expert_offsets [E+1] i32 |
+//   num_padded [1] i32 | h [cap, m] fp16 | y [M*k, d] fp32
+namespace {
+struct LayerWs {
+    size_t sorted, block, offs, npad, h, y, total;
+};
+size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
+{
+    const size_t cap = static_cast<size_t>(align_capacity(M, k, E, bm));
+    LayerWs w;
+    w.sorted = 0;
+    w.block = up256(w.sorted + 4 * cap);
+    w.offs = up256(w.block + 4 * (cap / bm));
+    w.npad = up256(w.offs + 4 * (static_cast<size_t>(E) + 1));
+    w.h = up256(w.npad + 4);
+    w.y = up256(w.h + 2 * cap * static_cast<size_t>(m));
+    w.total = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
+    return w;
+}
+}  // namespace
+
+size_t w4_moe_layer_workspace_size(int M, int d, int m, int E, int k, int block_m)
+{
+    if (M < 0 || d <= 0 || m <= 0 || E <= 0 || k <= 0 || !valid_block_m(block_m))
+        return 0;
+    return layer_ws(M, d, m, E, k, block_m).total;
+}
+
+int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights, int M,
+                 int d, int m, int E, int k, int block_m, const uint8_t *gu_q,
+                 const uint16_t *gu_s, const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
+                 const uint16_t *dn_s, const uint16_t *dn_z, int dn_group, void *workspace,
+                 size_t workspace_bytes, uint16_t *out, int32_t *dev_status, w4_stream_t stream)
+{
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (M < 0 || d <= 0 || m <= 0 || E <= 0 || k <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes");
+    const LayerWs L = layer_ws(M, d, m, E, k, block_m);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(W4_ERR_WORKSPACE, "workspace needs %zu bytes", L.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(W4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    int32_t *block = reinterpret_cast<int32_t *>(ws + L.block);
+    int32_t *offs = reinterpret_cast<int32_t *>(ws + L.offs);
+    int32_t *npad = reinterpret_cast<int32_t *>(ws + L.npad);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    float *y = reinterpret_cast<float *>(ws + L.y);
+    int rc = w4_moe_align(topk_ids, M, k, E, block_m, sorted, block, offs, npad, dev_status,
+                          stream);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return W4_OK;
+    rc = w4_grouped_gemm_gate_up(x, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group, sorted,
+                                 offs, h, dev_status, stream);
+    if (rc)
+        return rc;
+    rc = w4_grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs,
+                              y, dev_status, stream);
+    if (rc)
+        return rc;
+    return w4_moe_combine_fixed_order(y, topk_ids, topk_weights, M, k, d, E, out, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// combine.cu -- fixed-order, atomics-free weighted combine
+// ("Inference: Making every denoising pass fast" -- Quantisation alone leaves
+// a sparse execution problem: a token's eight expert outputs are reduced in a
+// fixed order instead of index_add_, because reordered floating-point sums
+// change low bits and a one-ulp change can fork a denoising trajectory).
+//
+// Each thread owns four consecutive output columns of one token and runs the
+// fp32 chain acc = fma(w_j, y_j, acc) for j = 0..k-1, always in that order,
+// then rounds once to bf16.  Every output element has exactly one writer, so
+// the result is bit-identical from run to run.
+#include <cuda_bf16.h>
+
+#include "launch.h"
+
+namespace w4 {
+
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y,
+                                                      const int32_t *__restrict__ ids,
+                                                      const float *__restrict__ w, int M, int k,
+                                                      int d, int E, uint16_t *__restrict__ out)
+{
+    const int d4 = d / 4;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(M) * d4)
+        return;
+    const int t = static_cast<int>(i / d4);
+    const int c = static_cast<int>(i % d4) * 4;
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    for (int j = 0; j < k; j++) {
+        const int64_t a = static_cast<int64_t>(t) * k + j;
+        const int e = __ldg(ids + a);
+        if (e < 0 || e >= E)
+            continue;
+        const float wj = __ldg(w + a);
+        const float4 v = __ldcs(reinterpret_cast<const float4 *>(y + a * d + c));
+        a0 = fmaf(wj, v.x, a0);
+        a1 = fmaf(wj, v.y, a1);
+        a2 = fmaf(wj, v.z, a2);
+        a3 = fmaf(wj, v.w, a3);
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a0, a1);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(a2, a3);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(t) * d + c) = pk;
+}
+
+cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
+                           int d, int E, uint16_t *out, cudaStream_t stream)
+{
+    const int64_t n = static_cast<int64_t>(M) * (d / 4);
+    if (n == 0)
+        return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = (n + threads - 1) / threads;
+    combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(y, ids, w, M, k, d, E,
+                                                                          out);
+    return cudaGetLastError();
+}
+
+}  // namespace w4

@@ -1,0 +1,53 @@
+// launch.h -- internal launchers shared between the kernel translation units
+// and the C-ABI layer (api.cu).  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+// Device status bits (mirrors include/w4moe.h).
+constexpr int32_t kDevBadExpertId = 0x1;
+constexpr int32_t kDevPipelineTimeout = 0x2;
+constexpr int32_t kDevTooManyJobs = 0x4;
+
+cudaError_t launch_quantize(const float *W, int64_t rows, int K, int group, uint8_t *q,
+                            uint16_t *s, uint16_t *z, cudaStream_t stream);
+
+cudaError_t launch_route(const float *logits, int M, int E, int k, int32_t *ids, float *w,
+                         cudaStream_t stream);
+
+size_t align_smem_bytes(int E);
+cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
+                         int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
+                         int32_t *num_padded, int32_t *dev_status, cudaStream_t stream);
+
+cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
+                           int d, int E, uint16_t *out, cudaStream_t stream);
+
+// Grouped W4A16 GEMM (tcgen05).  gate_up=true: x bf16 -> h fp16 with the
+// gated activation; gate_up=false: h fp16 -> y fp32.
+struct GroupedGemmProblem {
+    bool gate_up;
+    const uint16_t *act;        // x [M, K] bf16 or h [cap, K] fp16
+    const uint8_t *wq;          // [E, R, K/2]
+    const uint16_t *ws, *wz;    // [E, R, K/group]
+    const int32_t *sorted_ids;  // [cap]
+    const int32_t *expert_offsets;  // [E+1]
+    void *out;                  // h [cap, m] fp16 or y [A, d] fp32
+    int32_t *dev_status;
+    int M, k, E, K, R, group;
+    int out_cols;               // m (gate_up) or d (down)
+    int64_t cap;
+};
+
+// Returns cudaSuccess, or an error; *why receives a static description when
+// the problem is rejected before launch (shape or resource limits).
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem &p, cudaStream_t stream,
+                                const char **why);
+
+}  // namespace w4
