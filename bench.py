@@ -1,0 +1,507 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 routed mixture-of-experts layer on GB300.
+
+One step = one pass of the whole layer over one batch: token-to-expert
+alignment, grouped gate_up GEMM with the gated activation, grouped down GEMM,
+fixed-order combine (four launches of libw4moe.so on one stream).  The
+workload is one 256-token canvas at the pages' layer shape: M=256, d=2816,
+m=704, E=128, top-8, uint4 weights with fp16 scale/zero (groups of 128 for
+gate_up, 64 for down), bf16 activations; inputs are seeded synthetic tensors
+(the pages' synthetic one-layer microbenchmark: "Inference: Making every
+denoising pass fast" -- The final best W4 MoE kernel).
+
+value = algorithmic bytes per step / device time per step (GB/s):
+  bytes = packed weights + fp16 scales/zeros of the experts the batch touches
+          + x read (M*d*2) + out write (M*d*2) + ids and weights (M*k*8).
+The L2 is flushed (256 MiB write) before every timed step, outside the timed
+events.  --impl reference times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload, in the same unit.
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent
+replicas of the same layer, one per GPU, with no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 MoE layer µs & HBM GB/s (% GB300 roofline) at M=256,d2816,m704,E128,top8"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def per_expert_bytes(d, m, gu_group=128, dn_group=64):
+    gu = 2 * m * d // 2 + 2 * (2 * m * (d // gu_group) * 2)
+    dn = d * m // 2 + 2 * (d * (m // dn_group) * 2)
+    return gu, dn
+
+
+def layer_alg_bytes(M, d, m, k, touched):
+    gu, dn = per_expert_bytes(d, m)
+    return touched * (gu + dn) + M * d * 2 + M * d * 2 + M * k * 8
+
+
+def gate_up_alg_bytes(M, d, m, touched):
+    gu, _ = per_expert_bytes(d, m)
+    return touched * gu + M * d * 2
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("grouped_gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "w4a16_moe_expert_sync_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec[kernel][workload]
+        if e.get("source_sha") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str, interval_ms: int = 20):
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", str(interval_ms), "-i", gpu_id]
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)      # let the first sample land before the timed region
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons, power = [], None, set(), []
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(self.REASONS, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def gpu_smi_id(dev):
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return str(dev)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas; barrier + max over ranks only)
+# ----------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+        except Exception:
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample_setup(cfg, experts=None):
+    """Oracle-side inputs: its own routing and its own quantisation of the
+    experts a sample needs (untimed preparation)."""
+    import oracle
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    x_bits = wl.activations(cfg)
+    ids, w = oracle.route(wl.router_logits(cfg), cfg.k)
+    if experts is None:
+        experts = range(cfg.E)
+    gu_q = np.zeros((cfg.E, 2 * cfg.m, cfg.d // 2), np.uint8)
+    gu_s = np.zeros((cfg.E, 2 * cfg.m, cfg.d // cfg.gu_group), np.uint16)
+    gu_z = np.zeros_like(gu_s)
+    dn_q = np.zeros((cfg.E, cfg.d, cfg.m // 2), np.uint8)
+    dn_s = np.zeros((cfg.E, cfg.d, cfg.m // cfg.dn_group), np.uint16)
+    dn_z = np.zeros_like(dn_s)
+    for e in sorted(set(int(v) for v in experts)):
+        gu_q[e], gu_s[e], gu_z[e] = oracle.quantize_w4(wl.gate_up_weight(cfg, e), cfg.gu_group)
+        dn_q[e], dn_s[e], dn_z[e] = oracle.quantize_w4(wl.down_weight(cfg, e), cfg.dn_group)
+    return x_bits, ids, w, (gu_q, gu_s, gu_z), (dn_q, dn_s, dn_z)
+
+
+def time_oracle_assignments(cfg, assign, setup, nthreads):
+    """Oracle layer on a list of flat assignments a = t*k + j, each run as its
+    own one-expert row (x_t, expert ids[a], weight w[a]).  Returns
+    (seconds, algorithmic bytes of that sample)."""
+    import oracle
+    x_bits, ids, w, gu, dn = setup
+    t = assign // cfg.k
+    e = ids.ravel()[assign]
+    wt = w.ravel()[assign]
+    t0 = time.perf_counter()
+    oracle.moe_layer(x_bits[t], gu, dn, e[:, None].astype(np.int32),
+                     wt[:, None].astype(np.float32), nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    touched = len(set(int(v) for v in e))
+    gu_b, dn_b = per_expert_bytes(cfg.d, cfg.m)
+    nbytes = touched * (gu_b + dn_b) + len(assign) * (cfg.d * 4 + 8)
+    return dt, nbytes
+
+
+def cpu_baseline(cfg, n_tokens):
+    """The oracle on n_tokens evenly spaced tokens of the workload (all k
+    experts each), on every host core; GB/s of that sample's algorithmic bytes."""
+    import oracle
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    nthreads = os.cpu_count() or 1
+    tokens = np.linspace(0, cfg.M - 1, n_tokens).round().astype(int)
+    ids, _ = oracle.route(wl.router_logits(cfg), cfg.k)
+    x_bits, ids, w, gu, dn = oracle_sample_setup(cfg, ids[tokens].ravel())
+    t0 = time.perf_counter()
+    oracle.moe_layer(x_bits[tokens], gu, dn, ids[tokens], w[tokens], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    touched = len(set(int(v) for v in ids[tokens].ravel()))
+    nbytes = layer_alg_bytes(len(tokens), cfg.d, cfg.m, cfg.k, touched)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{n_tokens} of {cfg.M} tokens of the {cfg.name} workload (all {cfg.k} "
+                      f"experts each, {n_tokens * cfg.k} assignments, {touched} experts), "
+                      f"float64 C oracle on {nthreads} threads, {dt:.2f} s wall"}
+
+
+def run_reference(args, cfg, world, rank):
+    """The reference arm: the float64 oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    nthreads = os.cpu_count() or 1
+    steps, warm = args.steps, args.warmup
+    setup = oracle_sample_setup(cfg)
+    A = cfg.M * cfg.k
+    # one step = `per` assignments (one per core), rotating through the
+    # canvas's M*k assignments
+    per = max(1, min(nthreads, A))
+    times, nbytes = [], []
+    for i in range(warm + steps):
+        assign = (np.arange(per) + i * per) % A
+        dt, nb = time_oracle_assignments(cfg, assign, setup, nthreads)
+        if i >= warm:
+            times.append(dt)
+            nbytes.append(nb)
+    total_t, total_b = sum(times), sum(nbytes)
+    value = total_b / total_t / 1e9
+    sample = (f"{per} (token, expert) assignments per step of the {cfg.name} workload, "
+              f"rotating over its {A} assignments; float64 C oracle on {nthreads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": 1e3 * total_t / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(cfg, args),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg, args):
+    return {"workload": f"{cfg.name}: W4A16 routed-MoE layer M={cfg.M} d={cfg.d} m={cfg.m} "
+                        f"E={cfg.E} top-{cfg.k}, uint4 weights with fp16 scale/zero "
+                        f"(g{cfg.gu_group} gate_up, g{cfg.dn_group} down), bf16 activations, "
+                        f"seed {cfg.seed}",
+            "M": cfg.M, "d": cfg.d, "m": cfg.m, "E": cfg.E, "k": cfg.k,
+            "block_m": args.block_m, "routing": cfg.routing,
+            "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+            "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+def prepare_gpu(cfg, dev):
+    import torch
+    import w4a16_moe_expert_sync_gb300 as w4
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    x = torch.from_numpy(wl.activations(cfg).view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(wl.router_logits(cfg)).to(dev)
+    gu = (torch.empty((cfg.E, 2 * cfg.m, cfg.d // 2), dtype=torch.uint8, device=dev),
+          torch.empty((cfg.E, 2 * cfg.m, cfg.d // cfg.gu_group), dtype=torch.float16, device=dev),
+          torch.empty((cfg.E, 2 * cfg.m, cfg.d // cfg.gu_group), dtype=torch.float16, device=dev))
+    dn = (torch.empty((cfg.E, cfg.d, cfg.m // 2), dtype=torch.uint8, device=dev),
+          torch.empty((cfg.E, cfg.d, cfg.m // cfg.dn_group), dtype=torch.float16, device=dev),
+          torch.empty((cfg.E, cfg.d, cfg.m // cfg.dn_group), dtype=torch.float16, device=dev))
+    for e in range(cfg.E):
+        w4.w4_quantize(torch.from_numpy(wl.gate_up_weight(cfg, e)).to(dev), cfg.gu_group,
+                       out=tuple(t[e:e + 1] for t in gu))
+        w4.w4_quantize(torch.from_numpy(wl.down_weight(cfg, e)).to(dev), cfg.dn_group,
+                       out=tuple(t[e:e + 1] for t in dn))
+    ids, w = w4.w4_moe_route(logits, cfg.k)
+    torch.cuda.synchronize()
+    return x, ids, w, gu, dn
+
+
+def run_gpu(args, cfg, world, rank, local):
+    import torch
+    import w4a16_moe_expert_sync_gb300 as w4
+    w4.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x, ids, w, gu, dn = prepare_gpu(cfg, dev)
+    touched = int(torch.unique(ids).numel())
+    nbytes = layer_alg_bytes(cfg.M, cfg.d, cfg.m, cfg.k, touched)
+    gu_bytes = gate_up_alg_bytes(cfg.M, cfg.d, cfg.m, touched)
+
+    bm = args.block_m
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    al = w4.w4_moe_align(ids, cfg.E, bm, dev_status=status)
+    h = torch.empty((al["sorted_ids"].numel(), cfg.m), dtype=torch.float16, device=dev)
+    y = torch.empty((cfg.M * cfg.k, cfg.d), dtype=torch.float32, device=dev)
+    out = torch.empty((cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        w4.w4_moe_align(ids, cfg.E, bm, dev_status=status, out=al)
+        if ev:
+            ev[1].record()
+        w4.w4_grouped_gemm_gate_up(x, *gu, al, h=h, dev_status=status)
+        if ev:
+            ev[2].record()
+        w4.w4_grouped_gemm_down(h, *dn, al, y=y, dev_status=status)
+        if ev:
+            ev[3].record()
+        w4.w4_moe_combine_fixed_order(y, ids, w, cfg.E, out=out)
+        if ev:
+            ev[4].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_smi_id(local)) if not args.skip_clocks else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__enter__()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if sampler:
+        sampler.__exit__(None, None, None)
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} in the timed region")
+
+    per_step = [e[0].elapsed_time(e[4]) for e in evs]               # ms
+    per_kernel = {name: [e[i].elapsed_time(e[i + 1]) for e in evs]
+                  for i, name in enumerate(("moe_align", "gate_up", "down", "combine"))}
+    mean_ms = statistics.fmean(per_step)
+    mean_ms_all = max_over_ranks(world, mean_ms, dev)
+    value = world * nbytes / (mean_ms_all * 1e-3) / 1e9
+
+    # ---------------------------------------------------------------- e2e
+    e2e = None
+    if not args.skip_e2e:
+        x_h = x.cpu().pin_memory()
+        ids_h = ids.cpu().pin_memory()
+        w_h = w.cpu().pin_memory()
+        out_h = torch.empty_like(out, device="cpu").pin_memory()
+        ws = torch.empty(w4.w4_moe_layer_workspace_size(cfg.M, cfg.d, cfg.m, cfg.E, cfg.k, bm),
+                         dtype=torch.uint8, device=dev)
+        x_d, ids_d, w_d = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(w)
+
+        def e2e_step():
+            x_d.copy_(x_h, non_blocking=True)
+            ids_d.copy_(ids_h, non_blocking=True)
+            w_d.copy_(w_h, non_blocking=True)
+            w4.w4_moe_layer(x_d, ids_d, w_d, gu, dn, block_m=bm, workspace=ws, out=out,
+                            dev_status=status)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize()
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            pairs[i][0].record()
+            e2e_step()
+            pairs[i][1].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(world, statistics.fmean(a.elapsed_time(b) for a, b in pairs), dev)
+        h2d = x.numel() * 2 + ids.numel() * 4 + w.numel() * 4
+        d2h = out.numel() * 2
+        e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms,
+               "api": "w4_moe_layer (one C-ABI call: align, gate_up, down, combine) "
+                      "with pinned-host inputs copied in and the output copied out each step"}
+        if not torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16)):
+            raise RuntimeError("e2e output copy mismatch")
+
+    # ------------------------------------------------------------ roofline
+    peak, peak_kind = measured_peaks()
+    gu_ms = statistics.fmean(per_kernel["gate_up"])
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": recorded_traffic("gate_up", cfg.name),
+                "kernel": "grouped_gemm_kernel<gate_up> (w4_grouped_gemm_gate_up)",
+                "alg_bytes_per_launch": gu_bytes,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_all,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16", "data": "synthetic", "config": config_dict(cfg, args),
+        "us_per_layer": mean_ms_all * 1e3,
+        "us_per_layer_median": statistics.median(per_step) * 1e3,
+        "layer_frac_of_hbm_peak": value / world / peak,
+        "alg_bytes_per_step": nbytes, "touched_experts": touched,
+        "kernels_us": {k: statistics.fmean(v) * 1e3 for k, v in per_kernel.items()},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": sampler.summary() if sampler else None,
+        "timed_region_wall_s": t_wall,
+        "precision": "uint4 weights dequantised to fp16 in registers, fp16 x fp16 tcgen05 MMA "
+                     "with fp32 accumulation, bf16 activations in and out",
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in cpu_baseline(cfg, args.cpu_tokens).items()
+                                if k != "seconds"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["w4moe", "reference"], default="w4moe")
+    ap.add_argument("--config", default="layer256")
+    ap.add_argument("--block-m", type=int, default=16)
+    ap.add_argument("--cpu-tokens", type=int, default=16)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-clocks", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    cfg = wl.CONFIGS[args.config]
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+    else:
+        run_gpu(args, cfg, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -347,62 +347,68 @@ typedef struct {
     const uint16_t *dn_s, *dn_z;
     int dn_group;
     const int32_t *ids;
-    const float *weights;
-    double *h_out, *y_out, *out;
+    double *h_all, *y_all;      /* [M*k, m], [M*k, d] */
     int tid, nthreads;
 } layer_job;
 
-static void *layer_worker(void *arg)
+/* Phase 1: every flat assignment a = t*k + j is independent; threads take
+ * a = tid, tid + nthreads, ... and write h_a and y_a. */
+static void *expert_worker(void *arg)
 {
     layer_job *J = (layer_job *)arg;
     const int d = J->d, m = J->m, k = J->k;
     double *xr = (double *)malloc(sizeof(double) * (size_t)d);
-    double *h = (double *)malloc(sizeof(double) * (size_t)m);
-    double *y = (double *)malloc(sizeof(double) * (size_t)d);
-    if (!xr || !h || !y)
-        goto done;
+    if (!xr)
+        return NULL;
     const int64_t Ggu = d / J->gu_group, Gdn = m / J->dn_group;
-    for (int t = J->tid; t < J->M; t += J->nthreads) {
-        for (int c = 0; c < d; c++) {
-            xr[c] = oracle_bf16_to_f64(J->x[(int64_t)t * d + c]);
-            J->out[(int64_t)t * d + c] = 0.0;
+    const int64_t A = (int64_t)J->M * k;
+    for (int64_t a = J->tid; a < A; a += J->nthreads) {
+        const int64_t t = a / k;
+        double *h = J->h_all + a * m;
+        double *y = J->y_all + a * d;
+        int e = J->ids[a];
+        if (e < 0 || e >= J->E) {                   /* R7: skipped */
+            memset(h, 0, sizeof(double) * (size_t)m);
+            memset(y, 0, sizeof(double) * (size_t)d);
+            continue;
         }
-        for (int j = 0; j < k; j++) {               /* R8: slot order */
-            int64_t a = (int64_t)t * k + j;
-            int e = J->ids[a];
-            if (e < 0 || e >= J->E) {               /* R7: skipped */
-                if (J->h_out) memset(J->h_out + a * m, 0, sizeof(double) * (size_t)m);
-                if (J->y_out) memset(J->y_out + a * d, 0, sizeof(double) * (size_t)d);
-                continue;
-            }
-            /* gate_up: rows [0, m) gate, [m, 2m) up (R2) */
-            const int64_t gu_rows = 2 * (int64_t)m;
-            for (int i = 0; i < m; i++) {
-                int64_t rg = (int64_t)e * gu_rows + i, ru = rg + m;
-                double g = w4_row_dot(J->gu_q + rg * (d / 2), J->gu_s + rg * Ggu,
-                                      J->gu_z + rg * Ggu, d, J->gu_group, xr);
-                double u = w4_row_dot(J->gu_q + ru * (d / 2), J->gu_s + ru * Ggu,
-                                      J->gu_z + ru * Ggu, d, J->gu_group, xr);
-                h[i] = oracle_gelu_tanh(g) * u;   /* R1 */
-            }
-            /* down: d rows, contraction over m */
-            for (int r = 0; r < d; r++) {
-                int64_t rr = (int64_t)e * d + r;
-                y[r] = w4_row_dot(J->dn_q + rr * (m / 2), J->dn_s + rr * Gdn,
-                                  J->dn_z + rr * Gdn, m, J->dn_group, h);
-            }
-            if (J->h_out) memcpy(J->h_out + a * m, h, sizeof(double) * (size_t)m);
-            if (J->y_out) memcpy(J->y_out + a * d, y, sizeof(double) * (size_t)d);
-            double w = (double)J->weights[a];
-            for (int c = 0; c < d; c++)
-                J->out[(int64_t)t * d + c] += w * y[c];
+        for (int c = 0; c < d; c++)
+            xr[c] = oracle_bf16_to_f64(J->x[t * d + c]);
+        /* gate_up: rows [0, m) gate, [m, 2m) up (R2) */
+        const int64_t gu_rows = 2 * (int64_t)m;
+        for (int i = 0; i < m; i++) {
+            int64_t rg = (int64_t)e * gu_rows + i, ru = rg + m;
+            double g = w4_row_dot(J->gu_q + rg * (d / 2), J->gu_s + rg * Ggu,
+                                  J->gu_z + rg * Ggu, d, J->gu_group, xr);
+            double u = w4_row_dot(J->gu_q + ru * (d / 2), J->gu_s + ru * Ggu,
+                                  J->gu_z + ru * Ggu, d, J->gu_group, xr);
+            h[i] = oracle_gelu_tanh(g) * u;   /* R1 */
+        }
+        /* down: d rows, contraction over m */
+        for (int r = 0; r < d; r++) {
+            int64_t rr = (int64_t)e * d + r;
+            y[r] = w4_row_dot(J->dn_q + rr * (m / 2), J->dn_s + rr * Gdn,
+                              J->dn_z + rr * Gdn, m, J->dn_group, h);
         }
     }
-done:
     free(xr);
-    free(h);
-    free(y);
     return NULL;
+}
+
+static void run_threads(void *(*fn)(void *), layer_job *jobs, int nthreads)
+{
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 1; i < nthreads; i++) {
+        if (pthread_create(&th[i], NULL, fn, &jobs[i]) != 0)
+            break;
+        started = i;
+    }
+    fn(&jobs[0]);
+    for (int i = 1; i <= started; i++)
+        pthread_join(th[i], NULL);
+    for (int i = started + 1; i < nthreads; i++)   /* threads that failed to start */
+        fn(&jobs[i]);
 }
 
 /* The whole layer in float64.
@@ -411,9 +417,10 @@ done:
  *   dn_q     [E, d, m/2],  dn_s/dn_z [E, d, m/dn_group]
  *   ids, weights [M, k]
  *   h_out [M*k, m], y_out [M*k, d] (either may be NULL), out [M, d].
- * Tokens are split over nthreads POSIX threads; every output element is
- * produced by one thread in a fixed order, so the result does not depend on
- * the thread count.  Returns 0, or 1 on bad arguments. */
+ * Assignments (t, j) are split over nthreads POSIX threads, each writing its
+ * own h and y rows; the combine then runs token by token in slot order.  Every
+ * value is produced by one fixed sequence of operations, so the result does
+ * not depend on the thread count.  Returns 0, or 1 on bad arguments. */
 int oracle_moe_layer(const uint16_t *x, int M, int d, int m, int E, int k,
                      const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z, int gu_group,
                      const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
@@ -427,24 +434,35 @@ int oracle_moe_layer(const uint16_t *x, int M, int d, int m, int E, int k,
         nthreads = 1;
     if (nthreads > 256)
         nthreads = 256;
-    pthread_t th[256];
+    const int64_t A = (int64_t)M * k;
+    double *h_all = h_out ? h_out : (double *)malloc(sizeof(double) * (size_t)(A * m + 1));
+    double *y_all = y_out ? y_out : (double *)malloc(sizeof(double) * (size_t)(A * d + 1));
+    if (!h_all || !y_all) {
+        if (!h_out) free(h_all);
+        if (!y_out) free(y_all);
+        return 1;
+    }
     layer_job jobs[256];
     for (int i = 0; i < nthreads; i++) {
         layer_job J = {x, M, d, m, E, k, gu_q, gu_s, gu_z, gu_group, dn_q, dn_s, dn_z,
-                       dn_group, ids, weights, h_out, y_out, out, i, nthreads};
+                       dn_group, ids, h_all, y_all, i, nthreads};
         jobs[i] = J;
     }
-    int started = 0;
-    for (int i = 1; i < nthreads; i++) {
-        if (pthread_create(&th[i], NULL, layer_worker, &jobs[i]) != 0)
-            break;
-        started = i;
+    run_threads(expert_worker, jobs, nthreads);
+    /* Phase 2, R8: out_t = sum over slots j = 0..k-1, in that order */
+    for (int64_t t = 0; t < M; t++) {
+        for (int c = 0; c < d; c++) {
+            double acc = 0.0;
+            for (int j = 0; j < k; j++) {
+                const int64_t a = t * k + j;
+                if (ids[a] < 0 || ids[a] >= E)
+                    continue;
+                acc += (double)weights[a] * y_all[a * d + c];
+            }
+            out[t * d + c] = acc;
+        }
     }
-    layer_worker(&jobs[0]);
-    for (int i = 1; i <= started; i++)
-        pthread_join(th[i], NULL);
-    /* threads that failed to start: run their share here */
-    for (int i = started + 1; i < nthreads; i++)
-        layer_worker(&jobs[i]);
+    if (!h_out) free(h_all);
+    if (!y_out) free(y_all);
     return 0;
 }

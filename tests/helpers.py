@@ -22,6 +22,13 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def bf16_round(a: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (via torch), as float64:
+    the error floor any bf16 output carries."""
+    import torch
+    return torch.from_numpy(np.asarray(a, np.float64)).to(torch.bfloat16).double().numpy()
+
+
 def torch_bf16_to_f64(t) -> np.ndarray:
     import torch
     return bf16_bits_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))

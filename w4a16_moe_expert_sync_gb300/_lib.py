@@ -141,18 +141,28 @@ def w4_moe_align_capacity(M: int, k: int, E: int, block_m: int) -> int:
     return int(cap)
 
 
-def w4_moe_align(topk_ids, E: int, block_m: int = 16, dev_status=None, stream=None):
-    """Alignment: topk_ids [M, k] int32 -> dict of device tensors."""
+def w4_moe_align(topk_ids, E: int, block_m: int = 16, dev_status=None, out=None,
+                 stream=None):
+    """Alignment: topk_ids [M, k] int32 -> dict of device tensors (sorted_ids,
+    block_expert, expert_offsets, num_padded) plus the shape keys the GEMMs
+    need.  Pass a previous result as ``out`` to reuse its buffers."""
     import torch
     _require_cuda(topk_ids, dev_status)
     M, k = topk_ids.shape
     cap = w4_moe_align_capacity(M, k, E, block_m)
     dev = topk_ids.device
-    r = dict(sorted_ids=torch.empty(cap, dtype=torch.int32, device=dev),
-             block_expert=torch.empty(cap // block_m, dtype=torch.int32, device=dev),
-             expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
-             num_padded=torch.empty(1, dtype=torch.int32, device=dev),
-             M=M, k=k, E=E, block_m=block_m)
+    if out is not None:
+        if (out["sorted_ids"].numel() != cap or out["expert_offsets"].numel() != E + 1
+                or out["block_expert"].numel() != cap // block_m):
+            raise ValueError("w4_moe_align: reused buffers have the wrong sizes")
+        r = out
+        r.update(M=M, k=k, E=E, block_m=block_m)
+    else:
+        r = dict(sorted_ids=torch.empty(cap, dtype=torch.int32, device=dev),
+                 block_expert=torch.empty(cap // block_m, dtype=torch.int32, device=dev),
+                 expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                 num_padded=torch.empty(1, dtype=torch.int32, device=dev),
+                 M=M, k=k, E=E, block_m=block_m)
     _check(load_library().w4_moe_align(_ptr(topk_ids), M, k, E, block_m, _ptr(r["sorted_ids"]),
                                        _ptr(r["block_expert"]), _ptr(r["expert_offsets"]),
                                        _ptr(r["num_padded"]), _ptr(dev_status),
