@@ -136,28 +136,61 @@ int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m,
                  int32_t *num_padded, int32_t *dev_status, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * Contraction order of the grouped GEMMs ("block order")
+ * The GEMMs expand eight packed codes at a time into fp16 pairs
+ * (q0,q4) (q1,q5) (q2,q6) (q3,q7), so inside every block of 8 columns of an
+ * activation row, column p holds element k(p) = (p >> 1) + 4 * (p & 1), i.e.
+ * the order 0,4,1,5,2,6,3,7.  Gathered activations (xg) and h use this
+ * order; it is an implementation layout, not part of the checkpoint format.
+ *
+ * w4_gather_activations -- the gate_up GEMM's input in slot order:
+ *   xg [cap, d] fp16 out: for every slot < num_padded, the row of token
+ *   sorted_ids[slot] / k of x converted to fp16 in block order, or zeros for
+ *   a padding slot; rows >= num_padded are not written.
+ * x [M, d] bf16; sorted_ids / num_padded from w4_moe_align with the same k,
+ * E, block_m.  bf16 -> fp16 rounds to nearest even: exact for magnitudes in
+ * [2^-14, 65504], within 2^-25 below that (fp16 subnormals); larger
+ * magnitudes saturate to +-65504.  Requires d % 8 == 0, x and xg 16-byte
+ * aligned.
+ * ------------------------------------------------------------------------ */
+int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m,
+                          const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
+                          w4_stream_t stream);
+
+/* w4_moe_align_gather -- w4_moe_align and w4_gather_activations in one launch:
+ * every CTA computes the alignment in its own shared memory (so no CTA waits
+ * on another), CTA 0 writes the alignment outputs, and each CTA copies the
+ * rows of a range of tokens to the slots of their assignments.  The first
+ * launch of w4_moe_layer.  Arguments and outputs as in those two calls;
+ * when the assignments do not fit in shared memory it issues them as two
+ * launches. */
+int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d, int k, int E,
+                        int block_m, int32_t *sorted_ids, int32_t *block_expert,
+                        int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
+                        int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * w4_grouped_gemm_gate_up -- grouped W4A16 gate_up GEMM with the gated
  * activation in its epilogue
  * ("dg-w4-kernels" -- Grouped MoE: one launch for all experts, activation
  *  folded into the first GEMM's epilogue; "diffusiongemma-26B-A4B-w4a16" --
  *  Checkpoint format: gate_up groups of 128 along the contraction dim).
  *
- *   x              [M, d] bf16
+ *   xg             [cap, d] fp16 from w4_gather_activations (slot order)
  *   gu_q           [E, 2m, d/2] uint8 (w4_quantize layout), gu_s/gu_z
  *                  [E, 2m, d/group] fp16; rows [0, m) gate, [m, 2m) up
  *   sorted_ids, expert_offsets   from w4_moe_align with the same block_m
- *   h              [cap, m] fp16 out, row = alignment slot:
+ *   h              [cap, m] fp16 out in block order, row = alignment slot:
  *                  h[slot] = gelu_tanh(g) * u for the token of sorted_ids[slot],
  *                  zero rows for padding slots inside an expert's range;
  *                  rows at slots >= num_padded are not written
  * Weights are dequantised in registers to fp16 (s*q + (-z*s), one rounding)
- * and multiplied on the tensor cores (tcgen05, fp16 x fp16 -> fp32); x is
- * converted to fp16 (exact within fp16 range); h is rounded to fp16 with
- * saturation at +-65504.
+ * and multiplied on the tensor cores (tcgen05, fp16 x fp16 -> fp32); h is
+ * rounded to fp16 with saturation at +-65504.
  * Requires d % 128 == 0, m % 64 == 0, group == 128.
  * dev_status may be NULL.
  * ------------------------------------------------------------------------ */
-int w4_grouped_gemm_gate_up(const uint16_t *x, int M, int d, int m, int E, int k, int block_m,
+int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
                             const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
                             int group, const int32_t *sorted_ids,
                             const int32_t *expert_offsets, uint16_t *h,
@@ -169,7 +202,7 @@ int w4_grouped_gemm_gate_up(const uint16_t *x, int M, int d, int m, int E, int k
  * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: down_proj groups of
  *  64 because 128 does not divide 704).
  *
- *   h              [cap, m] fp16 (from w4_grouped_gemm_gate_up)
+ *   h              [cap, m] fp16 in block order (from w4_grouped_gemm_gate_up)
  *   dn_q           [E, d, m/2] uint8, dn_s/dn_z [E, d, m/group] fp16
  *   y              [M*k, d] fp32 out, row a = flat assignment index
  *                  (y[a] = h[slot of a] . deq(Wdn[e])^T); rows of skipped
@@ -199,14 +232,15 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids,
                                uint16_t *out, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
- * w4_moe_layer -- the whole routed-expert layer: align, gate_up + activation,
- * down, fixed-order combine, as four launches on one stream
+ * w4_moe_layer -- the whole routed-expert layer: alignment fused with the
+ * activation gather, gate_up + activation, down, fixed-order combine, as
+ * four launches on one stream
  * ("dg-w4-kernels" -- Grouped MoE: out = fused_moe_w4_v2(hidden, experts,
  *  topk_ids, topk_weights)).
  *
  * workspace: caller-owned device buffer of at least
  * w4_moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds the
- * alignment outputs, h and y.  Its contents on return are the intermediates
+ * alignment outputs, the gathered activations, h and y.  Its contents on return are the intermediates
  * of this call (layout: see the implementation; not part of the ABI).
  * Same shape rules as the individual calls; dev_status may be NULL.
  * ------------------------------------------------------------------------ */

@@ -34,12 +34,14 @@ def _run_steps(lib, cfg, gu, dn, x_bits, ids, block_m):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     x = _cuda(x_bits.view(np.int16)).view(torch.bfloat16)
     al = lib.w4_moe_align(_cuda(ids), cfg.E, block_m, dev_status=status)
-    h = lib.w4_grouped_gemm_gate_up(x, *gu, al, dev_status=status)
+    xg = lib.w4_gather_activations(x, al)
+    h = lib.w4_grouped_gemm_gate_up(xg, *gu, al, dev_status=status)
     y = lib.w4_grouped_gemm_down(h, *dn, al, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    # h is stored in the GEMMs' block order; compare it in natural order
     return (al["sorted_ids"].cpu().numpy(), int(al["num_padded"].item()),
-            h.float().cpu().numpy(), y.cpu().numpy())
+            lib.korder_to_natural(h.float().cpu().numpy()), y.cpu().numpy())
 
 
 def _compare(cfg, sorted_ids, npad, h, y, h_ref, y_ref, rows=None):
@@ -114,3 +116,33 @@ def test_gemm_steps_full_size_sampled(lib, name):
             full_h[t * cfg.k + j] = h_ref[i * cfg.k + j]
             full_y[t * cfg.k + j] = y_ref[i * cfg.k + j]
     _compare(cfg, sorted_ids, npad, h, y, full_h, full_y, rows=rows)
+
+
+@pytest.mark.parametrize("block_m", [16, 64])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "layer256", "canvas2048"])
+def test_gather_and_fused_align_gather(lib, name, block_m):
+    """Gathered activations hold x[token of slot] rounded to fp16 (block
+    order), zero rows for padding; the fused launch writes the same bytes and
+    the same alignment as the two separate calls."""
+    import torch
+    from helpers import bf16_bits_to_f64
+    cfg = wl.CONFIGS[name]
+    x_bits = wl.activations(cfg)
+    x = _cuda(x_bits.view(np.int16)).view(torch.bfloat16)
+    ids, _ = oracle.route(wl.router_logits(cfg), cfg.k)
+    al1 = lib.w4_moe_align(_cuda(ids), cfg.E, block_m)
+    xg1 = lib.w4_gather_activations(x, al1)
+    al2, xg2 = lib.w4_moe_align_gather(_cuda(ids), x, cfg.E, block_m)
+    torch.cuda.synchronize()
+    npad = int(al1["num_padded"].item())
+    for key in ("sorted_ids", "block_expert", "expert_offsets", "num_padded"):
+        assert torch.equal(al1[key], al2[key])
+    assert torch.equal(xg1[:npad].view(torch.int16), xg2[:npad].view(torch.int16))
+    sorted_ids = al1["sorted_ids"].cpu().numpy()[:npad]
+    got = lib.korder_to_natural(xg1[:npad].float().cpu().numpy())
+    # fp16 holds every bf16 value of fp16's normal range exactly; below 2^-14
+    # the value rounds to an fp16 subnormal (round to nearest even)
+    xf = bf16_bits_to_f64(x_bits).astype(np.float16).astype(np.float64)
+    real = sorted_ids < cfg.A
+    assert np.array_equal(got[real], xf[sorted_ids[real] // cfg.k])
+    assert np.all(got[~real] == 0.0)

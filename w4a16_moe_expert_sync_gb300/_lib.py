@@ -62,6 +62,8 @@ def load_library(path: str | None = None):
             "w4_moe_route": ([V, I, I, I, V, V, V], I),
             "w4_moe_align_capacity": ([I, I, I, I], I64),
             "w4_moe_align": ([V, I, I, I, I, V, V, V, V, V, V], I),
+            "w4_gather_activations": ([V, I, I, I, I, I, V, V, V, V], I),
+            "w4_moe_align_gather": ([V, V, I, I, I, I, I, V, V, V, V, V, V, V], I),
             "w4_grouped_gemm_gate_up": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_grouped_gemm_down": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_moe_combine_fixed_order": ([V, V, V, I, I, I, I, V, V], I),
@@ -170,22 +172,74 @@ def w4_moe_align(topk_ids, E: int, block_m: int = 16, dev_status=None, out=None,
     return r
 
 
-def w4_grouped_gemm_gate_up(x, gu_q, gu_s, gu_z, align: dict, group: int = 128, h=None,
-                            dev_status=None, stream=None):
-    """x [M, d] bf16 -> h [cap, m] fp16 = gelu_tanh(gate) * up per alignment slot."""
+def w4_gather_activations(x, align: dict, out=None, stream=None):
+    """x [M, d] bf16 -> xg [cap, d] fp16 in slot order and block order (zero
+    rows for padding slots; rows past num_padded are left untouched)."""
     import torch
-    _require_cuda(x, gu_q, gu_s, gu_z, h, dev_status)
+    _require_cuda(x, out)
     M, d = x.shape
+    cap = align["sorted_ids"].numel()
+    if out is None:
+        out = torch.empty((cap, d), dtype=torch.float16, device=x.device)
+    _check(load_library().w4_gather_activations(
+        _ptr(x), M, d, align["k"], align["E"], align["block_m"], _ptr(align["sorted_ids"]),
+        _ptr(align["num_padded"]), _ptr(out), _stream(stream)), "w4_gather_activations")
+    return out
+
+
+def w4_moe_align_gather(topk_ids, x, E: int, block_m: int = 16, dev_status=None, out=None,
+                        xg=None, stream=None):
+    """Alignment and activation gather in one launch.  Returns (align dict, xg)."""
+    import torch
+    _require_cuda(topk_ids, x, dev_status, xg)
+    M, k = topk_ids.shape
+    d = x.shape[1]
+    cap = w4_moe_align_capacity(M, k, E, block_m)
+    dev = x.device
+    if out is None:
+        out = dict(sorted_ids=torch.empty(cap, dtype=torch.int32, device=dev),
+                   block_expert=torch.empty(cap // block_m, dtype=torch.int32, device=dev),
+                   expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   num_padded=torch.empty(1, dtype=torch.int32, device=dev))
+    out.update(M=M, k=k, E=E, block_m=block_m)
+    if xg is None:
+        xg = torch.empty((cap, d), dtype=torch.float16, device=dev)
+    _check(load_library().w4_moe_align_gather(
+        _ptr(topk_ids), _ptr(x), M, d, k, E, block_m, _ptr(out["sorted_ids"]),
+        _ptr(out["block_expert"]), _ptr(out["expert_offsets"]), _ptr(out["num_padded"]),
+        _ptr(xg), _ptr(dev_status), _stream(stream)), "w4_moe_align_gather")
+    return out, xg
+
+
+def w4_grouped_gemm_gate_up(xg, gu_q, gu_s, gu_z, align: dict, group: int = 128, h=None,
+                            dev_status=None, stream=None):
+    """xg [cap, d] fp16 (from w4_gather_activations) -> h [cap, m] fp16 in block
+    order: gelu_tanh(gate) * up per alignment slot."""
+    import torch
+    _require_cuda(xg, gu_q, gu_s, gu_z, h, dev_status)
+    M, d = align["M"], xg.shape[1]
     E, two_m, _ = gu_q.shape
     m = two_m // 2
     cap = align["sorted_ids"].numel()
     if h is None:
-        h = torch.empty((cap, m), dtype=torch.float16, device=x.device)
+        h = torch.empty((cap, m), dtype=torch.float16, device=xg.device)
     _check(load_library().w4_grouped_gemm_gate_up(
-        _ptr(x), M, d, m, E, align["k"], align["block_m"], _ptr(gu_q), _ptr(gu_s), _ptr(gu_z),
+        _ptr(xg), M, d, m, E, align["k"], align["block_m"], _ptr(gu_q), _ptr(gu_s), _ptr(gu_z),
         group, _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(h),
         _ptr(dev_status), _stream(stream)), "w4_grouped_gemm_gate_up")
     return h
+
+
+def korder_to_natural(a):
+    """Undo the GEMMs' block order along the last axis (for inspection and
+    tests): column p of every block of 8 holds element (p >> 1) + 4 * (p & 1)."""
+    import numpy as np
+    n = a.shape[-1]
+    perm = np.array([(p >> 1) + 4 * (p & 1) for p in range(8)])
+    src = (np.arange(n) // 8) * 8
+    inv = np.empty(8, dtype=np.int64)
+    inv[perm] = np.arange(8)
+    return a[..., src + inv[np.arange(n) % 8]]
 
 
 def w4_grouped_gemm_down(h, dn_q, dn_s, dn_z, align: dict, group: int = 64, y=None,

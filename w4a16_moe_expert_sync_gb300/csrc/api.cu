@@ -172,12 +172,73 @@ int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m, int3
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "align launch");
 }
 
-int w4_grouped_gemm_gate_up(const uint16_t *x, int M, int d, int m, int E, int k, int block_m,
+int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m,
+                          const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
+                          w4_stream_t stream)
+{
+    if (!xg || !sorted_ids || !num_padded || (M > 0 && !x))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || d <= 0 || k <= 0 || E <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (d % 8)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "d must be a multiple of 8");
+    if (!aligned16(x) || !aligned16(xg) || !aligned4(sorted_ids) || !aligned4(num_padded))
+        return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
+    if (int rc = check_device())
+        return rc;
+    const int64_t cap = align_capacity(M, k, E, block_m);
+    cudaError_t err =
+        w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "gather launch");
+}
+
+int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d, int k, int E,
+                        int block_m, int32_t *sorted_ids, int32_t *block_expert,
+                        int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
+                        int32_t *dev_status, w4_stream_t stream)
+{
+    if (!sorted_ids || !block_expert || !expert_offsets || !num_padded || !xg ||
+        (M > 0 && (!topk_ids || !x)))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || d <= 0 || k <= 0 || E <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (E > 1024 || d % 8)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need E <= 1024 and d %% 8 == 0");
+    if (!aligned16(x) || !aligned16(xg))
+        return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
+    const int64_t cap = align_capacity(M, k, E, block_m);
+    if (cap > (1ll << 30))
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "too many assignments");
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err;
+    if (w4::align_gather_smem_bytes(M, k, E) <= 200 * 1024) {
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        err = w4::launch_align_gather(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
+                                      expert_offsets, num_padded, dev_status, x, d, xg, sms,
+                                      as_stream(stream));
+    } else {   // too many assignments to keep their slots in shared memory
+        err = w4::launch_align(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
+                               expert_offsets, num_padded, dev_status, as_stream(stream));
+        if (err == cudaSuccess)
+            err = w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg,
+                                    as_stream(stream));
+    }
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "align+gather launch");
+}
+
+int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
                             const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
                             int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
                             uint16_t *h, int32_t *dev_status, w4_stream_t stream)
 {
-    if (int rc = check_gemm_common(M, d, m, E, k, block_m, x, gu_q, gu_s, gu_z, sorted_ids,
+    if (int rc = check_gemm_common(M, d, m, E, k, block_m, xg, gu_q, gu_s, gu_z, sorted_ids,
                                    expert_offsets, h))
         return rc;
     if (group != 128)
@@ -186,7 +247,7 @@ int w4_grouped_gemm_gate_up(const uint16_t *x, int M, int d, int m, int E, int k
         return rc;
     w4::GroupedGemmProblem p{};
     p.gate_up = true;
-    p.act = x;
+    p.act = xg;
     p.wq = gu_q;
     p.ws = gu_s;
     p.wz = gu_z;
@@ -270,10 +331,10 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const fl
 
 // Workspace layout of w4_moe_layer (each piece 256-byte aligned):
 //   sorted_ids [cap] i32 | block_expert [cap/bm] i32 | expert_offsets [E+1] i32 |
-//   num_padded [1] i32 | h [cap, m] fp16 | y [M*k, d] fp32
+//   num_padded [1] i32 | xg [cap, d] fp16 | h [cap, m] fp16 | y [M*k, d] fp32
 namespace {
 struct LayerWs {
-    size_t sorted, block, offs, npad, h, y, total;
+    size_t sorted, block, offs, npad, xg, h, y, total;
 };
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
@@ -284,7 +345,8 @@ LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
     w.block = up256(w.sorted + 4 * cap);
     w.offs = up256(w.block + 4 * (cap / bm));
     w.npad = up256(w.offs + 4 * (static_cast<size_t>(E) + 1));
-    w.h = up256(w.npad + 4);
+    w.xg = up256(w.npad + 4);
+    w.h = up256(w.xg + 2 * cap * static_cast<size_t>(d));
     w.y = up256(w.h + 2 * cap * static_cast<size_t>(m));
     w.total = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
     return w;
@@ -318,16 +380,17 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
     int32_t *block = reinterpret_cast<int32_t *>(ws + L.block);
     int32_t *offs = reinterpret_cast<int32_t *>(ws + L.offs);
     int32_t *npad = reinterpret_cast<int32_t *>(ws + L.npad);
+    uint16_t *xg = reinterpret_cast<uint16_t *>(ws + L.xg);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
     float *y = reinterpret_cast<float *>(ws + L.y);
-    int rc = w4_moe_align(topk_ids, M, k, E, block_m, sorted, block, offs, npad, dev_status,
-                          stream);
-    if (rc)
-        return rc;
+    // alignment and the activation gather share one launch
+    if (int rc0 = w4_moe_align_gather(topk_ids, x, M, d, k, E, block_m, sorted, block, offs, npad,
+                                      xg, dev_status, stream))
+        return rc0;
     if (M == 0)
         return W4_OK;
-    rc = w4_grouped_gemm_gate_up(x, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group, sorted,
-                                 offs, h, dev_status, stream);
+    int rc = w4_grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
+                                     sorted, offs, h, dev_status, stream);
     if (rc)
         return rc;
     rc = w4_grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs,

@@ -21,10 +21,23 @@ cudaError_t launch_quantize(const float *W, int64_t rows, int K, int group, uint
 cudaError_t launch_route(const float *logits, int M, int E, int k, int32_t *ids, float *w,
                          cudaStream_t stream);
 
-size_t align_smem_bytes(int E);
+__host__ __device__ size_t align_smem_bytes(int E);
 cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
                          int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                          int32_t *num_padded, int32_t *dev_status, cudaStream_t stream);
+
+// xg[slot] = x[sorted_ids[slot] / k] in fp16 block order (zero for padding)
+// for slots below *num_padded.
+cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
+                          const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
+                          cudaStream_t stream);
+
+// Alignment and gather in one launch (every CTA aligns in shared memory).
+size_t align_gather_smem_bytes(int M, int k, int E);
+cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
+                                int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
+                                int32_t *num_padded, int32_t *dev_status, const uint16_t *x,
+                                int d, uint16_t *xg, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
                            int d, int E, uint16_t *out, cudaStream_t stream);
@@ -33,7 +46,7 @@ cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, i
 // gated activation; gate_up=false: h fp16 -> y fp32.
 struct GroupedGemmProblem {
     bool gate_up;
-    const uint16_t *act;        // x [M, K] bf16 or h [cap, K] fp16
+    const uint16_t *act;        // xg or h, [cap, K] fp16 in block order
     const uint8_t *wq;          // [E, R, K/2]
     const uint16_t *ws, *wz;    // [E, R, K/group]
     const int32_t *sorted_ids;  // [cap]

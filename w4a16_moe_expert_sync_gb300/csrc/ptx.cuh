@@ -59,22 +59,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread is suspended until the phase
+// completes or about `hint_ns` elapse, so a waiting warp does not spin on the
+// issue slots the working warps of its sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // A pipeline wait with a time limit.  Returns false (and raises the CTA's
 // abort flag and the device status bit) when the phase did not complete
 // within `limit_ns`, or when another role of the CTA has already aborted.
+// Each try suspends the thread for up to 20 us; between tries the abort
+// flag and the clock are checked.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           int32_t *dev_status, int32_t timeout_bit,
                                           uint64_t limit_ns = 1000000000ull)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    const uint64_t t0 = global_timer_ns();
+    uint64_t t0 = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
             return true;
         if (*abort_flag)
             return false;
-        if (global_timer_ns() - t0 > limit_ns) {
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > limit_ns) {
             *abort_flag = 1;
             if (dev_status)
                 atomicOr(dev_status, timeout_bit);
@@ -105,6 +127,31 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// 2-D tiled TMA load without a cache hint.
+__device__ __forceinline__ void tma_load_2d_nohint(void *dst, const CUtensorMap *map, int x, int y,
+                                                   uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Four rows r0..r3 (any order, any rows of the tensor) of one box column
+// starting at x, gathered by a 2-D tensor map whose box is one row high, into
+// four consecutive box rows at dst.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int x, int r0,
+                                            int r1, int r2, int r3, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -235,6 +282,26 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7])
         : "r"(taddr)
+        : "memory");
+}
+
+// Four loads of 8 columns each (at four TMEM addresses of this warp's lane
+// quarter) followed by one wait, so the four round trips overlap.
+__device__ __forceinline__ void tmem_ld_4x_32x32b_x8(uint32_t t0, uint32_t t1, uint32_t t2,
+                                                     uint32_t t3, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%33];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%34];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%35];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
         : "memory");
 }
 

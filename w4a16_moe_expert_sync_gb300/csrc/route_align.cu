@@ -18,8 +18,15 @@
 // each assignment at its warp's running position plus its rank among earlier
 // lanes with the same expert, which keeps the order stable.  No global
 // atomics, no host round trip.
+//
+// Activation gather: the grouped gate_up GEMM reads its activations in slot
+// order, xg[slot] = x[token of slot] converted to fp16 in the GEMMs'
+// contraction order (korder.cuh), zero rows for padding slots.  The layer
+// fuses alignment and gather into one launch.
+#include <algorithm>
 #include <cfloat>
 
+#include "korder.cuh"
 #include "launch.h"
 
 namespace w4 {
@@ -118,17 +125,25 @@ cudaError_t launch_route(const float *logits, int M, int E, int k, int32_t *ids,
 // --------------------------------------------------------------- alignment
 constexpr int kAlignWarps = 32;
 
-size_t align_smem_bytes(int E)
+__host__ __device__ size_t align_smem_bytes(int E)
 {
     // per-warp histograms, expert totals, offsets, warp partial sums
     return sizeof(int) * (static_cast<size_t>(kAlignWarps) * E + E + (E + 1) + kAlignWarps);
 }
 
-__global__ void __launch_bounds__(kAlignWarps * 32, 1)
-    moe_align_kernel(const int32_t *__restrict__ ids, int A, int E, int bm, int cap,
-                     int32_t *__restrict__ sorted_ids, int32_t *__restrict__ block_expert,
-                     int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
-                     int32_t *__restrict__ dev_status)
+// The alignment computed by one CTA of 1024 threads.  With write_global the
+// CTA writes sorted_ids / block_expert / expert_offsets / num_padded and
+// reports invalid ids; with pos_sm it records the slot of every flat
+// assignment (or -1) in shared memory.  Returns through shared memory: the
+// padded offsets (offs_out[E+1]) and per-expert counts (total_out[E]).
+__device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int A, int E, int bm,
+                                            int cap, bool write_global,
+                                            int32_t *__restrict__ sorted_ids,
+                                            int32_t *__restrict__ block_expert,
+                                            int32_t *__restrict__ offsets,
+                                            int32_t *__restrict__ num_padded,
+                                            int32_t *__restrict__ dev_status, int *pos_sm,
+                                            int **offs_out, int **total_out)
 {
     extern __shared__ int sm[];
     int *hist = sm;                          // [32][E]
@@ -145,21 +160,22 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
 
     const int chunk = (A + kAlignWarps - 1) / kAlignWarps;
     const int a0 = min(A, warp * chunk), a1 = min(A, a0 + chunk);
-
     // pass 1: per-warp histogram
     bool bad = false;
-    for (int base = a0; base < a1; base += 32) {
-        const int a = base + lane;
-        const int e = a < a1 ? __ldg(ids + a) : -1;
-        const bool valid = a < a1 && e >= 0 && e < E;
-        bad |= (a < a1) && !valid;
-        const int key = valid ? e : E + lane;      // invalid lanes match nobody
-        const unsigned grp = __match_any_sync(full, key);
-        if (valid && lane == __ffs(grp) - 1)
-            hist[warp * E + e] += __popc(grp);
-        __syncwarp();
+    {
+        for (int base = a0; base < a1; base += 32) {
+            const int a = base + lane;
+            const int e = a < a1 ? __ldg(ids + a) : -1;
+            const bool valid = a < a1 && e >= 0 && e < E;
+            bad |= (a < a1) && !valid;
+            const int key = valid ? e : E + lane;      // invalid lanes match nobody
+            const unsigned grp = __match_any_sync(full, key);
+            if (valid && lane == __ffs(grp) - 1)
+                hist[warp * E + e] += __popc(grp);
+            __syncwarp();
+        }
     }
-    if (__any_sync(full, bad) && lane == 0 && dev_status)
+    if (write_global && __any_sync(full, bad) && lane == 0 && dev_status)
         atomicOr(dev_status, kDevBadExpertId);
     __syncthreads();
 
@@ -182,14 +198,14 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
         wsum[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        int s = wsum[lane];
+        int s2 = wsum[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(full, s, o);
+            const int v = __shfl_up_sync(full, s2, o);
             if (lane >= o)
-                s += v;
+                s2 += v;
         }
-        wsum[lane] = s - wsum[lane];          // exclusive prefix of warp sums
+        wsum[lane] = s2 - wsum[lane];          // exclusive prefix of warp sums
     }
     __syncthreads();
     if (tid < E) {
@@ -207,39 +223,136 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
     __syncthreads();
 
     // pass 3: stable placement
-    for (int base = a0; base < a1; base += 32) {
-        const int a = base + lane;
-        const int e = a < a1 ? __ldg(ids + a) : -1;
-        const bool valid = a < a1 && e >= 0 && e < E;
-        const int key = valid ? e : E + lane;
-        const unsigned grp = __match_any_sync(full, key);
-        int pos = 0;
-        if (valid)
-            pos = hist[warp * E + e] + __popc(grp & lt_mask);
-        __syncwarp();
-        if (valid && lane == __ffs(grp) - 1)
-            hist[warp * E + e] += __popc(grp);
-        __syncwarp();
-        if (valid)
-            sorted_ids[pos] = a;
+    {
+        for (int base = a0; base < a1; base += 32) {
+            const int a = base + lane;
+            const int e = a < a1 ? __ldg(ids + a) : -1;
+            const bool valid = a < a1 && e >= 0 && e < E;
+            const int key = valid ? e : E + lane;
+            const unsigned grp = __match_any_sync(full, key);
+            int pos = 0;
+            if (valid)
+                pos = hist[warp * E + e] + __popc(grp & lt_mask);
+            __syncwarp();
+            if (valid && lane == __ffs(grp) - 1)
+                hist[warp * E + e] += __popc(grp);
+            __syncwarp();
+            if (a < a1) {
+                if (write_global && valid)
+                    sorted_ids[pos] = a;
+                if (pos_sm)
+                    pos_sm[a] = valid ? pos : -1;
+            }
+        }
     }
 
     // pass 4: padding, block owners, offsets
-    if (tid < E) {
-        for (int sl = offs[tid] + total[tid]; sl < offs[tid + 1]; sl++)
+    if (write_global) {
+        if (tid < E) {
+            for (int sl = offs[tid] + total[tid]; sl < offs[tid + 1]; sl++)
+                sorted_ids[sl] = A;
+            for (int b = offs[tid] / bm; b < offs[tid + 1] / bm; b++)
+                block_expert[b] = tid;
+        }
+        const int npad = offs[E];
+        for (int sl = npad + tid; sl < cap; sl += blockDim.x)
             sorted_ids[sl] = A;
-        for (int b = offs[tid] / bm; b < offs[tid + 1] / bm; b++)
-            block_expert[b] = tid;
+        for (int b = npad / bm + tid; b < cap / bm; b += blockDim.x)
+            block_expert[b] = -1;
+        for (int i = tid; i <= E; i += blockDim.x)
+            offsets[i] = offs[i];
+        if (tid == 0)
+            num_padded[0] = npad;
     }
-    const int npad = offs[E];
-    for (int sl = npad + tid; sl < cap; sl += blockDim.x)
-        sorted_ids[sl] = A;
-    for (int b = npad / bm + tid; b < cap / bm; b += blockDim.x)
-        block_expert[b] = -1;
-    for (int i = tid; i <= E; i += blockDim.x)
-        offsets[i] = offs[i];
-    if (tid == 0)
-        num_padded[0] = npad;
+    *offs_out = offs;
+    *total_out = total;
+}
+
+__global__ void __launch_bounds__(kAlignWarps * 32, 1)
+    moe_align_kernel(const int32_t *__restrict__ ids, int A, int E, int bm, int cap,
+                     int32_t *__restrict__ sorted_ids, int32_t *__restrict__ block_expert,
+                     int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
+                     int32_t *__restrict__ dev_status)
+{
+    int *offs, *total;
+    align_block(ids, A, E, bm, cap, true, sorted_ids, block_expert, offsets, num_padded,
+                dev_status, nullptr, &offs, &total);
+}
+
+// One 16-byte chunk (8 activations) of token row t, converted to fp16 in the
+// GEMMs' block order.
+__device__ __forceinline__ uint4 load_korder(const uint16_t *__restrict__ x, int64_t t, int d,
+                                             int c8)
+{
+    return bf16x8_to_f16_korder(__ldg(reinterpret_cast<const uint4 *>(x + t * d + 8 * c8)));
+}
+
+// Standalone gather: xg[slot] = x[token of slot] (fp16, block order), zero
+// for padding slots, for every slot below num_padded.
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, int d, int k,
+                                                     int A, const int32_t *__restrict__ sorted_ids,
+                                                     const int32_t *__restrict__ num_padded,
+                                                     uint16_t *__restrict__ xg)
+{
+    const int c8n = d / 8;
+    const int64_t total = static_cast<int64_t>(__ldg(num_padded)) * c8n;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t slot = i / c8n;
+        const int c8 = static_cast<int>(i - slot * c8n);
+        const int a = __ldg(sorted_ids + slot);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (static_cast<unsigned>(a) < static_cast<unsigned>(A))
+            o = load_korder(x, a / k, d, c8);
+        *reinterpret_cast<uint4 *>(xg + slot * d + 8 * c8) = o;
+    }
+}
+
+// Fused alignment + gather.  Every CTA computes the (cheap) alignment in its
+// own shared memory, so no CTA waits for another; CTA 0 also writes the
+// alignment outputs.  CTA b then copies the rows of tokens
+// [b*tpc, (b+1)*tpc) to the slots of their k assignments (each x row is read
+// once) and zeroes the padding slots of experts e = b, b + G, ...
+__global__ void __launch_bounds__(kAlignWarps * 32, 1)
+    moe_align_gather_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int bm, int cap,
+                            int32_t *__restrict__ sorted_ids, int32_t *__restrict__ block_expert,
+                            int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
+                            int32_t *__restrict__ dev_status, const uint16_t *__restrict__ x,
+                            int d, uint16_t *__restrict__ xg, int tpc)
+{
+    extern __shared__ int sm[];
+    const int A = M * k;
+    int *pos = sm + align_smem_bytes(E) / sizeof(int);   // [A]
+    int *offs, *total;
+    align_block(ids, A, E, bm, cap, blockIdx.x == 0, sorted_ids, block_expert, offsets, num_padded,
+                dev_status, pos, &offs, &total);
+    __syncthreads();
+    const int c8n = d / 8;
+    const int t0 = blockIdx.x * tpc, t1 = min(M, t0 + tpc);
+    const int64_t n = static_cast<int64_t>(max(0, t1 - t0)) * c8n;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int t = t0 + static_cast<int>(i / c8n);
+        const int c8 = static_cast<int>(i % c8n);
+        const uint4 o = load_korder(x, t, d, c8);
+        for (int j = 0; j < k; j++) {
+            const int slot = pos[t * k + j];
+            if (slot >= 0)
+                *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(slot) * d + 8 * c8) = o;
+        }
+    }
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int s0 = offs[e] + total[e], s1 = offs[e + 1];
+        const int64_t m = static_cast<int64_t>(s1 - s0) * c8n;
+        for (int64_t i = threadIdx.x; i < m; i += blockDim.x) {
+            const int64_t slot = s0 + i / c8n;
+            *reinterpret_cast<uint4 *>(xg + slot * d + 8 * (i % c8n)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+static cudaError_t set_align_smem(const void *fn)
+{
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
 cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
@@ -247,17 +360,46 @@ cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, i
                          int32_t *num_padded, int32_t *dev_status, cudaStream_t stream)
 {
     const size_t smem = align_smem_bytes(E);
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t err = cudaFuncSetAttribute(
-            moe_align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (err != cudaSuccess)
-            return err;
-        attr_set = true;
-    }
+    cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_kernel));
+    if (err != cudaSuccess)
+        return err;
     moe_align_kernel<<<1, kAlignWarps * 32, smem, stream>>>(
         ids, M * k, E, block_m, static_cast<int>(cap), sorted_ids, block_expert, offsets,
         num_padded, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
+                          const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
+                          cudaStream_t stream)
+{
+    const int64_t total = cap * (d / 8);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 4096));
+    gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, d, k, M * k, sorted_ids,
+                                                                      num_padded, xg);
+    return cudaGetLastError();
+}
+
+size_t align_gather_smem_bytes(int M, int k, int E)
+{
+    return align_smem_bytes(E) + sizeof(int) * static_cast<size_t>(M) * k;
+}
+
+cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
+                                int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
+                                int32_t *num_padded, int32_t *dev_status, const uint16_t *x,
+                                int d, uint16_t *xg, int num_sms, cudaStream_t stream)
+{
+    const size_t smem = align_gather_smem_bytes(M, k, E);
+    cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel));
+    if (err != cudaSuccess)
+        return err;
+    // about two tokens per CTA at the pages' canvas, at most one CTA per SM
+    const int grid = std::max(1, std::min(num_sms, (M + 1) / 2));
+    const int tpc = (M + grid - 1) / grid;
+    moe_align_gather_kernel<<<grid, kAlignWarps * 32, smem, stream>>>(
+        ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids, block_expert, offsets,
+        num_padded, dev_status, x, d, xg, tpc);
     return cudaGetLastError();
 }
 
