@@ -252,6 +252,41 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
                  void *workspace, size_t workspace_bytes, uint16_t *out,
                  int32_t *dev_status, w4_stream_t stream);
 
+/* --------------------------------------------------------------------------
+ * w4_moe_layer_static_scratch -- w4_moe_layer without a workspace argument.
+ * The paper has no counterpart: this is a library convenience for callers
+ * that cannot allocate device memory when they call the layer, e.g. a plain
+ * C host with no device allocator of its own, or a server that reserves its
+ * memory at start-up and must not call cudaMalloc/cudaFree (which
+ * synchronise the device) or re-enter its allocator afterwards.
+ *
+ * The intermediates live in one library-owned device array of
+ * W4_STATIC_SCRATCH_BYTES (64 MiB) per device; that holds the M = 256,
+ * d = 2816, m = 704, E = 128, k = 8 layer at block_m = 16 (about 51 MB).
+ * Shapes whose w4_moe_layer_workspace_size(...) exceeds it are rejected with
+ * W4_ERR_WORKSPACE before anything is launched.  Nothing is allocated: no
+ * cudaMalloc, no cudaFree, no allocating library routine.  Nothing in the
+ * array needs to start at zero.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, which may load the module onto that device); make
+ * that first call before any stream capture.
+ *
+ * Every call on a device shares the one array: calls whose GPU work overlaps
+ * (different streams, or different host threads with different streams)
+ * race and corrupt each other's results.  Issue them on one stream.
+ * Arguments, outputs, shape rules and errors otherwise as w4_moe_layer.
+ * ------------------------------------------------------------------------ */
+#define W4_STATIC_SCRATCH_BYTES (64u << 20)
+int w4_moe_layer_static_scratch(const uint16_t *x, const int32_t *topk_ids,
+                                const float *topk_weights,
+                                int M, int d, int m, int E, int k, int block_m,
+                                const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                                int gu_group,
+                                const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z,
+                                int dn_group, uint16_t *out, int32_t *dev_status,
+                                w4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,8 @@ def load_library(path: str | None = None):
             "w4_moe_layer_workspace_size": ([I, I, I, I, I, I], SZ),
             "w4_moe_layer": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V, SZ, V, V,
                               V], I),
+            "w4_moe_layer_static_scratch": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I,
+                                             V, V, V], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -300,4 +302,27 @@ def w4_moe_layer(x, topk_ids, topk_weights, gu, dn, block_m: int = 16, gu_group:
         _ptr(gu_s), _ptr(gu_z), gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), dn_group,
         _ptr(workspace), workspace.numel(), _ptr(out), _ptr(dev_status), _stream(stream)),
         "w4_moe_layer")
+    return out
+
+
+def w4_moe_layer_static_scratch(x, topk_ids, topk_weights, gu, dn, out, block_m: int = 16,
+                                gu_group: int = 128, dn_group: int = 64, dev_status=None,
+                                stream=None):
+    """w4_moe_layer with the intermediates in the library's own static device
+    array instead of a workspace: for callers that cannot allocate device
+    memory when they run the layer.  Nothing is allocated here either, so the
+    caller passes `out` ([M, d] bf16).  Calls that overlap on the GPU share
+    the array and race: keep them on one stream."""
+    gu_q, gu_s, gu_z = gu
+    dn_q, dn_s, dn_z = dn
+    _require_cuda(x, topk_ids, topk_weights, gu_q, gu_s, gu_z, dn_q, dn_s, dn_z, out,
+                  dev_status)
+    M, d = x.shape
+    E, two_m, _ = gu_q.shape
+    m = two_m // 2
+    k = topk_ids.shape[1]
+    _check(load_library().w4_moe_layer_static_scratch(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, d, m, E, k, block_m, _ptr(gu_q),
+        _ptr(gu_s), _ptr(gu_z), gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), dn_group,
+        _ptr(out), _ptr(dev_status), _stream(stream)), "w4_moe_layer_static_scratch")
     return out

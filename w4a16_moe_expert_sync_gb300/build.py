@@ -11,7 +11,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libw4moe.so")
-SOURCES = ["api.cu", "quantize.cu", "route_align.cu", "combine.cu", "grouped_gemm.cu"]
+SOURCES = ["api.cu", "quantize.cu", "route_align.cu", "combine.cu", "grouped_gemm.cu",
+           "static_scratch.cu"]
 HEADERS = ["launch.h", "ptx.cuh", "korder.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -86,6 +86,11 @@ int check_gemm_common(int M, int d, int m, int E, int k, int block_m, const void
 
 }  // namespace
 
+int w4::set_error_detail(int status, const char *detail)
+{
+    return fail(status, "%s", detail);
+}
+
 extern "C" {
 
 const char *w4_status_string(int status)

@@ -63,4 +63,8 @@ struct GroupedGemmProblem {
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem &p, cudaStream_t stream,
                                 const char **why);
 
+// Records `detail` as the text w4_last_error_detail() returns on this thread
+// and passes `status` through.
+int set_error_detail(int status, const char *detail);
+
 }  // namespace w4
