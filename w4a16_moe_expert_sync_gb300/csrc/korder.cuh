@@ -1,9 +1,9 @@
 // korder.cuh -- the contraction order used inside every block of 8 elements
-// by the grouped GEMMs, and the conversions that produce activations in it.
+// by the grouped GEMMs, and the helpers that produce activations in it.
 //
 // Eight uint4 codes sit in one 32-bit word (code i in bits 4i..4i+3).  Masking
-// the word (and the word >> 8) with 0x000F000F and 0x00F000F0 gives the fp16
-// pairs (q0,q4) (q1,q5) (q2,q6) (q3,q7) with one LOP3 each, so position p of
+// the word >> 4i with 0x000F000F gives the 16-bit pairs (q0,q4) (q1,q5)
+// (q2,q6) (q3,q7) with one shift and one LOP3 each, so position p of
 // a block holds original index k(p) = (p >> 1) + 4 * (p & 1), and original
 // index k sits at position pos(k) = 2 * (k & 3) + (k >> 2).  Permuting both
 // operands of a dot product the same way leaves it unchanged.
@@ -28,7 +28,8 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi)
 
 // 8 bf16 values x0..x7 (16 bytes) -> 8 fp16 values in block order
 // x0 x4 x1 x5 x2 x6 x3 x7.  bf16 -> fp16 is exact for magnitudes in
-// [2^-14, 65504] and rounds to the nearest fp16 subnormal below that.
+// [2^-14, 65504] and rounds to the nearest fp16 subnormal below that;
+// larger magnitudes saturate to +-65504.
 __device__ __forceinline__ uint4 bf16x8_to_f16_korder(uint4 v)
 {
     const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xffff0000u);
@@ -41,6 +42,17 @@ __device__ __forceinline__ uint4 bf16x8_to_f16_korder(uint4 v)
     o.z = f16x2_sat(x2, x6);
     o.w = f16x2_sat(x3, x7);
     return o;
+}
+
+// fp32 sum of 8 fp16 values (a 16-byte block in any order) in a fixed
+// pairwise order.
+__device__ __forceinline__ float f16x8_sum(uint4 v)
+{
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+    const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+    return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
 }
 
 }  // namespace w4

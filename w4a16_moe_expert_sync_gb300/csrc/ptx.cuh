@@ -156,6 +156,29 @@ __device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, i
 }
 
 // Contiguous bulk copy global -> shared (both 16-byte aligned, size % 16 == 0).
+// 1-D bulk copy global -> shared without a cache hint; dst, src 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_nohint(void *dst, const void *src, uint32_t bytes,
+                                                 uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tile copy global -> shared (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar, uint64_t policy)
 {
@@ -238,6 +261,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N)
            | ((M >> 4) << 24);      // M / 16
 }
 
+// Instruction descriptor for kind::f16 with both operands bf16 (bf16 = true)
+// or both fp16, fp32 accumulator, K-major A and B.
+__host__ __device__ constexpr uint32_t idesc_16bit_f32(uint32_t M, uint32_t N, bool bf16)
+{
+    return idesc_f16_f32(M, N) | (bf16 ? ((1u << 7) | (1u << 10)) : 0u);
+}
+
 // Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B,
 // 8-row atoms of 1024 B (stride between atoms = SBO = 1024 B).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr)
@@ -281,6 +311,20 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[
         "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Load 16 consecutive 32-bit columns of this thread's lane and wait for them.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 }
