@@ -341,8 +341,8 @@ def run_gpu(args, cfg, world, rank, local):
 
     bm = args.block_m
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    al, xg, xs = w4.w4_moe_align_gather(ids, x, cfg.E, bm, dev_status=status)
-    h, hs = w4.w4_grouped_gemm_gate_up(xg, xs, *gu, al, dev_status=status)
+    al, xg = w4.w4_moe_align_gather(ids, x, cfg.E, bm, dev_status=status)
+    h = w4.w4_grouped_gemm_gate_up(xg, *gu, al, dev_status=status)
     y = torch.empty((cfg.M * cfg.k, cfg.d), dtype=torch.float32, device=dev)
     out = torch.empty((cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -352,13 +352,13 @@ def run_gpu(args, cfg, world, rank, local):
     def step(ev=None):
         if ev:
             ev[0].record()
-        w4.w4_moe_align_gather(ids, x, cfg.E, bm, dev_status=status, out=al, xg=xg, xs=xs)
+        w4.w4_moe_align_gather(ids, x, cfg.E, bm, dev_status=status, out=al, xg=xg)
         if ev:
             ev[1].record()
-        w4.w4_grouped_gemm_gate_up(xg, xs, *gu, al, h=h, hs=hs, dev_status=status)
+        w4.w4_grouped_gemm_gate_up(xg, *gu, al, h=h, dev_status=status)
         if ev:
             ev[2].record()
-        w4.w4_grouped_gemm_down(h, hs, *dn, al, y=y, dev_status=status)
+        w4.w4_grouped_gemm_down(h, *dn, al, y=y, dev_status=status)
         if ev:
             ev[3].record()
         w4.w4_moe_combine_fixed_order(y, ids, w, cfg.E, out=out)
@@ -468,9 +468,9 @@ def run_gpu(args, cfg, world, rank, local):
         "gpu_launches": 4 * args.steps,
         "clocks": sampler.summary() if sampler else None,
         "timed_region_wall_s": t_wall,
-        "precision": "weights enter tcgen05 MMAs as fp16(s*q) (one rounding) against fp16 "
-                     "activations and h, fp32 accumulation; zero points applied in fp32 through "
-                     "per-group activation sums; bf16 in and out",
+        "precision": "uint4 weights dequantised to fp16 in registers (q*s + fp16(-z*s), one "
+                     "fused rounding), fp16 x fp16 tcgen05 MMA with fp32 accumulation, bf16 "
+                     "activations in and out",
     }
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(cfg, args.cpu_tokens).items()

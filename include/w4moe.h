@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 2
+#define W4MOE_ABI_VERSION 3
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -137,40 +137,25 @@ int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m,
 
 /* --------------------------------------------------------------------------
  * Contraction order of the grouped GEMMs ("block order")
- * The GEMMs expand eight packed codes at a time into 16-bit pairs
+ * The GEMMs expand eight packed codes at a time into fp16 pairs
  * (q0,q4) (q1,q5) (q2,q6) (q3,q7), so inside every block of 8 columns of an
  * activation row, column p holds element k(p) = (p >> 1) + 4 * (p & 1), i.e.
  * the order 0,4,1,5,2,6,3,7.  Gathered activations (xg) and h use this
  * order; it is an implementation layout, not part of the checkpoint format.
  *
- * Group sums.  The GEMMs multiply fp16(s * q) on the tensor cores and apply
- * the zero points afterwards, once per output:
- *   sum_k s_g (q_k - z_g) a_k = sum_k fp16(s_g q_k) a_k - sum_g s_g z_g X_g,
- *   X_g = sum_{k in g} a_k,
- * so every activation row travels with the fp32 sums of its groups.  A
- * group-sum table is [cap, pitch] fp32 with pitch = w4_group_sum_pitch(K,
- * group) (K/group rounded up to a multiple of 4; entries past K/group are
- * unused).  Returns -1 if group does not divide K.
- * ------------------------------------------------------------------------ */
-int w4_group_sum_pitch(int K, int group);
-
-/* w4_gather_activations -- the gate_up GEMM's input in slot order:
+ * w4_gather_activations -- the gate_up GEMM's input in slot order:
  *   xg [cap, d] fp16 out: for every slot < num_padded, the row of token
- *      sorted_ids[slot] / k of x converted to fp16 in block order, or zeros
- *      for a padding slot;
- *   xs [cap, w4_group_sum_pitch(d, group)] fp32 out: xs[slot, g] = the sum
- *      of that fp16 row's elements in group g (fp32, fixed order), 0 for
- *      padding;
- *   rows >= num_padded are not written.
+ *   sorted_ids[slot] / k of x converted to fp16 in block order, or zeros for
+ *   a padding slot; rows >= num_padded are not written.
  * x [M, d] bf16; sorted_ids / num_padded from w4_moe_align with the same k,
  * E, block_m.  bf16 -> fp16 rounds to nearest even: exact for magnitudes in
  * [2^-14, 65504], within 2^-25 below that (fp16 subnormals); larger
- * magnitudes saturate to +-65504.  group is 64 or 128 and divides d
- * (gate_up uses 128).  x, xg and xs 16-byte aligned.
+ * magnitudes saturate to +-65504.  Requires d % 8 == 0, x and xg 16-byte
+ * aligned.
  * ------------------------------------------------------------------------ */
-int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m, int group,
+int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          float *xs, w4_stream_t stream);
+                          w4_stream_t stream);
 
 /* w4_moe_align_gather -- w4_moe_align and w4_gather_activations in one launch:
  * every CTA computes the alignment in its own shared memory (so no CTA waits
@@ -180,8 +165,8 @@ int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int blo
  * when the assignments do not fit in shared memory it issues them as two
  * launches. */
 int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d, int k, int E,
-                        int block_m, int group, int32_t *sorted_ids, int32_t *block_expert,
-                        int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg, float *xs,
+                        int block_m, int32_t *sorted_ids, int32_t *block_expert,
+                        int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
                         int32_t *dev_status, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
@@ -191,7 +176,7 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
  *  folded into the first GEMM's epilogue; "diffusiongemma-26B-A4B-w4a16" --
  *  Checkpoint format: gate_up groups of 128 along the contraction dim).
  *
- *   xg, xs         from w4_gather_activations (slot order, group 128)
+ *   xg             [cap, d] fp16 from w4_gather_activations (slot order)
  *   gu_q           [E, 2m, d/2] uint8 (w4_quantize layout), gu_s/gu_z
  *                  [E, 2m, d/group] fp16; rows [0, m) gate, [m, 2m) up
  *   sorted_ids, expert_offsets   from w4_moe_align with the same block_m
@@ -199,20 +184,16 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
  *                  h[slot] = gelu_tanh(g) * u for the token of sorted_ids[slot],
  *                  zero rows for padding slots inside an expert's range;
  *                  rows at slots >= num_padded are not written
- *   hs             [cap, w4_group_sum_pitch(m, 64)] fp32 out: hs[slot, c] =
- *                  sum of the fp16 values h[slot, 64c .. 64c+63] (fixed
- *                  order), the group sums the down GEMM needs
- * Weights enter the tensor cores as fp16(s * q) (one rounding) against the
- * fp16 activations, fp32 accumulation; the zero points are applied in fp32
- * through xs; |s| must not exceed 64.  h is rounded to fp16 with
- * saturation at +-65504.
+ * Weights are dequantised in registers to fp16 as q * s + fp16(-z * s) (one
+ * fused rounding) and multiplied on the tensor cores (tcgen05, fp16 x fp16
+ * -> fp32); h is rounded to fp16 with saturation at +-65504.
  * Requires d % 128 == 0, m % 64 == 0, group == 128.
  * dev_status may be NULL.
  * ------------------------------------------------------------------------ */
-int w4_grouped_gemm_gate_up(const uint16_t *xg, const float *xs, int M, int d, int m, int E,
-                            int k, int block_m, const uint8_t *gu_q, const uint16_t *gu_s,
-                            const uint16_t *gu_z, int group, const int32_t *sorted_ids,
-                            const int32_t *expert_offsets, uint16_t *h, float *hs,
+int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
+                            const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                            int group, const int32_t *sorted_ids,
+                            const int32_t *expert_offsets, uint16_t *h,
                             int32_t *dev_status, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
@@ -221,18 +202,17 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, const float *xs, int M, int d, i
  * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: down_proj groups of
  *  64 because 128 does not divide 704).
  *
- *   h, hs          from w4_grouped_gemm_gate_up
+ *   h              [cap, m] fp16 in block order (from w4_grouped_gemm_gate_up)
  *   dn_q           [E, d, m/2] uint8, dn_s/dn_z [E, d, m/group] fp16
  *   y              [M*k, d] fp32 out, row a = flat assignment index
  *                  (y[a] = h[slot of a] . deq(Wdn[e])^T); rows of skipped
  *                  (invalid-id) assignments are not written
- * Weights enter the tensor cores as fp16(s * q) against fp16 h; the zero
- * points are applied in fp32 through hs; |s| must not exceed 64.
+ * Same dequantisation as gate_up.
  * Requires d % 128 == 0, m % 64 == 0, group == 64.  dev_status may be NULL.
  * ------------------------------------------------------------------------ */
-int w4_grouped_gemm_down(const uint16_t *h, const float *hs, int M, int d, int m, int E, int k,
-                         int block_m, const uint8_t *dn_q, const uint16_t *dn_s,
-                         const uint16_t *dn_z, int group, const int32_t *sorted_ids,
+int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
+                         const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z,
+                         int group, const int32_t *sorted_ids,
                          const int32_t *expert_offsets, float *y,
                          int32_t *dev_status, w4_stream_t stream);
 
@@ -261,8 +241,7 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids,
  *
  * workspace: caller-owned device buffer of at least
  * w4_moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds the
- * alignment outputs, the gathered activations and their group sums, h and
- * its group sums, and y.  Its contents on return are the intermediates
+ * alignment outputs, the gathered activations, h and y.  Its contents on return are the intermediates
  * of this call (layout: see the implementation; not part of the ABI).
  * Same shape rules as the individual calls; dev_status may be NULL.
  * ------------------------------------------------------------------------ */

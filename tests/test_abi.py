@@ -39,7 +39,7 @@ def test_header_compiles_as_plain_c():
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4_abi_version() == 2
+    assert clib.w4_abi_version() == 3
     assert clib.w4_status_string(0) == b"W4_OK"
     assert clib.w4_status_string(2) == b"W4_ERR_UNSUPPORTED_SHAPE"
     assert clib.w4_status_string(99) == b"W4_ERR_UNKNOWN"
@@ -65,34 +65,21 @@ def test_argument_validation_without_launching(clib):
     # block_m must be a supported power of two
     assert clib.w4_moe_align(fake, 4, 2, 8, 24, fake, fake, fake, fake, None, None) == 1
     # gate_up needs d % 128 == 0, m % 64 == 0, group == 128
-    args = [fake, fake, 16, 200, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake, fake,
-            None, None]
+    args = [fake, 16, 200, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake, None, None]
     assert clib.w4_grouped_gemm_gate_up(*args) == 2
-    args[3] = 256
-    args[11] = 64
+    args[2] = 256
+    args[10] = 64
     assert clib.w4_grouped_gemm_gate_up(*args) == 2
-    # misaligned activation pointer, missing or misaligned group sums
-    args[11] = 128
+    # misaligned activation pointer
+    args[10] = 128
     args[0] = odd
     assert clib.w4_grouped_gemm_gate_up(*args) == 3
     assert b"aligned" in clib.w4_last_error_detail()
-    args[0] = fake
-    args[1] = None
-    assert clib.w4_grouped_gemm_gate_up(*args) == 1
-    args[1] = odd
-    assert clib.w4_grouped_gemm_gate_up(*args) == 3
     # down group must be 64
-    dargs = [fake, fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake, None,
-             None]
+    dargs = [fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake, None, None]
     assert clib.w4_grouped_gemm_down(*dargs) == 2
-    # gather: group must divide d
-    assert clib.w4_gather_activations(fake, 4, 256, 2, 8, 16, 96, fake, fake, fake, fake,
-                                      None) == 2
-    # group-sum pitch: K/group rounded up to a multiple of 4, -1 if group does not divide K
-    assert clib.w4_group_sum_pitch(2816, 128) == 24
-    assert clib.w4_group_sum_pitch(704, 64) == 12
-    assert clib.w4_group_sum_pitch(512, 128) == 4
-    assert clib.w4_group_sum_pitch(700, 64) == -1
+    # gather: d must be a multiple of 8
+    assert clib.w4_gather_activations(fake, 4, 252, 2, 8, 16, fake, fake, fake, None) == 2
     # workspace too small
     assert clib.w4_moe_layer(fake, fake, fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128,
                              fake, fake, fake, 64, fake, 16, fake, None, None) == 6

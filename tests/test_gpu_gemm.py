@@ -4,14 +4,13 @@ format).
 
 h is compared slot by slot with the oracle's h of the assignment in that slot;
 y row by row, with the metric of the layer, max|gpu - oracle| / rms(oracle).
-Error sources: every weight enters the tensor cores as fp16(s*q) (one
-rounding, relative <= 2^-11, independent from weight to weight), the zero
-point is applied exactly in fp32 through the group sums, and h is rounded to
-fp16.  The metric divides by rms(h) while the largest |h| is 15-20x that, so
-one half-ulp at the largest element alone is ~1e-2: the h bound is 2.5e-2.  y averages the h errors over m terms: bound 1e-2.  The
-layer's own bound (2e-2 on the bf16 output) is checked in test_gpu_layer.py.
-The group sums the GEMMs pass along (xs from the gather, hs from gate_up)
-are checked against float64 sums of the values they summarise.
+Error sources: each dequantised weight is rounded to fp16 (relative <= 2^-11),
+the per-group constant -z*s is rounded to fp16 once (a systematic error per
+group, multiplied by the group's activation sum) and h is rounded to fp16.
+Together they give ~7e-4 relative rms error in h; the metric is dominated by
+the largest |h| (~15-20x rms(h)), hence the h bound of 2.5e-2.  y averages
+the h errors over m terms: bound 1e-2.  The layer's own bound (2e-2 on the
+bf16 output) is checked in test_gpu_layer.py.
 """
 import numpy as np
 import pytest
@@ -35,25 +34,14 @@ def _run_steps(lib, cfg, gu, dn, x_bits, ids, block_m):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     x = _cuda(x_bits.view(np.int16)).view(torch.bfloat16)
     al = lib.w4_moe_align(_cuda(ids), cfg.E, block_m, dev_status=status)
-    xg, xs = lib.w4_gather_activations(x, al)
-    h, hs = lib.w4_grouped_gemm_gate_up(xg, xs, *gu, al, dev_status=status)
-    y = lib.w4_grouped_gemm_down(h, hs, *dn, al, dev_status=status)
+    xg = lib.w4_gather_activations(x, al)
+    h = lib.w4_grouped_gemm_gate_up(xg, *gu, al, dev_status=status)
+    y = lib.w4_grouped_gemm_down(h, *dn, al, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    npad = int(al["num_padded"].item())
-    _check_h_sums(h.float().cpu().numpy()[:npad], hs.cpu().numpy()[:npad])
     # h is stored in the GEMMs' block order; compare it in natural order
-    return (al["sorted_ids"].cpu().numpy(), npad,
+    return (al["sorted_ids"].cpu().numpy(), int(al["num_padded"].item()),
             lib.korder_to_natural(h.float().cpu().numpy()), y.cpu().numpy())
-
-
-def _check_h_sums(h, hs):
-    """hs[slot, c] is the fp32 sum of the fp16 values h[slot, 64c:64c+64]:
-    within fp32 rounding of the float64 sum (63 additions)."""
-    P = h.shape[1] // 64
-    exact = h.astype(np.float64).reshape(h.shape[0], P, 64).sum(axis=2)
-    mag = np.abs(h.astype(np.float64)).reshape(h.shape[0], P, 64).sum(axis=2)
-    assert np.all(np.abs(hs[:, :P] - exact) <= 64 * 2.0 ** -24 * mag + 1e-30)
 
 
 def _compare(cfg, sorted_ids, npad, h, y, h_ref, y_ref, rows=None):
@@ -135,9 +123,8 @@ def test_gemm_steps_full_size_sampled(lib, name):
 @pytest.mark.parametrize("name", ["tiny", "ragged", "layer256", "canvas2048"])
 def test_gather_and_fused_align_gather(lib, name, block_m):
     """Gathered activations hold x[token of slot] rounded to fp16 (block
-    order), zero rows for padding; xs holds the sums of the fp16 row per group
-    of 128 within fp32 rounding; the fused launch writes the same bytes and the
-    same alignment as the two separate calls."""
+    order), zero rows for padding; the fused launch writes the same bytes and
+    the same alignment as the two separate calls."""
     import torch
     from helpers import bf16_bits_to_f64
     cfg = wl.CONFIGS[name]
@@ -145,15 +132,13 @@ def test_gather_and_fused_align_gather(lib, name, block_m):
     x = _cuda(x_bits.view(np.int16)).view(torch.bfloat16)
     ids, _ = oracle.route(wl.router_logits(cfg), cfg.k)
     al1 = lib.w4_moe_align(_cuda(ids), cfg.E, block_m)
-    xg1, xs1 = lib.w4_gather_activations(x, al1)
-    al2, xg2, xs2 = lib.w4_moe_align_gather(_cuda(ids), x, cfg.E, block_m)
+    xg1 = lib.w4_gather_activations(x, al1)
+    al2, xg2 = lib.w4_moe_align_gather(_cuda(ids), x, cfg.E, block_m)
     torch.cuda.synchronize()
     npad = int(al1["num_padded"].item())
     for key in ("sorted_ids", "block_expert", "expert_offsets", "num_padded"):
         assert torch.equal(al1[key], al2[key])
     assert torch.equal(xg1[:npad].view(torch.int16), xg2[:npad].view(torch.int16))
-    G = cfg.d // 128
-    assert torch.equal(xs1[:npad, :G], xs2[:npad, :G])
     sorted_ids = al1["sorted_ids"].cpu().numpy()[:npad]
     got = lib.korder_to_natural(xg1[:npad].float().cpu().numpy())
     # fp16 holds every bf16 value of fp16's normal range exactly; below 2^-14
@@ -162,9 +147,3 @@ def test_gather_and_fused_align_gather(lib, name, block_m):
     real = sorted_ids < cfg.A
     assert np.array_equal(got[real], xf[sorted_ids[real] // cfg.k])
     assert np.all(got[~real] == 0.0)
-    rows = xf[sorted_ids[real] // cfg.k]
-    exact = rows.reshape(-1, G, 128).sum(axis=2)
-    mag = np.abs(rows).reshape(-1, G, 128).sum(axis=2)
-    xs = xs1[:npad, :G].cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(xs[real] - exact) <= 128 * 2.0 ** -24 * mag)
-    assert np.all(xs[~real] == 0.0)

@@ -10,7 +10,7 @@ synthetic workloads (``workloads``) used by the tests and the benchmark.
     out = w4.w4_moe_layer(x_bf16, ids, w, (gu_q, gu_s, gu_z), (dn_q, dn_s, dn_z))
 """
 from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_PIPELINE_TIMEOUT, W4_DEV_TOO_MANY_JOBS,
-                   W4Error, header_functions, w4_group_sum_pitch, korder_to_natural, load_library,
+                   W4Error, header_functions, korder_to_natural, load_library,
                    w4_gather_activations, w4_grouped_gemm_down, w4_moe_align_gather,
                    w4_grouped_gemm_gate_up, w4_moe_align, w4_moe_align_capacity,
                    w4_moe_combine_fixed_order, w4_moe_layer, w4_moe_layer_static_scratch,
@@ -18,7 +18,7 @@ from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_PIPELINE_TIMEOUT, W4_DEV_TOO_MAN
                    w4_moe_route, w4_quantize)
 
 __all__ = [
-    "W4Error", "load_library", "w4_group_sum_pitch", "header_functions", "korder_to_natural", "w4_gather_activations",
+    "W4Error", "load_library", "header_functions", "korder_to_natural", "w4_gather_activations",
     "w4_moe_align_gather",
     "w4_quantize", "w4_moe_route", "w4_moe_align", "w4_moe_align_capacity",
     "w4_grouped_gemm_gate_up", "w4_grouped_gemm_down", "w4_moe_combine_fixed_order",

@@ -62,12 +62,10 @@ def load_library(path: str | None = None):
             "w4_moe_route": ([V, I, I, I, V, V, V], I),
             "w4_moe_align_capacity": ([I, I, I, I], I64),
             "w4_moe_align": ([V, I, I, I, I, V, V, V, V, V, V], I),
-            "w4_group_sum_pitch": ([I, I], I),
-            "w4_gather_activations": ([V, I, I, I, I, I, I, V, V, V, V, V], I),
-            "w4_moe_align_gather": ([V, V, I, I, I, I, I, I, V, V, V, V, V, V, V, V], I),
-            "w4_grouped_gemm_gate_up": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V, V],
-                                        I),
-            "w4_grouped_gemm_down": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
+            "w4_gather_activations": ([V, I, I, I, I, I, V, V, V, V], I),
+            "w4_moe_align_gather": ([V, V, I, I, I, I, I, V, V, V, V, V, V, V], I),
+            "w4_grouped_gemm_gate_up": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
+            "w4_grouped_gemm_down": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_moe_combine_fixed_order": ([V, V, V, I, I, I, I, V, V], I),
             "w4_moe_layer_workspace_size": ([I, I, I, I, I, I], SZ),
             "w4_moe_layer": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V, SZ, V, V,
@@ -176,39 +174,26 @@ def w4_moe_align(topk_ids, E: int, block_m: int = 16, dev_status=None, out=None,
     return r
 
 
-def w4_group_sum_pitch(K: int, group: int) -> int:
-    """Row pitch (floats) of a [cap, pitch] table of per-group sums."""
-    p = load_library().w4_group_sum_pitch(K, group)
-    if p < 0:
-        raise W4Error(1, "W4_ERR_INVALID_ARG", "w4_group_sum_pitch: group must divide K")
-    return int(p)
-
-
-def w4_gather_activations(x, align: dict, group: int = 128, out=None, xs=None, stream=None):
-    """x [M, d] bf16 -> (xg [cap, d] fp16 in slot order and block order,
-    xs [cap, pitch] fp32 group sums of xg's rows); zero rows for padding
-    slots, rows past num_padded left untouched."""
+def w4_gather_activations(x, align: dict, out=None, stream=None):
+    """x [M, d] bf16 -> xg [cap, d] fp16 in slot order and block order (zero
+    rows for padding slots; rows past num_padded are left untouched)."""
     import torch
-    _require_cuda(x, out, xs)
+    _require_cuda(x, out)
     M, d = x.shape
     cap = align["sorted_ids"].numel()
     if out is None:
         out = torch.empty((cap, d), dtype=torch.float16, device=x.device)
-    if xs is None:
-        xs = torch.empty((cap, w4_group_sum_pitch(d, group)), dtype=torch.float32,
-                         device=x.device)
     _check(load_library().w4_gather_activations(
-        _ptr(x), M, d, align["k"], align["E"], align["block_m"], group,
-        _ptr(align["sorted_ids"]), _ptr(align["num_padded"]), _ptr(out), _ptr(xs),
-        _stream(stream)), "w4_gather_activations")
-    return out, xs
+        _ptr(x), M, d, align["k"], align["E"], align["block_m"], _ptr(align["sorted_ids"]),
+        _ptr(align["num_padded"]), _ptr(out), _stream(stream)), "w4_gather_activations")
+    return out
 
 
-def w4_moe_align_gather(topk_ids, x, E: int, block_m: int = 16, group: int = 128,
-                        dev_status=None, out=None, xg=None, xs=None, stream=None):
-    """Alignment and activation gather in one launch.  Returns (align dict, xg, xs)."""
+def w4_moe_align_gather(topk_ids, x, E: int, block_m: int = 16, dev_status=None, out=None,
+                        xg=None, stream=None):
+    """Alignment and activation gather in one launch.  Returns (align dict, xg)."""
     import torch
-    _require_cuda(topk_ids, x, dev_status, xg, xs)
+    _require_cuda(topk_ids, x, dev_status, xg)
     M, k = topk_ids.shape
     d = x.shape[1]
     cap = w4_moe_align_capacity(M, k, E, block_m)
@@ -221,35 +206,30 @@ def w4_moe_align_gather(topk_ids, x, E: int, block_m: int = 16, group: int = 128
     out.update(M=M, k=k, E=E, block_m=block_m)
     if xg is None:
         xg = torch.empty((cap, d), dtype=torch.float16, device=dev)
-    if xs is None:
-        xs = torch.empty((cap, w4_group_sum_pitch(d, group)), dtype=torch.float32, device=dev)
     _check(load_library().w4_moe_align_gather(
-        _ptr(topk_ids), _ptr(x), M, d, k, E, block_m, group, _ptr(out["sorted_ids"]),
+        _ptr(topk_ids), _ptr(x), M, d, k, E, block_m, _ptr(out["sorted_ids"]),
         _ptr(out["block_expert"]), _ptr(out["expert_offsets"]), _ptr(out["num_padded"]),
-        _ptr(xg), _ptr(xs), _ptr(dev_status), _stream(stream)), "w4_moe_align_gather")
-    return out, xg, xs
+        _ptr(xg), _ptr(dev_status), _stream(stream)), "w4_moe_align_gather")
+    return out, xg
 
 
-def w4_grouped_gemm_gate_up(xg, xs, gu_q, gu_s, gu_z, align: dict, group: int = 128, h=None,
-                            hs=None, dev_status=None, stream=None):
-    """(xg, xs) from the gather -> (h [cap, m] fp16 in block order, hs [cap,
-    pitch] fp32 sums of h per 64 columns): gelu_tanh(gate) * up per slot."""
+def w4_grouped_gemm_gate_up(xg, gu_q, gu_s, gu_z, align: dict, group: int = 128, h=None,
+                            dev_status=None, stream=None):
+    """xg [cap, d] fp16 (from w4_gather_activations) -> h [cap, m] fp16 in block
+    order: gelu_tanh(gate) * up per alignment slot."""
     import torch
-    _require_cuda(xg, xs, gu_q, gu_s, gu_z, h, hs, dev_status)
+    _require_cuda(xg, gu_q, gu_s, gu_z, h, dev_status)
     M, d = align["M"], xg.shape[1]
     E, two_m, _ = gu_q.shape
     m = two_m // 2
     cap = align["sorted_ids"].numel()
     if h is None:
         h = torch.empty((cap, m), dtype=torch.float16, device=xg.device)
-    if hs is None:
-        hs = torch.empty((cap, w4_group_sum_pitch(m, 64)), dtype=torch.float32,
-                         device=xg.device)
     _check(load_library().w4_grouped_gemm_gate_up(
-        _ptr(xg), _ptr(xs), M, d, m, E, align["k"], align["block_m"], _ptr(gu_q), _ptr(gu_s),
-        _ptr(gu_z), group, _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(h),
-        _ptr(hs), _ptr(dev_status), _stream(stream)), "w4_grouped_gemm_gate_up")
-    return h, hs
+        _ptr(xg), M, d, m, E, align["k"], align["block_m"], _ptr(gu_q), _ptr(gu_s), _ptr(gu_z),
+        group, _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(h),
+        _ptr(dev_status), _stream(stream)), "w4_grouped_gemm_gate_up")
+    return h
 
 
 def korder_to_natural(a):
@@ -264,18 +244,18 @@ def korder_to_natural(a):
     return a[..., src + inv[np.arange(n) % 8]]
 
 
-def w4_grouped_gemm_down(h, hs, dn_q, dn_s, dn_z, align: dict, group: int = 64, y=None,
+def w4_grouped_gemm_down(h, dn_q, dn_s, dn_z, align: dict, group: int = 64, y=None,
                          dev_status=None, stream=None):
-    """(h, hs) from gate_up -> y [M*k, d] fp32 (row = flat assignment index)."""
+    """h [cap, m] fp16 -> y [M*k, d] fp32 (row = flat assignment index)."""
     import torch
-    _require_cuda(h, hs, dn_q, dn_s, dn_z, y, dev_status)
+    _require_cuda(h, dn_q, dn_s, dn_z, y, dev_status)
     E, d, half_m = dn_q.shape
     m = half_m * 2
     M, k = align["M"], align["k"]
     if y is None:
         y = torch.empty((M * k, d), dtype=torch.float32, device=h.device)
     _check(load_library().w4_grouped_gemm_down(
-        _ptr(h), _ptr(hs), M, d, m, E, k, align["block_m"], _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), group,
+        _ptr(h), M, d, m, E, k, align["block_m"], _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), group,
         _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(y), _ptr(dev_status),
         _stream(stream)), "w4_grouped_gemm_down")
     return y

@@ -177,54 +177,44 @@ int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m, int3
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "align launch");
 }
 
-int w4_group_sum_pitch(int K, int group)
-{
-    if (K <= 0 || group <= 0 || K % group)
-        return -1;
-    return w4::sum_pitch(K, group);
-}
-
-int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m, int group,
+int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          float *xs, w4_stream_t stream)
+                          w4_stream_t stream)
 {
-    if (!xg || !xs || !sorted_ids || !num_padded || (M > 0 && !x))
+    if (!xg || !sorted_ids || !num_padded || (M > 0 && !x))
         return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
     if (M < 0 || d <= 0 || k <= 0 || E <= 0)
         return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
     if (!valid_block_m(block_m))
         return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
-    if ((group != 64 && group != 128) || d % group)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "group must be 64 or 128 and divide d");
-    if (!aligned16(x) || !aligned16(xg) || !aligned16(xs) || !aligned4(sorted_ids) ||
-        !aligned4(num_padded))
-        return fail(W4_ERR_MISALIGNED, "x, xg and xs must be 16-byte aligned");
+    if (d % 8)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "d must be a multiple of 8");
+    if (!aligned16(x) || !aligned16(xg) || !aligned4(sorted_ids) || !aligned4(num_padded))
+        return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
     if (int rc = check_device())
         return rc;
     const int64_t cap = align_capacity(M, k, E, block_m);
-    cudaError_t err = w4::launch_gather(x, M, d, k, group, cap, sorted_ids, num_padded, xg, xs,
-                                        as_stream(stream));
+    cudaError_t err =
+        w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg, as_stream(stream));
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "gather launch");
 }
 
 int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d, int k, int E,
-                        int block_m, int group, int32_t *sorted_ids, int32_t *block_expert,
-                        int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg, float *xs,
+                        int block_m, int32_t *sorted_ids, int32_t *block_expert,
+                        int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
                         int32_t *dev_status, w4_stream_t stream)
 {
-    if (!sorted_ids || !block_expert || !expert_offsets || !num_padded || !xg || !xs ||
+    if (!sorted_ids || !block_expert || !expert_offsets || !num_padded || !xg ||
         (M > 0 && (!topk_ids || !x)))
         return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
     if (M < 0 || d <= 0 || k <= 0 || E <= 0)
         return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
     if (!valid_block_m(block_m))
         return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
-    if (E > 1024)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "E must be <= 1024");
-    if ((group != 64 && group != 128) || d % group)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "group must be 64 or 128 and divide d");
-    if (!aligned16(x) || !aligned16(xg) || !aligned16(xs))
-        return fail(W4_ERR_MISALIGNED, "x, xg and xs must be 16-byte aligned");
+    if (E > 1024 || d % 8)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need E <= 1024 and d %% 8 == 0");
+    if (!aligned16(x) || !aligned16(xg))
+        return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
     const int64_t cap = align_capacity(M, k, E, block_m);
     if (cap > (1ll << 30))
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "too many assignments");
@@ -236,31 +226,26 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         err = w4::launch_align_gather(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
-                                      expert_offsets, num_padded, dev_status, x, d, group, xg,
-                                      xs, sms, as_stream(stream));
+                                      expert_offsets, num_padded, dev_status, x, d, xg, sms,
+                                      as_stream(stream));
     } else {   // too many assignments to keep their slots in shared memory
         err = w4::launch_align(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
                                expert_offsets, num_padded, dev_status, as_stream(stream));
         if (err == cudaSuccess)
-            err = w4::launch_gather(x, M, d, k, group, cap, sorted_ids, num_padded, xg, xs,
+            err = w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg,
                                     as_stream(stream));
     }
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "align+gather launch");
 }
 
-int w4_grouped_gemm_gate_up(const uint16_t *xg, const float *xs, int M, int d, int m, int E,
-                            int k, int block_m, const uint8_t *gu_q, const uint16_t *gu_s,
-                            const uint16_t *gu_z, int group, const int32_t *sorted_ids,
-                            const int32_t *expert_offsets, uint16_t *h, float *hs,
-                            int32_t *dev_status, w4_stream_t stream)
+int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
+                            const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                            int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
+                            uint16_t *h, int32_t *dev_status, w4_stream_t stream)
 {
     if (int rc = check_gemm_common(M, d, m, E, k, block_m, xg, gu_q, gu_s, gu_z, sorted_ids,
                                    expert_offsets, h))
         return rc;
-    if (!xs || !hs)
-        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
-    if (!aligned16(xs) || !aligned16(hs))
-        return fail(W4_ERR_MISALIGNED, "xs and hs must be 16-byte aligned");
     if (group != 128)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "gate_up group must be 128 (got %d)", group);
     if (int rc = check_device())
@@ -268,10 +253,6 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, const float *xs, int M, int d, i
     w4::GroupedGemmProblem p{};
     p.gate_up = true;
     p.act = xg;
-    p.act_sum = xs;
-    p.act_sum_pitch = w4::sum_pitch(d, group);
-    p.out_sum = hs;
-    p.out_sum_pitch = w4::sum_pitch(m, 64);
     p.wq = gu_q;
     p.ws = gu_s;
     p.wz = gu_z;
@@ -296,19 +277,14 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, const float *xs, int M, int d, i
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "gate_up launch");
 }
 
-int w4_grouped_gemm_down(const uint16_t *h, const float *hs, int M, int d, int m, int E, int k,
-                         int block_m, const uint8_t *dn_q, const uint16_t *dn_s,
-                         const uint16_t *dn_z, int group, const int32_t *sorted_ids,
-                         const int32_t *expert_offsets, float *y, int32_t *dev_status,
-                         w4_stream_t stream)
+int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
+                         const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
+                         const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
+                         int32_t *dev_status, w4_stream_t stream)
 {
     if (int rc = check_gemm_common(M, d, m, E, k, block_m, h, dn_q, dn_s, dn_z, sorted_ids,
                                    expert_offsets, y))
         return rc;
-    if (!hs)
-        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
-    if (!aligned16(hs))
-        return fail(W4_ERR_MISALIGNED, "hs must be 16-byte aligned");
     if (group != 64)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "down group must be 64 (got %d)", group);
     if (int rc = check_device())
@@ -316,10 +292,6 @@ int w4_grouped_gemm_down(const uint16_t *h, const float *hs, int M, int d, int m
     w4::GroupedGemmProblem p{};
     p.gate_up = false;
     p.act = h;
-    p.act_sum = hs;
-    p.act_sum_pitch = w4::sum_pitch(m, 64);
-    p.out_sum = nullptr;
-    p.out_sum_pitch = 0;
     p.wq = dn_q;
     p.ws = dn_s;
     p.wz = dn_z;
@@ -364,11 +336,10 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const fl
 
 // Workspace layout of w4_moe_layer (each piece 256-byte aligned):
 //   sorted_ids [cap] i32 | block_expert [cap/bm] i32 | expert_offsets [E+1] i32 |
-//   num_padded [1] i32 | xg [cap, d] bf16 | xs [cap, pitch(d,128)] f32 |
-//   h [cap, m] fp16 | hs [cap, pitch(m,64)] f32 | y [M*k, d] fp32
+//   num_padded [1] i32 | xg [cap, d] fp16 | h [cap, m] fp16 | y [M*k, d] fp32
 namespace {
 struct LayerWs {
-    size_t sorted, block, offs, npad, xg, xs, h, hs, y, total;
+    size_t sorted, block, offs, npad, xg, h, y, total;
 };
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
@@ -380,10 +351,8 @@ LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
     w.offs = up256(w.block + 4 * (cap / bm));
     w.npad = up256(w.offs + 4 * (static_cast<size_t>(E) + 1));
     w.xg = up256(w.npad + 4);
-    w.xs = up256(w.xg + 2 * cap * static_cast<size_t>(d));
-    w.h = up256(w.xs + 4 * cap * static_cast<size_t>(w4::sum_pitch(d, 128)));
-    w.hs = up256(w.h + 2 * cap * static_cast<size_t>(m));
-    w.y = up256(w.hs + 4 * cap * static_cast<size_t>(w4::sum_pitch(m, 64)));
+    w.h = up256(w.xg + 2 * cap * static_cast<size_t>(d));
+    w.y = up256(w.h + 2 * cap * static_cast<size_t>(m));
     w.total = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
     return w;
 }
@@ -417,24 +386,20 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
     int32_t *offs = reinterpret_cast<int32_t *>(ws + L.offs);
     int32_t *npad = reinterpret_cast<int32_t *>(ws + L.npad);
     uint16_t *xg = reinterpret_cast<uint16_t *>(ws + L.xg);
-    float *xs = reinterpret_cast<float *>(ws + L.xs);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    float *hs = reinterpret_cast<float *>(ws + L.hs);
     float *y = reinterpret_cast<float *>(ws + L.y);
-    if (gu_group != 128 || dn_group != 64)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "groups must be 128 (gate_up) and 64 (down)");
     // alignment and the activation gather share one launch
-    if (int rc0 = w4_moe_align_gather(topk_ids, x, M, d, k, E, block_m, gu_group, sorted, block,
-                                      offs, npad, xg, xs, dev_status, stream))
+    if (int rc0 = w4_moe_align_gather(topk_ids, x, M, d, k, E, block_m, sorted, block, offs, npad,
+                                      xg, dev_status, stream))
         return rc0;
     if (M == 0)
         return W4_OK;
-    int rc = w4_grouped_gemm_gate_up(xg, xs, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
-                                     sorted, offs, h, hs, dev_status, stream);
+    int rc = w4_grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
+                                     sorted, offs, h, dev_status, stream);
     if (rc)
         return rc;
-    rc = w4_grouped_gemm_down(h, hs, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted,
-                              offs, y, dev_status, stream);
+    rc = w4_grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs,
+                              y, dev_status, stream);
     if (rc)
         return rc;
     return w4_moe_combine_fixed_order(y, topk_ids, topk_weights, M, k, d, E, out, stream);

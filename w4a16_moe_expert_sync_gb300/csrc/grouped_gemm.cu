@@ -11,18 +11,14 @@
 // with deq(W) = s_g * (q - z_g) for uint4 codes q packed two per byte and fp16
 // s, z per group of `group` elements along the contraction dim.
 //
-// Split of the zero point.  Per output row r and token n,
-//     sum_k s_g(k) (q_k - z_g(k)) a_k = sum_k fp16(s q_k) a_k - sum_g s_g z_g X_g
-// with X_g = sum_{k in g} a_k.  The first sum runs on the tensor cores with
-// A = fp16(s * q) made in registers; the second is one fp32 dot product of
-// length K/group per output, done once in the epilogue from the group sums
-// that travel with the activations (the gather writes those of x, the
-// gate_up epilogue those of h).  fp16(s * q) costs, per 8 codes in a word,
-// three shifts and four LOP3 on the integer pipe (the nibble ORed into the
-// mantissa of fp16 1024, an exact 1024 + q) and four HFMA2 on the FMA pipe
-// ((1024 + q) * s - 1024 * s, one rounding), which issue in parallel.
+// Dequantisation.  Eight codes sit in one 32-bit word; ORing a masked pair
+// of nibbles into the mantissa of fp16 1024.0 gives 1024 + q (or 1024 + 16q
+// for the high nibbles) exactly; one HADD2 (or HFMA2 by 1/16) leaves q, and
+// one HFMA2 makes q * s + c with c = fp16(-z * s), a single rounding of the
+// product.  Per word that is one shift and four LOP3 on the integer pipe and
+// eight fp16 operations on the FMA pipe, which issue in parallel.
 //
-// Design (one persistent CTA per SM, 18 warps, static round-robin schedule):
+// Design (one persistent CTA per SM, 26 warps, static round-robin schedule):
 //   * A work unit is (job, panel).  A job is at most 32 consecutive slots of
 //     one expert; a panel is 128 weight rows (gate_up: 64 gate rows and the
 //     matching 64 up rows; down: 128 output rows).
@@ -37,12 +33,12 @@
 //   * Warp roles
 //       warps 0-3   tcgen05.mma issuers (one lane each).
 //       warps 4-7   epilogue (one TMEM lane quarter each).
-//       warps 8-15  dequant: two per lane quarter, 128 codes of each 256-code
-//                   chunk each, written as two 64-code sub-chunks.
-//       warp 16     TMA: packed codes (128 rows x 256 codes per stage, two
+//       warps 8-23  dequant: four per lane quarter, one 64-code sub-chunk of
+//                   each 256-code chunk each (warps 8 + 4 i + q feed issuer i).
+//       warp 24     TMA: packed codes (128 rows x 256 codes per stage, two
 //                   64-row boxes, evict-first), per unit the scales, zeros
 //                   and activation group sums (bulk copies).
-//       warp 17     TMA: activation slots.
+//       warp 25     TMA: activation slots.
 //   * Tensor memory: columns 0-255 eight A sub-chunk buffers (64 codes, 32
 //     columns each), two per issuer, so every buffer has one producer group
 //     (the dequant warps of one half) and one consumer, both in order;
@@ -128,10 +124,10 @@ constexpr int kIssuers = 4;                 // warps 0-3
 constexpr int kFirstEpiWarp = 4;            // warps 4-7
 constexpr int kNumEpiWarps = 4;
 constexpr int kFirstDqWarp = 8;             // warps 8-15
-constexpr int kNumDqWarps = 8;
-constexpr int kWarpTmaW = 16;
-constexpr int kWarpTmaB = 17;
-constexpr int kNumWarps = 20;               // warps 18-19 idle: registers come in 4-warp units
+constexpr int kNumDqWarps = 16;            // warps 8-23
+constexpr int kWarpTmaW = 24;
+constexpr int kWarpTmaB = 25;
+constexpr int kNumWarps = 26;
 constexpr int kThreads = 32 * kNumWarps;
 constexpr int kStagesW = 5;                 // packed-code stages
 constexpr int kStagesB = 2;                 // activation slots
@@ -145,29 +141,24 @@ constexpr int kStageBBytes = 32768;
 constexpr int kMaxN = 32;                   // slots per job
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;           // acc[set][i] at 256 + 128 set + 32 i
-constexpr int kHpartFloats = 2 * kNumEpiWarps * kMaxN;
 
 struct GemmArgs {
     CUtensorMap tmap_w;       // packed codes u8 [E*R rows, K/2 B], box 128 B x 64 rows, SW128
     CUtensorMap tmap_b[2];    // activations [cap, K] fp16 as {64, cap, K/64}, box {64, 16(i+1), kcols}
     const uint16_t *sc;       // [E*R, G] fp16
     const uint16_t *zp;       // [E*R, G] fp16
-    const float *act_sum;     // [cap, sum_pitch] group sums of the activations
-    float *out_sum;           // gate_up: h sums per 64-column panel [cap, out_sum_pitch]
     const int32_t *sorted_ids;
     const int32_t *expert_offsets;
     void *out;
     int32_t *dev_status;
     int E, A, K, R, m_up, out_cols, group, G, n_panels, n_kchunks, n_sub;
-    int sum_pitch, out_sum_pitch;
 };
 
-constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kSubBufs + 2 + 2 + 2 * kStagesSZ + 2 +
-                         2 + kIssuers;
+constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kSubBufs + 2 + 2 + 2 * kStagesSZ + kIssuers;
 
 struct Bars {
     uint64_t *w_full, *w_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty,
-        *sz_full, *sz_empty, *hp_full, *hp_empty, *drain;
+        *sz_full, *sz_empty, *drain;
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t *base)
@@ -184,28 +175,23 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
     r.acc_empty = r.acc_full + 2;
     r.sz_full = r.acc_empty + 2;
     r.sz_empty = r.sz_full + kStagesSZ;
-    r.hp_full = r.sz_empty + kStagesSZ;
-    r.hp_empty = r.hp_full + 2;
-    r.drain = r.hp_empty + 2;
+    r.drain = r.sz_empty + kStagesSZ;
     return r;
 }
 
 struct SmemLayout {
-    int off_b, off_sz, off_hp, off_bar, off_misc, off_offs, off_jp;
-    int sz_stride, xs_off, total;
+    int off_b, off_sz, off_bar, off_misc, off_offs, off_jp;
+    int sz_stride, total;
 };
 
-// One sz stage: s [128 rows][G] fp16, z [128][G] fp16, then the job's
-// activation group sums [kMaxN][sum_pitch] fp32.
-__host__ __device__ inline SmemLayout smem_layout(int G, int sum_pitch, int E)
+// One sz stage: s [128 rows][G] fp16, then z [128][G] fp16.
+__host__ __device__ inline SmemLayout smem_layout(int G, int E)
 {
     SmemLayout L;
     L.off_b = kStagesW * kStageWBytes;
-    L.xs_off = ((kTileRows * G * 2 * 2) + 15) & ~15;
-    L.sz_stride = (L.xs_off + kMaxN * sum_pitch * 4 + 127) & ~127;
+    L.sz_stride = ((kTileRows * G * 2 * 2) + 127) & ~127;
     L.off_sz = L.off_b + kStagesB * kStageBBytes;
-    L.off_hp = L.off_sz + kStagesSZ * L.sz_stride;
-    L.off_bar = L.off_hp + kHpartFloats * 4;
+    L.off_bar = L.off_sz + kStagesSZ * L.sz_stride;
     L.off_misc = L.off_bar + kNumBars * 8;
     L.off_offs = L.off_misc + 16;
     L.off_jp = L.off_offs + (E + 1) * 4;
@@ -243,16 +229,22 @@ __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<ui
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 // 8 codes (one word, code i in bits 4i..4i+3) -> 4 words of fp16 pairs
-// fp16(s * q) in the block order (q0,q4) (q1,q5) (q2,q6) (q3,q7).
-// v = 1024 + q exactly (nibble ORed into the mantissa of 1024.0), then
-// v * s + (-1024 s) with one rounding; -1024 s is exact for |s| <= 64.
+// q * s + c in the block order (q0,q4) (q1,q5) (q2,q6) (q3,q7).
 __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2, uint32_t *o)
 {
-    constexpr uint32_t kMagic = 0x64006400u;
-    o[0] = h2u(__hfma2(u2h((w & 0x000F000Fu) | kMagic), s2, c2));
-    o[1] = h2u(__hfma2(u2h(((w >> 4) & 0x000F000Fu) | kMagic), s2, c2));
-    o[2] = h2u(__hfma2(u2h(((w >> 8) & 0x000F000Fu) | kMagic), s2, c2));
-    o[3] = h2u(__hfma2(u2h(((w >> 12) & 0x000F000Fu) | kMagic), s2, c2));
+    constexpr uint32_t kMagic = 0x64006400u;               // fp16 1024.0 twice
+    const __half2 k1024 = u2h(kMagic);
+    const __half2 kSixteenth = u2h(0x2C002C00u);           // 1/16
+    const __half2 kMinus64 = u2h(0xD400D400u);             // -64
+    const uint32_t w8 = w >> 8;
+    const __half2 q04 = __hsub2(u2h((w & 0x000F000Fu) | kMagic), k1024);
+    const __half2 q15 = __hfma2(u2h((w & 0x00F000F0u) | kMagic), kSixteenth, kMinus64);
+    const __half2 q26 = __hsub2(u2h((w8 & 0x000F000Fu) | kMagic), k1024);
+    const __half2 q37 = __hfma2(u2h((w8 & 0x00F000F0u) | kMagic), kSixteenth, kMinus64);
+    o[0] = h2u(__hfma2(q04, s2, c2));
+    o[1] = h2u(__hfma2(q15, s2, c2));
+    o[2] = h2u(__hfma2(q26, s2, c2));
+    o[3] = h2u(__hfma2(q37, s2, c2));
 }
 
 __device__ __forceinline__ float gelu_tanh(float v)
@@ -314,11 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const SmemLayout L = smem_layout(p.G, p.sum_pitch, p.E);
+    const SmemLayout L = smem_layout(p.G, p.E);
     uint8_t *stage_w = smem;
     uint8_t *stage_b = smem + L.off_b;
     uint8_t *sz_base = smem + L.off_sz;
-    float *hpart = reinterpret_cast<float *>(smem + L.off_hp);
     const Bars bar = carve_bars(smem + L.off_bar);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
@@ -346,12 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         for (int i = 0; i < 2; i++) {
             mbar_init(&bar.acc_full[i], kIssuers);
             mbar_init(&bar.acc_empty[i], kNumEpiWarps);
-            mbar_init(&bar.hp_full[i], kNumEpiWarps);
-            mbar_init(&bar.hp_empty[i], 1);
         }
         for (int i = 0; i < kStagesSZ; i++) {
             mbar_init(&bar.sz_full[i], 1);
-            mbar_init(&bar.sz_empty[i], kNumDqWarps + kNumEpiWarps);
+            mbar_init(&bar.sz_empty[i], kNumDqWarps);
         }
         for (int i = 0; i < kIssuers; i++)
             mbar_init(&bar.drain[i], 1);
@@ -492,8 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     break;
                 {
                     uint8_t *dst = sz_base + szb * L.sz_stride;
-                    const uint32_t xb = static_cast<uint32_t>(J.n) * p.sum_pitch * 4;
-                    mbar_arrive_expect_tx(&bar.sz_full[szb], 4 * hb + xb);
+                    mbar_arrive_expect_tx(&bar.sz_full[szb], 4 * hb);
                     bulk_load(dst, p.sc + static_cast<int64_t>(row0) * p.G, hb, &bar.sz_full[szb],
                               pol);
                     bulk_load(dst + hb, p.sc + static_cast<int64_t>(row1) * p.G, hb,
@@ -502,9 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                               &bar.sz_full[szb], pol);
                     bulk_load(dst + 3 * hb, p.zp + static_cast<int64_t>(row1) * p.G, hb,
                               &bar.sz_full[szb], pol);
-                    bulk_load_nohint(dst + L.xs_off,
-                                     p.act_sum + static_cast<int64_t>(J.start) * p.sum_pitch, xb,
-                                     &bar.sz_full[szb]);
                 }
                 issued_sz |= 1u << szb;
                 issue_ph_sz = (issue_ph_sz & ~(1u << szb)) | (ph_sz << szb);
@@ -579,10 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
     } else if (warp >= kFirstDqWarp && warp < kFirstDqWarp + kNumDqWarps) {
         // ---------------------------------------------------------- dequant
+        // Warp (q4, sub) expands sub-chunk sub of every chunk for its 32 rows:
+        // sub-chunk j = 4 kc + sub goes to issuer sub, into that issuer's
+        // buffers sub and sub + 4, alternating.
         const int q4 = warp & 3;
-        const int hh = (warp - kFirstDqWarp) >> 2;    // which 128 codes of the chunk
+        const int sub = (warp - kFirstDqWarp) >> 2;
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        const uint32_t m_i = static_cast<uint32_t>(p.n_sub - sub + kIssuers - 1) / kIssuers;
         int sa = 0, szb = 0, n_tr = 0;
         uint32_t ph_a = 0, ph_sz = 0, n_unit = 0;
         bool ok = true;
@@ -598,18 +587,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 if (warp == kFirstDqWarp && lane == 0)
                     W4_TRACE_POINT(2, n_tr);
+                const int j = kc * (kChunkK / kSubK) + sub;   // sub-chunk in unit
+                const bool mine = j < p.n_sub;
                 const uint8_t *rp = stage_w + sa * kStageWBytes + row * 128;
-                // the scale of each of this warp's two sub-chunks
-                __half sh[2];
-#pragma unroll
-                for (int pp = 0; pp < 2; pp++) {
-                    const int j = min(kc * (kChunkK / kSubK) + 2 * hh + pp, p.n_sub - 1);
-                    sh[pp] = s_row[(j * kSubK) / p.group];
+                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                float sf = 0.0f, zf = 0.0f;
+                if (mine) {
+                    w0 = *reinterpret_cast<const uint4 *>(rp + (((2 * sub) ^ (row & 7)) << 4));
+                    w1 = *reinterpret_cast<const uint4 *>(rp + (((2 * sub + 1) ^ (row & 7)) << 4));
+                    const int g = (j * kSubK) / p.group;
+                    sf = __half2float(s_row[g]);
+                    zf = __half2float(s_row[kTileRows * p.G + g]);
                 }
-                uint4 w[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    w[i] = *reinterpret_cast<const uint4 *>(rp + (((4 * hh + i) ^ (row & 7)) << 4));
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&bar.w_empty[sa]);
@@ -617,50 +606,39 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     sa = 0;
                     ph_a ^= 1;
                 }
-#pragma unroll
-                for (int pp = 0; pp < 2; pp++) {
-                    const int j = kc * (kChunkK / kSubK) + 2 * hh + pp;   // sub-chunk in unit
-                    if (j >= p.n_sub)
-                        break;
-                    // sub-chunk j belongs to issuer j % 4, which owns buffers
-                    // i and i + 4 and takes its sub-chunks in order
-                    const int i = j & (kIssuers - 1);
-                    const uint32_t m_i = static_cast<uint32_t>(p.n_sub - i + kIssuers - 1) / kIssuers;
-                    const uint32_t k = n_unit * m_i + (j >> 2);
-                    const int buf = i + kIssuers * (k & 1);
-                    if (!warp_all_wait(&bar.a_empty[buf], ((k >> 1) & 1) ^ 1, lane, abort_flag,
-                                       status)) {
-                        ok = false;
-                        break;
-                    }
-                    if (warp == kFirstDqWarp && lane == 0)
-                        W4_TRACE_POINT(pp == 0 ? 4 : 7, n_tr);
-                    tc_fence_after();
-                    const __half2 s2 = __half2half2(sh[pp]);
-                    const __half2 c2 = __hmul2(s2, __float2half2_rn(-1024.0f));
-                    uint32_t o[32];
-                    const uint4 a = w[2 * pp], b = w[2 * pp + 1];
-                    dequant_word(a.x, s2, c2, &o[0]);
-                    dequant_word(a.y, s2, c2, &o[4]);
-                    dequant_word(a.z, s2, c2, &o[8]);
-                    dequant_word(a.w, s2, c2, &o[12]);
-                    dequant_word(b.x, s2, c2, &o[16]);
-                    dequant_word(b.y, s2, c2, &o[20]);
-                    dequant_word(b.z, s2, c2, &o[24]);
-                    dequant_word(b.w, s2, c2, &o[28]);
-                    if (warp == kFirstDqWarp && lane == 0)
-                        W4_TRACE_POINT(pp == 0 ? 8 : 9, n_tr);
-                    tmem_st_32x32b_x32(tmem + lane_base + buf * 32, o);
-                    tmem_wait_st();
-                    if (warp == kFirstDqWarp && lane == 0)
-                        W4_TRACE_POINT(pp == 0 ? 14 : 15, n_tr);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&bar.a_full[buf]);
-                }
-                if (!ok)
+                if (!mine)
+                    continue;
+                const uint32_t k = n_unit * m_i + kc;         // this issuer's sub-chunk count
+                const int buf = sub + kIssuers * (k & 1);
+                if (!warp_all_wait(&bar.a_empty[buf], ((k >> 1) & 1) ^ 1, lane, abort_flag,
+                                   status)) {
+                    ok = false;
                     break;
+                }
+                if (warp == kFirstDqWarp && lane == 0)
+                    W4_TRACE_POINT(4, n_tr);
+                tc_fence_after();
+                const __half2 s2 = __float2half2_rn(sf);
+                const __half2 c2 = __float2half2_rn(-zf * sf);
+                uint32_t o[32];
+                dequant_word(w0.x, s2, c2, &o[0]);
+                dequant_word(w0.y, s2, c2, &o[4]);
+                dequant_word(w0.z, s2, c2, &o[8]);
+                dequant_word(w0.w, s2, c2, &o[12]);
+                dequant_word(w1.x, s2, c2, &o[16]);
+                dequant_word(w1.y, s2, c2, &o[20]);
+                dequant_word(w1.z, s2, c2, &o[24]);
+                dequant_word(w1.w, s2, c2, &o[28]);
+                if (warp == kFirstDqWarp && lane == 0)
+                    W4_TRACE_POINT(8, n_tr);
+                tmem_st_32x32b_x32(tmem + lane_base + buf * 32, o);
+                tmem_wait_st();
+                if (warp == kFirstDqWarp && lane == 0)
+                    W4_TRACE_POINT(14, n_tr);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bar.a_full[buf]);
                 if (warp == kFirstDqWarp && lane == 0)
                     W4_TRACE_POINT(3, n_tr);
                 n_tr++;
@@ -678,49 +656,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kNumEpiWarps) {
         // ---------------------------------------------------------- epilogue
         const int q4 = warp & 3;
-        const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        int szb = 0;
-        uint32_t ph_sz = 0, n_unit = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
+        const int n_acc = min(kIssuers, p.n_sub);
+        // gate_up: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
+        // the gate lane finishes even slots, the up lane odd ones
+        const bool is_gate = lane < 16;
+        const int il = 16 * q4 + (lane & 15);     // intermediate index in the panel
+        uint32_t n_unit = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, n_unit++) {
             const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
             const int pnl = u % p.n_panels;
             const int set = n_unit & 1;
-            if (!warp_all_wait(&bar.sz_full[szb], ph_sz, lane, abort_flag, status) ||
-                !warp_all_wait(&bar.acc_full[set], (n_unit >> 1) & 1, lane, abort_flag, status))
-                break;
-            if (warp == kFirstEpiWarp && lane == 0)
-                W4_TRACE_POINT(10, n_unit);
-            tc_fence_after();
             // down: the assignment of every slot of the job, fetched early
             int my_a = -1;
             if constexpr (!GATE_UP)
                 my_a = lane < J.n ? __ldg(p.sorted_ids + J.start + lane) : -1;
-            const uint8_t *stg = sz_base + szb * L.sz_stride;
-            const __half *s_row = reinterpret_cast<const __half *>(stg) + row * p.G;
-            const __half *z_row = s_row + kTileRows * p.G;
-            const float *xs = reinterpret_cast<const float *>(stg + L.xs_off);
-            // Per block of 8 slots: v[n] = sum of the issuers' accumulators
-            // (fixed order) - sum_g s_g z_g X_g[n], then the output.
+            if (!warp_all_wait(&bar.acc_full[set], (n_unit >> 1) & 1, lane, abort_flag, status))
+                break;
+            if (warp == kFirstEpiWarp && lane == 0)
+                W4_TRACE_POINT(10, n_unit);
+            tc_fence_after();
             const uint32_t acc = tmem + lane_base + kAccCol + set * 128;
-            const int n_acc = min(kIssuers, p.n_sub);
-            // gate_up: lanes 0-15 hold gate rows, lanes 16-31 the matching up
-            // rows; the gate lane finishes even slots, the up lane odd ones
-            const bool is_gate = lane < 16;
-            const int il = 16 * q4 + (lane & 15);     // intermediate index in the panel
-            const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);
-            const int hb = n_unit & 1;
-            const uint32_t hph = (n_unit >> 1) & 1;
-            float *hp = hpart + hb * (kNumEpiWarps * kMaxN) + q4 * kMaxN;
-            if constexpr (GATE_UP) {
-                if (!warp_all_wait(&bar.hp_empty[hb], hph ^ 1, lane, abort_flag, status))
-                    break;
-            }
 #pragma unroll
             for (int b = 0; b < kMaxN / 8; b++) {
                 if (b * 8 >= J.n)
                     break;
+                // the issuers' accumulators for 8 slots, added in a fixed order
+                // (issuers without a sub-chunk in this unit never wrote theirs)
                 float v[8];
                 {
                     uint32_t r[32];
@@ -728,8 +690,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                          acc + 96 + 8 * b, r);
 #pragma unroll
                     for (int i = 0; i < 8; i++) {
-                        // issuers without a sub-chunk in this unit (n_sub < 4)
-                        // never wrote their accumulator
                         float t = __uint_as_float(r[i]);
                         if (n_acc > 1)
                             t += __uint_as_float(r[8 + i]);
@@ -740,50 +700,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         v[i] = t;
                     }
                 }
-                // zero points, four groups at a time (one 16-byte load of X
-                // per slot)
-                for (int g0 = 0; g0 < p.G; g0 += 4) {
-                    const int ng = min(4, p.G - g0);
-                    float sz[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        sz[i] = i < ng ? __half2float(s_row[g0 + i]) * __half2float(z_row[g0 + i])
-                                       : 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const float4 X =
-                            *reinterpret_cast<const float4 *>(xs + (8 * b + i) * p.sum_pitch + g0);
-                        float t = fmaf(-sz[0], X.x, v[i]);
-                        if (ng > 1)
-                            t = fmaf(-sz[1], X.y, t);
-                        if (ng > 2)
-                            t = fmaf(-sz[2], X.z, t);
-                        if (ng > 3)
-                            t = fmaf(-sz[3], X.w, t);
-                        v[i] = t;
-                    }
-                }
                 if constexpr (GATE_UP) {
                     __half *hout = reinterpret_cast<__half *>(p.out);
+                    const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);
 #pragma unroll
                     for (int i = 0; i < 8; i += 2) {
-                        const int n = 8 * b + i;
                         const float send = is_gate ? v[i + 1] : v[i];
                         const float recv = __shfl_xor_sync(full, send, 16);
                         const float gv = is_gate ? v[i] : recv;
                         const float uv = is_gate ? recv : v[i + 1];
-                        const uint16_t hbits =
-                            static_cast<uint16_t>(f16x2_sat(gelu_tanh(gv) * uv, 0.0f));
-                        const int64_t slot = J.start + n + (is_gate ? 0 : 1);
-                        hout[slot * p.out_cols + pos] = __ushort_as_half(hbits);
-                        // sum of the 16 rounded h values of this half warp
-                        float hr = __half2float(__ushort_as_half(hbits));
-                        hr += __shfl_xor_sync(full, hr, 8);
-                        hr += __shfl_xor_sync(full, hr, 4);
-                        hr += __shfl_xor_sync(full, hr, 2);
-                        hr += __shfl_xor_sync(full, hr, 1);
-                        if ((lane & 15) == 0)
-                            hp[n + (is_gate ? 0 : 1)] = hr;
+                        const int64_t slot = J.start + 8 * b + i + (is_gate ? 0 : 1);
+                        hout[slot * p.out_cols + pos] = __ushort_as_half(
+                            static_cast<uint16_t>(f16x2_sat(gelu_tanh(gv) * uv, 0.0f)));
                     }
                 } else {
                     float *yout = reinterpret_cast<float *>(p.out);
@@ -796,36 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                 }
             }
-            // accumulators, scales, zeros and sums consumed: release them
+            // the accumulator set is consumed: hand it back to the issuers
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0)
                 mbar_arrive(&bar.acc_empty[set]);
-                mbar_arrive(&bar.sz_empty[szb]);
-            }
-            if (++szb == kStagesSZ) {
-                szb = 0;
-                ph_sz ^= 1;
-            }
-            if constexpr (GATE_UP) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&bar.hp_full[hb]);
-                if (q4 == 0) {
-                    // the panel's 64 values per slot, summed in warp order
-                    if (!warp_all_wait(&bar.hp_full[hb], hph, lane, abort_flag, status))
-                        break;
-                    const float *h0 = hpart + hb * (kNumEpiWarps * kMaxN);
-                    for (int n = lane; n < J.n; n += 32) {
-                        const float val = ((h0[n] + h0[kMaxN + n]) + h0[2 * kMaxN + n]) +
-                                          h0[3 * kMaxN + n];
-                        p.out_sum[static_cast<int64_t>(J.start + n) * p.out_sum_pitch + pnl] = val;
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&bar.hp_empty[hb]);
-                }
-            }
             if (warp == kFirstEpiWarp && lane == 0)
                 W4_TRACE_POINT(11, n_unit);
         }
@@ -913,17 +816,13 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
                                 const char **why)
 {
     *why = nullptr;
-    if (q.K % q.group != 0 || q.K % 64 != 0 || (q.group != 64 && q.group != 128) ||
-        (!q.gate_up && q.group != 64)) {
-        *why = "contraction dim must be a multiple of the group (64 or 128, 64 for down, whose "
-               "group sums are h's 64-column panels) and of 64";
+    if (q.K % q.group != 0 || q.K % 64 != 0 || (q.group != 64 && q.group != 128)) {
+        *why = "contraction dim must be a multiple of the group (64 or 128) and of 64";
         return cudaErrorInvalidValue;
     }
     GemmArgs a;
     a.sc = q.ws;
     a.zp = q.wz;
-    a.act_sum = q.act_sum;
-    a.out_sum = q.out_sum;
     a.sorted_ids = q.sorted_ids;
     a.expert_offsets = q.expert_offsets;
     a.out = q.out;
@@ -939,10 +838,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.n_panels = q.gate_up ? (q.R / 2) / 64 : q.R / 128;
     a.n_kchunks = (q.K + kChunkK - 1) / kChunkK;
     a.n_sub = q.K / kSubK;
-    a.sum_pitch = q.act_sum_pitch;
-    a.out_sum_pitch = q.out_sum_pitch;
 
-    const SmemLayout L = smem_layout(a.G, a.sum_pitch, a.E);
+    const SmemLayout L = smem_layout(a.G, a.E);
     const size_t smem = static_cast<size_t>(L.total) + 1024;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);

@@ -44,15 +44,4 @@ __device__ __forceinline__ uint4 bf16x8_to_f16_korder(uint4 v)
     return o;
 }
 
-// fp32 sum of 8 fp16 values (a 16-byte block in any order) in a fixed
-// pairwise order.
-__device__ __forceinline__ float f16x8_sum(uint4 v)
-{
-    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-    const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-    const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
-    return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
-}
-
 }  // namespace w4

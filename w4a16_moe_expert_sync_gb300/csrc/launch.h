@@ -26,38 +26,27 @@ cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, i
                          int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                          int32_t *num_padded, int32_t *dev_status, cudaStream_t stream);
 
-// Row pitch (in floats) of a per-slot table of group sums over a
-// contraction dim of K elements in groups of `group`: K/group rounded up to
-// a multiple of 4, so every row starts on a 16-byte boundary.
-__host__ __device__ constexpr int sum_pitch(int K, int group) { return ((K / group) + 3) & ~3; }
-
-// xg[slot] = x[sorted_ids[slot] / k] (bf16, block order) and
-// xs[slot, g] = fp32 sum of that row's group g (`group` elements), zero for
-// padding slots, for slots below *num_padded.
-cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int group, int64_t cap,
+// xg[slot] = x[sorted_ids[slot] / k] in fp16 block order (zero for padding)
+// for slots below *num_padded.
+cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          float *xs, cudaStream_t stream);
+                          cudaStream_t stream);
 
 // Alignment and gather in one launch (every CTA aligns in shared memory).
 size_t align_gather_smem_bytes(int M, int k, int E);
 cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
                                 int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                                 int32_t *num_padded, int32_t *dev_status, const uint16_t *x,
-                                int d, int group, uint16_t *xg, float *xs, int num_sms,
-                                cudaStream_t stream);
+                                int d, uint16_t *xg, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
                            int d, int E, uint16_t *out, cudaStream_t stream);
 
-// Grouped W4A16 GEMM (tcgen05).  gate_up=true: xg bf16 -> h fp16 with the
-// gated activation (and h's per-panel sums); gate_up=false: h fp16 -> y fp32.
+// Grouped W4A16 GEMM (tcgen05).  gate_up=true: xg fp16 -> h fp16 with the
+// gated activation; gate_up=false: h fp16 -> y fp32.
 struct GroupedGemmProblem {
     bool gate_up;
-    const uint16_t *act;        // xg (bf16) or h (fp16), [cap, K] in block order
-    const float *act_sum;       // [cap, act_sum_pitch]: xs (per group) or hs (per 64 cols)
-    int act_sum_pitch;
-    float *out_sum;             // gate_up: hs [cap, out_sum_pitch]; down: unused
-    int out_sum_pitch;
+    const uint16_t *act;        // xg or h, [cap, K] fp16 in block order
     const uint8_t *wq;          // [E, R, K/2]
     const uint16_t *ws, *wz;    // [E, R, K/group]
     const int32_t *sorted_ids;  // [cap]

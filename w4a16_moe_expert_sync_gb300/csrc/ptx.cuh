@@ -81,26 +81,41 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // within `limit_ns`, or when another role of the CTA has already aborted.
 // Each try suspends the thread for up to 20 us; between tries the abort
 // flag and the clock are checked.
+// Suspend-time hint of a retried try_wait, in ns.
+#ifndef W4_WAIT_HINT_NS
+#define W4_WAIT_HINT_NS 20000u
+#endif
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           int32_t *dev_status, int32_t timeout_bit,
                                           uint64_t limit_ns = 1000000000ull)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    uint64_t t0 = 0;
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u))
+    // Every retry is one suspending try_wait and a branch; the abort flag and
+    // the clock are looked at on every 16th retry only, so waiting warps take
+    // few issue slots from the working ones.
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+#ifdef W4_WAIT_NOHINT
+        if (mbar_try_wait(bar, parity))
             return true;
-        if (*abort_flag)
-            return false;
-        const uint64_t now = global_timer_ns();
-        if (t0 == 0) {
-            t0 = now;
-        } else if (now - t0 > limit_ns) {
-            *abort_flag = 1;
-            if (dev_status)
-                atomicOr(dev_status, timeout_bit);
-            return false;
+#else
+        if (mbar_try_wait_sleep(bar, parity, W4_WAIT_HINT_NS))
+            return true;
+#endif
+#ifdef W4_WAIT_BACKOFF_NS
+        __nanosleep(W4_WAIT_BACKOFF_NS);
+#endif
+        if ((it & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                if (dev_status)
+                    atomicOr(dev_status, timeout_bit);
+                return false;
+            }
         }
     }
 }

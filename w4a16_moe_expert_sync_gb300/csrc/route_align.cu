@@ -21,9 +21,8 @@
 //
 // Activation gather: the grouped gate_up GEMM reads its activations in slot
 // order, xg[slot] = x[token of slot] converted to fp16 in the GEMMs'
-// contraction order (korder.cuh), with the fp32 sum of every quantisation
-// group of the converted row, zero rows for padding slots.  The layer fuses
-// alignment and gather into one launch.
+// contraction order (korder.cuh), zero rows for padding slots.  The layer
+// fuses alignment and gather into one launch.
 #include <algorithm>
 #include <cfloat>
 
@@ -280,45 +279,25 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
                 dev_status, nullptr, &offs, &total);
 }
 
-// Sum over the `lpg` consecutive lanes (a power of two <= 16, aligned) that
-// hold one group; lane (l & ~(lpg-1)) ends with the sum of its group in the
-// fixed butterfly order.  All 32 lanes must take part.
-__device__ __forceinline__ float group_lane_sum(float v, int lpg)
-{
-    for (int o = lpg >> 1; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Standalone gather: for every slot below num_padded, xg[slot] = x[token of
-// slot] (fp16, block order) and xs[slot, g] = the fp32 sum of its group g;
-// zero for padding slots.  One lane per 8 elements, group/8 lanes per group.
+// Standalone gather: xg[slot] = x[token of slot] (fp16, block order), zero
+// for padding slots, for every slot below num_padded.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, int d, int k,
-                                                     int group, int A,
-                                                     const int32_t *__restrict__ sorted_ids,
+                                                     int A, const int32_t *__restrict__ sorted_ids,
                                                      const int32_t *__restrict__ num_padded,
-                                                     uint16_t *__restrict__ xg,
-                                                     float *__restrict__ xs)
+                                                     uint16_t *__restrict__ xg)
 {
-    const int c8n = d / 8, lpg = group / 8, pitch = sum_pitch(d, group);
+    const int c8n = d / 8;
     const int64_t total = static_cast<int64_t>(__ldg(num_padded)) * c8n;
-    const int64_t rounded = (total + 31) & ~static_cast<int64_t>(31);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < rounded;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const bool valid = i < total;
         const int64_t slot = i / c8n;
         const int c8 = static_cast<int>(i - slot * c8n);
-        const int a = valid ? __ldg(sorted_ids + slot) : -1;
-        uint4 v = make_uint4(0, 0, 0, 0);
+        const int a = __ldg(sorted_ids + slot);
+        uint4 o = make_uint4(0, 0, 0, 0);
         if (static_cast<unsigned>(a) < static_cast<unsigned>(A))
-            v = bf16x8_to_f16_korder(__ldg(
+            o = bf16x8_to_f16_korder(__ldg(
                 reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(a / k) * d + 8 * c8)));
-        const float gsum = group_lane_sum(f16x8_sum(v), lpg);
-        if (valid) {
-            *reinterpret_cast<uint4 *>(xg + slot * d + 8 * c8) = v;
-            if ((c8 & (lpg - 1)) == 0)
-                xs[slot * pitch + c8 / lpg] = gsum;
-        }
+        *reinterpret_cast<uint4 *>(xg + slot * d + 8 * c8) = o;
     }
 }
 
@@ -326,15 +305,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
 // own shared memory, so no CTA waits for another; CTA 0 also writes the
 // alignment outputs.  CTA b then copies the rows of tokens
 // [b*tpc, (b+1)*tpc) to the slots of their k assignments (each x row is read
-// once), with their group sums, and zeroes the padding slots of experts
-// e = b, b + G, ...
+// once) and zeroes the padding slots of experts e = b, b + G, ...
 __global__ void __launch_bounds__(kAlignWarps * 32, 1)
     moe_align_gather_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int bm, int cap,
                             int32_t *__restrict__ sorted_ids, int32_t *__restrict__ block_expert,
                             int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
                             int32_t *__restrict__ dev_status, const uint16_t *__restrict__ x,
-                            int d, int group, uint16_t *__restrict__ xg, float *__restrict__ xs,
-                            int tpc)
+                            int d, uint16_t *__restrict__ xg, int tpc)
 {
     extern __shared__ int sm[];
     const int A = M * k;
@@ -343,29 +320,18 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
     align_block(ids, A, E, bm, cap, blockIdx.x == 0, sorted_ids, block_expert, offsets, num_padded,
                 dev_status, pos, &offs, &total);
     __syncthreads();
-    const int c8n = d / 8, lpg = group / 8, pitch = sum_pitch(d, group), G = d / group;
+    const int c8n = d / 8;
     const int t0 = blockIdx.x * tpc, t1 = min(M, t0 + tpc);
-    const int n = max(0, t1 - t0) * c8n;
-    const int rounded = (n + 31) & ~31;
-    for (int i = threadIdx.x; i < rounded; i += blockDim.x) {
-        const bool valid = i < n;
-        const int t = t0 + i / c8n;
-        const int c8 = i % c8n;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid)
-            v = bf16x8_to_f16_korder(
-                __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * d + 8 * c8)));
-        const float gsum = group_lane_sum(f16x8_sum(v), lpg);
-        if (valid) {
-            const uint4 o = v;
-            for (int j = 0; j < k; j++) {
-                const int slot = pos[t * k + j];
-                if (slot >= 0) {
-                    *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(slot) * d + 8 * c8) = o;
-                    if ((c8 & (lpg - 1)) == 0)
-                        xs[static_cast<int64_t>(slot) * pitch + c8 / lpg] = gsum;
-                }
-            }
+    const int64_t n = static_cast<int64_t>(max(0, t1 - t0)) * c8n;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int t = t0 + static_cast<int>(i / c8n);
+        const int c8 = static_cast<int>(i % c8n);
+        const uint4 o = bf16x8_to_f16_korder(
+            __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * d + 8 * c8)));
+        for (int j = 0; j < k; j++) {
+            const int slot = pos[t * k + j];
+            if (slot >= 0)
+                *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(slot) * d + 8 * c8) = o;
         }
     }
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
@@ -373,12 +339,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
         const int64_t m = static_cast<int64_t>(s1 - s0) * c8n;
         for (int64_t i = threadIdx.x; i < m; i += blockDim.x) {
             const int64_t slot = s0 + i / c8n;
-            const int c8 = static_cast<int>(i % c8n);
-            *reinterpret_cast<uint4 *>(xg + slot * d + 8 * c8) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(xg + slot * d + 8 * (i % c8n)) = make_uint4(0, 0, 0, 0);
         }
-        const int64_t mg = static_cast<int64_t>(s1 - s0) * G;
-        for (int64_t i = threadIdx.x; i < mg; i += blockDim.x)
-            xs[(s0 + i / G) * pitch + i % G] = 0.0f;
     }
 }
 
@@ -401,14 +363,14 @@ cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int group, int64_t cap,
+cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          float *xs, cudaStream_t stream)
+                          cudaStream_t stream)
 {
     const int64_t total = cap * (d / 8);
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 4096));
-    gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        x, d, k, group, M * k, sorted_ids, num_padded, xg, xs);
+    gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, d, k, M * k, sorted_ids,
+                                                                      num_padded, xg);
     return cudaGetLastError();
 }
 
@@ -420,8 +382,7 @@ size_t align_gather_smem_bytes(int M, int k, int E)
 cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
                                 int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                                 int32_t *num_padded, int32_t *dev_status, const uint16_t *x,
-                                int d, int group, uint16_t *xg, float *xs, int num_sms,
-                                cudaStream_t stream)
+                                int d, uint16_t *xg, int num_sms, cudaStream_t stream)
 {
     const size_t smem = align_gather_smem_bytes(M, k, E);
     cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel));
@@ -432,7 +393,7 @@ cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int blo
     const int tpc = (M + grid - 1) / grid;
     moe_align_gather_kernel<<<grid, kAlignWarps * 32, smem, stream>>>(
         ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids, block_expert, offsets,
-        num_padded, dev_status, x, d, group, xg, xs, tpc);
+        num_padded, dev_status, x, d, xg, tpc);
     return cudaGetLastError();
 }
 
