@@ -253,22 +253,16 @@ __device__ __forceinline__ float gelu_tanh(float v)
     return 0.5f * v * (1.0f + tanhf(c * (v + 0.044715f * v * v * v)));
 }
 
-// A bounded wait for a whole warp: lane 0 polls, the warp follows its
-// outcome, and on success every lane observes the completed phase once
-// itself (a single try_wait that succeeds) so each lane acquires the data.
+// A bounded wait by every lane of a warp (each lane observes the phase
+// itself, which gives it acquire ordering); the vote keeps the warp's
+// control flow uniform if the wait ever times out.
 __device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity, int lane,
                                               volatile int *abort_flag, int32_t *status)
 {
-    int ok = 1;
-    if (lane == 0) {
-        ok = mbar_wait(bar, parity, abort_flag, status, kDevPipelineTimeout) ? 1 : 0;
-        if (!ok)
-            W4_TIMEOUT_RECORD(bar, parity, status);
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok)
-        mbar_try_wait(bar, parity);
-    return ok != 0;
+    const bool ok = mbar_wait(bar, parity, abort_flag, status, kDevPipelineTimeout);
+    if (!ok && lane == 0)
+        W4_TIMEOUT_RECORD(bar, parity, status);
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -393,9 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (lane == 0) {
             const int me = warp;
             const uint32_t b_base = smem_u32(stage_b);
-            // this issuer's sub-chunks per unit: j = me, me + 4, ... < n_sub
-            const uint32_t m_i = static_cast<uint32_t>(p.n_sub - me + kIssuers - 1) / kIssuers;
             uint32_t b_seq = 0, n_unit = 0;
+            uint32_t kcount = 0;    // sub-chunks this issuer has taken, all units
             int n_tr = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -423,27 +416,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint32_t b_slot = b_base + sb * kStageBBytes;
                     const int j0 = t * (kb_cap / kSubK);
                     const int j1 = min(p.n_sub, j0 + kb_cap / kSubK);
-                    // my sub-chunks in this slot: j = me (mod kIssuers)
+                    // my sub-chunks in this slot: j = me (mod kIssuers); sub-chunk
+                    // j - j0 of the slot is its (j - j0)-th 64-wide column block
                     for (int j = j0 + ((me - j0) % kIssuers + kIssuers) % kIssuers; j < j1;
                          j += kIssuers) {
-                        const uint32_t k = n_unit * m_i + (j >> 2);   // my sub-chunk count
-                        const int buf = me + kIssuers * (k & 1);
-                        if (!lane_wait(&bar.a_full[buf], (k >> 1) & 1, abort_flag, status)) {
+                        const int buf = me + kIssuers * (kcount & 1);
+                        if (!lane_wait(&bar.a_full[buf], (kcount >> 1) & 1, abort_flag, status)) {
                             ok = false;
                             break;
                         }
+                        ++kcount;
                         tc_fence_after();
                         if (me == 0)
                             W4_TRACE_POINT(5, n_tr);
-#pragma unroll
-                        for (int k = 0; k < kSubK / 16; k++) {
-                            const int kl = (j - j0) * kSubK + k * 16;   // K offset in the slot
-                            const uint32_t baddr = b_slot + (kl >> 6) * col_bytes +
-                                                   ((kl & 63) >> 4) * 32;
-                            tc_mma_ts(d_tmem, tmem + buf * 32 + k * 8, sdesc_sw128(baddr), idesc,
-                                      first ? 0u : 1u);
-                            first = false;
-                        }
+                        const uint64_t bdesc =
+                            sdesc_sw128(b_slot + static_cast<uint32_t>(j - j0) * col_bytes);
+                        const uint32_t a_tmem = tmem + buf * 32;
+                        // K steps of 16: +32 B in the swizzled row (+2 in the
+                        // descriptor's address field), +8 columns of A
+                        tc_mma_ts(d_tmem, a_tmem, bdesc, idesc, first ? 0u : 1u);
+                        tc_mma_ts(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1u);
+                        tc_mma_ts(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1u);
+                        tc_mma_ts(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1u);
+                        first = false;
                         tc_commit(&bar.a_empty[buf]);
                         if (me == 0)
                             W4_TRACE_POINT(6, n_tr);
@@ -571,9 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int sub = (warp - kFirstDqWarp) >> 2;
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        const uint32_t m_i = static_cast<uint32_t>(p.n_sub - sub + kIssuers - 1) / kIssuers;
         int sa = 0, szb = 0, n_tr = 0;
         uint32_t ph_a = 0, ph_sz = 0, n_unit = 0;
+        uint32_t kcount = 0;    // sub-chunks this warp has written, all units
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
             if (!warp_all_wait(&bar.sz_full[szb], ph_sz, lane, abort_flag, status))
@@ -608,13 +603,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 if (!mine)
                     continue;
-                const uint32_t k = n_unit * m_i + kc;         // this issuer's sub-chunk count
-                const int buf = sub + kIssuers * (k & 1);
-                if (!warp_all_wait(&bar.a_empty[buf], ((k >> 1) & 1) ^ 1, lane, abort_flag,
+                const int buf = sub + kIssuers * (kcount & 1);
+                if (!warp_all_wait(&bar.a_empty[buf], ((kcount >> 1) & 1) ^ 1, lane, abort_flag,
                                    status)) {
                     ok = false;
                     break;
                 }
+                ++kcount;
                 if (warp == kFirstDqWarp && lane == 0)
                     W4_TRACE_POINT(4, n_tr);
                 tc_fence_after();
