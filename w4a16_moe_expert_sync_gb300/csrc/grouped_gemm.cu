@@ -130,7 +130,7 @@ constexpr int kWarpTmaB = 25;
 constexpr int kNumWarps = 26;
 constexpr int kThreads = 32 * kNumWarps;
 constexpr int kStagesW = 5;                 // packed-code stages
-constexpr int kStagesB = 2;                 // activation slots
+constexpr int kStagesB = 3;                 // activation slots
 constexpr int kStagesSZ = 3;                // per-unit scales, zeros, group sums
 constexpr int kTileRows = 128;              // MMA M
 constexpr int kChunkK = 256;                // codes per row per stage
@@ -151,7 +151,7 @@ struct GemmArgs {
     const int32_t *expert_offsets;
     void *out;
     int32_t *dev_status;
-    int E, A, K, R, m_up, out_cols, group, G, n_panels, n_kchunks, n_sub;
+    int E, A, K, R, m_up, out_cols, group, group_shift, G, n_panels, n_kchunks, n_sub;
 };
 
 constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kSubBufs + 2 + 2 + 2 * kStagesSZ + kIssuers;
@@ -228,23 +228,50 @@ __host__ __device__ constexpr int b_kcols(int n) { return n == 16 ? 16 : 8; }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// 8 codes (one word, code i in bits 4i..4i+3) -> 4 words of fp16 pairs
-// q * s + c in the block order (q0,q4) (q1,q5) (q2,q6) (q3,q7).
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2, uint32_t *o)
+// (a & MASK) | magic in one LOP3, the mask an immediate and the magic
+// constant in a register (two immediates would cost a second LOP3).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t magic)
 {
-    constexpr uint32_t kMagic = 0x64006400u;               // fp16 1024.0 twice
-    const __half2 k1024 = u2h(kMagic);
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(magic));
+    return r;
+}
+
+// 8 codes (one word, code i in bits 4i..4i+3) -> 4 words of fp16 pairs
+// q * s + c in the block order (q0,q4) (q1,q5) (q2,q6) (q3,q7).  `magic` holds
+// fp16 1024.0 twice.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2, uint32_t magic,
+                                             uint32_t *o)
+{
+    const __half2 k1024 = u2h(magic);
     const __half2 kSixteenth = u2h(0x2C002C00u);           // 1/16
     const __half2 kMinus64 = u2h(0xD400D400u);             // -64
     const uint32_t w8 = w >> 8;
-    const __half2 q04 = __hsub2(u2h((w & 0x000F000Fu) | kMagic), k1024);
-    const __half2 q15 = __hfma2(u2h((w & 0x00F000F0u) | kMagic), kSixteenth, kMinus64);
-    const __half2 q26 = __hsub2(u2h((w8 & 0x000F000Fu) | kMagic), k1024);
-    const __half2 q37 = __hfma2(u2h((w8 & 0x00F000F0u) | kMagic), kSixteenth, kMinus64);
+    const __half2 q04 = __hsub2(u2h(and_or<0x000F000Fu>(w, magic)), k1024);
+    const __half2 q15 = __hfma2(u2h(and_or<0x00F000F0u>(w, magic)), kSixteenth, kMinus64);
+    const __half2 q26 = __hsub2(u2h(and_or<0x000F000Fu>(w8, magic)), k1024);
+    const __half2 q37 = __hfma2(u2h(and_or<0x00F000F0u>(w8, magic)), kSixteenth, kMinus64);
     o[0] = h2u(__hfma2(q04, s2, c2));
     o[1] = h2u(__hfma2(q15, s2, c2));
     o[2] = h2u(__hfma2(q26, s2, c2));
     o[3] = h2u(__hfma2(q37, s2, c2));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_half_as_float(uint32_t saddr)
+{
+    unsigned short h;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(saddr));
+    return __half2float(__ushort_as_half(h));
 }
 
 __device__ __forceinline__ float gelu_tanh(float v)
@@ -569,12 +596,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         int sa = 0, szb = 0, n_tr = 0;
         uint32_t ph_a = 0, ph_sz = 0, n_unit = 0;
         uint32_t kcount = 0;    // sub-chunks this warp has written, all units
+        const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
+        const uint32_t code_off0 = static_cast<uint32_t>(row * 128 + (((2 * sub) ^ (row & 7)) << 4));
+        const uint32_t code_off1 =
+            static_cast<uint32_t>(row * 128 + (((2 * sub + 1) ^ (row & 7)) << 4));
+        uint32_t magic;   // fp16 1024.0 twice, kept in a register
+        asm("mov.b32 %0, 0x64006400;" : "=r"(magic));
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
             if (!warp_all_wait(&bar.sz_full[szb], ph_sz, lane, abort_flag, status))
                 break;
-            const __half *s_row =
-                reinterpret_cast<const __half *>(sz_base + szb * L.sz_stride) + row * p.G;
+            const uint32_t s_addr = sz_base_s + szb * L.sz_stride + 2 * row * p.G;
             for (int kc = 0; kc < p.n_kchunks; kc++) {
                 if (!warp_all_wait(&bar.w_full[sa], ph_a, lane, abort_flag, status)) {
                     ok = false;
@@ -584,15 +616,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     W4_TRACE_POINT(2, n_tr);
                 const int j = kc * (kChunkK / kSubK) + sub;   // sub-chunk in unit
                 const bool mine = j < p.n_sub;
-                const uint8_t *rp = stage_w + sa * kStageWBytes + row * 128;
+                const uint32_t rp = stage_w_s + sa * kStageWBytes;
                 uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
                 float sf = 0.0f, zf = 0.0f;
                 if (mine) {
-                    w0 = *reinterpret_cast<const uint4 *>(rp + (((2 * sub) ^ (row & 7)) << 4));
-                    w1 = *reinterpret_cast<const uint4 *>(rp + (((2 * sub + 1) ^ (row & 7)) << 4));
-                    const int g = (j * kSubK) / p.group;
-                    sf = __half2float(s_row[g]);
-                    zf = __half2float(s_row[kTileRows * p.G + g]);
+                    w0 = lds128(rp + code_off0);
+                    w1 = lds128(rp + code_off1);
+                    const uint32_t g = static_cast<uint32_t>(j * kSubK) >> p.group_shift;
+                    sf = lds_half_as_float(s_addr + 2 * g);
+                    zf = lds_half_as_float(s_addr + 2 * (kTileRows * p.G + g));
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -616,14 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const __half2 s2 = __float2half2_rn(sf);
                 const __half2 c2 = __float2half2_rn(-zf * sf);
                 uint32_t o[32];
-                dequant_word(w0.x, s2, c2, &o[0]);
-                dequant_word(w0.y, s2, c2, &o[4]);
-                dequant_word(w0.z, s2, c2, &o[8]);
-                dequant_word(w0.w, s2, c2, &o[12]);
-                dequant_word(w1.x, s2, c2, &o[16]);
-                dequant_word(w1.y, s2, c2, &o[20]);
-                dequant_word(w1.z, s2, c2, &o[24]);
-                dequant_word(w1.w, s2, c2, &o[28]);
+                dequant_word(w0.x, s2, c2, magic, &o[0]);
+                dequant_word(w0.y, s2, c2, magic, &o[4]);
+                dequant_word(w0.z, s2, c2, magic, &o[8]);
+                dequant_word(w0.w, s2, c2, magic, &o[12]);
+                dequant_word(w1.x, s2, c2, magic, &o[16]);
+                dequant_word(w1.y, s2, c2, magic, &o[20]);
+                dequant_word(w1.z, s2, c2, magic, &o[24]);
+                dequant_word(w1.w, s2, c2, magic, &o[28]);
                 if (warp == kFirstDqWarp && lane == 0)
                     W4_TRACE_POINT(8, n_tr);
                 tmem_st_32x32b_x32(tmem + lane_base + buf * 32, o);
@@ -829,6 +861,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.m_up = q.gate_up ? q.R / 2 : 0;
     a.out_cols = q.out_cols;
     a.group = q.group;
+    a.group_shift = q.group == 128 ? 7 : 6;
     a.G = q.K / q.group;
     a.n_panels = q.gate_up ? (q.R / 2) / 64 : q.R / 128;
     a.n_kchunks = (q.K + kChunkK - 1) / kChunkK;
