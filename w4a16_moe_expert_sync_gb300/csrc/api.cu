@@ -277,10 +277,15 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int 
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "gate_up launch");
 }
 
-int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
-                         const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
-                         const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
-                         int32_t *dev_status, w4_stream_t stream)
+}  // extern "C"
+
+namespace {
+// early_schedule: see GroupedGemmProblem (set only by w4_moe_layer, where the
+// alignment is two launches back and gate_up waits for it before triggering)
+int grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
+                      const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
+                      const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
+                      int32_t *dev_status, w4_stream_t stream, bool early_schedule)
 {
     if (int rc = check_gemm_common(M, d, m, E, k, block_m, h, dn_q, dn_s, dn_z, sorted_ids,
                                    expert_offsets, y))
@@ -307,6 +312,7 @@ int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, i
     p.group = group;
     p.out_cols = d;
     p.cap = align_capacity(M, k, E, block_m);
+    p.early_schedule = early_schedule;
     if (M == 0)
         return W4_OK;
     const char *why = nullptr;
@@ -314,6 +320,18 @@ int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, i
     if (why)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "%s", why);
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "down launch");
+}
+}  // namespace
+
+extern "C" {
+
+int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
+                         const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
+                         const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
+                         int32_t *dev_status, w4_stream_t stream)
+{
+    return grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, group, sorted_ids,
+                             expert_offsets, y, dev_status, stream, false);
 }
 
 int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const float *topk_weights,
@@ -398,8 +416,8 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
                                      sorted, offs, h, dev_status, stream);
     if (rc)
         return rc;
-    rc = w4_grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs,
-                              y, dev_status, stream);
+    rc = grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs, y,
+                           dev_status, stream, true);
     if (rc)
         return rc;
     return w4_moe_combine_fixed_order(y, topk_ids, topk_weights, M, k, d, E, out, stream);

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace w4 {
 
@@ -19,6 +20,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const float *__restrict__ w, int M, int k,
                                                       int d, int E, uint16_t *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int d4 = d / 4;
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= static_cast<int64_t>(M) * d4)
@@ -26,17 +29,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     const int t = static_cast<int>(i / d4);
     const int c = static_cast<int>(i % d4) * 4;
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-    for (int j = 0; j < k; j++) {
-        const int64_t a = static_cast<int64_t>(t) * k + j;
-        const int e = __ldg(ids + a);
-        if (e < 0 || e >= E)
-            continue;
-        const float wj = __ldg(w + a);
-        const float4 v = __ldcs(reinterpret_cast<const float4 *>(y + a * d + c));
-        a0 = fmaf(wj, v.x, a0);
-        a1 = fmaf(wj, v.y, a1);
-        a2 = fmaf(wj, v.z, a2);
-        a3 = fmaf(wj, v.w, a3);
+    // eight assignments at a time: every load issued before the first FMA
+    // (each assignment's y row exists; an invalid expert id only drops its
+    // term), then the chain in assignment order
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        float4 v[8];
+        float wj[8];
+        bool ok[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int j = j0 + u;
+            ok[u] = false;
+            if (j < k) {
+                const int64_t a = static_cast<int64_t>(t) * k + j;
+                const int e = __ldg(ids + a);
+                ok[u] = e >= 0 && e < E;
+                wj[u] = __ldg(w + a);
+                v[u] = __ldcs(reinterpret_cast<const float4 *>(y + a * d + c));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            if (ok[u]) {
+                a0 = fmaf(wj[u], v[u].x, a0);
+                a1 = fmaf(wj[u], v[u].y, a1);
+                a2 = fmaf(wj[u], v[u].z, a2);
+                a3 = fmaf(wj[u], v[u].w, a3);
+            }
+        }
     }
     const __nv_bfloat162 lo = __floats2bfloat162_rn(a0, a1);
     const __nv_bfloat162 hi = __floats2bfloat162_rn(a2, a3);
@@ -54,9 +74,8 @@ cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, i
         return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (n + threads - 1) / threads;
-    combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(y, ids, w, M, k, d, E,
-                                                                          out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                      y, ids, w, M, k, d, E, out);
 }
 
 }  // namespace w4

@@ -135,12 +135,24 @@ constexpr int kStagesSZ = 3;                // per-unit scales, zeros, group sum
 constexpr int kTileRows = 128;              // MMA M
 constexpr int kChunkK = 256;                // codes per row per stage
 constexpr int kSubK = 64;                   // codes per A sub-chunk
-constexpr int kSubBufs = 8;                 // A ring in tensor memory
+constexpr int kMaxSubBufs = 12;             // A buffers in tensor memory (kIssuers x BUFS)
 constexpr int kStageWBytes = kTileRows * kChunkK / 2;   // 16 KB
 constexpr int kStageBBytes = 32768;
+constexpr int kResSlotBytes = kStagesB * kStageBBytes / 2;   // resident mode: 2 x 48 KB
 constexpr int kMaxN = 32;                   // slots per job
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 256;           // acc[set][i] at 256 + 128 set + 32 i
+// Tensor memory: A buffer b at column 32 b (b = issuer + kIssuers * slot), then
+// the accumulators acc[set][issuer] at acc_col<BUFS> + 128 set + 32 issuer.
+// BUFS = 3 A buffers per issuer leave room for one accumulator set, BUFS = 2
+// for two (the next unit's MMAs need not wait for the epilogue).
+template <int BUFS>
+__host__ __device__ constexpr int acc_sets() { return BUFS >= 3 ? 1 : 2; }
+template <int BUFS>
+__host__ __device__ constexpr uint32_t acc_col() { return 32u * kIssuers * BUFS; }
+static_assert(acc_col<3>() + 128u * acc_sets<3>() <= kTmemCols, "tensor memory budget");
+static_assert(acc_col<2>() + 128u * acc_sets<2>() <= kTmemCols, "tensor memory budget");
+constexpr int kBufsGateUp = 2;
+constexpr int kBufsDown = 2;
 
 struct GemmArgs {
     CUtensorMap tmap_w;       // packed codes u8 [E*R rows, K/2 B], box 128 B x 64 rows, SW128
@@ -152,9 +164,10 @@ struct GemmArgs {
     void *out;
     int32_t *dev_status;
     int E, A, K, R, m_up, out_cols, group, group_shift, G, n_panels, n_kchunks, n_sub;
+    int early_schedule;       // the schedule may be read before the grid-dependency wait
 };
 
-constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kSubBufs + 2 + 2 + 2 * kStagesSZ + kIssuers;
+constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kMaxSubBufs + 2 + 2 + 2 * kStagesSZ + kIssuers;
 
 struct Bars {
     uint64_t *w_full, *w_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty,
@@ -170,8 +183,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
     r.b_full = r.w_empty + kStagesW;
     r.b_empty = r.b_full + kStagesB;
     r.a_full = r.b_empty + kStagesB;
-    r.a_empty = r.a_full + kSubBufs;
-    r.acc_full = r.a_empty + kSubBufs;
+    r.a_empty = r.a_full + kMaxSubBufs;
+    r.acc_full = r.a_empty + kMaxSubBufs;
     r.acc_empty = r.acc_full + 2;
     r.sz_full = r.acc_empty + 2;
     r.sz_empty = r.sz_full + kStagesSZ;
@@ -224,6 +237,13 @@ __device__ __forceinline__ Job decode_job(const int *jp, const int *offs, int E,
 
 // 64-code column blocks per activation slot for a job of n slots (32 KB).
 __host__ __device__ constexpr int b_kcols(int n) { return n == 16 ? 16 : 8; }
+
+// Resident mode: the activation block of a full job (kMaxN slots x K) fits
+// one of two 48 KB slots and is loaded once per job, not once per unit.
+__host__ __device__ constexpr bool b_fits_resident(int K)
+{
+    return K / 64 <= 256 && static_cast<int64_t>(K) * 2 * kMaxN <= kResSlotBytes;
+}
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
@@ -321,9 +341,13 @@ __device__ __forceinline__ int tile_row(int q4, int lane)
         return 32 * q4 + lane;
 }
 
-template <bool GATE_UP>
+// RESIDENT: each job's activations are loaded once into one of two 48 KB
+// slots (contraction dim <= 768); otherwise they stream through 32 KB slots.
+template <bool GATE_UP, int BUFS, bool RESIDENT>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p)
 {
+    constexpr int kSets = acc_sets<BUFS>();
+    constexpr uint32_t kAccCol = acc_col<BUFS>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -351,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             mbar_init(&bar.b_full[i], 1);
             mbar_init(&bar.b_empty[i], kIssuers);
         }
-        for (int i = 0; i < kSubBufs; i++) {
+        for (int i = 0; i < kMaxSubBufs; i++) {
             mbar_init(&bar.a_full[i], 4);            // the four lane quarters
             mbar_init(&bar.a_empty[i], 1);           // the issuer's commit
         }
@@ -376,6 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         prefetch_tmap(&p.tmap_w);
         prefetch_tmap(&p.tmap_b[0]);
         prefetch_tmap(&p.tmap_b[1]);
+    }
+    // everything above touched only this CTA; from here on the inputs of the
+    // preceding kernels are read (the schedule possibly early, see GemmArgs)
+    if (!p.early_schedule) {
+        pdl_wait();
+        pdl_trigger();
     }
     for (int i = tid; i <= p.E; i += kThreads)
         offs[i] = __ldg(p.expert_offsets + i);
@@ -415,70 +445,109 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int me = warp;
             const uint32_t b_base = smem_u32(stage_b);
             uint32_t b_seq = 0, n_unit = 0;
-            uint32_t kcount = 0;    // sub-chunks this issuer has taken, all units
+            uint32_t a_slot = 0, a_ph = 0;   // this issuer's next A buffer and its phase
             int n_tr = 0;
+            int cur_job = -1;       // resident mode: the job whose activations are held
+            uint32_t res_slot = 0;
             bool ok = true;
+            // One 64-code sub-chunk: wait for its A buffer, four K=16 MMAs, and
+            // hand the buffer back when they complete.
+            auto issue = [&](uint32_t d_tmem, uint64_t bdesc, uint32_t idesc, bool first) -> bool {
+                const int buf = me + kIssuers * a_slot;
+                if (!lane_wait(&bar.a_full[buf], a_ph, abort_flag, status))
+                    return false;
+                if (++a_slot == BUFS) {
+                    a_slot = 0;
+                    a_ph ^= 1;
+                }
+                tc_fence_after();
+                if (me == 0)
+                    W4_TRACE_POINT(5, n_tr);
+                const uint32_t a_tmem = tmem + buf * 32;
+                // K steps of 16: +32 B in the swizzled row (+2 in the
+                // descriptor's address field), +8 columns of A
+                tc_mma_ts(d_tmem, a_tmem, bdesc, idesc, first ? 0u : 1u);
+                tc_mma_ts(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1u);
+                tc_mma_ts(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1u);
+                tc_mma_ts(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1u);
+                tc_commit(&bar.a_empty[buf]);
+                if (me == 0)
+                    W4_TRACE_POINT(6, n_tr);
+                n_tr++;
+                return true;
+            };
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
-                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                const int job = u / p.n_panels;
+                const Job J = decode_job(jp, offs, p.E, job);
                 const uint32_t idesc = idesc_f16_f32(kTileRows, J.n);
-                const int kb_cap = 64 * b_kcols(J.n);
-                const int n_bslots = (K + kb_cap - 1) / kb_cap;
                 const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
-                const int set = n_unit & 1;
-                if (!lane_wait(&bar.acc_empty[set], ((n_unit >> 1) & 1) ^ 1, abort_flag, status)) {
+                const int set = kSets == 1 ? 0 : (n_unit & 1);
+                const uint32_t acc_ph = (kSets == 1 ? n_unit : n_unit >> 1) & 1;
+                if (!lane_wait(&bar.acc_empty[set], acc_ph ^ 1, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + kAccCol + set * 128 + me * 32;
-                bool first = true;
-                for (int t = 0; t < n_bslots && ok; t++) {
-                    const int sb = (b_seq + t) % kStagesB;
-                    if (!lane_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, abort_flag,
-                                   status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t b_slot = b_base + sb * kStageBBytes;
-                    const int j0 = t * (kb_cap / kSubK);
-                    const int j1 = min(p.n_sub, j0 + kb_cap / kSubK);
-                    // my sub-chunks in this slot: j = me (mod kIssuers); sub-chunk
-                    // j - j0 of the slot is its (j - j0)-th 64-wide column block
-                    for (int j = j0 + ((me - j0) % kIssuers + kIssuers) % kIssuers; j < j1;
-                         j += kIssuers) {
-                        const int buf = me + kIssuers * (kcount & 1);
-                        if (!lane_wait(&bar.a_full[buf], (kcount >> 1) & 1, abort_flag, status)) {
+                if constexpr (RESIDENT) {
+                    // the job's activations stay in one slot for all its units
+                    if (job != cur_job) {
+                        if (cur_job >= 0)
+                            tc_commit(&bar.b_empty[res_slot]);
+                        res_slot = b_seq & 1;
+                        if (!lane_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, abort_flag,
+                                       status)) {
                             ok = false;
                             break;
                         }
-                        ++kcount;
                         tc_fence_after();
-                        if (me == 0)
-                            W4_TRACE_POINT(5, n_tr);
-                        const uint64_t bdesc =
-                            sdesc_sw128(b_slot + static_cast<uint32_t>(j - j0) * col_bytes);
-                        const uint32_t a_tmem = tmem + buf * 32;
-                        // K steps of 16: +32 B in the swizzled row (+2 in the
-                        // descriptor's address field), +8 columns of A
-                        tc_mma_ts(d_tmem, a_tmem, bdesc, idesc, first ? 0u : 1u);
-                        tc_mma_ts(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1u);
-                        tc_mma_ts(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1u);
-                        tc_mma_ts(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1u);
-                        first = false;
-                        tc_commit(&bar.a_empty[buf]);
-                        if (me == 0)
-                            W4_TRACE_POINT(6, n_tr);
-                        n_tr++;
+                        b_seq++;
+                        cur_job = job;
                     }
-                    if (!ok)
-                        break;
-                    tc_commit(&bar.b_empty[sb]);
+                    const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
+                    for (int j = me; j < p.n_sub; j += kIssuers) {
+                        if (!issue(d_tmem, sdesc_sw128(b_slot + static_cast<uint32_t>(j) * col_bytes),
+                                   idesc, j == me)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                } else {
+                    const int kb_cap = 64 * b_kcols(J.n);
+                    const int n_bslots = (K + kb_cap - 1) / kb_cap;
+                    bool first = true;
+                    for (int t = 0; t < n_bslots && ok; t++) {
+                        const int sb = (b_seq + t) % kStagesB;
+                        if (!lane_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, abort_flag,
+                                       status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t b_slot = b_base + sb * kStageBBytes;
+                        const int j0 = t * (kb_cap / kSubK);
+                        const int j1 = min(p.n_sub, j0 + kb_cap / kSubK);
+                        // my sub-chunks in this slot: j = me (mod kIssuers); sub-chunk
+                        // j - j0 of the slot is its (j - j0)-th 64-wide column block
+                        for (int j = j0 + ((me - j0) % kIssuers + kIssuers) % kIssuers; j < j1;
+                             j += kIssuers) {
+                            if (!issue(d_tmem,
+                                       sdesc_sw128(b_slot + static_cast<uint32_t>(j - j0) * col_bytes),
+                                       idesc, first)) {
+                                ok = false;
+                                break;
+                            }
+                            first = false;
+                        }
+                        if (!ok)
+                            break;
+                        tc_commit(&bar.b_empty[sb]);
+                    }
+                    b_seq += n_bslots;
                 }
                 if (!ok)
                     break;
                 tc_commit(&bar.acc_full[set]);
-                b_seq += n_bslots;
             }
             // every MMA of this thread completes before tensor memory is freed
             tc_commit(&bar.drain[me]);
@@ -551,30 +620,64 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
     } else if (warp == kWarpTmaB) {
         // --------------------------------------------------- TMA: activations
+        if (p.early_schedule && lane == 0) {
+            // the activations are the preceding kernel's output
+            pdl_wait();
+            pdl_trigger();
+        }
         if (lane == 0) {
             int sb = 0, n_tr = 0;
             uint32_t ph_b = 0, issued_b = 0, issue_ph_b = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
-                const CUtensorMap *map = &p.tmap_b[J.n / 16 - 1];
-                const int kcols = b_kcols(J.n);
-                const uint32_t bytes = static_cast<uint32_t>(J.n) * 128 * kcols;
-                for (int k_lo = 0; k_lo < K; k_lo += 64 * kcols) {
-                    if (!lane_wait(&bar.b_empty[sb], ph_b ^ 1, abort_flag, status)) {
+            if constexpr (RESIDENT) {
+                // one load per job into slot b_seq & 1, once the issuers have
+                // released that slot's previous job
+                int cur_job = -1;
+                uint32_t b_seq = 0;
+                for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                    const int job = u / p.n_panels;
+                    if (job == cur_job)
+                        continue;
+                    cur_job = job;
+                    const Job J = decode_job(jp, offs, p.E, job);
+                    const int s = b_seq & 1;
+                    const uint32_t ph = (b_seq >> 1) & 1;
+                    if (!lane_wait(&bar.b_empty[s], ph ^ 1, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     W4_TRACE_POINT(1, n_tr);
                     n_tr++;
-                    mbar_arrive_expect_tx(&bar.b_full[sb], bytes);
-                    tma_load_3d(stage_b + sb * kStageBBytes, map, 0, J.start, k_lo / 64,
-                                &bar.b_full[sb]);
-                    issued_b |= 1u << sb;
-                    issue_ph_b = (issue_ph_b & ~(1u << sb)) | (ph_b << sb);
-                    if (++sb == kStagesB) {
-                        sb = 0;
-                        ph_b ^= 1;
+                    mbar_arrive_expect_tx(&bar.b_full[s],
+                                          static_cast<uint32_t>(J.n) * 128 * p.n_sub);
+                    tma_load_3d(stage_b + s * kResSlotBytes, &p.tmap_b[J.n / 16 - 1], 0, J.start,
+                                0, &bar.b_full[s]);
+                    issued_b |= 1u << s;
+                    issue_ph_b = (issue_ph_b & ~(1u << s)) | (ph << s);
+                    b_seq++;
+                }
+            } else {
+                for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                    const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                    const CUtensorMap *map = &p.tmap_b[J.n / 16 - 1];
+                    const int kcols = b_kcols(J.n);
+                    const uint32_t bytes = static_cast<uint32_t>(J.n) * 128 * kcols;
+                    for (int k_lo = 0; k_lo < K; k_lo += 64 * kcols) {
+                        if (!lane_wait(&bar.b_empty[sb], ph_b ^ 1, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        W4_TRACE_POINT(1, n_tr);
+                        n_tr++;
+                        mbar_arrive_expect_tx(&bar.b_full[sb], bytes);
+                        tma_load_3d(stage_b + sb * kStageBBytes, map, 0, J.start, k_lo / 64,
+                                    &bar.b_full[sb]);
+                        issued_b |= 1u << sb;
+                        issue_ph_b = (issue_ph_b & ~(1u << sb)) | (ph_b << sb);
+                        if (++sb == kStagesB) {
+                            sb = 0;
+                            ph_b ^= 1;
+                        }
                     }
                 }
             }
@@ -595,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
         int sa = 0, szb = 0, n_tr = 0;
         uint32_t ph_a = 0, ph_sz = 0, n_unit = 0;
-        uint32_t kcount = 0;    // sub-chunks this warp has written, all units
+        uint32_t a_slot = 0, a_ph = 0;   // next A buffer of issuer `sub`, and its phase
         const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
         const uint32_t code_off0 = static_cast<uint32_t>(row * 128 + (((2 * sub) ^ (row & 7)) << 4));
         const uint32_t code_off1 =
@@ -635,13 +738,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 if (!mine)
                     continue;
-                const int buf = sub + kIssuers * (kcount & 1);
-                if (!warp_all_wait(&bar.a_empty[buf], ((kcount >> 1) & 1) ^ 1, lane, abort_flag,
-                                   status)) {
+                const int buf = sub + kIssuers * a_slot;
+                if (!warp_all_wait(&bar.a_empty[buf], a_ph ^ 1, lane, abort_flag, status)) {
                     ok = false;
                     break;
                 }
-                ++kcount;
+                if (++a_slot == BUFS) {
+                    a_slot = 0;
+                    a_ph ^= 1;
+                }
                 if (warp == kFirstDqWarp && lane == 0)
                     W4_TRACE_POINT(4, n_tr);
                 tc_fence_after();
@@ -693,23 +798,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, n_unit++) {
             const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
             const int pnl = u % p.n_panels;
-            const int set = n_unit & 1;
+            const int set = kSets == 1 ? 0 : (n_unit & 1);
+            const uint32_t acc_ph = (kSets == 1 ? n_unit : n_unit >> 1) & 1;
             // down: the assignment of every slot of the job, fetched early
             int my_a = -1;
             if constexpr (!GATE_UP)
                 my_a = lane < J.n ? __ldg(p.sorted_ids + J.start + lane) : -1;
-            if (!warp_all_wait(&bar.acc_full[set], (n_unit >> 1) & 1, lane, abort_flag, status))
+            if (!warp_all_wait(&bar.acc_full[set], acc_ph, lane, abort_flag, status))
                 break;
             if (warp == kFirstEpiWarp && lane == 0)
                 W4_TRACE_POINT(10, n_unit);
             tc_fence_after();
+            // Per block of 8 slots: the issuers' accumulators, added in a fixed
+            // order (issuers without a sub-chunk in this unit never wrote
+            // theirs), then the outputs.  The set goes back to the issuers as
+            // soon as its last block is in registers.
             const uint32_t acc = tmem + lane_base + kAccCol + set * 128;
+            const int n_blk = J.n / 8;
 #pragma unroll
             for (int b = 0; b < kMaxN / 8; b++) {
-                if (b * 8 >= J.n)
+                if (b >= n_blk)
                     break;
-                // the issuers' accumulators for 8 slots, added in a fixed order
-                // (issuers without a sub-chunk in this unit never wrote theirs)
                 float v[8];
                 {
                     uint32_t r[32];
@@ -726,6 +835,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                             t += __uint_as_float(r[24 + i]);
                         v[i] = t;
                     }
+                }
+                if (b == n_blk - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bar.acc_empty[set]);
                 }
                 if constexpr (GATE_UP) {
                     __half *hout = reinterpret_cast<__half *>(p.out);
@@ -751,11 +866,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                 }
             }
-            // the accumulator set is consumed: hand it back to the issuers
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bar.acc_empty[set]);
             if (warp == kFirstEpiWarp && lane == 0)
                 W4_TRACE_POINT(11, n_unit);
         }
@@ -791,7 +901,7 @@ EncodeTiledFn get_encode_fn()
 
 struct DeviceInfo {
     int sms = 0, smem_optin = 0;
-    bool attr_set[2] = {false, false};
+    bool attr_set[3] = {false, false, false};
 };
 
 DeviceInfo &device_info(int dev)
@@ -866,6 +976,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.n_panels = q.gate_up ? (q.R / 2) / 64 : q.R / 128;
     a.n_kchunks = (q.K + kChunkK - 1) / kChunkK;
     a.n_sub = q.K / kSubK;
+    a.early_schedule = q.early_schedule ? 1 : 0;
+    const bool resident = !q.gate_up && b_fits_resident(q.K);
 
     const SmemLayout L = smem_layout(a.G, a.E);
     const size_t smem = static_cast<size_t>(L.total) + 1024;
@@ -892,14 +1004,17 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     }
     for (int i = 0; i < 2; i++) {
         const int rows = 16 * (i + 1);
-        if (!encode_act(encode, &a.tmap_b[i], q.act, q.cap, q.K, rows, b_kcols(rows))) {
+        const int kcols = resident ? q.K / 64 : b_kcols(rows);
+        if (!encode_act(encode, &a.tmap_b[i], q.act, q.cap, q.K, rows, kcols)) {
             *why = "cuTensorMapEncodeTiled rejected the activation tensor";
             return cudaErrorInvalidValue;
         }
     }
 
-    auto kern = q.gate_up ? grouped_gemm_kernel<true> : grouped_gemm_kernel<false>;
-    const int which = q.gate_up ? 1 : 0;
+    auto kern = q.gate_up ? grouped_gemm_kernel<true, kBufsGateUp, false>
+                : resident ? grouped_gemm_kernel<false, kBufsDown, true>
+                           : grouped_gemm_kernel<false, kBufsDown, false>;
+    const int which = q.gate_up ? 2 : (resident ? 1 : 0);
     if (!di.attr_set[which]) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    di.smem_optin);
@@ -907,8 +1022,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
             return err;
         di.attr_set[which] = true;
     }
-    kern<<<di.sms, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(di.sms), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace w4

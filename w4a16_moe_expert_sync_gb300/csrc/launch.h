@@ -56,6 +56,12 @@ struct GroupedGemmProblem {
     int M, k, E, K, R, group;
     int out_cols;               // m (gate_up) or d (down)
     int64_t cap;
+    // true only when the kernel that wrote sorted_ids / expert_offsets is at
+    // least two launches back in the stream and the launch in between waits
+    // for it before triggering (the layer's align -> gate_up -> down order):
+    // down may then read its schedule, and stream its weights, before its
+    // grid-dependency wait.  Activations are read only after that wait.
+    bool early_schedule = false;
 };
 
 // Returns cudaSuccess, or an error; *why receives a static description when
@@ -66,5 +72,27 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &p, cudaStream_t stream
 // Records `detail` as the text w4_last_error_detail() returns on this thread
 // and passes `status` through.
 int set_error_detail(int status, const char *detail);
+
+// Launch `kern` as a programmatic dependent of the preceding kernel in the
+// stream.  Every kernel launched this way calls pdl_wait() before it reads
+// anything an earlier kernel wrote and pdl_trigger() only after that wait,
+// so at most two adjacent kernels of a stream overlap and, while the later
+// one runs ahead of its wait, every kernel before the earlier one is done.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 }  // namespace w4

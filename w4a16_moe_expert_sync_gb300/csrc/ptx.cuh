@@ -364,4 +364,15 @@ __device__ __forceinline__ void tmem_ld_4x_32x32b_x8(uint32_t t0, uint32_t t1, u
         : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait: block until the grid this one
+// depends on (the preceding kernel in the stream, when this kernel was
+// launched as its dependent) has completed and its writes are visible; a
+// no-op otherwise.  pdl_trigger: allow the next dependent kernel to start
+// launching; it still waits for this grid's completion in its own pdl_wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace w4

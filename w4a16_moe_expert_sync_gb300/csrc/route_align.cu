@@ -28,6 +28,7 @@
 
 #include "korder.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace w4 {
 
@@ -314,6 +315,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
                             int d, uint16_t *__restrict__ xg, int tpc)
 {
     extern __shared__ int sm[];
+    pdl_wait();
+    pdl_trigger();
     const int A = M * k;
     int *pos = sm + align_smem_bytes(E) / sizeof(int);   // [A]
     int *offs, *total;
@@ -391,10 +394,9 @@ cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int blo
     // about two tokens per CTA at the pages' canvas, at most one CTA per SM
     const int grid = std::max(1, std::min(num_sms, (M + 1) / 2));
     const int tpc = (M + grid - 1) / grid;
-    moe_align_gather_kernel<<<grid, kAlignWarps * 32, smem, stream>>>(
-        ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids, block_expert, offsets,
-        num_padded, dev_status, x, d, xg, tpc);
-    return cudaGetLastError();
+    return launch_pdl(moe_align_gather_kernel, dim3(grid), dim3(kAlignWarps * 32), smem, stream,
+                      ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids, block_expert,
+                      offsets, num_padded, dev_status, x, d, xg, tpc);
 }
 
 }  // namespace w4
