@@ -441,7 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     if (warp < kIssuers) {
         // ------------------------------------------------------- MMA issuers
-        if (lane == 0) {
+        // Each issuer warp runs this loop converged (every value in it is
+        // warp-uniform) and one elected lane issues each tcgen05 instruction,
+        // which costs the warp far fewer cycles than issuing from a lone lane.
+        {
             const int me = warp;
             const uint32_t b_base = smem_u32(stage_b);
             uint32_t b_seq = 0, n_unit = 0;
@@ -454,24 +457,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             // hand the buffer back when they complete.
             auto issue = [&](uint32_t d_tmem, uint64_t bdesc, uint32_t idesc, bool first) -> bool {
                 const int buf = me + kIssuers * a_slot;
-                if (!lane_wait(&bar.a_full[buf], a_ph, abort_flag, status))
+                if (!warp_all_wait(&bar.a_full[buf], a_ph, lane, abort_flag, status))
                     return false;
                 if (++a_slot == BUFS) {
                     a_slot = 0;
                     a_ph ^= 1;
                 }
                 tc_fence_after();
-                if (me == 0)
+                if (me == 0 && lane == 0)
                     W4_TRACE_POINT(5, n_tr);
                 const uint32_t a_tmem = tmem + buf * 32;
                 // K steps of 16: +32 B in the swizzled row (+2 in the
                 // descriptor's address field), +8 columns of A
-                tc_mma_ts(d_tmem, a_tmem, bdesc, idesc, first ? 0u : 1u);
-                tc_mma_ts(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1u);
-                tc_mma_ts(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1u);
-                tc_mma_ts(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1u);
-                tc_commit(&bar.a_empty[buf]);
-                if (me == 0)
+                tc_mma_ts_elect(d_tmem, a_tmem, bdesc, idesc, first ? 0u : 1u);
+                tc_mma_ts_elect(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1u);
+                tc_mma_ts_elect(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1u);
+                tc_mma_ts_elect(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1u);
+                tc_commit_elect(&bar.a_empty[buf]);
+                if (me == 0 && lane == 0)
                     W4_TRACE_POINT(6, n_tr);
                 n_tr++;
                 return true;
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
                 const int set = kSets == 1 ? 0 : (n_unit & 1);
                 const uint32_t acc_ph = (kSets == 1 ? n_unit : n_unit >> 1) & 1;
-                if (!lane_wait(&bar.acc_empty[set], acc_ph ^ 1, abort_flag, status)) {
+                if (!warp_all_wait(&bar.acc_empty[set], acc_ph ^ 1, lane, abort_flag, status)) {
                     ok = false;
                     break;
                 }
@@ -493,10 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     // the job's activations stay in one slot for all its units
                     if (job != cur_job) {
                         if (cur_job >= 0)
-                            tc_commit(&bar.b_empty[res_slot]);
+                            tc_commit_elect(&bar.b_empty[res_slot]);
                         res_slot = b_seq & 1;
-                        if (!lane_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, abort_flag,
-                                       status)) {
+                        if (!warp_all_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, lane, abort_flag, status)) {
                             ok = false;
                             break;
                         }
@@ -518,8 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     bool first = true;
                     for (int t = 0; t < n_bslots && ok; t++) {
                         const int sb = (b_seq + t) % kStagesB;
-                        if (!lane_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, abort_flag,
-                                       status)) {
+                        if (!warp_all_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, lane, abort_flag, status)) {
                             ok = false;
                             break;
                         }
@@ -541,16 +542,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         }
                         if (!ok)
                             break;
-                        tc_commit(&bar.b_empty[sb]);
+                        tc_commit_elect(&bar.b_empty[sb]);
                     }
                     b_seq += n_bslots;
                 }
                 if (!ok)
                     break;
-                tc_commit(&bar.acc_full[set]);
+                tc_commit_elect(&bar.acc_full[set]);
             }
-            // every MMA of this thread completes before tensor memory is freed
-            tc_commit(&bar.drain[me]);
+            // every MMA of this warp completes before tensor memory is freed
+            tc_commit_elect(&bar.drain[me]);
             drain_wait(&bar.drain[me], 0);
         }
         __syncwarp();

@@ -263,6 +263,32 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// The same MMA and commit issued by one elected lane of a converged warp.
+// With the whole warp on the same path its operands stay warp-uniform (in
+// uniform registers), which makes the issue several times cheaper than from a
+// lone lane in a divergent branch.
+__device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
 // Instruction descriptor for kind::f16: fp16 A and B (both K-major), fp32
 // accumulator, M = 128, N in [16, 256] step 16.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N)
@@ -346,6 +372,21 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 // Four loads of 8 columns each (at four TMEM addresses of this warp's lane
 // quarter) followed by one wait, so the four round trips overlap.
+// Two 32x32b.x8 loads (columns t0 .. t0+7 and t1 .. t1+7 of the warp's lane
+// quarter) into r[0..7] and r[8..15], then wait for both.
+__device__ __forceinline__ void tmem_ld_2x_32x32b_x8(uint32_t t0, uint32_t t1, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(t0), "r"(t1)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_4x_32x32b_x8(uint32_t t0, uint32_t t1, uint32_t t2,
                                                      uint32_t t3, uint32_t (&r)[32])
 {
