@@ -221,10 +221,10 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
     if (int rc = check_device())
         return rc;
     cudaError_t err;
-    if (w4::align_gather_smem_bytes(M, k, E) <= 200 * 1024) {
-        int dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (w4::align_gather_smem_bytes(M, k, E, sms) <= 200 * 1024) {
         err = w4::launch_align_gather(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
                                       expert_offsets, num_padded, dev_status, x, d, xg, sms,
                                       as_stream(stream));

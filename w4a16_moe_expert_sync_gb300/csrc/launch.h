@@ -21,7 +21,7 @@ cudaError_t launch_quantize(const float *W, int64_t rows, int K, int group, uint
 cudaError_t launch_route(const float *logits, int M, int E, int k, int32_t *ids, float *w,
                          cudaStream_t stream);
 
-__host__ __device__ size_t align_smem_bytes(int E);
+__host__ __device__ size_t align_smem_bytes(int E, int nw);
 cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
                          int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                          int32_t *num_padded, int32_t *dev_status, cudaStream_t stream);
@@ -33,7 +33,7 @@ cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
                           cudaStream_t stream);
 
 // Alignment and gather in one launch (every CTA aligns in shared memory).
-size_t align_gather_smem_bytes(int M, int k, int E);
+size_t align_gather_smem_bytes(int M, int k, int E, int num_sms);
 cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
                                 int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                                 int32_t *num_padded, int32_t *dev_status, const uint16_t *x,

@@ -120,6 +120,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// A pipeline wait for roles whose wake-up latency matters little (producers
+// running ahead, an epilogue waiting for a whole unit): between tries the
+// thread sleeps `backoff_ns`, so a waiting warp takes almost no issue slots
+// from the working warps of its sub-partition.  Same time limit and abort
+// handling as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_lazy(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               int32_t *dev_status, int32_t timeout_bit,
+                                               uint32_t backoff_ns,
+                                               uint64_t limit_ns = 1000000000ull)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(backoff_ns);
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                if (dev_status)
+                    atomicOr(dev_status, timeout_bit);
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ TMA / bulk
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
@@ -324,6 +354,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr)
 
 // 32 lanes x 32 columns of 32 bit: thread i of the warp writes lane
 // (warp quarter base + i), columns [col, col + 32).
+// 32 lanes x 16 columns of 32 bit (thread i: lane quarter base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(

@@ -10,14 +10,16 @@
 //
 // Alignment ("dg-w4-kernels" -- Grouped MoE: sync-free and CUDA-graph safe;
 // the grouped kernel "sorts assignments by expert, pads into regular
-// blocks"): a single CTA of 32 warps.  Warp w owns a contiguous range of flat
-// assignment indices.  Pass 1 builds one histogram per warp with
-// __match_any_sync (lanes that share an expert are counted by their group's
-// leader).  Pass 2 turns counts into padded expert offsets with a block scan
-// and into per-warp start positions.  Pass 3 re-walks the range and places
-// each assignment at its warp's running position plus its rank among earlier
-// lanes with the same expert, which keeps the order stable.  No global
-// atomics, no host round trip.
+// blocks"): one CTA computes it with its warps; warp w owns a contiguous
+// range of flat assignment indices (the expert ids staged in shared memory).
+// Pass 1 builds one histogram per warp: the lanes that share an expert are
+// found with one ballot per bit of the expert index and counted by their
+// group's leader.  Pass 2 turns counts into padded expert offsets with a
+// block scan and into per-warp start positions.  Pass 3 re-walks the range
+// and places each assignment at its warp's running position plus its rank
+// among earlier lanes with the same expert, which keeps the order stable.  No
+// global atomics, no host round trip.  The fused launch runs this in every
+// CTA, each writing a share of the outputs.
 //
 // Activation gather: the grouped gate_up GEMM reads its activations in slot
 // order, xg[slot] = x[token of slot] converted to fp16 in the GEMMs'
@@ -124,66 +126,95 @@ cudaError_t launch_route(const float *logits, int M, int E, int k, int32_t *ids,
 }
 
 // --------------------------------------------------------------- alignment
-constexpr int kAlignWarps = 32;
+constexpr int kAlignWarps = 32;     // the standalone alignment: one CTA of 1024 threads
 
-__host__ __device__ size_t align_smem_bytes(int E)
+__host__ __device__ size_t align_smem_bytes(int E, int nw)
 {
     // per-warp histograms, expert totals, offsets, warp partial sums
-    return sizeof(int) * (static_cast<size_t>(kAlignWarps) * E + E + (E + 1) + kAlignWarps);
+    return sizeof(int) * (static_cast<size_t>(nw) * E + E + (E + 1) + 32);
 }
 
-// The alignment computed by one CTA of 1024 threads.  With write_global the
-// CTA writes sorted_ids / block_expert / expert_offsets / num_padded and
-// reports invalid ids; with pos_sm it records the slot of every flat
-// assignment (or -1) in shared memory.  Returns through shared memory: the
-// padded offsets (offs_out[E+1]) and per-expert counts (total_out[E]).
+// Assignments whose expert ids the alignment stages in shared memory (one
+// coalesced load instead of one dependent load per pass and round).
+constexpr int kAlignStagedIds = 16384;
+
+// The lanes of the warp whose key equals this lane's, among the lanes with
+// `valid` set (meaningful for valid lanes), from one ballot per key bit: a
+// lane agrees with this one on bit b when the ballot of bit b has that lane
+// set exactly when this lane's own bit b is set.  Costs nbits + 1 ballots
+// whatever the number of distinct keys in the warp.
+__device__ __forceinline__ unsigned match_key(int key, int nbits, bool valid)
+{
+    const unsigned full = 0xffffffffu;
+    unsigned m = __ballot_sync(full, valid);
+    for (int b = 0; b < nbits; b++) {
+        const bool bit = (key >> b) & 1;
+        const unsigned bal = __ballot_sync(full, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
+// The alignment computed by one CTA of nw = blockDim.x / 32 warps, with
+// blockDim.x >= E.  Every CTA of the grid computes the whole alignment in its
+// own shared memory; the global outputs are split among the CTAs: a CTA
+// writes sorted_ids for the assignments [own0, own1), the grid's threads
+// split the padding slots and block owners one expert each, and CTA 0
+// writes expert_offsets and num_padded and reports invalid ids.  With pos_sm
+// the CTA also records the slot of each of its own assignments (or -1) at
+// pos_sm[a - own0].  Returns through shared memory the padded offsets
+// (offs_out[E+1]) and the per-expert counts (total_out[E]).
 __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int A, int E, int bm,
-                                            int cap, bool write_global,
+                                            int cap, int own0, int own1,
                                             int32_t *__restrict__ sorted_ids,
                                             int32_t *__restrict__ block_expert,
                                             int32_t *__restrict__ offsets,
                                             int32_t *__restrict__ num_padded,
                                             int32_t *__restrict__ dev_status, int *pos_sm,
-                                            int **offs_out, int **total_out)
+                                            int *ids_sm, int **offs_out, int **total_out)
 {
     extern __shared__ int sm[];
-    int *hist = sm;                          // [32][E]
-    int *total = hist + kAlignWarps * E;     // [E]
+    const int nw = blockDim.x >> 5;
+    int *hist = sm;                          // [nw][E]
+    int *total = hist + nw * E;              // [E]
     int *offs = total + E;                   // [E+1]
     int *wsum = offs + E + 1;                // [32]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned full = 0xffffffffu;
     const unsigned lt_mask = (1u << lane) - 1u;
+    const int nbits = 32 - __clz(max(E - 1, 1));   // bits of an expert index
 
-    for (int i = tid; i < kAlignWarps * E; i += blockDim.x)
+    // the ids, staged in shared memory when the caller gave room (ids_sm)
+    if (ids_sm)
+        for (int i = tid; i < A; i += blockDim.x)
+            ids_sm[i] = __ldg(ids + i);
+    auto id_at = [&](int a) { return ids_sm ? ids_sm[a] : __ldg(ids + a); };
+    for (int i = tid; i < nw * E; i += blockDim.x)
         hist[i] = 0;
     __syncthreads();
 
-    const int chunk = (A + kAlignWarps - 1) / kAlignWarps;
+    const int chunk = (A + nw - 1) / nw;
     const int a0 = min(A, warp * chunk), a1 = min(A, a0 + chunk);
     // pass 1: per-warp histogram
     bool bad = false;
-    {
-        for (int base = a0; base < a1; base += 32) {
-            const int a = base + lane;
-            const int e = a < a1 ? __ldg(ids + a) : -1;
-            const bool valid = a < a1 && e >= 0 && e < E;
-            bad |= (a < a1) && !valid;
-            const int key = valid ? e : E + lane;      // invalid lanes match nobody
-            const unsigned grp = __match_any_sync(full, key);
-            if (valid && lane == __ffs(grp) - 1)
-                hist[warp * E + e] += __popc(grp);
-            __syncwarp();
-        }
+    for (int base = a0; base < a1; base += 32) {
+        const int a = base + lane;
+        const int e = a < a1 ? id_at(a) : -1;
+        const bool valid = a < a1 && e >= 0 && e < E;
+        bad |= (a < a1) && !valid;
+        const unsigned grp = match_key(e, nbits, valid);
+        if (valid && lane == __ffs(grp) - 1)
+            hist[warp * E + e] += __popc(grp);
+        __syncwarp();
     }
-    if (write_global && __any_sync(full, bad) && lane == 0 && dev_status)
+    if (blockIdx.x == 0 && __any_sync(full, bad) && lane == 0 && dev_status)
         atomicOr(dev_status, kDevBadExpertId);
     __syncthreads();
 
     // pass 2: totals, padded sizes, exclusive scan over experts
     int padded = 0, cnt = 0;
     if (tid < E) {
-        for (int w = 0; w < kAlignWarps; w++)
+        for (int w = 0; w < nw; w++)
             cnt += hist[w * E + tid];
         padded = (cnt + bm - 1) / bm * bm;
         total[tid] = cnt;
@@ -199,14 +230,16 @@ __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int
         wsum[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        int s2 = wsum[lane];
+        const int own = lane < nw ? wsum[lane] : 0;
+        int s2 = own;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(full, s2, o);
             if (lane >= o)
                 s2 += v;
         }
-        wsum[lane] = s2 - wsum[lane];          // exclusive prefix of warp sums
+        if (lane < nw)
+            wsum[lane] = s2 - own;             // exclusive prefix of warp sums
     }
     __syncthreads();
     if (tid < E) {
@@ -215,7 +248,7 @@ __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int
         if (tid == E - 1)
             offs[E] = excl + padded;
         int run = excl;                        // per-warp start positions
-        for (int w = 0; w < kAlignWarps; w++) {
+        for (int w = 0; w < nw; w++) {
             const int c = hist[w * E + tid];
             hist[w * E + tid] = run;
             run += c;
@@ -224,46 +257,47 @@ __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int
     __syncthreads();
 
     // pass 3: stable placement
-    {
-        for (int base = a0; base < a1; base += 32) {
-            const int a = base + lane;
-            const int e = a < a1 ? __ldg(ids + a) : -1;
-            const bool valid = a < a1 && e >= 0 && e < E;
-            const int key = valid ? e : E + lane;
-            const unsigned grp = __match_any_sync(full, key);
-            int pos = 0;
-            if (valid)
-                pos = hist[warp * E + e] + __popc(grp & lt_mask);
-            __syncwarp();
-            if (valid && lane == __ffs(grp) - 1)
-                hist[warp * E + e] += __popc(grp);
-            __syncwarp();
-            if (a < a1) {
-                if (write_global && valid)
-                    sorted_ids[pos] = a;
-                if (pos_sm)
-                    pos_sm[a] = valid ? pos : -1;
-            }
+    for (int base = a0; base < a1; base += 32) {
+        const int a = base + lane;
+        const int e = a < a1 ? id_at(a) : -1;
+        const bool valid = a < a1 && e >= 0 && e < E;
+        const unsigned grp = match_key(e, nbits, valid);
+        int pos = 0;
+        if (valid)
+            pos = hist[warp * E + e] + __popc(grp & lt_mask);
+        __syncwarp();
+        if (valid && lane == __ffs(grp) - 1)
+            hist[warp * E + e] += __popc(grp);
+        __syncwarp();
+        if (a < a1 && a >= own0 && a < own1) {   // lanes past a1 are another warp's
+            if (sorted_ids && valid)
+                sorted_ids[pos] = a;
+            if (pos_sm)
+                pos_sm[a - own0] = valid ? pos : -1;
         }
     }
 
-    // pass 4: padding, block owners, offsets
-    if (write_global) {
-        if (tid < E) {
-            for (int sl = offs[tid] + total[tid]; sl < offs[tid + 1]; sl++)
+    // pass 4: padding slots, block owners, offsets (split among the grid's
+    // threads, one expert per thread)
+    if (sorted_ids) {
+        const int gtid = blockIdx.x * blockDim.x + tid, gstride = gridDim.x * blockDim.x;
+        for (int e = gtid; e < E; e += gstride) {
+            for (int sl = offs[e] + total[e]; sl < offs[e + 1]; sl++)
                 sorted_ids[sl] = A;
-            for (int b = offs[tid] / bm; b < offs[tid + 1] / bm; b++)
-                block_expert[b] = tid;
+            for (int b = offs[e] / bm; b < offs[e + 1] / bm; b++)
+                block_expert[b] = e;
         }
         const int npad = offs[E];
-        for (int sl = npad + tid; sl < cap; sl += blockDim.x)
+        for (int sl = npad + gtid; sl < cap; sl += gstride)
             sorted_ids[sl] = A;
-        for (int b = npad / bm + tid; b < cap / bm; b += blockDim.x)
+        for (int b = npad / bm + gtid; b < cap / bm; b += gstride)
             block_expert[b] = -1;
-        for (int i = tid; i <= E; i += blockDim.x)
-            offsets[i] = offs[i];
-        if (tid == 0)
-            num_padded[0] = npad;
+        if (blockIdx.x == 0) {
+            for (int i = tid; i <= E; i += blockDim.x)
+                offsets[i] = offs[i];
+            if (tid == 0)
+                num_padded[0] = npad;
+        }
     }
     *offs_out = offs;
     *total_out = total;
@@ -275,9 +309,12 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
                      int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
                      int32_t *__restrict__ dev_status)
 {
+    extern __shared__ int sm[];
+    int *ids_sm = A <= kAlignStagedIds ? sm + align_smem_bytes(E, kAlignWarps) / sizeof(int)
+                                       : nullptr;
     int *offs, *total;
-    align_block(ids, A, E, bm, cap, true, sorted_ids, block_expert, offsets, num_padded,
-                dev_status, nullptr, &offs, &total);
+    align_block(ids, A, E, bm, cap, 0, A, sorted_ids, block_expert, offsets, num_padded,
+                dev_status, nullptr, ids_sm, &offs, &total);
 }
 
 // Standalone gather: xg[slot] = x[token of slot] (fp16, block order), zero
@@ -302,12 +339,20 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
     }
 }
 
-// Fused alignment + gather.  Every CTA computes the (cheap) alignment in its
-// own shared memory, so no CTA waits for another; CTA 0 also writes the
-// alignment outputs.  CTA b then copies the rows of tokens
-// [b*tpc, (b+1)*tpc) to the slots of their k assignments (each x row is read
-// once) and zeroes the padding slots of experts e = b, b + G, ...
-__global__ void __launch_bounds__(kAlignWarps * 32, 1)
+// Fused alignment + gather.  Every CTA computes the alignment in its own
+// shared memory (so no CTA waits for another) and writes its share of the
+// alignment outputs.  CTA b copies the rows of tokens [b*tpc, (b+1)*tpc) to
+// the slots of their k assignments (each x row is read once; the first
+// kAheadTok x kAheadCols 16-byte chunks of a thread are loaded before the
+// alignment so that their latency overlaps it) and zeroes the padding slots
+// of experts b, b + G, ...
+constexpr int kAheadTok = 2, kAheadCols = 2;
+
+// 16 warps: the alignment is bound by its instruction count, which splits
+// evenly over the warps; fewer warps leave the SM idle, more add scan work.
+__host__ __device__ inline int align_gather_threads(int E) { return E <= 512 ? 512 : (E + 31) / 32 * 32; }
+
+__global__ void __launch_bounds__(1024, 1)
     moe_align_gather_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int bm, int cap,
                             int32_t *__restrict__ sorted_ids, int32_t *__restrict__ block_expert,
                             int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
@@ -318,32 +363,51 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
     pdl_wait();
     pdl_trigger();
     const int A = M * k;
-    int *pos = sm + align_smem_bytes(E) / sizeof(int);   // [A]
-    int *offs, *total;
-    align_block(ids, A, E, bm, cap, blockIdx.x == 0, sorted_ids, block_expert, offsets, num_padded,
-                dev_status, pos, &offs, &total);
-    __syncthreads();
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    int *pos = sm + align_smem_bytes(E, nthr >> 5) / sizeof(int);   // [tpc * k]
+    int *ids_sm = A <= kAlignStagedIds ? pos + tpc * k : nullptr;    // [A]
     const int c8n = d / 8;
-    const int t0 = blockIdx.x * tpc, t1 = min(M, t0 + tpc);
-    const int64_t n = static_cast<int64_t>(max(0, t1 - t0)) * c8n;
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int t = t0 + static_cast<int>(i / c8n);
-        const int c8 = static_cast<int>(i % c8n);
-        const uint4 o = bf16x8_to_f16_korder(
-            __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * d + 8 * c8)));
+    const int t0 = min(M, static_cast<int>(blockIdx.x) * tpc), t1 = min(M, t0 + tpc);
+    const int ntok = t1 - t0;
+    // chunk c8 of this CTA's token tl is xr[tl * c8n + c8]
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0) * d);
+    uint4 ahead[kAheadTok][kAheadCols];   // raw bf16: converted after the alignment
+#pragma unroll
+    for (int tl = 0; tl < kAheadTok; tl++)
+#pragma unroll
+        for (int r = 0; r < kAheadCols; r++) {
+            const int c8 = tid + r * nthr;
+            ahead[tl][r] = tl < ntok && c8 < c8n ? __ldg(xr + tl * c8n + c8) : make_uint4(0, 0, 0, 0);
+        }
+    int *offs, *total;
+    align_block(ids, A, E, bm, cap, t0 * k, t1 * k, sorted_ids, block_expert, offsets, num_padded,
+                dev_status, pos, ids_sm, &offs, &total);
+    __syncthreads();
+    auto put = [&](int tl, int c8, uint4 raw) {
+        const uint4 o = bf16x8_to_f16_korder(raw);
         for (int j = 0; j < k; j++) {
-            const int slot = pos[t * k + j];
+            const int slot = pos[tl * k + j];
             if (slot >= 0)
                 *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(slot) * d + 8 * c8) = o;
         }
-    }
+    };
+#pragma unroll
+    for (int tl = 0; tl < kAheadTok; tl++)
+#pragma unroll
+        for (int r = 0; r < kAheadCols; r++) {
+            const int c8 = tid + r * nthr;
+            if (tl < ntok && c8 < c8n)
+                put(tl, c8, ahead[tl][r]);
+        }
+    for (int tl = 0; tl < ntok; tl++)
+        for (int c8 = tid + (tl < kAheadTok ? kAheadCols * nthr : 0); c8 < c8n; c8 += nthr)
+            put(tl, c8, __ldg(xr + tl * c8n + c8));
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
         const int s0 = offs[e] + total[e], s1 = offs[e + 1];
-        const int64_t m = static_cast<int64_t>(s1 - s0) * c8n;
-        for (int64_t i = threadIdx.x; i < m; i += blockDim.x) {
-            const int64_t slot = s0 + i / c8n;
-            *reinterpret_cast<uint4 *>(xg + slot * d + 8 * (i % c8n)) = make_uint4(0, 0, 0, 0);
-        }
+        for (int sl = s0; sl < s1; sl++)
+            for (int c8 = tid; c8 < c8n; c8 += nthr)
+                *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(sl) * d + 8 * c8) =
+                    make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -356,7 +420,9 @@ cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, i
                          int32_t *sorted_ids, int32_t *block_expert, int32_t *offsets,
                          int32_t *num_padded, int32_t *dev_status, cudaStream_t stream)
 {
-    const size_t smem = align_smem_bytes(E);
+    const int A = M * k;
+    const size_t smem = align_smem_bytes(E, kAlignWarps) +
+                        (A <= kAlignStagedIds ? sizeof(int) * static_cast<size_t>(A) : 0);
     cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_kernel));
     if (err != cudaSuccess)
         return err;
@@ -377,9 +443,20 @@ cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
     return cudaGetLastError();
 }
 
-size_t align_gather_smem_bytes(int M, int k, int E)
+// one CTA per token (at most one per SM) and the tokens of a CTA contiguous
+static void align_gather_grid(int M, int num_sms, int *grid, int *tpc)
 {
-    return align_smem_bytes(E) + sizeof(int) * static_cast<size_t>(M) * k;
+    *grid = std::max(1, std::min(num_sms, M));
+    *tpc = (M + *grid - 1) / *grid;
+}
+
+size_t align_gather_smem_bytes(int M, int k, int E, int num_sms)
+{
+    int grid, tpc;
+    align_gather_grid(M, num_sms, &grid, &tpc);
+    const int64_t A = static_cast<int64_t>(M) * k;
+    return align_smem_bytes(E, align_gather_threads(E) / 32) +
+           sizeof(int) * (static_cast<size_t>(tpc) * k + (A <= kAlignStagedIds ? A : 0));
 }
 
 cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
@@ -387,16 +464,15 @@ cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int blo
                                 int32_t *num_padded, int32_t *dev_status, const uint16_t *x,
                                 int d, uint16_t *xg, int num_sms, cudaStream_t stream)
 {
-    const size_t smem = align_gather_smem_bytes(M, k, E);
+    const size_t smem = align_gather_smem_bytes(M, k, E, num_sms);
     cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel));
     if (err != cudaSuccess)
         return err;
-    // about two tokens per CTA at the pages' canvas, at most one CTA per SM
-    const int grid = std::max(1, std::min(num_sms, (M + 1) / 2));
-    const int tpc = (M + grid - 1) / grid;
-    return launch_pdl(moe_align_gather_kernel, dim3(grid), dim3(kAlignWarps * 32), smem, stream,
-                      ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids, block_expert,
-                      offsets, num_padded, dev_status, x, d, xg, tpc);
+    int grid, tpc;
+    align_gather_grid(M, num_sms, &grid, &tpc);
+    return launch_pdl(moe_align_gather_kernel, dim3(grid), dim3(align_gather_threads(E)), smem,
+                      stream, ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids,
+                      block_expert, offsets, num_padded, dev_status, x, d, xg, tpc);
 }
 
 }  // namespace w4
