@@ -306,10 +306,10 @@ __device__ __forceinline__ float gelu_tanh(float v)
 __device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity, int lane,
                                               volatile int *abort_flag, int32_t *status)
 {
-    const bool ok = mbar_wait(bar, parity, abort_flag, status, kDevPipelineTimeout);
+    const bool ok = mbar_wait_warp(bar, parity, abort_flag, status, kDevPipelineTimeout);
     if (!ok && lane == 0)
         W4_TIMEOUT_RECORD(bar, parity, status);
-    return __all_sync(0xffffffffu, ok);
+    return ok;
 }
 
 __device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -731,8 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     zf = lds_half_as_float(s_addr + 2 * (kTileRows * p.G + g));
                 }
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&bar.w_empty[sa]);
+                mbar_arrive_elect(&bar.w_empty[sa]);
                 if (++sa == kStagesW) {
                     sa = 0;
                     ph_a ^= 1;
@@ -770,8 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     W4_TRACE_POINT(14, n_tr);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&bar.a_full[buf]);
+                mbar_arrive_elect(&bar.a_full[buf]);
                 if (warp == kFirstDqWarp && lane == 0)
                     W4_TRACE_POINT(3, n_tr);
                 n_tr++;
@@ -779,8 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             if (!ok)
                 break;
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bar.sz_empty[szb]);
+            mbar_arrive_elect(&bar.sz_empty[szb]);
             if (++szb == kStagesSZ) {
                 szb = 0;
                 ph_sz ^= 1;
@@ -840,8 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 if (b == n_blk - 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&bar.acc_empty[set]);
+                    mbar_arrive_elect(&bar.acc_empty[set]);
                 }
                 if constexpr (GATE_UP) {
                     __half *hout = reinterpret_cast<__half *>(p.out);

@@ -120,6 +120,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// A pipeline wait by a whole warp with warp-uniform control flow: every lane
+// probes the phase (so every lane observes its completion) and one vote
+// decides each branch, so the loop needs no divergence handling.  Same time
+// limit and abort handling as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               int32_t *dev_status, int32_t timeout_bit,
+                                               uint64_t limit_ns = 1000000000ull)
+{
+    const unsigned full = 0xffffffffu;
+    if (__all_sync(full, mbar_try_wait(bar, parity)))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(full, mbar_try_wait_sleep(bar, parity, W4_WAIT_HINT_NS)))
+            return true;
+        if ((it & 15u) == 0) {
+            if (__any_sync(full, *abort_flag != 0))
+                return false;
+            if (__any_sync(full, global_timer_ns() - t0 > limit_ns)) {
+                if ((threadIdx.x & 31) == 0) {
+                    *abort_flag = 1;
+                    if (dev_status)
+                        atomicOr(dev_status, timeout_bit);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+// One arrival per warp, made by an elected lane without a branch (call with
+// the warp converged, after whatever the arrival must publish).
+__device__ __forceinline__ void mbar_arrive_elect(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 // A pipeline wait for roles whose wake-up latency matters little (producers
 // running ahead, an epilogue waiting for a whole unit): between tries the
 // thread sleeps `backoff_ns`, so a waiting warp takes almost no issue slots
