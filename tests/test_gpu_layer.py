@@ -110,3 +110,47 @@ def test_layer_with_no_tokens(lib):
     out = lib.w4_moe_layer(x, ids, w, gu, dn)
     torch.cuda.synchronize()
     assert out.shape == (0, cfg.d)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "layer256", "zipf256"])
+def test_layer_equals_the_separate_calls(lib, name):
+    """w4_moe_layer's out is bit-identical to align+gather, gate_up, down and
+    w4_moe_combine_fixed_order called one by one (its launches overlap at their
+    boundaries; the arithmetic and its order are the same), also from a dirty
+    workspace."""
+    import torch
+    cfg, x, lg, _, _ = gpu_inputs(name)
+    gu, dn = gpu_weights(name)
+    ids, w = lib.w4_moe_route(lg, cfg.k)
+    al, xg = lib.w4_moe_align_gather(ids, x, cfg.E, 16)
+    h = lib.w4_grouped_gemm_gate_up(xg, *gu, al)
+    y = lib.w4_grouped_gemm_down(h, *dn, al)
+    ref = lib.w4_moe_combine_fixed_order(y, ids, w, cfg.E)
+    ws = torch.full((lib.w4_moe_layer_workspace_size(cfg.M, cfg.d, cfg.m, cfg.E, cfg.k),),
+                    255, dtype=torch.uint8, device="cuda")
+    out = lib.w4_moe_layer(x, ids, w, gu, dn, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_layer_token_with_no_valid_expert_is_zero(lib):
+    """A token whose k ids are all invalid contributes to no expert: its output
+    row is exactly zero, the status flags the ids, other rows as separately."""
+    import torch
+    name = "tiny"
+    cfg, x, lg, _, logits = gpu_inputs(name)
+    gu, dn = gpu_weights(name)
+    oids, ow = oracle.route(logits, cfg.k)
+    bad = oids.copy()
+    bad[5, :] = -1
+    ids_d, w_d = torch.from_numpy(bad).cuda(), torch.from_numpy(ow).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = lib.w4_moe_layer(x, ids_d, w_d, gu, dn, dev_status=status)
+    al, xg = lib.w4_moe_align_gather(ids_d, x, cfg.E, 16)
+    h = lib.w4_grouped_gemm_gate_up(xg, *gu, al)
+    y = lib.w4_grouped_gemm_down(h, *dn, al)
+    ref = lib.w4_moe_combine_fixed_order(y, ids_d, w_d, cfg.E)
+    torch.cuda.synchronize()
+    assert int(status.item()) & lib.W4_DEV_BAD_EXPERT_ID
+    assert torch.count_nonzero(out[5].view(torch.int16)) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
