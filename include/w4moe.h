@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 3
+#define W4MOE_ABI_VERSION 4
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -159,15 +159,38 @@ int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int blo
 
 /* w4_moe_align_gather -- w4_moe_align and w4_gather_activations in one launch:
  * every CTA computes the alignment in its own shared memory (so no CTA waits
- * on another), CTA 0 writes the alignment outputs, and each CTA copies the
- * rows of a range of tokens to the slots of their assignments.  The first
- * launch of w4_moe_layer.  Arguments and outputs as in those two calls;
- * when the assignments do not fit in shared memory it issues them as two
- * launches. */
+ * on another) and writes a share of the alignment outputs, and each CTA
+ * copies the rows of a range of tokens to the slots of their assignments.
+ * The first launch of w4_moe_layer.  Arguments and outputs as in those two
+ * calls; when the assignments do not fit in shared memory it issues them as
+ * two launches. */
 int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d, int k, int E,
                         int block_m, int32_t *sorted_ids, int32_t *block_expert,
                         int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
                         int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_route_align_gather -- w4_moe_route, w4_moe_align and
+ * w4_gather_activations from the router logits.  For small batches it is one
+ * launch: every CTA routes every token (the same arithmetic as w4_moe_route,
+ * so topk_ids and topk_weights are bit-identical to it) into shared memory,
+ * computes the alignment there and gathers its own tokens' rows.  Routing
+ * every token in every CTA costs more than a second launch once the batch
+ * has more than a few tokens per warp, so beyond that the router runs as its
+ * own launch and w4_moe_align_gather follows it (same results).  The first
+ * step of w4_moe_layer_from_logits.
+ *
+ *   logits [M, E] fp32 in; topk_ids [M, k] int32 and topk_weights [M, k]
+ *   fp32 out, as w4_moe_route; the other arguments and outputs as
+ *   w4_moe_align_gather.
+ * One launch for E <= 128 and M <= 16; two launches otherwise.
+ * Requires what w4_moe_route and w4_moe_align_gather require.
+ * ------------------------------------------------------------------------ */
+int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int d, int k, int E,
+                              int block_m, int32_t *topk_ids, float *topk_weights,
+                              int32_t *sorted_ids, int32_t *block_expert,
+                              int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
+                              int32_t *dev_status, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * w4_grouped_gemm_gate_up -- grouped W4A16 gate_up GEMM with the gated
@@ -252,6 +275,22 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
                  const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
                  void *workspace, size_t workspace_bytes, uint16_t *out,
                  int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_layer_from_logits -- w4_moe_layer with the router in its first
+ * launch: from the router logits [M, E] fp32 instead of topk_ids and
+ * topk_weights, which it writes (caller-owned [M, k] int32 / fp32 outputs,
+ * as w4_moe_route) and then uses for the combine.  Same workspace as
+ * w4_moe_layer (w4_moe_layer_workspace_size); out is bit-identical to
+ * w4_moe_route followed by w4_moe_layer.
+ * ------------------------------------------------------------------------ */
+int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int d, int m, int E,
+                             int k, int block_m, const uint8_t *gu_q, const uint16_t *gu_s,
+                             const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
+                             const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
+                             void *workspace, size_t workspace_bytes, int32_t *topk_ids,
+                             float *topk_weights, uint16_t *out, int32_t *dev_status,
+                             w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * w4_moe_layer_static_scratch -- w4_moe_layer without a workspace argument.

@@ -82,3 +82,45 @@ def test_align_edge_cases(lib, case):
         ids = np.zeros((0, 8))
     _check_align(lib, ids, E, 16)
     _check_align(lib, ids, E, 64)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "sweep_M1", "sweep_M8", "sweep_M64",
+                                  "layer256", "zipf256", "canvas2048"])
+@pytest.mark.parametrize("bm", [16, 64])
+def test_route_align_gather_matches_the_separate_calls(lib, name, bm):
+    """Router + alignment + gather from the logits (one launch up to 16
+    tokens: tiny, sweep_M1; the router launch then the alignment launch
+    above that): ids and weights
+    bit-identical to w4_moe_route (and ids to the oracle), alignment outputs
+    and gathered rows bit-identical to w4_moe_align_gather."""
+    import torch
+    cfg = wl.CONFIGS[name]
+    logits = wl.router_logits(cfg)
+    x = _cuda(wl.activations(cfg).view(np.int16)).view(torch.bfloat16)
+    lg = _cuda(logits)
+    ids, w, al, xg = lib.w4_moe_route_align_gather(lg, x, cfg.k, bm)
+    rids, rw = lib.w4_moe_route(lg, cfg.k)
+    ral, rxg = lib.w4_moe_align_gather(rids, x, cfg.E, bm)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, rids)
+    assert torch.equal(w.view(torch.int32), rw.view(torch.int32))
+    oids, _ = oracle.route(logits, cfg.k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    for key in ("sorted_ids", "block_expert", "expert_offsets", "num_padded"):
+        assert torch.equal(al[key], ral[key])
+    npad = int(ral["num_padded"].item())
+    assert torch.equal(xg[:npad].view(torch.int16), rxg[:npad].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["ragged", "layer256"])
+def test_layer_from_logits_equals_route_then_layer(lib, name):
+    import torch
+    from helpers import gpu_inputs, gpu_weights
+    cfg, x, lg, _, _ = gpu_inputs(name)
+    gu, dn = gpu_weights(name)
+    out, ids, w = lib.w4_moe_layer_from_logits(x, lg, cfg.k, gu, dn)
+    rids, rw = lib.w4_moe_route(lg, cfg.k)
+    ref = lib.w4_moe_layer(x, rids, rw, gu, dn)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, rids)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

@@ -64,6 +64,8 @@ def load_library(path: str | None = None):
             "w4_moe_align": ([V, I, I, I, I, V, V, V, V, V, V], I),
             "w4_gather_activations": ([V, I, I, I, I, I, V, V, V, V], I),
             "w4_moe_align_gather": ([V, V, I, I, I, I, I, V, V, V, V, V, V, V], I),
+            "w4_moe_route_align_gather": ([V, V, I, I, I, I, I, V, V, V, V, V, V, V, V, V],
+                                          I),
             "w4_grouped_gemm_gate_up": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_grouped_gemm_down": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_moe_combine_fixed_order": ([V, V, V, I, I, I, I, V, V], I),
@@ -72,6 +74,8 @@ def load_library(path: str | None = None):
                               V], I),
             "w4_moe_layer_static_scratch": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I,
                                              V, V, V], I),
+            "w4_moe_layer_from_logits": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V,
+                                          SZ, V, V, V, V, V], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -303,6 +307,66 @@ def w4_moe_layer(x, topk_ids, topk_weights, gu, dn, block_m: int = 16, gu_group:
         _ptr(workspace), workspace.numel(), _ptr(out), _ptr(dev_status), _stream(stream)),
         "w4_moe_layer")
     return out
+
+
+def w4_moe_route_align_gather(logits, x, k: int, block_m: int = 16, dev_status=None, out=None,
+                              xg=None, ids=None, weights=None, stream=None):
+    """Router, alignment and activation gather in one launch, from the logits
+    [M, E] fp32.  Returns (topk_ids, topk_weights, align dict, xg)."""
+    import torch
+    _require_cuda(logits, x, dev_status, xg, ids, weights)
+    M, E = logits.shape
+    d = x.shape[1]
+    cap = w4_moe_align_capacity(M, k, E, block_m)
+    dev = x.device
+    if out is None:
+        out = dict(sorted_ids=torch.empty(cap, dtype=torch.int32, device=dev),
+                   block_expert=torch.empty(cap // block_m, dtype=torch.int32, device=dev),
+                   expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   num_padded=torch.empty(1, dtype=torch.int32, device=dev))
+    out.update(M=M, k=k, E=E, block_m=block_m)
+    if xg is None:
+        xg = torch.empty((cap, d), dtype=torch.float16, device=dev)
+    if ids is None:
+        ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((M, k), dtype=torch.float32, device=dev)
+    _check(load_library().w4_moe_route_align_gather(
+        _ptr(logits), _ptr(x), M, d, k, E, block_m, _ptr(ids), _ptr(weights),
+        _ptr(out["sorted_ids"]), _ptr(out["block_expert"]), _ptr(out["expert_offsets"]),
+        _ptr(out["num_padded"]), _ptr(xg), _ptr(dev_status), _stream(stream)),
+        "w4_moe_route_align_gather")
+    return ids, weights, out, xg
+
+
+def w4_moe_layer_from_logits(x, logits, k: int, gu, dn, block_m: int = 16, gu_group: int = 128,
+                             dn_group: int = 64, workspace=None, out=None, ids=None,
+                             weights=None, dev_status=None, stream=None):
+    """w4_moe_layer with the router in its first launch: from the logits
+    [M, E] fp32.  Returns (out, topk_ids, topk_weights)."""
+    import torch
+    gu_q, gu_s, gu_z = gu
+    dn_q, dn_s, dn_z = dn
+    _require_cuda(x, logits, gu_q, gu_s, gu_z, dn_q, dn_s, dn_z, workspace, out, ids, weights,
+                  dev_status)
+    M, d = x.shape
+    E, two_m, _ = gu_q.shape
+    m = two_m // 2
+    need = w4_moe_layer_workspace_size(M, d, m, E, k, block_m)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
+    if ids is None:
+        ids = torch.empty((M, k), dtype=torch.int32, device=x.device)
+    if weights is None:
+        weights = torch.empty((M, k), dtype=torch.float32, device=x.device)
+    _check(load_library().w4_moe_layer_from_logits(
+        _ptr(x), _ptr(logits), M, d, m, E, k, block_m, _ptr(gu_q), _ptr(gu_s), _ptr(gu_z),
+        gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), dn_group, _ptr(workspace),
+        workspace.numel(), _ptr(ids), _ptr(weights), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "w4_moe_layer_from_logits")
+    return out, ids, weights
 
 
 def w4_moe_layer_static_scratch(x, topk_ids, topk_weights, gu, dn, out, block_m: int = 16,

@@ -238,6 +238,48 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "align+gather launch");
 }
 
+int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int d, int k, int E,
+                              int block_m, int32_t *topk_ids, float *topk_weights,
+                              int32_t *sorted_ids, int32_t *block_expert,
+                              int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
+                              int32_t *dev_status, w4_stream_t stream)
+{
+    if (!topk_ids || !topk_weights || (M > 0 && !logits))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (k > 32 || k > E || E > 1024)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need 1 <= k <= 32, k <= E <= 1024");
+    if (!aligned4(logits) || !aligned4(topk_ids) || !aligned4(topk_weights))
+        return fail(W4_ERR_MISALIGNED, "logits, ids and weights must be 4-byte aligned");
+    if (!sorted_ids || !block_expert || !expert_offsets || !num_padded || !xg ||
+        (M > 0 && !x))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || d <= 0 || k <= 0 || E <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (d % 8)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need d %% 8 == 0");
+    if (!aligned16(x) || !aligned16(xg))
+        return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
+    if (int rc = check_device())
+        return rc;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (M > 0 && w4::route_align_gather_fits(M, k, E, sms)) {
+        const int64_t cap = align_capacity(M, k, E, block_m);
+        cudaError_t err = w4::launch_route_align_gather(
+            logits, M, k, E, block_m, cap, topk_ids, topk_weights, sorted_ids, block_expert,
+            expert_offsets, num_padded, dev_status, x, d, xg, sms, as_stream(stream));
+        return err == cudaSuccess ? W4_OK : cuda_fail(err, "route+align+gather launch");
+    }
+    // larger shapes: the router launch, then the fused alignment and gather
+    if (int rc = w4_moe_route(logits, M, E, k, topk_ids, topk_weights, stream))
+        return rc;
+    return w4_moe_align_gather(topk_ids, x, M, d, k, E, block_m, sorted_ids, block_expert,
+                               expert_offsets, num_padded, xg, dev_status, stream);
+}
+
 int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
                             const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
                             int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
@@ -409,6 +451,49 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
     // alignment and the activation gather share one launch
     if (int rc0 = w4_moe_align_gather(topk_ids, x, M, d, k, E, block_m, sorted, block, offs, npad,
                                       xg, dev_status, stream))
+        return rc0;
+    if (M == 0)
+        return W4_OK;
+    int rc = w4_grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
+                                     sorted, offs, h, dev_status, stream);
+    if (rc)
+        return rc;
+    rc = grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs, y,
+                           dev_status, stream, true);
+    if (rc)
+        return rc;
+    return w4_moe_combine_fixed_order(y, topk_ids, topk_weights, M, k, d, E, out, stream);
+}
+
+int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int d, int m, int E,
+                             int k, int block_m, const uint8_t *gu_q, const uint16_t *gu_s,
+                             const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
+                             const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
+                             void *workspace, size_t workspace_bytes, int32_t *topk_ids,
+                             float *topk_weights, uint16_t *out, int32_t *dev_status,
+                             w4_stream_t stream)
+{
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (M < 0 || d <= 0 || m <= 0 || E <= 0 || k <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes");
+    const LayerWs L = layer_ws(M, d, m, E, k, block_m);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(W4_ERR_WORKSPACE, "workspace needs %zu bytes", L.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(W4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    int32_t *block = reinterpret_cast<int32_t *>(ws + L.block);
+    int32_t *offs = reinterpret_cast<int32_t *>(ws + L.offs);
+    int32_t *npad = reinterpret_cast<int32_t *>(ws + L.npad);
+    uint16_t *xg = reinterpret_cast<uint16_t *>(ws + L.xg);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    float *y = reinterpret_cast<float *>(ws + L.y);
+    // router, alignment and activation gather share one launch
+    if (int rc0 = w4_moe_route_align_gather(logits, x, M, d, k, E, block_m, topk_ids,
+                                            topk_weights, sorted, block, offs, npad, xg,
+                                            dev_status, stream))
         return rc0;
     if (M == 0)
         return W4_OK;

@@ -39,6 +39,17 @@ cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int blo
                                 int32_t *num_padded, int32_t *dev_status, const uint16_t *x,
                                 int d, uint16_t *xg, int num_sms, cudaStream_t stream);
 
+// Router + alignment + gather in one launch, from the logits: ids and w are
+// written as by launch_route.  Only for shapes route_align_gather_fits()
+// accepts (E <= 128, M <= 512); cudaErrorInvalidValue otherwise.
+bool route_align_gather_fits(int M, int k, int E, int num_sms);
+cudaError_t launch_route_align_gather(const float *logits, int M, int k, int E, int block_m,
+                                      int64_t cap, int32_t *ids, float *w, int32_t *sorted_ids,
+                                      int32_t *block_expert, int32_t *offsets,
+                                      int32_t *num_padded, int32_t *dev_status,
+                                      const uint16_t *x, int d, uint16_t *xg, int num_sms,
+                                      cudaStream_t stream);
+
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
                            int d, int E, uint16_t *out, cudaStream_t stream);
 

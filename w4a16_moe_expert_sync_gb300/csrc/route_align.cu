@@ -35,16 +35,14 @@
 namespace w4 {
 
 // ------------------------------------------------------------------ router
+// The router for one token, computed by one warp: the k largest logits by k
+// rounds of a warp arg-max (ties to the lower expert index), then softmax
+// over them.  Lane j < k returns the j-th choice in id/w; other lanes return
+// id -1, w 0.  EPL = logits per lane (E <= 32 EPL).
 template <int EPL>
-__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int M,
-                                                    int E, int k, int32_t *__restrict__ ids,
-                                                    float *__restrict__ weights)
+__device__ __forceinline__ void route_token(const float *__restrict__ row, int E, int k, int lane,
+                                            int *id, float *w)
 {
-    const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    if (t >= M)
-        return;
-    const int lane = threadIdx.x & 31;
-    const float *row = logits + static_cast<int64_t>(t) * E;
     float v[EPL];
     uint32_t taken = 0;
 #pragma unroll
@@ -55,7 +53,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
             taken |= 1u << i;
     }
     float my_val = 0.0f, top = 0.0f;
-    int my_idx = 0;
+    int my_idx = -1;
     for (int j = 0; j < k; j++) {
         float bv = -FLT_MAX;
         int be = 0x7fffffff;
@@ -94,9 +92,27 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
     float sum = 0.0f;
     for (int j = 0; j < k; j++)
         sum += __shfl_sync(0xffffffffu, ex, j);
+    *id = lane < k ? my_idx : -1;
+    *w = lane < k ? ex / sum : 0.0f;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int M,
+                                                    int E, int k, int32_t *__restrict__ ids,
+                                                    float *__restrict__ weights)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (t >= M)
+        return;
+    const int lane = threadIdx.x & 31;
+    int id;
+    float w;
+    route_token<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, &id, &w);
     if (lane < k) {
-        ids[static_cast<int64_t>(t) * k + lane] = my_idx;
-        weights[static_cast<int64_t>(t) * k + lane] = ex / sum;
+        ids[static_cast<int64_t>(t) * k + lane] = id;
+        weights[static_cast<int64_t>(t) * k + lane] = w;
     }
 }
 
@@ -108,21 +124,22 @@ cudaError_t launch_route(const float *logits, int M, int E, int k, int32_t *ids,
     const int wpb = 8;
     const dim3 grid((M + wpb - 1) / wpb), block(32 * wpb);
     const int epl = (E + 31) / 32;
+    cudaError_t err;
     if (epl <= 1)
-        route_kernel<1><<<grid, block, 0, stream>>>(logits, M, E, k, ids, w);
+        err = launch_pdl(route_kernel<1>, grid, block, 0, stream, logits, M, E, k, ids, w);
     else if (epl <= 2)
-        route_kernel<2><<<grid, block, 0, stream>>>(logits, M, E, k, ids, w);
+        err = launch_pdl(route_kernel<2>, grid, block, 0, stream, logits, M, E, k, ids, w);
     else if (epl <= 4)
-        route_kernel<4><<<grid, block, 0, stream>>>(logits, M, E, k, ids, w);
+        err = launch_pdl(route_kernel<4>, grid, block, 0, stream, logits, M, E, k, ids, w);
     else if (epl <= 8)
-        route_kernel<8><<<grid, block, 0, stream>>>(logits, M, E, k, ids, w);
+        err = launch_pdl(route_kernel<8>, grid, block, 0, stream, logits, M, E, k, ids, w);
     else if (epl <= 16)
-        route_kernel<16><<<grid, block, 0, stream>>>(logits, M, E, k, ids, w);
+        err = launch_pdl(route_kernel<16>, grid, block, 0, stream, logits, M, E, k, ids, w);
     else if (epl <= 32)
-        route_kernel<32><<<grid, block, 0, stream>>>(logits, M, E, k, ids, w);
+        err = launch_pdl(route_kernel<32>, grid, block, 0, stream, logits, M, E, k, ids, w);
     else
         return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    return err;
 }
 
 // --------------------------------------------------------------- alignment
@@ -184,8 +201,9 @@ __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int
     const unsigned lt_mask = (1u << lane) - 1u;
     const int nbits = 32 - __clz(max(E - 1, 1));   // bits of an expert index
 
-    // the ids, staged in shared memory when the caller gave room (ids_sm)
-    if (ids_sm)
+    // the ids, staged in shared memory when the caller gave room (ids_sm);
+    // with ids == nullptr the caller has already put them there
+    if (ids_sm && ids)
         for (int i = tid; i < A; i += blockDim.x)
             ids_sm[i] = __ldg(ids + i);
     auto id_at = [&](int a) { return ids_sm ? ids_sm[a] : __ldg(ids + a); };
@@ -339,7 +357,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
     }
 }
 
-// Fused alignment + gather.  Every CTA computes the alignment in its own
+// Fused alignment + gather (with ROUTE, router + alignment + gather from the
+// logits: every CTA routes every token into shared memory first, with the
+// same arithmetic as route_kernel, and writes ids and weights of its own
+// tokens).  Every CTA computes the alignment in its own
 // shared memory (so no CTA waits for another) and writes its share of the
 // alignment outputs.  CTA b copies the rows of tokens [b*tpc, (b+1)*tpc) to
 // the slots of their k assignments (each x row is read once; the first
@@ -352,12 +373,17 @@ constexpr int kAheadTok = 2, kAheadCols = 2;
 // evenly over the warps; fewer warps leave the SM idle, more add scan work.
 __host__ __device__ inline int align_gather_threads(int E) { return E <= 512 ? 512 : (E + 31) / 32 * 32; }
 
+constexpr int kRouteEpl = 4;    // the fused router: E <= 128
+
+template <bool ROUTE>
 __global__ void __launch_bounds__(1024, 1)
     moe_align_gather_kernel(const int32_t *__restrict__ ids, int M, int k, int E, int bm, int cap,
                             int32_t *__restrict__ sorted_ids, int32_t *__restrict__ block_expert,
                             int32_t *__restrict__ offsets, int32_t *__restrict__ num_padded,
                             int32_t *__restrict__ dev_status, const uint16_t *__restrict__ x,
-                            int d, uint16_t *__restrict__ xg, int tpc)
+                            int d, uint16_t *__restrict__ xg, int tpc,
+                            const float *__restrict__ logits, int32_t *__restrict__ ids_out,
+                            float *__restrict__ w_out)
 {
     extern __shared__ int sm[];
     pdl_wait();
@@ -379,9 +405,27 @@ __global__ void __launch_bounds__(1024, 1)
             const int c8 = tid + r * nthr;
             ahead[tl][r] = tl < ntok && c8 < c8n ? __ldg(xr + tl * c8n + c8) : make_uint4(0, 0, 0, 0);
         }
+    if constexpr (ROUTE) {
+        // every token's top-k into shared memory (ids_sm is always there on
+        // this path), this CTA's tokens also to ids_out / w_out
+        const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+        for (int t = warp; t < M; t += nw) {
+            int id;
+            float w;
+            route_token<kRouteEpl>(logits + static_cast<int64_t>(t) * E, E, k, lane, &id, &w);
+            if (lane < k) {
+                ids_sm[t * k + lane] = id;
+                if (t >= t0 && t < t1) {
+                    ids_out[static_cast<int64_t>(t) * k + lane] = id;
+                    w_out[static_cast<int64_t>(t) * k + lane] = w;
+                }
+            }
+        }
+        __syncthreads();
+    }
     int *offs, *total;
-    align_block(ids, A, E, bm, cap, t0 * k, t1 * k, sorted_ids, block_expert, offsets, num_padded,
-                dev_status, pos, ids_sm, &offs, &total);
+    align_block(ROUTE ? nullptr : ids, A, E, bm, cap, t0 * k, t1 * k, sorted_ids, block_expert,
+                offsets, num_padded, dev_status, pos, ids_sm, &offs, &total);
     __syncthreads();
     auto put = [&](int tl, int c8, uint4 raw) {
         const uint4 o = bf16x8_to_f16_korder(raw);
@@ -402,10 +446,13 @@ __global__ void __launch_bounds__(1024, 1)
     for (int tl = 0; tl < ntok; tl++)
         for (int c8 = tid + (tl < kAheadTok ? kAheadCols * nthr : 0); c8 < c8n; c8 += nthr)
             put(tl, c8, __ldg(xr + tl * c8n + c8));
-    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    // padding rows: row sl of the padded range belongs to CTA sl mod grid; the
+    // warps of a CTA take the experts in turn
+    const int G = gridDim.x, b = blockIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = warp; e < E; e += nthr >> 5) {
         const int s0 = offs[e] + total[e], s1 = offs[e + 1];
-        for (int sl = s0; sl < s1; sl++)
-            for (int c8 = tid; c8 < c8n; c8 += nthr)
+        for (int sl = s0 + (b - s0 % G + G) % G; sl < s1; sl += G)
+            for (int c8 = lane; c8 < c8n; c8 += 32)
                 *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(sl) * d + 8 * c8) =
                     make_uint4(0, 0, 0, 0);
     }
@@ -443,11 +490,12 @@ cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
     return cudaGetLastError();
 }
 
-// one CTA per token (at most one per SM) and the tokens of a CTA contiguous
+// one CTA per SM whatever the batch (the padding rows are spread over all of
+// them), the tokens of a CTA contiguous
 static void align_gather_grid(int M, int num_sms, int *grid, int *tpc)
 {
-    *grid = std::max(1, std::min(num_sms, M));
-    *tpc = (M + *grid - 1) / *grid;
+    *grid = std::max(1, num_sms);
+    *tpc = std::max(1, (M + *grid - 1) / *grid);
 }
 
 size_t align_gather_smem_bytes(int M, int k, int E, int num_sms)
@@ -465,14 +513,49 @@ cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int blo
                                 int d, uint16_t *xg, int num_sms, cudaStream_t stream)
 {
     const size_t smem = align_gather_smem_bytes(M, k, E, num_sms);
-    cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel));
+    cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel<false>));
     if (err != cudaSuccess)
         return err;
     int grid, tpc;
     align_gather_grid(M, num_sms, &grid, &tpc);
-    return launch_pdl(moe_align_gather_kernel, dim3(grid), dim3(align_gather_threads(E)), smem,
-                      stream, ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids,
-                      block_expert, offsets, num_padded, dev_status, x, d, xg, tpc);
+    return launch_pdl(moe_align_gather_kernel<false>, dim3(grid), dim3(align_gather_threads(E)),
+                      smem, stream, ids, M, k, E, block_m, static_cast<int>(cap), sorted_ids,
+                      block_expert, offsets, num_padded, dev_status, x, d, xg, tpc,
+                      static_cast<const float *>(nullptr), static_cast<int32_t *>(nullptr),
+                      static_cast<float *>(nullptr));
+}
+
+bool route_align_gather_fits(int M, int k, int E, int num_sms)
+{
+    // Every CTA routes every token, a warp per token, each a chain of k
+    // dependent warp reductions.  A separate router launch overlaps the
+    // alignment launch's start (programmatic dependent launch) and costs ~3 us
+    // more, which routing in the CTA exceeds beyond one token per warp
+    // (measured: 22.5 us against 17.4 us at 32 tokens, 26.8 against 15.3 at 64).
+    return E <= 32 * kRouteEpl && M <= align_gather_threads(E) / 32 &&
+           static_cast<int64_t>(M) * k <= kAlignStagedIds &&
+           align_gather_smem_bytes(M, k, E, num_sms) <= 200 * 1024;
+}
+
+cudaError_t launch_route_align_gather(const float *logits, int M, int k, int E, int block_m,
+                                      int64_t cap, int32_t *ids, float *w, int32_t *sorted_ids,
+                                      int32_t *block_expert, int32_t *offsets,
+                                      int32_t *num_padded, int32_t *dev_status,
+                                      const uint16_t *x, int d, uint16_t *xg, int num_sms,
+                                      cudaStream_t stream)
+{
+    if (!route_align_gather_fits(M, k, E, num_sms))
+        return cudaErrorInvalidValue;
+    const size_t smem = align_gather_smem_bytes(M, k, E, num_sms);
+    cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel<true>));
+    if (err != cudaSuccess)
+        return err;
+    int grid, tpc;
+    align_gather_grid(M, num_sms, &grid, &tpc);
+    return launch_pdl(moe_align_gather_kernel<true>, dim3(grid), dim3(align_gather_threads(E)),
+                      smem, stream, static_cast<const int32_t *>(nullptr), M, k, E, block_m,
+                      static_cast<int>(cap), sorted_ids, block_expert, offsets, num_padded,
+                      dev_status, x, d, xg, tpc, logits, ids, w);
 }
 
 }  // namespace w4
