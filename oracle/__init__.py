@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
 ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
 package.  It shares nothing with the CUDA library: the arithmetic lives in
-``w4moe_oracle.c`` (plain C, float64) and this module only compiles it with
-gcc, loads it with ctypes and marshals numpy arrays.
+``w4moe_oracle.c`` (the MoE layer) and ``sampler_norm_oracle.c`` (RMSNorm,
+entropy, Gumbel-max sampler), plain C in float64, and this module only
+compiles them with gcc, loads them with ctypes and marshals numpy arrays.
 
 Each wrapper names the passage of the pages it follows (page title and
 section); the readings taken where the pages are silent are listed at the top
@@ -20,7 +21,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "w4moe_oracle.c")
+_SRCS = [os.path.join(_HERE, "w4moe_oracle.c"), os.path.join(_HERE, "sampler_norm_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
@@ -31,11 +32,11 @@ def build(force: bool = False) -> str:
     """Compile the C oracle with gcc (no FMA contraction, IEEE semantics)."""
     os.makedirs(_BUILD, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off",
-           "-fno-fast-math", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+           "-fno-fast-math", "-fPIC", "-shared", "-pthread", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -72,6 +73,15 @@ def _load():
                                          P, P, P, i32, P, P, P, i32,
                                          P, P, i32, P, P, P]
         lib.oracle_moe_layer.restype = i32
+        u32, u64 = ctypes.c_uint32, ctypes.c_uint64
+        lib.oracle_rmsnorm.argtypes = [P, P, i32, i32, ctypes.c_double, P]
+        lib.oracle_philox4x32_10.argtypes = [P, P, P]
+        lib.oracle_noise_word.argtypes = [u64, u64, i64, i64]
+        lib.oracle_noise_word.restype = u32
+        lib.oracle_gumbel_of_word.argtypes = [u32]
+        lib.oracle_gumbel_of_word.restype = ctypes.c_double
+        lib.oracle_entropy.argtypes = [P, i32, i64, P, i32]
+        lib.oracle_gumbel_argmax.argtypes = [P, i32, i64, u64, u64, P, P, P, P, i32]
         _lib = lib
         return lib
 
@@ -237,3 +247,69 @@ def moe_layer(x_bf16_bits: np.ndarray, gu, dn, ids: np.ndarray, weights: np.ndar
     if rc != 0:
         raise ValueError("oracle_moe_layer: bad arguments")
     return (out, h, y) if want_intermediates else out
+
+
+# --------------------------------------------------------------------------
+# "dg-w4-kernels" -- RMSNorm
+# --------------------------------------------------------------------------
+def rmsnorm(x_bf16_bits: np.ndarray, w_bf16_bits: np.ndarray, eps: float) -> np.ndarray:
+    """y = x / sqrt(mean(x^2) + eps) * weight per row, float64, unrounded.
+
+    x [M, d] and weight [d] are bf16 bit patterns (uint16)."""
+    x = _c(x_bf16_bits, np.uint16)
+    w = _c(w_bf16_bits, np.uint16)
+    M, d = x.shape
+    assert w.shape == (d,)
+    y = np.empty((M, d), np.float64)
+    _load().oracle_rmsnorm(_ptr(x), _ptr(w), M, d, float(eps), _ptr(y))
+    return y
+
+
+# --------------------------------------------------------------------------
+# "dg-w4-kernels" -- Sampler: fused_entropy, gumbel_argmax_sample
+# --------------------------------------------------------------------------
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox4x32-10 (Salmon et al., SC 2011) of one counter under one key."""
+    c = np.array(counter, np.uint32)
+    k = np.array(key, np.uint32)
+    out = np.empty(4, np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def noise_word(seed: int, offset: int, t: int, i: int) -> int:
+    """The 32-bit Philox word of row t, column i: key (seed lo, seed hi),
+    counter (i // 4, t, offset lo, offset hi), word i % 4."""
+    return int(_load().oracle_noise_word(seed, offset, t, i))
+
+
+def gumbel_of_word(r: int) -> float:
+    """g = -ln(-ln(1 - v)), v = (r + 1/2) / 2^32."""
+    return float(_load().oracle_gumbel_of_word(int(r) & 0xFFFFFFFF))
+
+
+def entropy(logits: np.ndarray, nthreads: int | None = None) -> np.ndarray:
+    """-sum p ln p of softmax over the last axis, float64 nats."""
+    l = _c(logits, np.float32)
+    M, V = l.shape
+    H = np.empty(M, np.float64)
+    _load().oracle_entropy(_ptr(l), M, V, _ptr(H), int(nthreads or os.cpu_count() or 1))
+    return H
+
+
+def gumbel_argmax(logits: np.ndarray, seed: int, offset: int = 0,
+                  nthreads: int | None = None):
+    """Gumbel-max sample and plain argmax per row (ties to the lower index).
+
+    Returns dict(sample, argmax, best, second): best and second are the two
+    largest perturbed scores logit + g in float64."""
+    l = _c(logits, np.float32)
+    M, V = l.shape
+    sample = np.empty(M, np.int64)
+    amax = np.empty(M, np.int64)
+    best = np.empty(M, np.float64)
+    second = np.empty(M, np.float64)
+    _load().oracle_gumbel_argmax(_ptr(l), M, V, seed & (2**64 - 1), offset & (2**64 - 1),
+                                 _ptr(sample), _ptr(amax), _ptr(best), _ptr(second),
+                                 int(nthreads or os.cpu_count() or 1))
+    return dict(sample=sample, argmax=amax, best=best, second=second)
