@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 4
+#define W4MOE_ABI_VERSION 5
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -326,6 +326,69 @@ int w4_moe_layer_static_scratch(const uint16_t *x, const int32_t *topk_ids,
                                 const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z,
                                 int dn_group, uint16_t *out, int32_t *dev_status,
                                 w4_stream_t stream);
+
+/* ==========================================================================
+ * Beside the layer: the per-step kernels of the denoising loop
+ * ========================================================================== */
+
+/* --------------------------------------------------------------------------
+ * w4_rmsnorm -- fused_rmsnorm: y = x / sqrt(mean(x^2) + eps) * weight over
+ * the last axis, one kernel
+ * ("dg-w4-kernels" -- RMSNorm; "Inference: Making every denoising pass
+ *  fast" -- RMSNorm: each activation rescaled by its root-mean-square
+ *  magnitude).
+ *
+ *   x       [M, d] bf16 in (16-byte aligned)
+ *   weight  [d] bf16 in (16-byte aligned); multiplies as is (no 1 + weight)
+ *   y       [M, d] bf16 out (16-byte aligned; may equal x)
+ * Arithmetic in fp32 (sum of squares, reciprocal square root, two products),
+ * y rounded to bf16 once.  One warp per row with the row in registers for
+ * d <= 4096; wider rows take a CTA per row.  Requires d % 8 == 0, eps >= 0.
+ * ------------------------------------------------------------------------ */
+int w4_rmsnorm(const uint16_t *x, const uint16_t *weight, int M, int d, float eps, uint16_t *y,
+               w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_sample_logits -- fused_entropy and gumbel_argmax_sample in one
+ * streaming pass over vocabulary logits
+ * ("dg-w4-kernels" -- Sampler: the entropy of Categorical(logits) in one
+ *  pass instead of a logsumexp/sub/exp/mul/sum chain; a Gumbel-max draw from
+ *  the same Categorical with Philox noise made inline, and the plain argmax
+ *  from the same reduction).
+ *
+ *   logits   [M, V] fp32 in; -inf entries are masked out; a row needs one
+ *            finite entry (an all -inf row gives a NaN entropy)
+ *   seed, offset  the noise stream: Philox4x32-10 (Salmon et al., SC 2011)
+ *            with key (seed lo, seed hi) and counter (c / 4, t, offset lo,
+ *            offset hi) for row t, column c, which takes output word c % 4;
+ *            a word r gives g = -ln(-ln(1 - v)), v = (r + 1/2) 2^-32
+ *   entropy  [M] fp32 out, -sum p ln p in nats, or NULL to skip
+ *   sample   [M] int64 out, argmax_c (logit + g), or NULL to skip
+ *   argmax   [M] int64 out, argmax_c logit, or NULL to skip
+ *   workspace  device scratch of w4_sample_logits_workspace_size(M, V)
+ *            bytes (partials per row segment); contents need no initialisation
+ * Ties go to the lower column.  Results do not depend on scheduling: every
+ * reduction runs in a fixed order.  Quads of logits that cannot win the draw
+ * (their largest logit + 23 below the running best; g < 22.9 always) skip
+ * their noise, which changes no result.  Two launches: persistent CTAs
+ * stream equal spans of the rows laid end to end and write one partial per
+ * row segment, then one warp per row merges them.  The split depends on the
+ * GPU's SM count, so results are bit-identical run to run on one GPU model.
+ * Requires 0 < V < 2^31.
+ * ------------------------------------------------------------------------ */
+size_t w4_sample_logits_workspace_size(int M, int64_t V);
+int w4_sample_logits(const float *logits, int M, int64_t V, uint64_t seed, uint64_t offset,
+                     float *entropy, int64_t *sample, int64_t *argmax, void *workspace,
+                     size_t workspace_bytes, w4_stream_t stream);
+
+/* fused_entropy: w4_sample_logits with only the entropy. */
+int w4_fused_entropy(const float *logits, int M, int64_t V, float *entropy, void *workspace,
+                     size_t workspace_bytes, w4_stream_t stream);
+
+/* gumbel_argmax_sample: w4_sample_logits with the sample and the argmax. */
+int w4_gumbel_argmax_sample(const float *logits, int M, int64_t V, uint64_t seed,
+                            uint64_t offset, int64_t *sample, int64_t *argmax, void *workspace,
+                            size_t workspace_bytes, w4_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -15,7 +15,9 @@ from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_PIPELINE_TIMEOUT, W4_DEV_TOO_MAN
                    w4_grouped_gemm_gate_up, w4_moe_align, w4_moe_align_capacity,
                    w4_moe_combine_fixed_order, w4_moe_layer, w4_moe_layer_static_scratch,
                    w4_moe_layer_workspace_size, w4_moe_layer_from_logits,
-                   w4_moe_route, w4_moe_route_align_gather, w4_quantize)
+                   w4_moe_route, w4_moe_route_align_gather, w4_quantize, w4_rmsnorm,
+                   w4_sample_logits, w4_sample_logits_workspace_size, w4_fused_entropy,
+                   w4_gumbel_argmax_sample)
 
 __all__ = [
     "W4Error", "load_library", "header_functions", "korder_to_natural", "w4_gather_activations",
@@ -23,6 +25,7 @@ __all__ = [
     "w4_quantize", "w4_moe_route", "w4_moe_align", "w4_moe_align_capacity",
     "w4_grouped_gemm_gate_up", "w4_grouped_gemm_down", "w4_moe_combine_fixed_order",
     "w4_moe_layer", "w4_moe_layer_workspace_size", "w4_moe_layer_static_scratch",
-    "w4_moe_route_align_gather", "w4_moe_layer_from_logits",
+    "w4_moe_route_align_gather", "w4_moe_layer_from_logits", "w4_rmsnorm", "w4_sample_logits",
+    "w4_sample_logits_workspace_size", "w4_fused_entropy", "w4_gumbel_argmax_sample",
     "W4_DEV_BAD_EXPERT_ID", "W4_DEV_PIPELINE_TIMEOUT", "W4_DEV_TOO_MANY_JOBS",
 ]

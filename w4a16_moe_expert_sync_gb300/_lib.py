@@ -54,6 +54,7 @@ def load_library(path: str | None = None):
                                "(python -c 'import __graft_entry__ as g; g.build()')")
         lib = ctypes.CDLL(p)
         V, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        U64 = ctypes.c_uint64
         sig = {
             "w4_status_string": ([I], ctypes.c_char_p),
             "w4_last_error_detail": ([], ctypes.c_char_p),
@@ -76,6 +77,11 @@ def load_library(path: str | None = None):
                                              V, V, V], I),
             "w4_moe_layer_from_logits": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V,
                                           SZ, V, V, V, V, V], I),
+            "w4_rmsnorm": ([V, V, I, I, ctypes.c_float, V, V], I),
+            "w4_sample_logits_workspace_size": ([I, I64], SZ),
+            "w4_sample_logits": ([V, I, I64, U64, U64, V, V, V, V, SZ, V], I),
+            "w4_fused_entropy": ([V, I, I64, V, V, SZ, V], I),
+            "w4_gumbel_argmax_sample": ([V, I, I64, U64, U64, V, V, V, SZ, V], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -390,3 +396,74 @@ def w4_moe_layer_static_scratch(x, topk_ids, topk_weights, gu, dn, out, block_m:
         _ptr(gu_s), _ptr(gu_z), gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), dn_group,
         _ptr(out), _ptr(dev_status), _stream(stream)), "w4_moe_layer_static_scratch")
     return out
+
+
+# --------------------------------------------------------------------------
+# Beside the layer: RMSNorm and the sampler ("dg-w4-kernels" -- RMSNorm, Sampler)
+# --------------------------------------------------------------------------
+def w4_rmsnorm(x, weight, eps: float = 1e-6, out=None, stream=None):
+    """fused_rmsnorm: y = x / sqrt(mean(x^2) + eps) * weight over the last
+    axis; x [..., d] and weight [d] bf16, y bf16."""
+    import torch
+    _require_cuda(x, weight, out)
+    d = x.shape[-1]
+    M = x.numel() // d if d else 0
+    if out is None:
+        out = torch.empty_like(x)
+    _check(load_library().w4_rmsnorm(_ptr(x), _ptr(weight), M, d, float(eps), _ptr(out),
+                                     _stream(stream)), "w4_rmsnorm")
+    return out
+
+
+def w4_sample_logits_workspace_size(M: int, V: int) -> int:
+    return int(load_library().w4_sample_logits_workspace_size(M, V))
+
+
+def _sampler_ws(logits, workspace):
+    import torch
+    M, V = logits.shape
+    need = w4_sample_logits_workspace_size(M, V)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=logits.device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def w4_sample_logits(logits, seed: int = 0, offset: int = 0, entropy=True, sample=True,
+                     argmax=True, workspace=None, stream=None):
+    """One pass over logits [M, V] fp32: (entropy [M] fp32 nats, Gumbel-max
+    sample [M] int64, argmax [M] int64); an output passed as False is skipped
+    (None in its place), a tensor is written in place."""
+    import torch
+    _require_cuda(logits, workspace)
+    M, V = logits.shape
+    dev = logits.device
+
+    def out(spec, dtype):
+        if spec is False or spec is None:
+            return None
+        if spec is True:
+            return torch.empty(M, dtype=dtype, device=dev)
+        _require_cuda(spec)
+        return spec
+    ent = out(entropy, torch.float32)
+    smp = out(sample, torch.int64)
+    amx = out(argmax, torch.int64)
+    ws, ws_bytes = _sampler_ws(logits, workspace)
+    _check(load_library().w4_sample_logits(
+        _ptr(logits), M, V, seed & (2**64 - 1), offset & (2**64 - 1), _ptr(ent), _ptr(smp),
+        _ptr(amx), _ptr(ws), ws_bytes, _stream(stream)), "w4_sample_logits")
+    return ent, smp, amx
+
+
+def w4_fused_entropy(logits, workspace=None, stream=None):
+    """fused_entropy: [M, V] fp32 -> [M] fp32 nats, one pass."""
+    ent, _, _ = w4_sample_logits(logits, entropy=True, sample=False, argmax=False,
+                                 workspace=workspace, stream=stream)
+    return ent
+
+
+def w4_gumbel_argmax_sample(logits, seed: int, offset: int = 0, workspace=None, stream=None):
+    """gumbel_argmax_sample: (sample, argmax), both [M] int64, one pass."""
+    _, smp, amx = w4_sample_logits(logits, seed, offset, entropy=False, sample=True,
+                                   argmax=True, workspace=workspace, stream=stream)
+    return smp, amx

@@ -509,3 +509,75 @@ int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ RMSNorm
+int w4_rmsnorm(const uint16_t *x, const uint16_t *weight, int M, int d, float eps, uint16_t *y,
+               w4_stream_t stream)
+{
+    if (!weight || (M > 0 && (!x || !y)))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || d <= 0 || !(eps >= 0.0f))
+        return fail(W4_ERR_INVALID_ARG, "bad sizes or eps (M=%d d=%d)", M, d);
+    if (d % 8)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "d must be a multiple of 8 (got %d)", d);
+    if (static_cast<int64_t>(M) * d >= (1ll << 31))
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "M * d must be below 2^31");
+    if (!aligned16(x) || !aligned16(weight) || !aligned16(y))
+        return fail(W4_ERR_MISALIGNED, "x, weight and y must be 16-byte aligned");
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err = w4::launch_rmsnorm(x, weight, M, d, eps, y, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "rmsnorm launch");
+}
+
+// ------------------------------------------------------------------ sampler
+size_t w4_sample_logits_workspace_size(int M, int64_t V)
+{
+    if (M <= 0 || V <= 0 || V >= (1ll << 31))
+        return 0;
+    return w4::sampler_workspace_bytes(M, V);
+}
+
+int w4_sample_logits(const float *logits, int M, int64_t V, uint64_t seed, uint64_t offset,
+                     float *entropy, int64_t *sample, int64_t *argmax, void *workspace,
+                     size_t workspace_bytes, w4_stream_t stream)
+{
+    if (M < 0 || V <= 0 || V >= (1ll << 31))
+        return fail(W4_ERR_INVALID_ARG, "need M >= 0 and 0 < V < 2^31 (M=%d V=%lld)", M,
+                    static_cast<long long>(V));
+    if (M == 0)
+        return W4_OK;
+    if (!logits)
+        return fail(W4_ERR_INVALID_ARG, "NULL logits");
+    if (!entropy && !sample && !argmax)
+        return fail(W4_ERR_INVALID_ARG, "no output requested");
+    if (!aligned4(logits))
+        return fail(W4_ERR_MISALIGNED, "logits must be 4-byte aligned");
+    if (!workspace || workspace_bytes < w4::sampler_workspace_bytes(M, V) || !aligned16(workspace))
+        return fail(W4_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes",
+                    w4::sampler_workspace_bytes(M, V));
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err = w4::launch_sampler(logits, M, V, seed, offset, entropy, sample, argmax,
+                                         workspace, as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "sampler launch");
+}
+
+int w4_fused_entropy(const float *logits, int M, int64_t V, float *entropy, void *workspace,
+                     size_t workspace_bytes, w4_stream_t stream)
+{
+    if (!entropy)
+        return fail(W4_ERR_INVALID_ARG, "NULL entropy");
+    return w4_sample_logits(logits, M, V, 0, 0, entropy, nullptr, nullptr, workspace,
+                            workspace_bytes, stream);
+}
+
+int w4_gumbel_argmax_sample(const float *logits, int M, int64_t V, uint64_t seed,
+                            uint64_t offset, int64_t *sample, int64_t *argmax, void *workspace,
+                            size_t workspace_bytes, w4_stream_t stream)
+{
+    if (!sample)
+        return fail(W4_ERR_INVALID_ARG, "NULL sample");
+    return w4_sample_logits(logits, M, V, seed, offset, nullptr, sample, argmax, workspace,
+                            workspace_bytes, stream);
+}

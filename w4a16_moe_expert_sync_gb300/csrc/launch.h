@@ -50,6 +50,12 @@ cudaError_t launch_route_align_gather(const float *logits, int M, int k, int E, 
                                       const uint16_t *x, int d, uint16_t *xg, int num_sms,
                                       cudaStream_t stream);
 
+cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *w, int M, int d, float eps,
+                           uint16_t *y, cudaStream_t stream);
+size_t sampler_workspace_bytes(int M, int64_t V);
+cudaError_t launch_sampler(const float *logits, int M, int64_t V, uint64_t seed, uint64_t offset,
+                           float *entropy, int64_t *sample, int64_t *amax, void *workspace,
+                           cudaStream_t stream);
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
                            int d, int E, uint16_t *out, cudaStream_t stream);
 

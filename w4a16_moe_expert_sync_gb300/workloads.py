@@ -112,3 +112,81 @@ def all_gate_up_weights(cfg: LayerShape) -> np.ndarray:
 
 def all_down_weights(cfg: LayerShape) -> np.ndarray:
     return np.stack([down_weight(cfg, e) for e in range(cfg.E)])
+
+
+# --------------------------------------------------------------------------
+# Beside the layer: RMSNorm inputs and vocabulary logits for the sampler
+# ("dg-w4-kernels" -- RMSNorm, Sampler: [256, 262144] fp32 logits per
+# denoising step).
+# --------------------------------------------------------------------------
+_TAG_NORM_X, _TAG_NORM_W, _TAG_VOCAB = 6, 7, 8
+
+
+@dataclasses.dataclass(frozen=True)
+class NormShape:
+    name: str
+    M: int
+    d: int
+    seed: int
+
+
+NORM_CONFIGS = {
+    "tiny": NormShape("tiny", 3, 64, seed=30),
+    "ragged": NormShape("ragged", 37, 1032, seed=31),       # 129 vectors per row
+    "layer256": NormShape("layer256", 256, 2816, seed=32),  # the pages' canvas x hidden
+    "wide": NormShape("wide", 5, 8192, seed=33),            # the one-CTA-per-row path
+    "canvas2048": NormShape("canvas2048", 2048, 2816, seed=34),
+}
+
+
+def norm_inputs(cfg: NormShape):
+    """x [M, d] and weight [d] as bf16 bits: x row t ~ N(0, s_t^2) with s_t
+    log-uniform in [0.1, 10] (residual-stream rows of different magnitude),
+    weight ~ 1 + 0.1 N(0, 1)."""
+    r = _rng(cfg.seed, _TAG_NORM_X)
+    scale = np.exp(r.uniform(np.log(0.1), np.log(10.0), (cfg.M, 1)))
+    x = (r.standard_normal((cfg.M, cfg.d)) * scale).astype(np.float32)
+    w = (1.0 + 0.1 * _rng(cfg.seed, _TAG_NORM_W).standard_normal(cfg.d)).astype(np.float32)
+    return f32_to_bf16_bits(x), f32_to_bf16_bits(w)
+
+
+@dataclasses.dataclass(frozen=True)
+class LogitsShape:
+    name: str
+    M: int          # canvas positions
+    V: int          # vocabulary
+    seed: int
+    mask_frac: float = 0.0   # fraction of each row set to -inf
+
+
+SAMPLER_CONFIGS = {
+    "tiny": LogitsShape("tiny", 4, 1000, seed=40),
+    # V % 4 == 3: the scalar-load path, several chunks and a ragged tail
+    "ragged": LogitsShape("ragged", 5, 24579, seed=41),
+    "masked": LogitsShape("masked", 6, 20000, seed=42, mask_frac=0.5),
+    # one denoising step's logits at the pages' shape
+    "canvas": LogitsShape("canvas", 256, 262144, seed=43),
+}
+
+
+def vocab_logits(cfg: LogitsShape) -> np.ndarray:
+    """Logits [M, V] fp32 with a spread of entropies, as a canvas has between
+    undecided and nearly committed positions: row t is N(0, sigma_t^2) with
+    sigma_t log-uniform in [0.5, 4]; half the rows (chosen by a coin per row)
+    add a peak h_t ~ U(5, 25) at one random column; with mask_frac > 0 that
+    fraction of each row's columns (random) is -inf, never the peak column."""
+    r = _rng(cfg.seed, _TAG_VOCAB)
+    sigma = np.exp(r.uniform(np.log(0.5), np.log(4.0), (cfg.M, 1))).astype(np.float32)
+    l = r.standard_normal((cfg.M, cfg.V), dtype=np.float32)
+    l *= sigma
+    peaked = r.random(cfg.M) < 0.5
+    col = r.integers(0, cfg.V, cfg.M)
+    h = r.uniform(5.0, 25.0, cfg.M).astype(np.float32)
+    rows = np.nonzero(peaked)[0]
+    l[rows, col[rows]] += h[rows]
+    if cfg.mask_frac > 0:
+        for t in range(cfg.M):
+            masked = r.random(cfg.V) < cfg.mask_frac
+            masked[col[t]] = False
+            l[t, masked] = -np.inf
+    return l
