@@ -73,6 +73,8 @@ def _load():
                                          P, P, P, i32, P, P, P, i32,
                                          P, P, i32, P, P, P]
         lib.oracle_moe_layer.restype = i32
+        lib.oracle_w4a16_linear.argtypes = [P, i32, i32, i32, P, P, P, i32, i32, P]
+        lib.oracle_w4a16_linear.restype = i32
         u32, u64 = ctypes.c_uint32, ctypes.c_uint64
         lib.oracle_rmsnorm.argtypes = [P, P, i32, i32, ctypes.c_double, P]
         lib.oracle_philox4x32_10.argtypes = [P, P, P]
@@ -247,6 +249,30 @@ def moe_layer(x_bf16_bits: np.ndarray, gu, dn, ids: np.ndarray, weights: np.ndar
     if rc != 0:
         raise ValueError("oracle_moe_layer: bad arguments")
     return (out, h, y) if want_intermediates else out
+
+
+# --------------------------------------------------------------------------
+# "dg-w4-kernels" -- W4A16: the dense linear
+# --------------------------------------------------------------------------
+def w4a16_linear(x_bf16_bits: np.ndarray, q: np.ndarray, s: np.ndarray, z: np.ndarray,
+                 group: int = 128, nthreads: int | None = None) -> np.ndarray:
+    """y = x . deq(W)^T in float64 (F.linear of the dequantised weight).
+
+    x [M, K] bf16 bits; q [N, K/2] packed codes, s/z [N, K/group] fp16 bits;
+    returns y [M, N] float64."""
+    x = _c(x_bf16_bits, np.uint16)
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint16)
+    z = _c(z, np.uint16)
+    M, K = x.shape
+    N = q.shape[0]
+    assert q.shape == (N, K // 2) and s.shape == (N, K // group) and z.shape == s.shape
+    y = np.empty((M, N), np.float64)
+    rc = _load().oracle_w4a16_linear(_ptr(x), M, K, N, _ptr(q), _ptr(s), _ptr(z), group,
+                                     int(nthreads or os.cpu_count() or 1), _ptr(y))
+    if rc != 0:
+        raise ValueError("oracle_w4a16_linear: bad arguments")
+    return y
 
 
 # --------------------------------------------------------------------------

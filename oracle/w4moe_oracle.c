@@ -26,6 +26,10 @@
  *   [GM] "dg-w4-kernels" -- Grouped MoE: alignment is sync-free, the
  *        activation is folded into the first GEMM's epilogue, the weighted
  *        combine is a fixed-order reduction.
+ *   [DL] "dg-w4-kernels" -- W4A16: w4a16_linear(x, qw, scale, zero) equals
+ *        F.linear(x, dequant(W)), groups of 128 along the contraction dim;
+ *        "Inference: Making every denoising pass fast" -- Dense W4 everywhere:
+ *        attention, the shared MLP and the LM head as dense W4A16 layers.
  *
  * Readings where the pages are silent (each is repeated at its function):
  *   R1 gated activation: h = gelu_tanh(gate) * up.
@@ -464,5 +468,68 @@ int oracle_moe_layer(const uint16_t *x, int M, int d, int m, int E, int k,
     }
     if (!h_out) free(h_all);
     if (!y_out) free(y_all);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [DL] the dense W4A16 linear: y[t, n] = sum_k x[t, k] * deq(W)[n, k], in   */
+/* float64, x given as bf16 bits.  Rows of y are split over POSIX threads;   */
+/* every value is one fixed sequence of operations.                           */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const uint16_t *x;
+    int M, K, N;
+    const uint8_t *q;
+    const uint16_t *s, *z;
+    int group;
+    double *y;
+    int tid, nthreads;
+} linear_job;
+
+static void *linear_worker(void *arg)
+{
+    linear_job *J = (linear_job *)arg;
+    double *xr = (double *)malloc(sizeof(double) * (size_t)J->K);
+    if (!xr)
+        return NULL;
+    const int64_t G = J->K / J->group;
+    for (int t = J->tid; t < J->M; t += J->nthreads) {
+        for (int kk = 0; kk < J->K; kk++)
+            xr[kk] = oracle_bf16_to_f64(J->x[(int64_t)t * J->K + kk]);
+        for (int n = 0; n < J->N; n++)
+            J->y[(int64_t)t * J->N + n] =
+                w4_row_dot(J->q + (int64_t)n * (J->K / 2), J->s + (int64_t)n * G,
+                           J->z + (int64_t)n * G, J->K, J->group, xr);
+    }
+    free(xr);
+    return NULL;
+}
+
+int oracle_w4a16_linear(const uint16_t *x, int M, int K, int N, const uint8_t *q,
+                        const uint16_t *s, const uint16_t *z, int group, int nthreads, double *y)
+{
+    if (M < 0 || K <= 0 || N <= 0 || group <= 0 || K % group || K % 2)
+        return 1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    linear_job jobs[256];
+    pthread_t th[256];
+    for (int i = 0; i < nthreads; i++) {
+        linear_job J = {x, M, K, N, q, s, z, group, y, i, nthreads};
+        jobs[i] = J;
+    }
+    int started = 0;
+    for (int i = 1; i < nthreads; i++) {
+        if (pthread_create(&th[i], NULL, linear_worker, &jobs[i]) != 0)
+            break;
+        started = i;
+    }
+    linear_worker(&jobs[0]);
+    for (int i = 1; i <= started; i++)
+        pthread_join(th[i], NULL);
+    for (int i = started + 1; i < nthreads; i++)
+        linear_worker(&jobs[i]);
     return 0;
 }
