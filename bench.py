@@ -20,6 +20,17 @@ bounded sample of the same workload, in the same unit.
 
 Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent
 replicas of the same layer, one per GPU, with no collective on the data path.
+
+--workload sampler times the per-step sampler beside the layer instead: one
+pass over [256, 262144] fp32 vocabulary logits giving the entropy, a
+Gumbel-max sample and the argmax per row ("dg-w4-kernels" -- Sampler);
+value = logits bytes / device time.  --workload rmsnorm times fused_rmsnorm
+over [256, 2816] bf16 ("dg-w4-kernels" -- RMSNorm); value = (x + weight + y)
+bytes / device time.  --workload linear times the dense W4A16 linear
+("dg-w4-kernels" -- W4A16; "Inference: Making every denoising pass fast" --
+Dense W4 everywhere: 256-row QKV and LM-head-tile tests against cuBLAS BF16),
+value = TFLOP/s of the QKV shape, with torch's bf16 F.linear (cuBLAS) on the
+same shapes timed alongside.
 """
 from __future__ import annotations
 
@@ -38,6 +49,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "W4A16 MoE layer µs & HBM GB/s (% GB300 roofline) at M=256,d2816,m704,E128,top8"
+METRIC_SAMPLER = ("one-pass logits sampler (entropy + Gumbel-max sample + argmax) µs & HBM GB/s "
+                  "at [256, 262144] fp32")
+METRIC_RMSNORM = "fused RMSNorm µs & HBM GB/s at [256, 2816] bf16"
+METRIC_LINEAR = ("dense W4A16 linear µs & TFLOP/s at 256 rows (QKV 2816->4096, LM-head tile "
+                 "2816->16384) vs cuBLAS BF16")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -490,6 +506,439 @@ def run_gpu(args, cfg, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# beside the layer: the sampler and RMSNorm
+# ----------------------------------------------------------------------------
+def time_region(step, args, world, dev, local):
+    """Warm-up, then K back-to-back steps between one pair of CUDA events on the
+    current stream (barrier + synchronize on both sides), clocks sampled
+    meanwhile.  Returns (max-over-ranks ms per step, clocks summary, wall s)."""
+    import torch
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_smi_id(local)) if not args.skip_clocks else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__enter__()
+    wall = time.perf_counter()
+    t0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    t1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall
+    if sampler:
+        sampler.__exit__(None, None, None)
+    barrier(world)
+    ms = max_over_ranks(world, t0.elapsed_time(t1) / args.steps, dev)
+    return ms, (sampler.summary() if sampler else None), wall
+
+
+def time_e2e(step, args, world, dev):
+    import torch
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        pairs[i][0].record()
+        step(args.warmup + i)
+        pairs[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(world, statistics.fmean(a.elapsed_time(b) for a, b in pairs), dev)
+
+
+def hbm_roofline(nbytes, ms, kernel, note):
+    peak, kind = measured_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": None, "kernel": kernel,
+            "alg_bytes_per_launch": nbytes, "note": note,
+            "peak_source": f"{kind} (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+            if kind == "measured" else "fallback 6.8 TB/s"}
+
+
+def sampler_cpu(cfg, logits, rows, nthreads):
+    """The oracle's entropy and Gumbel-max pass on `rows` rows; GB/s of logits."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.entropy(logits[:rows], nthreads=nthreads)
+    oracle.gumbel_argmax(logits[:rows], 7, 0, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return rows * cfg.V * 4 / dt / 1e9, dt
+
+
+def run_sampler(args, world, rank, local):
+    import torch
+    import w4a16_moe_expert_sync_gb300 as w4
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    cfg = wl.SAMPLER_CONFIGS["canvas"]
+    logits_np = wl.vocab_logits(cfg)
+    nbytes = cfg.M * cfg.V * 4
+    config = {"workload": f"sampler {cfg.name}: vocabulary logits [{cfg.M}, {cfg.V}] fp32 "
+                          f"(rows N(0, s^2), s log-uniform in [0.5, 4], half the rows with a "
+                          f"peak of 5..25), seed {cfg.seed}; entropy, Gumbel-max sample (Philox "
+                          f"noise, offset = step) and argmax per row in one pass",
+              "M": cfg.M, "V": cfg.V,
+              "l2": "not flushed: the 268 MB of logits exceed the 126 MB L2",
+              "parallelism": "replicas"}
+    nthreads = os.cpu_count() or 1
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rows = 8
+        for _ in range(args.warmup):
+            sampler_cpu(cfg, logits_np, rows, nthreads)
+        vals, dts = zip(*[sampler_cpu(cfg, logits_np, rows, nthreads) for _ in range(args.steps)])
+        value = rows * cfg.V * 4 * args.steps / sum(dts) / 1e9
+        sample = (f"{rows} of {cfg.M} rows per step; float64 C oracle (entropy, Philox noise, "
+                  f"Gumbel-max) on {nthreads} threads")
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC_SAMPLER, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(dts) / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    w4.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lt = torch.from_numpy(logits_np).to(dev)
+    ws = torch.empty(w4.w4_sample_logits_workspace_size(cfg.M, cfg.V), dtype=torch.uint8,
+                     device=dev)
+    ent = torch.empty(cfg.M, device=dev)
+    smp = torch.empty(cfg.M, dtype=torch.int64, device=dev)
+    amx = torch.empty(cfg.M, dtype=torch.int64, device=dev)
+
+    def step(i):
+        w4.w4_sample_logits(lt, 7, i, ent, smp, amx, workspace=ws)
+
+    ms, clocks, wall = time_region(step, args, world, dev, local)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    # the two launches alone, serialised, for the roofline of the dominant one
+    # (the per-row merge is ~2 us)
+    parts = {}
+    for name, kw in (("all", dict(entropy=ent, sample=smp, argmax=amx)),
+                     ("entropy", dict(entropy=ent, sample=False, argmax=False)),
+                     ("argmax", dict(entropy=False, sample=False, argmax=amx))):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(20)]
+        for a, b in evs:
+            torch.cuda._sleep(200000)
+            a.record()
+            w4.w4_sample_logits(lt, 7, 0, workspace=ws, **kw)
+            b.record()
+        torch.cuda.synchronize()
+        parts[name] = statistics.median(a.elapsed_time(b) for a, b in evs[3:]) * 1e3
+    e2e = None
+    if not args.skip_e2e:
+        lh = lt.cpu().pin_memory()
+        eh = torch.empty(cfg.M).pin_memory()
+        sh = torch.empty(cfg.M, dtype=torch.int64).pin_memory()
+        ah = torch.empty(cfg.M, dtype=torch.int64).pin_memory()
+        ld = torch.empty_like(lt)
+
+        def e2e_step(i):
+            ld.copy_(lh, non_blocking=True)
+            w4.w4_sample_logits(ld, 7, i, ent, smp, amx, workspace=ws)
+            eh.copy_(ent, non_blocking=True)
+            sh.copy_(smp, non_blocking=True)
+            ah.copy_(amx, non_blocking=True)
+
+        e_ms = time_e2e(e2e_step, args, world, dev)
+        e2e = {"value": world * nbytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": cfg.M * 20,
+               "ms_per_step": e_ms,
+               "api": "w4_sample_logits with the logits copied in from pinned host memory and "
+                      "the three outputs copied back each step"}
+    line = {
+        "metric": METRIC_SAMPLER, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config, "us_per_step": ms * 1e3,
+        "variants_us": parts,
+        "roofline": hbm_roofline(nbytes, parts["all"] * 1e-3, "sampler_partial_kernel "
+                                 "(w4_sample_logits, all three outputs)",
+                                 "one pass over the logits is the floor; the kernel is bound "
+                                 "by instruction issue (Philox and the Gumbel transform per "
+                                 "logit), see the profile summary"),
+        "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "timed_region_wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        rows = 8
+        v, dt = sampler_cpu(cfg, logits_np, rows, nthreads)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                                "sample": f"{rows} of {cfg.M} rows, float64 C oracle on "
+                                          f"{nthreads} threads, {dt:.2f} s wall"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_rmsnorm(args, world, rank, local):
+    import torch
+    import w4a16_moe_expert_sync_gb300 as w4
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    cfg = wl.NORM_CONFIGS["layer256"]
+    x_np, w_np = wl.norm_inputs(cfg)
+    nbytes = 2 * cfg.M * cfg.d * 2 + cfg.d * 2
+    config = {"workload": f"rmsnorm {cfg.name}: x [{cfg.M}, {cfg.d}] bf16 (rows N(0, s^2), s "
+                          f"log-uniform in [0.1, 10]), weight 1 + 0.1 N(0, 1), eps 1e-6, "
+                          f"seed {cfg.seed}",
+              "M": cfg.M, "d": cfg.d,
+              "l2": "not flushed: 2.9 MB per step stays in L2, the figure is launch- and "
+                    "latency-bound, not HBM-bound",
+              "parallelism": "replicas"}
+    nthreads = os.cpu_count() or 1
+    if args.impl == "reference" or (rank == 0 and world == 1 and not args.skip_cpu_baseline):
+        import oracle
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < 2.0:
+            oracle.rmsnorm(x_np, w_np, 1e-6)
+            n += 1
+        dt = (time.perf_counter() - t0) / n
+        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole [{cfg.M}, {cfg.d}] input, float64 C oracle, one thread, "
+                         f"{n} runs"}
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({
+                    "impl": "reference", "metric": METRIC_RMSNORM, "value": cpu["value"],
+                    "unit": "GB/s", "n_gpus": world, "steps": n, "warmup": 0,
+                    "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                    "cpu_baseline": cpu,
+                    "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}), flush=True)
+            return
+    w4.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    wt = torch.from_numpy(w_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty_like(x)
+
+    # A launch costs more host time than the kernel takes on the device, so
+    # back-to-back calls from Python would time the host.  The steps are
+    # captured in a CUDA graph (the library is graph-safe) and the graph is
+    # replayed: device time per step with the launches back to back.
+    per_graph = min(args.steps, 1000)
+    replays = max(1, (args.steps + per_graph - 1) // per_graph)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            w4.w4_rmsnorm(x, wt, 1e-6, out=y)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(per_graph):
+            w4.w4_rmsnorm(x, wt, 1e-6, out=y)
+
+    def step(i):
+        graph.replay()
+
+    n_steps = replays * per_graph
+    g_args = argparse.Namespace(**{**vars(args), "steps": replays,
+                                   "warmup": max(1, args.warmup // per_graph + 1)})
+    ms_replay, clocks, wall = time_region(step, g_args, world, dev, local)
+    ms = ms_replay / per_graph
+    e2e = None
+    if not args.skip_e2e:
+        xh = x.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        xd = torch.empty_like(x)
+
+        def e2e_step(i):
+            xd.copy_(xh, non_blocking=True)
+            w4.w4_rmsnorm(xd, wt, 1e-6, out=y)
+            yh.copy_(y, non_blocking=True)
+
+        e_ms = time_e2e(e2e_step, args, world, dev)
+        e2e = {"value": world * nbytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": cfg.M * cfg.d * 2, "d2h_bytes_per_step": cfg.M * cfg.d * 2,
+               "ms_per_step": e_ms, "api": "w4_rmsnorm with x copied in and y copied out"}
+    line = {
+        "metric": METRIC_RMSNORM, "value": world * nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": n_steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config, "us_per_step": ms * 1e3,
+        "timing": f"{replays} replays of a CUDA graph of {per_graph} w4_rmsnorm calls",
+        "roofline": hbm_roofline(nbytes, ms, "rmsnorm_warp_kernel<12> (w4_rmsnorm)",
+                                 "back-to-back launches; 2.9 MB is far below what it takes to "
+                                 "reach HBM bandwidth, the time is the launch and one "
+                                 "load-reduce-store latency chain"),
+        "e2e": e2e, "gpu_launches": n_steps, "clocks": clocks, "timed_region_wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def graph_time(fn, per_graph, replays, warm_replays=2):
+    """Device time per call of fn, captured per_graph times in a CUDA graph and
+    replayed: back-to-back launches without the host in the way."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(per_graph):
+            fn()
+    for _ in range(warm_replays):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (replays * per_graph), graph
+
+
+def run_linear(args, world, rank, local):
+    import torch
+    import oracle
+    import w4a16_moe_expert_sync_gb300 as w4
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    shapes = [wl.LINEAR_CONFIGS["qkv256"], wl.LINEAR_CONFIGS["lmhead256"]]
+    config = {"workload": "dense W4A16 linear at 256 rows: qkv256 (K=2816, N=4096) and lmhead256 "
+                          "(K=2816, N=16384, a tile of the vocabulary head); x ~ N(0, 1) bf16, "
+                          "W ~ N(0, 0.02^2) quantised to uint4 with fp16 scale/zero per 128",
+              "shapes": [dataclasses_asdict(c) for c in shapes],
+              "l2": "not flushed: the graph replays the same weights (5.8 MB and 23 MB packed); "
+                    "the L2 holds the QKV weights between calls",
+              "parallelism": "replicas"}
+    nthreads = os.cpu_count() or 1
+    cfg0 = shapes[0]
+    if args.impl == "reference" or (rank == 0 and world == 1 and not args.skip_cpu_baseline):
+        x_np, W_np = wl.linear_inputs(cfg0)
+        q_np, s_np, z_np = oracle.quantize_w4(W_np, 128)
+        rows = 16
+        t0 = time.perf_counter()
+        oracle.w4a16_linear(x_np[:rows], q_np, s_np, z_np, 128, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        flops = 2.0 * rows * cfg0.K * cfg0.N
+        cpu = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+               "sample": f"{rows} of {cfg0.M} rows of qkv256, float64 C oracle on {nthreads} "
+                         f"threads, {dt:.2f} s wall"}
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({
+                    "impl": "reference", "metric": METRIC_LINEAR, "value": cpu["value"],
+                    "unit": "TFLOP/s", "n_gpus": world, "steps": 1, "warmup": 0,
+                    "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                    "cpu_baseline": cpu,
+                    "e2e": {"value": cpu["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}), flush=True)
+            return
+    w4.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    per_graph = 50
+    replays = max(1, args.steps // per_graph)
+    results, keep = {}, []
+    for cfg in shapes:
+        x_np, W_np = wl.linear_inputs(cfg)
+        x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+        W = torch.from_numpy(W_np).to(dev)
+        q, s_, z = (t[0] for t in w4.w4_quantize(W, cfg.group))
+        ws = torch.empty(w4.w4_w4a16_linear_workspace_size(cfg.M, cfg.K, cfg.N),
+                         dtype=torch.uint8, device=dev)
+        y = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
+        Wb = W.to(torch.bfloat16)
+        ms_w4, g1 = graph_time(lambda: w4.w4_w4a16_linear(x, q, s_, z, cfg.group, workspace=ws,
+                                                          out=y), per_graph, replays)
+        ms_bf, g2 = graph_time(lambda: torch.nn.functional.linear(x, Wb), per_graph, replays)
+        keep += [g1, g2]
+        flops = 2.0 * cfg.M * cfg.K * cfg.N
+        results[cfg.name] = {"us_w4a16": ms_w4 * 1e3, "us_cublas_bf16": ms_bf * 1e3,
+                             "tflops_w4a16": flops / (ms_w4 * 1e-3) / 1e12,
+                             "speed_vs_cublas_bf16": ms_bf / ms_w4,
+                             "weight_bytes": cfg.N * cfg.K // 2 + 2 * 2 * cfg.N * (cfg.K // cfg.group)}
+    # the timed region proper: replays of the QKV graph, clocks sampled
+    cfg = shapes[0]
+    x_np, W_np = wl.linear_inputs(cfg)
+    x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    q, s_, z = (t[0] for t in w4.w4_quantize(torch.from_numpy(W_np).to(dev), cfg.group))
+    ws = torch.empty(w4.w4_w4a16_linear_workspace_size(cfg.M, cfg.K, cfg.N), dtype=torch.uint8,
+                     device=dev)
+    y = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
+    _, graph = graph_time(lambda: w4.w4_w4a16_linear(x, q, s_, z, cfg.group, workspace=ws, out=y),
+                          per_graph, 1)
+    g_args = argparse.Namespace(**{**vars(args), "steps": replays, "warmup": 3})
+    ms_replay, clocks, wall = time_region(lambda i: graph.replay(), g_args, world, dev, local)
+    ms = ms_replay / per_graph
+    flops = 2.0 * cfg.M * cfg.K * cfg.N
+    value = world * flops / (ms * 1e-3) / 1e12
+    peak_bf16 = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_bf16 = float(json.load(f)["bf16_tflops"])
+        peak_kind = "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS bf16 burst; fp16 runs at the same rate)"
+    except Exception:
+        peak_bf16, peak_kind = 1900.0, "fallback 1.9 PFLOP/s"
+    e2e = None
+    if not args.skip_e2e:
+        xh = x.cpu().pin_memory()
+        yh = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16).pin_memory()
+        xd = torch.empty_like(x)
+
+        def e2e_step(i):
+            xd.copy_(xh, non_blocking=True)
+            w4.w4_w4a16_linear(xd, q, s_, z, cfg.group, workspace=ws, out=y)
+            yh.copy_(y, non_blocking=True)
+
+        e_ms = time_e2e(e2e_step, args, world, dev)
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": cfg.M * cfg.K * 2, "d2h_bytes_per_step": cfg.M * cfg.N * 2,
+               "ms_per_step": e_ms, "api": "w4_w4a16_linear with x copied in and y copied out"}
+    line = {
+        "metric": METRIC_LINEAR, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": replays * per_graph, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "data": "synthetic", "config": config, "us_per_step": ms * 1e3, "shapes": results,
+        "timing": f"{replays} replays of a CUDA graph of {per_graph} calls (qkv256)",
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak_bf16,
+                     "unit": "TFLOP/s", "frac": value / world / peak_bf16, "traffic": None,
+                     "kernel": "grouped_gemm_kernel<down> with one expert (w4_w4a16_linear)",
+                     "alg_flops_per_launch": flops, "peak_source": peak_kind,
+                     "note": "at 256 rows the contraction is compute-bound; this path "
+                             "dequantises the weight once per 32-token job (8 times at 256 "
+                             "rows), which bounds it instead"},
+        "e2e": e2e, "gpu_launches": 2 * replays * per_graph, "clocks": clocks,
+        "timed_region_wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def dataclasses_asdict(c):
+    import dataclasses
+    return dataclasses.asdict(c)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -502,13 +951,21 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-clocks", action="store_true")
+    ap.add_argument("--workload", choices=["layer", "sampler", "rmsnorm", "linear"],
+                    default="layer")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from w4a16_moe_expert_sync_gb300 import workloads as wl
     cfg = wl.CONFIGS[args.config]
     world, rank, local = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.workload == "sampler":
+        run_sampler(args, world, rank, local)
+    elif args.workload == "rmsnorm":
+        run_rmsnorm(args, world, rank, local)
+    elif args.workload == "linear":
+        run_linear(args, world, rank, local)
+    elif args.impl == "reference":
         run_reference(args, cfg, world, rank)
     else:
         run_gpu(args, cfg, world, rank, local)

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 5
+#define W4MOE_ABI_VERSION 6
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -326,6 +326,34 @@ int w4_moe_layer_static_scratch(const uint16_t *x, const int32_t *topk_ids,
                                 const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z,
                                 int dn_group, uint16_t *out, int32_t *dev_status,
                                 w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_w4a16_linear -- the dense W4A16 linear: y = x . deq(W)^T
+ * ("dg-w4-kernels" -- W4A16: w4a16_linear(x, qw, scale, zero) equals
+ *  F.linear(x, dequant(W)), reading packed nibbles and dequantising inline;
+ *  "Inference: Making every denoising pass fast" -- Dense W4 everywhere:
+ *  attention, the shared MLP and the LM head as dense W4A16 layers).
+ *
+ *   x          [M, K] bf16 in
+ *   q          [N, K/2] uint8, w4_quantize's layout; s, z [N, K/group] fp16
+ *   y          [M, N] bf16 out
+ *   workspace  device scratch of w4_w4a16_linear_workspace_size(M, K, N)
+ *              bytes, 256-byte aligned; contents need no initialisation
+ * The routed-expert machinery with one expert and one slot per token: the
+ * rows are converted to fp16 in the GEMM's operand order (the alignment of M
+ * tokens to a single expert is the identity), the grouped GEMM's
+ * plain-epilogue variant multiplies them by the dequantised weight (fp16 x
+ * fp16 tcgen05 MMA, fp32 accumulation) and writes the rows rounded to bf16.
+ * Two launches.  Every 32 tokens
+ * form one job that dequantises the whole weight, so the cost grows with M
+ * in steps of 32 tokens.
+ * Requires group 64 or 128, K a multiple of the group and of 64, N a
+ * multiple of 128.  dev_status may be NULL.
+ * ------------------------------------------------------------------------ */
+size_t w4_w4a16_linear_workspace_size(int M, int K, int N);
+int w4_w4a16_linear(const uint16_t *x, int M, int K, int N, const uint8_t *q, const uint16_t *s,
+                    const uint16_t *z, int group, void *workspace, size_t workspace_bytes,
+                    uint16_t *y, int32_t *dev_status, w4_stream_t stream);
 
 /* ==========================================================================
  * Beside the layer: the per-step kernels of the denoising loop

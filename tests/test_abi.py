@@ -39,7 +39,7 @@ def test_header_compiles_as_plain_c():
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4_abi_version() == 5
+    assert clib.w4_abi_version() == 6
     assert clib.w4_status_string(0) == b"W4_OK"
     assert clib.w4_status_string(2) == b"W4_ERR_UNSUPPORTED_SHAPE"
     assert clib.w4_status_string(99) == b"W4_ERR_UNKNOWN"

@@ -17,7 +17,7 @@ from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_PIPELINE_TIMEOUT, W4_DEV_TOO_MAN
                    w4_moe_layer_workspace_size, w4_moe_layer_from_logits,
                    w4_moe_route, w4_moe_route_align_gather, w4_quantize, w4_rmsnorm,
                    w4_sample_logits, w4_sample_logits_workspace_size, w4_fused_entropy,
-                   w4_gumbel_argmax_sample)
+                   w4_gumbel_argmax_sample, w4_w4a16_linear, w4_w4a16_linear_workspace_size)
 
 __all__ = [
     "W4Error", "load_library", "header_functions", "korder_to_natural", "w4_gather_activations",
@@ -27,5 +27,6 @@ __all__ = [
     "w4_moe_layer", "w4_moe_layer_workspace_size", "w4_moe_layer_static_scratch",
     "w4_moe_route_align_gather", "w4_moe_layer_from_logits", "w4_rmsnorm", "w4_sample_logits",
     "w4_sample_logits_workspace_size", "w4_fused_entropy", "w4_gumbel_argmax_sample",
+    "w4_w4a16_linear", "w4_w4a16_linear_workspace_size",
     "W4_DEV_BAD_EXPERT_ID", "W4_DEV_PIPELINE_TIMEOUT", "W4_DEV_TOO_MANY_JOBS",
 ]

@@ -77,6 +77,8 @@ def load_library(path: str | None = None):
                                              V, V, V], I),
             "w4_moe_layer_from_logits": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V,
                                           SZ, V, V, V, V, V], I),
+            "w4_w4a16_linear_workspace_size": ([I, I, I], SZ),
+            "w4_w4a16_linear": ([V, I, I, I, V, V, V, I, V, SZ, V, V, V], I),
             "w4_rmsnorm": ([V, V, I, I, ctypes.c_float, V, V], I),
             "w4_sample_logits_workspace_size": ([I, I64], SZ),
             "w4_sample_logits": ([V, I, I64, U64, U64, V, V, V, V, SZ, V], I),
@@ -395,6 +397,30 @@ def w4_moe_layer_static_scratch(x, topk_ids, topk_weights, gu, dn, out, block_m:
         _ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, d, m, E, k, block_m, _ptr(gu_q),
         _ptr(gu_s), _ptr(gu_z), gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), dn_group,
         _ptr(out), _ptr(dev_status), _stream(stream)), "w4_moe_layer_static_scratch")
+    return out
+
+
+def w4_w4a16_linear_workspace_size(M: int, K: int, N: int) -> int:
+    return int(load_library().w4_w4a16_linear_workspace_size(M, K, N))
+
+
+def w4_w4a16_linear(x, q, s, z, group: int = 128, workspace=None, out=None, dev_status=None,
+                    stream=None):
+    """w4a16_linear: y [M, N] bf16 = x [M, K] bf16 . deq(W)^T with W packed as
+    w4_quantize writes it (q [N, K/2] uint8, s/z [N, K/group] fp16)."""
+    import torch
+    _require_cuda(x, q, s, z, workspace, out, dev_status)
+    M, K = x.shape
+    N = q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = w4_w4a16_linear_workspace_size(M, K, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    _check(load_library().w4_w4a16_linear(
+        _ptr(x), M, K, N, _ptr(q), _ptr(s), _ptr(z), group, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "w4_w4a16_linear")
     return out
 
 

@@ -53,6 +53,7 @@
 //   * Every pipeline wait has a time limit; on expiry the CTA raises
 //     W4_DEV_PIPELINE_TIMEOUT, stops, drains its own copies and MMAs, frees
 //     its tensor memory and exits.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "korder.cuh"
@@ -165,6 +166,7 @@ struct GemmArgs {
     int32_t *dev_status;
     int E, A, K, R, m_up, out_cols, group, group_shift, G, n_panels, n_kchunks, n_sub;
     int early_schedule;       // the schedule may be read before the grid-dependency wait
+    int out_bf16;             // plain epilogue: bf16 rows instead of fp32
 };
 
 constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kMaxSubBufs + 2 + 2 + 2 * kStagesSZ + kIssuers;
@@ -853,13 +855,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                             static_cast<uint16_t>(f16x2_sat(gelu_tanh(gv) * uv, 0.0f)));
                     }
                 } else {
-                    float *yout = reinterpret_cast<float *>(p.out);
                     const int col = pnl * 128 + 32 * q4 + lane;
+                    if (p.out_bf16) {
+                        uint16_t *bout = reinterpret_cast<uint16_t *>(p.out);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const int a = __shfl_sync(full, my_a, 8 * b + i);
-                        if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
-                            yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
+                        for (int i = 0; i < 8; i++) {
+                            const int a = __shfl_sync(full, my_a, 8 * b + i);
+                            if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
+                                bout[static_cast<int64_t>(a) * p.out_cols + col] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+                        }
+                    } else {
+                        float *yout = reinterpret_cast<float *>(p.out);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            const int a = __shfl_sync(full, my_a, 8 * b + i);
+                            if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
+                                yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
+                        }
                     }
                 }
             }
@@ -974,6 +987,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.n_kchunks = (q.K + kChunkK - 1) / kChunkK;
     a.n_sub = q.K / kSubK;
     a.early_schedule = q.early_schedule ? 1 : 0;
+    a.out_bf16 = q.out_bf16 ? 1 : 0;
     const bool resident = !q.gate_up && b_fits_resident(q.K);
 
     const SmemLayout L = smem_layout(a.G, a.E);

@@ -56,6 +56,9 @@ size_t sampler_workspace_bytes(int M, int64_t V);
 cudaError_t launch_sampler(const float *logits, int M, int64_t V, uint64_t seed, uint64_t offset,
                            float *entropy, int64_t *sample, int64_t *amax, void *workspace,
                            cudaStream_t stream);
+cudaError_t launch_identity_align_gather(const uint16_t *x, int M, int d, int padded,
+                                         int32_t *sorted_ids, int32_t *offsets, uint16_t *xg,
+                                         cudaStream_t stream);
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
                            int d, int E, uint16_t *out, cudaStream_t stream);
 
@@ -79,6 +82,8 @@ struct GroupedGemmProblem {
     // down may then read its schedule, and stream its weights, before its
     // grid-dependency wait.  Activations are read only after that wait.
     bool early_schedule = false;
+    // plain (down) epilogue only: write bf16 rows instead of fp32 ones
+    bool out_bf16 = false;
 };
 
 // Returns cudaSuccess, or an error; *why receives a static description when

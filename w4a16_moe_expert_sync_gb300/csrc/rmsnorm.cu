@@ -65,12 +65,14 @@ __global__ void __launch_bounds__(32 * kNormWarps)
     if (t >= M)
         return;
     const uint4 *xr = x + static_cast<int64_t>(t) * d8;
-    uint4 v[VPL];
+    uint4 v[VPL], wv[VPL];
     float ss = 0.0f;
+    // x and weight loads all in flight together: one memory round trip
 #pragma unroll
     for (int i = 0; i < VPL; i++) {
         const int c = lane + 32 * i;
         v[i] = c < d8 ? __ldcs(xr + c) : make_uint4(0, 0, 0, 0);
+        wv[i] = c < d8 ? __ldg(w + c) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < VPL; i++)
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(32 * kNormWarps)
     for (int i = 0; i < VPL; i++) {
         const int c = lane + 32 * i;
         if (c < d8)
-            __stcs(yr + c, scale8(v[i], __ldg(w + c), inv));
+            __stcs(yr + c, scale8(v[i], wv[i], inv));
     }
 }
 

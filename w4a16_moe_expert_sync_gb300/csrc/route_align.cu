@@ -357,6 +357,47 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict_
     }
 }
 
+// The alignment of M tokens to a single expert with one slot each (the dense
+// linear): slot i holds token i, slots [M, padded) are padding (sentinel M,
+// zero rows); offsets = {0, padded}.  One thread per 16-byte chunk of xg.
+__global__ void __launch_bounds__(256)
+    identity_align_gather_kernel(const uint16_t *__restrict__ x, int M, int d, int padded,
+                                 int32_t *__restrict__ sorted_ids, int32_t *__restrict__ offsets,
+                                 uint16_t *__restrict__ xg)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int c8n = d / 8;
+    const int64_t total = static_cast<int64_t>(padded) * c8n;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = gtid; i < total; i += stride) {
+        const int slot = static_cast<int>(i / c8n);
+        const int c8 = static_cast<int>(i - static_cast<int64_t>(slot) * c8n);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (slot < M)
+            o = bf16x8_to_f16_korder(
+                __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(slot) * d) + c8));
+        *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(slot) * d + 8 * c8) = o;
+    }
+    for (int64_t i = gtid; i < padded; i += stride)
+        sorted_ids[i] = i < M ? static_cast<int32_t>(i) : M;
+    if (gtid == 0) {
+        offsets[0] = 0;
+        offsets[1] = padded;
+    }
+}
+
+cudaError_t launch_identity_align_gather(const uint16_t *x, int M, int d, int padded,
+                                         int32_t *sorted_ids, int32_t *offsets, uint16_t *xg,
+                                         cudaStream_t stream)
+{
+    const int64_t total = static_cast<int64_t>(padded) * (d / 8);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 2048));
+    return launch_pdl(identity_align_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                      0, stream, x, M, d, padded, sorted_ids, offsets, xg);
+}
+
 // Fused alignment + gather (with ROUTE, router + alignment + gather from the
 // logits: every CTA routes every token into shared memory first, with the
 // same arithmetic as route_kernel, and writes ids and weights of its own

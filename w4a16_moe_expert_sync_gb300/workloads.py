@@ -190,3 +190,40 @@ def vocab_logits(cfg: LogitsShape) -> np.ndarray:
             masked[col[t]] = False
             l[t, masked] = -np.inf
     return l
+
+
+# --------------------------------------------------------------------------
+# The dense W4A16 linear ("dg-w4-kernels" -- W4A16; "Inference: Making every
+# denoising pass fast" -- Dense W4 everywhere: 256-row tests of QKV and of an
+# LM-head tile).  The pages give neither the QKV width nor the tile width;
+# qkv256 uses 4096 output rows (e.g. 16 query heads of 128 plus 8 key and 8
+# value heads of 128 over the 2816 hidden size), lmhead256 a 16384-row tile of
+# the 262144-row vocabulary head.
+# --------------------------------------------------------------------------
+_TAG_LIN_X, _TAG_LIN_W = 9, 10
+
+
+@dataclasses.dataclass(frozen=True)
+class LinearShape:
+    name: str
+    M: int      # rows (tokens)
+    K: int      # input features (contraction dim)
+    N: int      # output features
+    seed: int
+    group: int = 128
+
+
+LINEAR_CONFIGS = {
+    "tiny": LinearShape("tiny", 5, 256, 128, seed=50),
+    "ragged": LinearShape("ragged", 37, 384, 256, seed=51),
+    "wide_k": LinearShape("wide_k", 33, 2816, 384, seed=52),     # K > 768: streamed activations
+    "qkv256": LinearShape("qkv256", 256, 2816, 4096, seed=53),
+    "lmhead256": LinearShape("lmhead256", 256, 2816, 16384, seed=54),
+}
+
+
+def linear_inputs(cfg: LinearShape):
+    """x [M, K] bf16 bits ~ N(0, 1); W [N, K] fp32 ~ N(0, 0.02^2)."""
+    x = _rng(cfg.seed, _TAG_LIN_X).standard_normal((cfg.M, cfg.K), dtype=np.float32)
+    W = (_rng(cfg.seed, _TAG_LIN_W).standard_normal((cfg.N, cfg.K), dtype=np.float32) * 0.02)
+    return f32_to_bf16_bits(x), W.astype(np.float32)
