@@ -862,7 +862,7 @@ def run_linear(args, world, rank, local):
         x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
         W = torch.from_numpy(W_np).to(dev)
         q, s_, z = (t[0] for t in w4.w4_quantize(W, cfg.group))
-        ws = torch.empty(w4.w4_w4a16_linear_workspace_size(cfg.M, cfg.K, cfg.N),
+        ws = torch.empty(w4.w4_w4a16_linear_workspace_size(cfg.M, cfg.K, cfg.N, cfg.group),
                          dtype=torch.uint8, device=dev)
         y = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
         Wb = W.to(torch.bfloat16)
@@ -880,7 +880,7 @@ def run_linear(args, world, rank, local):
     x_np, W_np = wl.linear_inputs(cfg)
     x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
     q, s_, z = (t[0] for t in w4.w4_quantize(torch.from_numpy(W_np).to(dev), cfg.group))
-    ws = torch.empty(w4.w4_w4a16_linear_workspace_size(cfg.M, cfg.K, cfg.N), dtype=torch.uint8,
+    ws = torch.empty(w4.w4_w4a16_linear_workspace_size(cfg.M, cfg.K, cfg.N, cfg.group), dtype=torch.uint8,
                      device=dev)
     y = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
     _, graph = graph_time(lambda: w4.w4_w4a16_linear(x, q, s_, z, cfg.group, workspace=ws, out=y),

@@ -337,20 +337,19 @@ int w4_moe_layer_static_scratch(const uint16_t *x, const int32_t *topk_ids,
  *   x          [M, K] bf16 in
  *   q          [N, K/2] uint8, w4_quantize's layout; s, z [N, K/group] fp16
  *   y          [M, N] bf16 out
- *   workspace  device scratch of w4_w4a16_linear_workspace_size(M, K, N)
- *              bytes, 256-byte aligned; contents need no initialisation
- * The routed-expert machinery with one expert and one slot per token: the
- * rows are converted to fp16 in the GEMM's operand order (the alignment of M
- * tokens to a single expert is the identity), the grouped GEMM's
- * plain-epilogue variant multiplies them by the dequantised weight (fp16 x
- * fp16 tcgen05 MMA, fp32 accumulation) and writes the rows rounded to bf16.
- * Two launches.  Every 32 tokens
- * form one job that dequantises the whole weight, so the cost grows with M
- * in steps of 32 tokens.
- * Requires group 64 or 128, K a multiple of the group and of 64, N a
- * multiple of 128.  dev_status may be NULL.
+ *   workspace  device scratch of w4_w4a16_linear_workspace_size(M, K, N,
+ *              group) bytes, 256-byte aligned; contents need no initialisation
+ * The rows are converted to fp16 in the GEMMs' operand order (one launch),
+ * then multiplied by the dequantised weight: fp16 x fp16 tcgen05 MMA with
+ * fp32 accumulation, rows rounded to bf16 once.  Each 128-row panel of W is
+ * dequantised once per pass of up to 256 token rows, and narrow outputs
+ * split the contraction (fp32 partial sums in the workspace, added in split
+ * order by one more launch; the split depends on the shape only, so results
+ * are the same on every GPU).  Two or three launches.
+ * Requires group 64 or 128, K >= 256 a multiple of the group and of 64 with
+ * K / group <= 32, N a multiple of 128.  dev_status may be NULL.
  * ------------------------------------------------------------------------ */
-size_t w4_w4a16_linear_workspace_size(int M, int K, int N);
+size_t w4_w4a16_linear_workspace_size(int M, int K, int N, int group);
 int w4_w4a16_linear(const uint16_t *x, int M, int K, int N, const uint8_t *q, const uint16_t *s,
                     const uint16_t *z, int group, void *workspace, size_t workspace_bytes,
                     uint16_t *y, int32_t *dev_status, w4_stream_t stream);

@@ -86,3 +86,14 @@ def test_linear_rejects_unsupported_shapes(lib):
     s = torch.zeros((100, 2), dtype=torch.float16, device="cuda")
     with pytest.raises(lib.W4Error):
         lib.w4_w4a16_linear(x, q, s, s, 128)
+
+
+def test_linear_rejects_more_than_32_groups(lib):
+    """The per-row scales and zeros of a panel are staged whole: at most 32
+    groups along the contraction dim."""
+    import torch
+    x = torch.zeros((4, 4352), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((128, 2176), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((128, 34), dtype=torch.float16, device="cuda")
+    with pytest.raises(lib.W4Error):
+        lib.w4_w4a16_linear(x, q, s, s, 128)

@@ -77,7 +77,7 @@ def load_library(path: str | None = None):
                                              V, V, V], I),
             "w4_moe_layer_from_logits": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V,
                                           SZ, V, V, V, V, V], I),
-            "w4_w4a16_linear_workspace_size": ([I, I, I], SZ),
+            "w4_w4a16_linear_workspace_size": ([I, I, I, I], SZ),
             "w4_w4a16_linear": ([V, I, I, I, V, V, V, I, V, SZ, V, V, V], I),
             "w4_rmsnorm": ([V, V, I, I, ctypes.c_float, V, V], I),
             "w4_sample_logits_workspace_size": ([I, I64], SZ),
@@ -400,8 +400,8 @@ def w4_moe_layer_static_scratch(x, topk_ids, topk_weights, gu, dn, out, block_m:
     return out
 
 
-def w4_w4a16_linear_workspace_size(M: int, K: int, N: int) -> int:
-    return int(load_library().w4_w4a16_linear_workspace_size(M, K, N))
+def w4_w4a16_linear_workspace_size(M: int, K: int, N: int, group: int = 128) -> int:
+    return int(load_library().w4_w4a16_linear_workspace_size(M, K, N, group))
 
 
 def w4_w4a16_linear(x, q, s, z, group: int = 128, workspace=None, out=None, dev_status=None,
@@ -414,7 +414,7 @@ def w4_w4a16_linear(x, q, s, z, group: int = 128, workspace=None, out=None, dev_
     N = q.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    need = w4_w4a16_linear_workspace_size(M, K, N)
+    need = w4_w4a16_linear_workspace_size(M, K, N, group)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     _check(load_library().w4_w4a16_linear(

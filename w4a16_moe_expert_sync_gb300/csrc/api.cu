@@ -584,32 +584,34 @@ int w4_gumbel_argmax_sample(const float *logits, int M, int64_t V, uint64_t seed
 
 // ----------------------------------------------------------- dense linear
 // Workspace of w4_w4a16_linear (each piece 256-byte aligned):
-//   sorted_ids [padded] i32 | offsets [2] i32 | xg [padded, K] fp16
+//   sorted_ids [padded] i32 | offsets [2] i32 | xg [padded, K] fp16 |
+//   partial sums [splits, M, N] fp32 (dense kernel with a split contraction)
 // with padded = M rounded up to 16 (the one expert's slots).
 namespace {
 constexpr int kLinearBlockM = 16;
 struct LinearWs {
-    size_t sorted, offs, xg, total;
+    size_t sorted, offs, xg, part, total;
     int padded;
 };
-LinearWs linear_ws(int M, int K, int N)
+LinearWs linear_ws(int M, int K, int N, int group)
 {
     LinearWs w;
     w.padded = (M + kLinearBlockM - 1) / kLinearBlockM * kLinearBlockM;
     w.sorted = 0;
     w.offs = up256(4 * static_cast<size_t>(w.padded));
     w.xg = up256(w.offs + 8);
-    w.total = up256(w.xg + 2 * static_cast<size_t>(w.padded) * K);
-    (void)N;
+    w.part = up256(w.xg + 2 * static_cast<size_t>(w.padded) * K);
+    const bool split = M > 0 && w4::dense_gemm_supported(M, N, K, group);
+    w.total = up256(w.part + (split ? w4::dense_gemm_partial_bytes(M, N, K) : 0));
     return w;
 }
 }  // namespace
 
-size_t w4_w4a16_linear_workspace_size(int M, int K, int N)
+size_t w4_w4a16_linear_workspace_size(int M, int K, int N, int group)
 {
     if (M < 0 || K <= 0 || N <= 0)
         return 0;
-    return linear_ws(M, K, N).total;
+    return linear_ws(M, K, N, group).total;
 }
 
 int w4_w4a16_linear(const uint16_t *x, int M, int K, int N, const uint8_t *q, const uint16_t *s,
@@ -624,16 +626,16 @@ int w4_w4a16_linear(const uint16_t *x, int M, int K, int N, const uint8_t *q, co
         return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
     if (group != 64 && group != 128)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "group must be 64 or 128 (got %d)", group);
-    if (K % group || K % 64 || N % 128)
+    if (K % group || K % 64 || K < 256 || N % 128 || K / group > 32)
         return fail(W4_ERR_UNSUPPORTED_SHAPE,
-                    "need K a multiple of the group and of 64, N a multiple of 128 (K=%d N=%d)",
-                    K, N);
+                    "need K >= 256, a multiple of the group and of 64, with at most 32 groups, "
+                    "N a multiple of 128 (K=%d N=%d group=%d)", K, N, group);
     if (static_cast<int64_t>(M) * K > (1ll << 30) || static_cast<int64_t>(M) * N > (1ll << 30) ||
         static_cast<int64_t>(N) * K > (1ll << 31))
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "problem too large for 32-bit indexing");
     if (!aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(z) || !aligned16(y))
         return fail(W4_ERR_MISALIGNED, "x, q, s, z and y must be 16-byte aligned");
-    const LinearWs L = linear_ws(M, K, N);
+    const LinearWs L = linear_ws(M, K, N, group);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(W4_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes",
                     L.total);
@@ -648,29 +650,21 @@ int w4_w4a16_linear(const uint16_t *x, int M, int K, int N, const uint8_t *q, co
                                                        as_stream(stream));
     if (err != cudaSuccess)
         return cuda_fail(err, "identity alignment launch");
-    w4::GroupedGemmProblem p{};
-    p.gate_up = false;
-    p.act = xg;
-    p.wq = q;
-    p.ws = s;
-    p.wz = z;
-    p.sorted_ids = sorted;
-    p.expert_offsets = offs;
-    p.out = y;
-    p.out_bf16 = true;
-    p.dev_status = dev_status;
-    p.M = M;
-    p.k = 1;
-    p.E = 1;
-    p.K = K;
-    p.R = N;
-    p.group = group;
-    p.out_cols = N;
-    p.cap = L.padded;
-    p.early_schedule = false;
+    w4::DenseGemmProblem d{};
+    d.xg = xg;
+    d.q = q;
+    d.s = s;
+    d.z = z;
+    d.y = y;
+    d.partials = reinterpret_cast<float *>(ws + L.part);
+    d.dev_status = dev_status;
+    d.M = M;
+    d.N = N;
+    d.K = K;
+    d.group = group;
     const char *why = nullptr;
-    err = w4::launch_grouped_gemm(p, as_stream(stream), &why);
+    err = w4::launch_dense_gemm(d, as_stream(stream), &why);
     if (why)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "%s", why);
-    return err == cudaSuccess ? W4_OK : cuda_fail(err, "linear GEMM launch");
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "dense GEMM launch");
 }

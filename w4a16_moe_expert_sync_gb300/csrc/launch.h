@@ -86,6 +86,24 @@ struct GroupedGemmProblem {
     bool out_bf16 = false;
 };
 
+// The dense W4A16 GEMM (dense_gemm.cu): y [M, N] bf16 = xg [Mpad, K] fp16
+// (block order, rows past M zero) . deq(W)^T, W [N, K/2] u8 with s, z
+// [N, K/group] fp16.  partials: fp32 [splits, M, N] when the contraction is
+// split (dense_gemm_partial_bytes > 0), else unused.
+struct DenseGemmProblem {
+    const uint16_t *xg;
+    const uint8_t *q;
+    const uint16_t *s, *z;
+    uint16_t *y;
+    float *partials;
+    int32_t *dev_status;
+    int M, N, K, group;
+};
+bool dense_gemm_supported(int M, int N, int K, int group);
+int dense_gemm_splits(int M, int N, int K);
+size_t dense_gemm_partial_bytes(int M, int N, int K);
+cudaError_t launch_dense_gemm(const DenseGemmProblem &p, cudaStream_t stream, const char **why);
+
 // Returns cudaSuccess, or an error; *why receives a static description when
 // the problem is rejected before launch (shape or resource limits).
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem &p, cudaStream_t stream,
