@@ -97,3 +97,13 @@ def test_linear_rejects_more_than_32_groups(lib):
     s = torch.zeros((128, 34), dtype=torch.float16, device="cuda")
     with pytest.raises(lib.W4Error):
         lib.w4_w4a16_linear(x, q, s, s, 128)
+
+
+@pytest.mark.parametrize("M", [300, 600])
+def test_linear_several_token_tiles(lib, M):
+    """More than 256 rows: token tiles of 256, the last one partial (its
+    token-tile loads read zero rows past the padded end), every row checked."""
+    cfg = wl.LinearShape("tiles", M, 512, 256, seed=80 + M)
+    x, W = wl.linear_inputs(cfg)
+    q, s, z = oracle.quantize_w4(W, 128)
+    _check(_run(lib, cfg, x, q, s, z), oracle.w4a16_linear(x, q, s, z, 128))
