@@ -52,13 +52,12 @@ constexpr int kDMaxTok = 256;     // token rows per pass (MMA N)
 constexpr int kDGroups = 4;        // dequantisation groups = A stages
 constexpr int kDGroupWarps = kDNumDq / kDGroups;
 constexpr int kDWChunk = 256;      // codes per row per code stage: one 128-byte row
-constexpr int kDStagesW = 3, kDStagesA = kDGroups, kDStagesB = 3;
+constexpr int kDStagesA = kDGroups;
 // each code stage holds one step per group, and every group waits on every
 // code stage, so no barrier can run two phases ahead of a waiting warp
-static_assert(kDWChunk / kDChunk == kDGroups && kDStagesA == kDGroups, "stage counts");
+static_assert(kDWChunk / kDChunk == kDGroups, "stage counts");
 constexpr int kDWBytes = kDRows * kDWChunk / 2;       // 16 KB of packed codes
 constexpr int kDABytes = kDRows * kDChunk * 2;        // 16 KB of fp16
-constexpr int kDBBytes = kDMaxTok * kDChunk * 2;      // 32 KB of fp16
 constexpr int kDMaxG = 32;                            // groups per weight row staged
 constexpr int kDZOff = kDRows * kDMaxG * 2;           // z after s in a buffer
 constexpr int kDSZBytes = 2 * kDZOff;                 // 16 KB per buffer
@@ -66,18 +65,29 @@ constexpr int kDSZBufs = 1;                           // scale/zero buffers (uni
 constexpr uint32_t kDTmemCols = 512;                  // two 256-column accumulators
 constexpr int kDMaxSplits = 8;
 
-// shared memory, from the 1024-byte-aligned base
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kDStagesA * kDABytes;
-constexpr int kOffW = kOffB + kDStagesB * kDBBytes;
-constexpr int kOffSZ = kOffW + kDStagesW * kDWBytes;
-constexpr int kOffBar = kOffSZ + kDSZBufs * kDSZBytes;
-constexpr int kNumDBars = 2 * kDStagesW + 2 * kDStagesA + 2 * kDStagesB + 2 + 2 + 2 * kDSZBufs + 1;
-constexpr int kOffMisc = kOffBar + 8 * kNumDBars;
-constexpr int kDSmemBytes = kOffMisc + 16;
-constexpr size_t kDSmemLaunch = kDSmemBytes + 1024;
-static_assert(kDSmemLaunch <= 227 * 1024, "shared memory budget");
-static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+// Shared-memory configurations, from the 1024-byte-aligned base: SW code
+// stages (16 KB), SB token stages of BROWS rows (BROWS x 128 B), four A stages.
+// Up to 256 token rows: 3 + 3 stages.  Up to 64 rows the token tiles are
+// small and the room goes to code stages (7), which keeps more weight bytes
+// in flight when the weights, not the tokens, set the pace.
+template <int SW, int SB, int BROWS>
+struct DCfg {
+    static constexpr int kStagesW = SW, kStagesB = SB, kBRows = BROWS;
+    static constexpr int kBBytes = BROWS * kDChunk * 2;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kDStagesA * kDABytes;
+    static constexpr int kOffW = kOffB + kStagesB * kBBytes;
+    static constexpr int kOffSZ = kOffW + kStagesW * kDWBytes;
+    static constexpr int kOffBar = kOffSZ + kDSZBufs * kDSZBytes;
+    static constexpr int kNumBars = 2 * SW + 2 * kDStagesA + 2 * SB + 2 + 2 + 2 * kDSZBufs + 1;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr size_t kSmemLaunch = kOffMisc + 16 + 1024;
+    static_assert(kSmemLaunch <= 227 * 1024, "shared memory budget");
+    static_assert(kOffB % 1024 == 0 && kOffW % 1024 == 0 && kBBytes % 1024 == 0,
+                  "swizzled tiles need 1024-byte alignment");
+};
+using DCfgLarge = DCfg<3, 3, kDMaxTok>;
+using DCfgSmall = DCfg<7, 4, 64>;
 
 struct DenseArgs {
     CUtensorMap tmap_w;   // q [N rows, K/2 bytes] u8, box {128 B, 128 rows}, 128-byte swizzle
@@ -95,17 +105,18 @@ struct DBars {
         *sz_full, *sz_empty, *drain;
 };
 
+template <class C>
 __device__ __forceinline__ DBars carve_dbars(uint8_t *base)
 {
     uint64_t *b = reinterpret_cast<uint64_t *>(base);
     DBars r;
     r.w_full = b;
-    r.w_empty = r.w_full + kDStagesW;
-    r.a_full = r.w_empty + kDStagesW;
+    r.w_empty = r.w_full + C::kStagesW;
+    r.a_full = r.w_empty + C::kStagesW;
     r.a_empty = r.a_full + kDStagesA;
     r.b_full = r.a_empty + kDStagesA;
-    r.b_empty = r.b_full + kDStagesB;
-    r.acc_full = r.b_empty + kDStagesB;
+    r.b_empty = r.b_full + C::kStagesB;
+    r.acc_full = r.b_empty + C::kStagesB;
     r.acc_empty = r.acc_full + 2;
     r.sz_full = r.acc_empty + 2;
     r.sz_empty = r.sz_full + kDSZBufs;
@@ -223,20 +234,21 @@ __device__ __forceinline__ void d_drain_wait(uint64_t *bar, uint32_t parity)
             return;
 }
 
+template <class C>
 __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_constant__ DenseArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const DBars bar = carve_dbars(smem + kOffBar);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    const DBars bar = carve_dbars<C>(smem + C::kOffBar);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *status = p.dev_status;
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
-        for (int i = 0; i < kDStagesW; i++) {
+        for (int i = 0; i < C::kStagesW; i++) {
             mbar_init(&bar.w_full[i], 1);
             mbar_init(&bar.w_empty[i], kDNumDq);
         }
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
             mbar_init(&bar.a_full[i], kDGroupWarps);
             mbar_init(&bar.a_empty[i], 1);
         }
-        for (int i = 0; i < kDStagesB; i++) {
+        for (int i = 0; i < C::kStagesB; i++) {
             mbar_init(&bar.b_full[i], 1);
             mbar_init(&bar.b_empty[i], 1);
         }
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
                 const DUnit d = decode_unit(p, u);
                 if (!d_lane_wait(&bar.sz_empty[szb], ph_sz ^ 1, abort_flag, status))
                     break;
-                uint8_t *dst = smem + kOffSZ + szb * kDSZBytes;
+                uint8_t *dst = smem + C::kOffSZ + szb * kDSZBytes;
                 mbar_arrive_expect_tx(&bar.sz_full[szb], 2 * szbytes);
                 bulk_load(dst, p.sc + static_cast<int64_t>(d.panel) * kDRows * p.G, szbytes,
                           &bar.sz_full[szb], pol);
@@ -311,18 +323,18 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
                         break;
                     }
                     mbar_arrive_expect_tx(&bar.w_full[sw], kDWBytes);
-                    tma_load_2d(smem + kOffW + sw * kDWBytes, &p.tmap_w, kc * (kDChunk / 2),
+                    tma_load_2d(smem + C::kOffW + sw * kDWBytes, &p.tmap_w, kc * (kDChunk / 2),
                                 d.panel * kDRows, &bar.w_full[sw], pol);
                     w_iss |= 1u << sw;
                     w_par = (w_par & ~(1u << sw)) | (ph_w << sw);
-                    if (++sw == kDStagesW) {
+                    if (++sw == C::kStagesW) {
                         sw = 0;
                         ph_w ^= 1;
                     }
                 }
             }
             // every copy issued here lands before the CTA may exit
-            for (int i = 0; i < kDStagesW; i++)
+            for (int i = 0; i < C::kStagesW; i++)
                 if (w_iss >> i & 1u)
                     d_drain_wait(&bar.w_full[i], w_par >> i & 1u);
             for (int i = 0; i < kDSZBufs; i++)
@@ -344,17 +356,17 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
                         break;
                     }
                     mbar_arrive_expect_tx(&bar.b_full[sb], static_cast<uint32_t>(p.box_rows) * 128);
-                    tma_load_2d_nohint(smem + kOffB + sb * kDBBytes, &p.tmap_b, kc * kDChunk, d.t0,
-                                       &bar.b_full[sb]);
+                    tma_load_2d_nohint(smem + C::kOffB + sb * C::kBBytes, &p.tmap_b, kc * kDChunk,
+                                       d.t0, &bar.b_full[sb]);
                     b_iss |= 1u << sb;
                     b_par = (b_par & ~(1u << sb)) | (ph_b << sb);
-                    if (++sb == kDStagesB) {
+                    if (++sb == C::kStagesB) {
                         sb = 0;
                         ph_b ^= 1;
                     }
                 }
             }
-            for (int i = 0; i < kDStagesB; i++)
+            for (int i = 0; i < C::kStagesB; i++)
                 if (b_iss >> i & 1u)
                     d_drain_wait(&bar.b_full[i], b_par >> i & 1u);
         }
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
         // parity of each A stage's next use
         int sb = 0;
         uint32_t ph_b = 0, n_unit = 0, apar = 0;
-        const uint32_t a_s = smem_u32(smem + kOffA), b_s = smem_u32(smem + kOffB);
+        const uint32_t a_s = smem_u32(smem + C::kOffA), b_s = smem_u32(smem + C::kOffB);
         bool ok = true;
         for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, n_unit++) {
             const DUnit d = decode_unit(p, u);
@@ -386,7 +398,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
                 // K steps of 16: +32 B along the swizzled rows (+2 in the
                 // descriptors' address field) of both operands
                 const uint64_t ad = sdesc_sw128(a_s + sa * kDABytes);
-                const uint64_t bd = sdesc_sw128(b_s + sb * kDBBytes);
+                const uint64_t bd = sdesc_sw128(b_s + sb * C::kBBytes);
 #pragma unroll
                 for (int k = 0; k < kDChunk / 16; k++)
                     mma_ss_elect(d_tmem, ad + 2 * k, bd + 2 * k, idesc,
@@ -394,7 +406,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
                 tc_commit_elect(&bar.a_empty[sa]);
                 tc_commit_elect(&bar.b_empty[sb]);
                 apar ^= 1u << sa;
-                if (++sb == kDStagesB) {
+                if (++sb == C::kStagesB) {
                     sb = 0;
                     ph_b ^= 1;
                 }
@@ -454,8 +466,8 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
         const int grp = dqw / kDGroupWarps;
         const int gt = (dqw % kDGroupWarps) * 32 + lane;
         const int r0 = gt, r1 = gt + 64;
-        const uint32_t w_base = smem_u32(smem + kOffW);
-        const uint32_t a_stage = smem_u32(smem + kOffA) + grp * kDABytes;
+        const uint32_t w_base = smem_u32(smem + C::kOffW);
+        const uint32_t a_stage = smem_u32(smem + C::kOffA) + grp * kDABytes;
         const uint32_t a_row0 = static_cast<uint32_t>((r0 >> 3) * 1024 + (r0 & 7) * 128);
         const uint32_t a_row1 = static_cast<uint32_t>((r1 >> 3) * 1024 + (r1 & 7) * 128);
         const uint32_t sw0 = static_cast<uint32_t>(r0 & 7), sw1 = static_cast<uint32_t>(r1 & 7);
@@ -465,7 +477,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
         const uint32_t wq0b = r0 * 128 + (((2u * grp + 1) ^ sw0) << 4);
         const uint32_t wq1a = r1 * 128 + (((2u * grp) ^ sw1) << 4);
         const uint32_t wq1b = r1 * 128 + (((2u * grp + 1) ^ sw1) << 4);
-        const uint32_t sz_base = smem_u32(smem + kOffSZ);
+        const uint32_t sz_base = smem_u32(smem + C::kOffSZ);
         uint32_t magic;   // fp16 1024.0 twice, kept in a register
         asm("mov.b32 %0, 0x64006400;" : "=r"(magic));
         int szb = 0, sw = 0;
@@ -499,7 +511,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
                 }
                 __syncwarp();
                 mbar_arrive_elect(&bar.w_empty[sw]);
-                if (++sw == kDStagesW) {
+                if (++sw == C::kStagesW) {
                     sw = 0;
                     ph_w ^= 1;
                 }
@@ -690,18 +702,21 @@ cudaError_t launch_dense_gemm(const DenseGemmProblem &q, cudaStream_t stream, co
     if (err != cudaSuccess)
         return err;
     static int sms[64] = {};
-    static bool attr[64] = {};
+    static bool attr[64][2] = {};
     if (sms[dev & 63] == 0)
         cudaDeviceGetAttribute(&sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-    if (!attr[dev & 63]) {
-        err = cudaFuncSetAttribute(dense_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kDSmemLaunch));
+    const bool small = a.box_rows <= DCfgSmall::kBRows;
+    auto kern = small ? dense_gemm_kernel<DCfgSmall> : dense_gemm_kernel<DCfgLarge>;
+    const size_t smem = small ? DCfgSmall::kSmemLaunch : DCfgLarge::kSmemLaunch;
+    if (!attr[dev & 63][small]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem));
         if (err != cudaSuccess)
             return err;
-        attr[dev & 63] = true;
+        attr[dev & 63][small] = true;
     }
     const int grid = std::min(a.n_units, std::max(1, sms[dev & 63]));
-    err = launch_pdl(dense_gemm_kernel, dim3(grid), dim3(kDThreads), kDSmemLaunch, stream, a);
+    err = launch_pdl(kern, dim3(grid), dim3(kDThreads), smem, stream, a);
     if (err != cudaSuccess || a.splits == 1)
         return err;
     const int64_t n4 = static_cast<int64_t>(q.M) * q.N / 4;
