@@ -86,6 +86,15 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s), burst."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("grouped_gemm.cu", "ptx.cuh"):
@@ -486,6 +495,11 @@ def run_gpu(args, cfg, world, rank, local):
         "us_per_layer": mean_ms_all * 1e3,
         "us_per_layer_serialised": serial_ms * 1e3,
         "layer_frac_of_hbm_peak": value / world / peak,
+        # the layer's dense-contraction work, A * 2 * (2 m d + d m) FLOP, against
+        # the measured bf16 tensor peak (the 2048-token canvas is compute-bound)
+        "layer_tflops": cfg.M * cfg.k * 2.0 * 3 * cfg.m * cfg.d / (mean_ms_all * 1e-3) / 1e12,
+        "layer_frac_of_tensor_peak": (cfg.M * cfg.k * 2.0 * 3 * cfg.m * cfg.d /
+                                      (mean_ms_all * 1e-3) / 1e12) / bf16_peak()[0],
         "alg_bytes_per_step": nbytes, "touched_experts": touched,
         "kernels_us": {k: statistics.fmean(v) * 1e3 for k, v in per_kernel.items()},
         "kernels_us_note": "serialised pass (events between the launches), "
