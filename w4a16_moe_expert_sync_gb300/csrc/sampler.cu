@@ -5,11 +5,12 @@
 // gumbel_argmax_sample draws from the same Categorical with Philox noise made
 // inline, the argmax coming out of the same reduction).
 //
-// Layout of the work: a row is cut into chunks of kChunkQuads quads (4
-// consecutive logits); one 256-thread CTA per (row, chunk) reduces its chunk
-// to a partial (online-softmax state, best perturbed score, best logit), and
-// a second launch merges each row's partials in chunk order.  Every reduction
-// runs in a fixed order, so results do not depend on scheduling.
+// Layout of the work: the rows are laid end to end as quads (4 consecutive
+// logits) and cut into equal spans, one per persistent 256-thread CTA (three
+// per SM); a CTA reduces each row segment of its span to a partial
+// (online-softmax state, best perturbed score, best logit), and a second
+// launch merges each row's partials.  Every reduction runs in a fixed order,
+// so results do not depend on scheduling (the spans depend on the SM count).
 //
 // Noise (Philox4x32-10, Salmon et al., SC 2011): key = (seed lo, seed hi);
 // the quad q of row t uses counter (q, t, offset lo, offset hi) and its
