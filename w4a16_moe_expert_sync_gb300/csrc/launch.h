@@ -82,7 +82,8 @@ struct GroupedGemmProblem {
     // down may then read its schedule, and stream its weights, before its
     // grid-dependency wait.  Activations are read only after that wait.
     bool early_schedule = false;
-    // plain (down) epilogue only: write bf16 rows instead of fp32 ones
+    // plain (down) epilogue only: write bf16 rows instead of fp32 ones (no
+    // entry point sets it at present: the dense linear has its own kernel)
     bool out_bf16 = false;
 };
 
