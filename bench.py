@@ -275,10 +275,18 @@ def cpu_baseline(cfg, n_tokens):
     dt = time.perf_counter() - t0
     touched = len(set(int(v) for v in ids[tokens].ravel()))
     nbytes = layer_alg_bytes(len(tokens), cfg.d, cfg.m, cfg.k, touched)
+    # the same oracle on one thread, two tokens (the per-token cost is the same
+    # work, so seconds per layer scale by tokens)
+    t1 = time.perf_counter()
+    oracle.moe_layer(x_bits[tokens[:2]], gu, dn, ids[tokens[:2]], w[tokens[:2]], nthreads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"{n_tokens} of {cfg.M} tokens of the {cfg.name} workload (all {cfg.k} "
                       f"experts each, {n_tokens * cfg.k} assignments, {touched} experts), "
-                      f"float64 C oracle on {nthreads} threads, {dt:.2f} s wall"}
+                      f"float64 C oracle on {nthreads} threads, {dt:.2f} s wall",
+            "s_per_layer": {"all_cores": dt / len(tokens) * cfg.M,
+                            "one_thread": dt1 / 2 * cfg.M,
+                            "note": f"extrapolated from the samples to all {cfg.M} tokens"}}
 
 
 def run_reference(args, cfg, world, rank):
