@@ -89,3 +89,49 @@ def test_binding_raises_on_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         w4.w4_moe_route(torch.zeros(4, 8), 2)
+
+
+def test_beside_the_layer_validates_without_launching(clib):
+    """RMSNorm, the sampler and the dense linear reject bad arguments on the
+    host, before any device call; empty batches are accepted."""
+    P = ctypes.c_void_p
+    fake = P(0x10000)          # never dereferenced: validation fails first
+    odd = P(0x10004)           # 4-byte but not 16-byte aligned
+    odd2 = P(0x10002)          # not 4-byte aligned
+    # RMSNorm
+    assert clib.w4_rmsnorm(fake, fake, 4, 100, 1e-6, fake, None) == 2      # d % 8
+    assert clib.w4_rmsnorm(fake, fake, 4, 64, -1.0, fake, None) == 1       # eps < 0
+    assert clib.w4_rmsnorm(odd, fake, 4, 64, 1e-6, fake, None) == 3        # misaligned x
+    assert clib.w4_rmsnorm(None, fake, 0, 64, 1e-6, None, None) == 0       # empty batch
+    # sampler
+    big = 1 << 24
+    assert clib.w4_sample_logits(fake, 4, 0, 1, 0, fake, None, None, fake, big, None) == 1
+    assert clib.w4_sample_logits(fake, 4, 1000, 1, 0, None, None, None, fake, big, None) == 1
+    assert clib.w4_sample_logits(odd2, 4, 1000, 1, 0, fake, None, None, fake, big, None) == 3
+    assert clib.w4_sample_logits(fake, 4, 1000, 1, 0, fake, None, None, fake, 16, None) == 6
+    assert clib.w4_sample_logits(None, 0, 1000, 1, 0, None, None, None, None, 0, None) == 0
+    assert clib.w4_sample_logits_workspace_size(256, 262144) == (2048 + 256) * 32
+    assert clib.w4_fused_entropy(fake, 4, 1000, None, fake, big, None) == 1
+    assert clib.w4_gumbel_argmax_sample(fake, 4, 1000, 1, 0, None, None, fake, big, None) == 1
+    # dense linear: shapes, groups, alignment, workspace
+    lin = [fake, 4, 512, 256, fake, fake, fake, 128, fake, big, fake, None, None]
+    assert clib.w4_w4a16_linear(*lin[:3], 200, *lin[4:]) == 2              # N % 128
+    assert clib.w4_w4a16_linear(*lin[:7], 96, *lin[8:]) == 2               # group
+    assert clib.w4_w4a16_linear(fake, 4, 128, 256, *lin[4:]) == 2          # K < 256
+    assert clib.w4_w4a16_linear(fake, 4, 8192, 256, *lin[4:]) == 2         # 64 groups
+    assert clib.w4_w4a16_linear(odd, *lin[1:]) == 3
+    assert clib.w4_w4a16_linear(*lin[:9], 16, *lin[10:]) == 6
+    assert clib.w4_w4a16_linear(None, 0, 512, 256, None, None, None, 128, None, 0, None, None,
+                                None) == 0
+
+
+def test_linear_split_rule_depends_on_the_shape_only(clib):
+    """The contraction split (visible in the workspace's partial sums): about
+    128 units of 128 weight rows x 256 tokens, at most 8 splits of at least
+    4 steps of 64 codes; no partial buffer when there is no split."""
+    ws = clib.w4_w4a16_linear_workspace_size
+    base = ws(256, 2816, 16384, 128)              # 128 panels: no split
+    assert ws(256, 2816, 4096, 128) - base == 4 * 256 * 4096 * 4     # 32 panels: 4 splits
+    one = ws(33, 2816, 128, 128)                  # one panel: 8 splits
+    assert one >= 8 * 33 * 128 * 4 and one - 8 * 33 * 128 * 4 < 2 * 48 * 2816 + 4096
+    assert ws(16, 256, 128, 128) < 16 * 256 * 2 + 4096                # 4 steps: no split

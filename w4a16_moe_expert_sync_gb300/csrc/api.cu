@@ -524,6 +524,8 @@ int w4_rmsnorm(const uint16_t *x, const uint16_t *weight, int M, int d, float ep
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "M * d must be below 2^31");
     if (!aligned16(x) || !aligned16(weight) || !aligned16(y))
         return fail(W4_ERR_MISALIGNED, "x, weight and y must be 16-byte aligned");
+    if (M == 0)
+        return W4_OK;
     if (int rc = check_device())
         return rc;
     cudaError_t err = w4::launch_rmsnorm(x, weight, M, d, eps, y, as_stream(stream));
