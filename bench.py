@@ -942,11 +942,11 @@ def run_linear(args, world, rank, local):
         "timing": f"{replays} replays of a CUDA graph of {per_graph} calls (qkv256)",
         "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak_bf16,
                      "unit": "TFLOP/s", "frac": value / world / peak_bf16, "traffic": None,
-                     "kernel": "grouped_gemm_kernel<down> with one expert (w4_w4a16_linear)",
+                     "kernel": "dense_gemm_kernel (w4_w4a16_linear, qkv256)",
                      "alg_flops_per_launch": flops, "peak_source": peak_kind,
-                     "note": "at 256 rows the contraction is compute-bound; this path "
-                             "dequantises the weight once per 32-token job (8 times at 256 "
-                             "rows), which bounds it instead"},
+                     "note": "each 128-row weight panel is dequantised once per pass of up "
+                             "to 256 token rows; at these sizes the call is bound by its "
+                             "fixed per-call and per-CTA latency, not by the tensor pipe"},
         "e2e": e2e, "gpu_launches": 2 * replays * per_graph, "clocks": clocks,
         "timed_region_wall_s": wall,
     }

@@ -78,10 +78,10 @@ int w4_abi_version(void);
 
 /* --------------------------------------------------------------------------
  * w4_quantize -- quantize_w4, the checkpoint packer
- * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: asymmetric uint4,
- *  fp16 scale and zero-point per group, two nibbles per byte,
- *  byte j = q[2j] | q[2j+1] << 4; -- Benchmarks: round-to-nearest min/max;
- *  "dg-w4-kernels" -- W4A16: qw, scale, zero = quantize_w4(W, group_size)).
+ * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: 4-bit unsigned
+ *  codes with an fp16 scale and zero point per group, packed low nibble
+ *  first; -- Benchmarks: min/max round-to-nearest with no calibration;
+ *  "dg-w4-kernels" -- W4A16: the packer's Python call, quantize_w4).
  *
  *   W   [E, N, K] fp32, row-major (contraction dim K innermost)
  *   q   [E, N, K/2] uint8 out, two codes per byte, low nibble first
@@ -308,9 +308,11 @@ int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int 
  * cudaMalloc, no cudaFree, no allocating library routine.  Nothing in the
  * array needs to start at zero.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, which may load the module onto that device); make
- * that first call before any stream capture.
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, host-only), so the address always belongs to the
+ * current context, also after a cudaDeviceReset.  The first call on a device
+ * may load the library's module onto it; make that first call before any
+ * stream capture.
  *
  * Every call on a device shares the one array: calls whose GPU work overlaps
  * (different streams, or different host threads with different streams)

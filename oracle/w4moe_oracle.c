@@ -8,10 +8,12 @@
  * includes or links the other.
  *
  * Sources (page title -- section):
- *   [CK] "diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: asymmetric
- *        uint4, fp16 scale and zero-point per group, two nibbles per byte
- *        (byte j = q[2j] | q[2j+1] << 4); gate_up groups of 128 along the
- *        contraction dim, down_proj groups of 64 (its contraction dim is 704).
+ *   [CK] "diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: each weight is
+ *        a 4-bit unsigned code with an fp16 scale and an fp16 (asymmetric)
+ *        zero point shared by a group of consecutive contraction elements;
+ *        byte j of a packed row holds code 2j in its low nibble and code
+ *        2j+1 in its high nibble; the group is 128 for gate_up and 64 for
+ *        down, whose 704-wide contraction 128 does not divide.
  *   [BM] same page -- Benchmarks: quantisation is round-to-nearest min/max,
  *        no calibration.
  *   [CAP] "Inference: Making every denoising pass fast" -- The first
@@ -19,10 +21,11 @@
  *        scale s_g and zero point z_g (the formula itself did not survive
  *        extraction; read as w_i = s_g * (q_i - z_g)).
  *   [SP] same post -- Quantisation alone leaves a sparse execution problem:
- *        the router picks 8 of 128, runs the token through those eight,
- *        weights the outputs and adds them; assignments are sorted by expert
- *        and padded into regular blocks; the eight outputs of a token are
- *        reduced in a fixed order, never with atomics.
+ *        each token is routed to k = 8 of E = 128 experts and its output is
+ *        the routing-weighted sum of those experts' outputs; the assignments
+ *        are grouped by expert and padded to whole blocks before the GEMMs,
+ *        and each token's k partial outputs are summed in one fixed order
+ *        with no atomic adds.
  *   [GM] "dg-w4-kernels" -- Grouped MoE: alignment is sync-free, the
  *        activation is folded into the first GEMM's epilogue, the weighted
  *        combine is a fixed-order reduction.

@@ -82,3 +82,65 @@ def gpu_inputs(name: str):
     x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
     lg = torch.from_numpy(logits).cuda()
     return cfg, x, lg, x_bits, logits
+
+
+def job_covering_tokens(ids: np.ndarray, E: int, block_m: int = 16, job_slots: int = 32):
+    """Tokens that together reach every job of every expert: the alignment
+    splits an expert's padded slot range into jobs of `job_slots`; walking
+    the jobs in order, the first token of each job not yet reached is taken.
+    Used where the oracle cannot afford every token (the 2048-token canvas)."""
+    import oracle
+    M, k = ids.shape
+    al = oracle.moe_align(ids, E, block_m)
+    offs, sorted_ids = al["expert_offsets"], al["sorted_ids"]
+    A = M * k
+    covered = set()
+    toks = []
+    for e in range(E):
+        for start in range(int(offs[e]), int(offs[e + 1]), job_slots):
+            job = (e, start)
+            if job in covered:
+                continue
+            a = int(sorted_ids[start])
+            if a >= A:
+                continue
+            t = a // k
+            toks.append(t)
+            # every job this token's assignments fall in
+            for j in range(k):
+                aa = t * k + j
+                slot = int(np.nonzero(sorted_ids == aa)[0][0])
+                ee = int(ids[t, j])
+                covered.add((ee, int(offs[ee]) + (slot - int(offs[ee])) // job_slots * job_slots))
+    return np.array(sorted(set(toks)), dtype=np.int64)
+
+
+@functools.lru_cache(maxsize=4)
+def oracle_layer(name: str, token_set: str = "all"):
+    """The oracle's layer on a workload, with its intermediates: returns
+    (toks, ids, w, out, h, y) where toks are the tokens evaluated ("all", or
+    "cover": job_covering_tokens), ids/w the oracle's routing of every
+    token, and out [len(toks), d], h/y [len(toks)*k, ...] the oracle's
+    results for those tokens only."""
+    import oracle
+    cfg = wl.CONFIGS[name]
+    x_bits = wl.activations(cfg)
+    ids, w = oracle.route(wl.router_logits(cfg), cfg.k)
+    toks = (np.arange(cfg.M) if token_set == "all" else job_covering_tokens(ids, cfg.E))
+    ogu, odn = oracle_weights(cfg, ids[toks].ravel())
+    out, h, y = oracle.moe_layer(x_bits[toks], ogu, odn, ids[toks], w[toks],
+                                 want_intermediates=True)
+    return toks, ids, w, out, h, y
+
+
+def elementwise_excess(got, ref, rel: float) -> float:
+    """max over elements of (|got - ref| - rel * |ref|) / rms(ref): the part of
+    each element's error that its own rounding (rel * |ref|) does not account
+    for, in units of the reference's rms.  <= tau means every element is
+    within rel * |ref| + tau * rms(ref)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = np.sqrt(np.mean(ref ** 2))
+    if not ref.size:
+        return 0.0
+    return float(np.max(np.abs(got - ref) - rel * np.abs(ref)) / rms)

@@ -42,26 +42,38 @@ def test_layer_matches_oracle(lib, name, block_m):
     assert int(status.item()) == 0
 
 
+# Elementwise bar beside the max/rms one: each output element may differ
+# from the oracle by its own bf16 rounding (<= 2^-8 |out|) plus TAU_OUT of the
+# output's rms.  TAU_OUT bounds the compute error before that rounding: every
+# dequantised weight and h carry one fp16 rounding (relative <= 2^-11) and
+# each group's constant -z*s one more, which after the two contractions and
+# the weighted sum leaves ~5e-4 rms relative error, so its largest value over
+# the ~720k outputs of a 256-token layer stays near 3e-3.
+TAU_OUT = 6e-3
+
+
 @pytest.mark.parametrize("name", ["layer256", "zipf256", "canvas2048", "sweep_M1", "sweep_M8",
                                   "sweep_M64"])
-def test_layer_full_size_sampled(lib, name):
+def test_layer_full_size(lib, name):
     """Pages' layer shape, every M of the sweep, skewed routing and the
-    multi-canvas batch: the sampled tokens' rows agree with the oracle."""
+    multi-canvas batch.  Every token is compared with the oracle, except on
+    the 2048-token canvas, where the tokens compared reach every 32-slot job
+    of every expert (each expert there spans several jobs)."""
     import torch
+    from helpers import elementwise_excess, oracle_layer
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     cfg, x_bits, logits, ids, w, out = _layer(lib, name, 16, status)
-    oids, ow = oracle.route(logits, cfg.k)
+    toks, oids, ow, ref, _, _ = oracle_layer(name, "cover" if name == "canvas2048" else "all")
     assert np.array_equal(ids.cpu().numpy(), oids)
-    n = min(cfg.M, 4)
-    toks = np.sort(np.random.default_rng(1).choice(cfg.M, size=n, replace=False))
-    ogu, odn = oracle_weights(cfg, oids[toks].ravel())
-    ref = oracle.moe_layer(x_bits[toks], ogu, odn, oids[toks], ow[toks])
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), ow.view(np.uint32))
     got = torch_bf16_to_f64(out)[toks]
     err = rel_max_err(got, ref)
     floor = rel_max_err(bf16_round(ref), ref)
-    print(f"{name}: sampled tokens {toks.tolist()} max|gpu-oracle|/rms = {err:.3e} "
-          f"(bf16 rounding alone: {floor:.3e})")
+    excess = elementwise_excess(got, ref, 2.0 ** -8)
+    print(f"{name}: {len(toks)} tokens, max|gpu-oracle|/rms = {err:.3e} (bf16 rounding alone: "
+          f"{floor:.3e}); elementwise excess over 2^-8|ref| = {excess:.3e} rms")
     assert err <= LAYER_TOL
+    assert excess <= TAU_OUT
     assert int(status.item()) == 0
 
 

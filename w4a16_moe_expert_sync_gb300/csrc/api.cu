@@ -86,6 +86,8 @@ int check_gemm_common(int M, int d, int m, int E, int k, int block_m, const void
 
 }  // namespace
 
+int w4::check_device_sm103() { return check_device(); }
+
 int w4::set_error_detail(int status, const char *detail)
 {
     return fail(status, "%s", detail);

@@ -110,6 +110,11 @@ cudaError_t launch_dense_gemm(const DenseGemmProblem &p, cudaStream_t stream, co
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem &p, cudaStream_t stream,
                                 const char **why);
 
+// W4_OK when the current device is an sm_103 part, else W4_ERR_NO_DEVICE or
+// W4_ERR_CUDA with the detail recorded (the argument checks of every entry
+// point call it before launching).
+int check_device_sm103();
+
 // Records `detail` as the text w4_last_error_detail() returns on this thread
 // and passes `status` through.
 int set_error_detail(int status, const char *detail);

@@ -88,12 +88,17 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
             my_idx = be;
         }
     }
-    const float ex = lane < k ? expf(my_val - top) : 0.0f;
-    float sum = 0.0f;
+    // The weights in float64, rounded to fp32 once: exp(l_j - l_top) over
+    // the sum of the k selected, summed in slot order.  That is the
+    // renormalised softmax of the k (the full softmax's normaliser cancels),
+    // so the fp32 result is the float64 softmax's, bar a float64 rounding
+    // difference that lands on an fp32 rounding boundary.
+    const double ex = lane < k ? exp(static_cast<double>(my_val) - static_cast<double>(top)) : 0.0;
+    double sum = 0.0;
     for (int j = 0; j < k; j++)
         sum += __shfl_sync(0xffffffffu, ex, j);
     *id = lane < k ? my_idx : -1;
-    *w = lane < k ? ex / sum : 0.0f;
+    *w = lane < k ? static_cast<float>(ex / sum) : 0.0f;
 }
 
 template <int EPL>

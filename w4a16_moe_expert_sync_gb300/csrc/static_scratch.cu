@@ -14,7 +14,6 @@
 // calls whose GPU work overlaps (two streams, or two host threads with
 // different streams) race on it; issue them on one stream, one after another.
 #include <cstdio>
-#include <mutex>
 
 #include "../../include/w4moe.h"
 #include "launch.h"
@@ -27,30 +26,21 @@ namespace {
 // before reading it.
 __device__ __align__(256) unsigned char g_layer_scratch[W4_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_layer_scratch on the current device, looked up once per
-// device.  The first lookup may load this library's module onto the device.
+// Device address of g_layer_scratch on the current device.  It is looked up
+// on every call (a host-side table lookup once the module is loaded), so an
+// address never outlives the context it belongs to: after cudaDeviceReset
+// the next call finds the array in the new context.  The first lookup on a
+// device may load this library's module onto it.
 int scratch_address(void **out)
 {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess)
-        return w4::set_error_detail(W4_ERR_CUDA, "cudaGetDevice failed");
-    if (dev < 0 || dev >= kMaxDevices)
-        return w4::set_error_detail(W4_ERR_NO_DEVICE, "device ordinal out of range");
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_layer_scratch);
-        if (err != cudaSuccess || !p)
-            return w4::set_error_detail(W4_ERR_CUDA,
-                                        "cudaGetSymbolAddress(static layer scratch) failed");
-        g_scratch_ptr[dev] = p;
+    void *p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_layer_scratch);
+    if (err != cudaSuccess || !p) {
+        (void)cudaGetLastError();   // leave no pending error for later launches to report
+        return w4::set_error_detail(W4_ERR_CUDA,
+                                    "cudaGetSymbolAddress(static layer scratch) failed");
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return W4_OK;
 }
 
@@ -73,6 +63,8 @@ extern "C" int w4_moe_layer_static_scratch(
                  need, static_cast<size_t>(W4_STATIC_SCRATCH_BYTES));
         return w4::set_error_detail(W4_ERR_WORKSPACE, msg);
     }
+    if (int rc = w4::check_device_sm103())   // before the lookup: a wrong device is not a CUDA error
+        return rc;
     void *scratch = nullptr;
     if (int rc = scratch_address(&scratch))
         return rc;
