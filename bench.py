@@ -362,6 +362,74 @@ def prepare_gpu(cfg, dev):
     return x, ids, w, gu, dn
 
 
+SWEEP_CONFIGS = ("sweep_M1", "sweep_M8", "sweep_M32", "sweep_M64", "sweep_M128", "sweep_M256",
+                 "zipf256", "canvas2048")
+
+
+def time_configs(args, gu, dn, dev, status):
+    """The layer across the survey's other configurations (the M sweep, Zipf
+    routing, the 2048-token canvas), compactly: each config's own activations
+    and routing (its seed) with the packed weights already on the device
+    (same shapes; the time does not depend on the weight values).  Per
+    config: back-to-back w4_moe_layer calls between one pair of events, then a
+    serialised pass for the two GEMMs."""
+    import torch
+    import w4a16_moe_expert_sync_gb300 as w4
+    from w4a16_moe_expert_sync_gb300 import workloads as wl
+    peak, _ = measured_peaks()
+    tpeak = bf16_peak()[0]
+    res = {}
+    for name in SWEEP_CONFIGS:
+        c = wl.CONFIGS[name]
+        x = torch.from_numpy(wl.activations(c).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids, w = w4.w4_moe_route(torch.from_numpy(wl.router_logits(c)).to(dev), c.k)
+        touched = int(torch.unique(ids).numel())
+        ws = torch.empty(w4.w4_moe_layer_workspace_size(c.M, c.d, c.m, c.E, c.k, args.block_m),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty((c.M, c.d), dtype=torch.bfloat16, device=dev)
+        steps = 50 if c.M <= 256 else 20
+
+        def layer():
+            w4.w4_moe_layer(x, ids, w, gu, dn, block_m=args.block_m, workspace=ws, out=out,
+                            dev_status=status)
+
+        for _ in range(3):
+            layer()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            layer()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        al, xg = w4.w4_moe_align_gather(ids, x, c.E, args.block_m, dev_status=status)
+        h = w4.w4_grouped_gemm_gate_up(xg, *gu, al, dev_status=status)
+        y = w4.w4_grouped_gemm_down(h, *dn, al, dev_status=status)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        gsum = [0.0, 0.0]
+        for i in range(12):
+            ev[0].record()
+            w4.w4_grouped_gemm_gate_up(xg, *gu, al, h=h, dev_status=status)
+            ev[1].record()
+            w4.w4_grouped_gemm_down(h, *dn, al, y=y, dev_status=status)
+            ev[2].record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                gsum[0] += ev[0].elapsed_time(ev[1]) / 10
+                gsum[1] += ev[1].elapsed_time(ev[2]) / 10
+        nbytes = layer_alg_bytes(c.M, c.d, c.m, c.k, touched)
+        flops = c.M * c.k * 2.0 * 3 * c.m * c.d
+        res[name] = {"M": c.M, "routing": c.routing, "touched_experts": touched,
+                     "us_per_layer": ms * 1e3,
+                     "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peak,
+                     "frac_tensor": flops / (ms * 1e-3) / 1e12 / tpeak,
+                     "gate_up_us": gsum[0] * 1e3, "down_us": gsum[1] * 1e3}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} in the config sweep")
+    return res
+
+
 def run_gpu(args, cfg, world, rank, local):
     import torch
     import w4a16_moe_expert_sync_gb300 as w4
@@ -521,6 +589,13 @@ def run_gpu(args, cfg, world, rank, local):
                      "fused rounding), fp16 x fp16 tcgen05 MMA with fp32 accumulation, bf16 "
                      "activations in and out",
     }
+    if rank == 0 and world == 1 and not args.skip_configs and cfg.name == "layer256":
+        line["configs"] = time_configs(args, gu, dn, dev, status)
+        line["configs_note"] = ("the other configurations of the layer, each with its own "
+                                "activations and routing and the layer256 packed weights: "
+                                "back-to-back w4_moe_layer calls (50, or 20 at M=2048); "
+                                "gate_up/down from a serialised pass; fractions of the "
+                                "measured HBM and bf16 peaks")
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(cfg, args.cpu_tokens).items()
                                 if k != "seconds"}
@@ -973,6 +1048,8 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-clocks", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="leave out the compact timing of the other layer configurations")
     ap.add_argument("--workload", choices=["layer", "sampler", "rmsnorm", "linear"],
                     default="layer")
     args = ap.parse_args()

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 6
+#define W4MOE_ABI_VERSION 7
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -66,6 +66,10 @@ typedef enum {
                                          incomplete                              */
 #define W4_DEV_TOO_MANY_JOBS 0x4      /* internal job list overflow (cannot
                                          happen for shapes the host accepted)   */
+#define W4_DEV_FP16_RANGE 0x8         /* an activation (x, or h after the gated
+                                         activation) lay outside fp16's finite
+                                         range and was saturated to +-65504:
+                                         the GEMMs' operands are fp16           */
 
 /* Human-readable name of a w4_status value (static string). */
 const char *w4_status_string(int status);
@@ -143,27 +147,41 @@ int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m,
  * the order 0,4,1,5,2,6,3,7.  Gathered activations (xg) and h use this
  * order; it is an implementation layout, not part of the checkpoint format.
  *
+ * Group sums.  Every xg and h row ends in one block of 64 fp16 columns of
+ * sums of its own fp16 values: xg column d + g holds the sum of group g (128
+ * consecutive elements of x), h column m + 4 g + i the sum of quarter i (16
+ * intermediates) of group g of 64; the columns past the last sum, up to a
+ * multiple of 16, hold zero, and the rest of the block is not written.  The GEMMs multiply them by the part of each
+ * group's dequantisation constant -z*s that its fp16 rounding dropped, so
+ * every dequantised weight is exact to its own fp16 rounding.  Hence
+ * d <= 8192 and m <= 1024.
+ *
  * w4_gather_activations -- the gate_up GEMM's input in slot order:
- *   xg [cap, d] fp16 out: for every slot < num_padded, the row of token
- *   sorted_ids[slot] / k of x converted to fp16 in block order, or zeros for
- *   a padding slot; rows >= num_padded are not written.
+ *   xg [cap, d + 64] fp16 out: for every slot < num_padded, the row of token
+ *   sorted_ids[slot] / k of x converted to fp16 in block order, then its
+ *   group sums, or zeros for a padding slot; rows >= num_padded are not
+ *   written.
  * x [M, d] bf16; sorted_ids / num_padded from w4_moe_align with the same k,
  * E, block_m.  bf16 -> fp16 rounds to nearest even: exact for magnitudes in
  * [2^-14, 65504], within 2^-25 below that (fp16 subnormals); larger
- * magnitudes saturate to +-65504.  Requires d % 8 == 0, x and xg 16-byte
- * aligned.
+ * magnitudes (and inf, NaN) do not fit: they saturate to +-65504 (NaN stays
+ * NaN) and set W4_DEV_FP16_RANGE in *dev_status (may be NULL), as does a
+ * group sum beyond that range.  Requires d % 128 == 0, d <= 8192, x and xg
+ * 16-byte aligned.
  * ------------------------------------------------------------------------ */
 int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          w4_stream_t stream);
+                          int32_t *dev_status, w4_stream_t stream);
 
 /* w4_moe_align_gather -- w4_moe_align and w4_gather_activations in one launch:
- * every CTA computes the alignment in its own shared memory (so no CTA waits
- * on another) and writes a share of the alignment outputs, and each CTA
- * copies the rows of a range of tokens to the slots of their assignments.
- * The first launch of w4_moe_layer.  Arguments and outputs as in those two
- * calls; when the assignments do not fit in shared memory it issues them as
- * two launches. */
+ * every CTA counts all assignments per expert in its own shared memory (so no
+ * CTA waits on another), places the assignments of its own range of tokens
+ * and copies those tokens' rows to their slots; the grid writes the padding
+ * slots and block owners.  The first launch of w4_moe_layer.  Arguments and
+ * outputs as in those two calls, except that the xg rows of padding slots
+ * are NOT written (their contents are unspecified; the GEMMs discard or
+ * zero what they produce for padding slots).  Activations outside fp16's
+ * range set W4_DEV_FP16_RANGE. */
 int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d, int k, int E,
                         int block_m, int32_t *sorted_ids, int32_t *block_expert,
                         int32_t *expert_offsets, int32_t *num_padded, uint16_t *xg,
@@ -199,18 +217,25 @@ int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int
  *  folded into the first GEMM's epilogue; "diffusiongemma-26B-A4B-w4a16" --
  *  Checkpoint format: gate_up groups of 128 along the contraction dim).
  *
- *   xg             [cap, d] fp16 from w4_gather_activations (slot order)
+ *   xg             [cap, d + 64] fp16 from w4_gather_activations (slot order,
+ *                  values then group sums)
  *   gu_q           [E, 2m, d/2] uint8 (w4_quantize layout), gu_s/gu_z
  *                  [E, 2m, d/group] fp16; rows [0, m) gate, [m, 2m) up
  *   sorted_ids, expert_offsets   from w4_moe_align with the same block_m
- *   h              [cap, m] fp16 out in block order, row = alignment slot:
- *                  h[slot] = gelu_tanh(g) * u for the token of sorted_ids[slot],
- *                  zero rows for padding slots inside an expert's range;
- *                  rows at slots >= num_padded are not written
+ *   h              [cap, m + 64] fp16 out, row = alignment slot: m values in
+ *                  block order, h[slot] = gelu_tanh(g) * u for the token of
+ *                  sorted_ids[slot], then the quarter sums of h's groups of
+ *                  64 (see "Group sums"); zero rows for padding slots inside
+ *                  an expert's range (whatever xg holds there); rows at slots
+ *                  >= num_padded are not written.  A value of h (or a sum)
+ *                  beyond fp16's range saturates to +-65504 and sets
+ *                  W4_DEV_FP16_RANGE.
  * Weights are dequantised in registers to fp16 as q * s + fp16(-z * s) (one
- * fused rounding) and multiplied on the tensor cores (tcgen05, fp16 x fp16
- * -> fp32); h is rounded to fp16 with saturation at +-65504.
- * Requires d % 128 == 0, m % 64 == 0, group == 128.
+ * fused rounding; scaled by a power of two per weight row, undone exactly in
+ * fp32), multiplied on the tensor cores (tcgen05, fp16 x fp16 -> fp32), and
+ * the part of -z * s lost to its fp16 rounding is added back through the
+ * group sums; h is rounded to fp16 with saturation at +-65504.
+ * Requires d % 128 == 0, d <= 8192, m % 64 == 0, m <= 1024, group == 128.
  * dev_status may be NULL.
  * ------------------------------------------------------------------------ */
 int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
@@ -225,13 +250,15 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int 
  * ("diffusiongemma-26B-A4B-w4a16" -- Checkpoint format: down_proj groups of
  *  64 because 128 does not divide 704).
  *
- *   h              [cap, m] fp16 in block order (from w4_grouped_gemm_gate_up)
+ *   h              [cap, m + 64] fp16 from w4_grouped_gemm_gate_up (values in
+ *                  block order, then quarter sums)
  *   dn_q           [E, d, m/2] uint8, dn_s/dn_z [E, d, m/group] fp16
  *   y              [M*k, d] fp32 out, row a = flat assignment index
  *                  (y[a] = h[slot of a] . deq(Wdn[e])^T); rows of skipped
  *                  (invalid-id) assignments are not written
- * Same dequantisation as gate_up.
- * Requires d % 128 == 0, m % 64 == 0, group == 64.  dev_status may be NULL.
+ * Same dequantisation and correction as gate_up.
+ * Requires d % 128 == 0, d <= 8192, m % 64 == 0, m <= 1024, group == 64.
+ * dev_status may be NULL.
  * ------------------------------------------------------------------------ */
 int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
                          const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z,

@@ -115,7 +115,7 @@ def job_covering_tokens(ids: np.ndarray, E: int, block_m: int = 16, job_slots: i
     return np.array(sorted(set(toks)), dtype=np.int64)
 
 
-@functools.lru_cache(maxsize=4)
+@functools.lru_cache(maxsize=8)
 def oracle_layer(name: str, token_set: str = "all"):
     """The oracle's layer on a workload, with its intermediates: returns
     (toks, ids, w, out, h, y) where toks are the tokens evaluated ("all", or

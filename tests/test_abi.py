@@ -39,7 +39,7 @@ def test_header_compiles_as_plain_c():
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4_abi_version() == 6
+    assert clib.w4_abi_version() == 7
     assert clib.w4_status_string(0) == b"W4_OK"
     assert clib.w4_status_string(2) == b"W4_ERR_UNSUPPORTED_SHAPE"
     assert clib.w4_status_string(99) == b"W4_ERR_UNKNOWN"
@@ -79,7 +79,7 @@ def test_argument_validation_without_launching(clib):
     dargs = [fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake, None, None]
     assert clib.w4_grouped_gemm_down(*dargs) == 2
     # gather: d must be a multiple of 8
-    assert clib.w4_gather_activations(fake, 4, 252, 2, 8, 16, fake, fake, fake, None) == 2
+    assert clib.w4_gather_activations(fake, 4, 252, 2, 8, 16, fake, fake, fake, None, None) == 2
     # workspace too small
     assert clib.w4_moe_layer(fake, fake, fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128,
                              fake, fake, fake, 64, fake, 16, fake, None, None) == 6

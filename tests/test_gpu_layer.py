@@ -44,12 +44,11 @@ def test_layer_matches_oracle(lib, name, block_m):
 
 # Elementwise bar beside the max/rms one: each output element may differ
 # from the oracle by its own bf16 rounding (<= 2^-8 |out|) plus TAU_OUT of the
-# output's rms.  TAU_OUT bounds the compute error before that rounding: every
-# dequantised weight and h carry one fp16 rounding (relative <= 2^-11) and
-# each group's constant -z*s one more, which after the two contractions and
-# the weighted sum leaves ~5e-4 rms relative error, so its largest value over
-# the ~720k outputs of a 256-token layer stays near 3e-3.
-TAU_OUT = 6e-3
+# output's rms.  TAU_OUT bounds the compute error before that rounding: fp16
+# rounding of every dequantised weight, of each group's constant -z*s and of
+# h leave ~1e-3 rms relative error in y (see test_gpu_gemm.py), which the
+# weighted sum of a token's k rows keeps at that level; ~10x that rms.
+TAU_OUT = 1e-2
 
 
 @pytest.mark.parametrize("name", ["layer256", "zipf256", "canvas2048", "sweep_M1", "sweep_M8",
@@ -166,3 +165,45 @@ def test_layer_token_with_no_valid_expert_is_zero(lib):
     assert int(status.item()) & lib.W4_DEV_BAD_EXPERT_ID
     assert torch.count_nonzero(out[5].view(torch.int16)) == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_layer_activation_range_is_flagged(lib):
+    """The GEMMs' operands are fp16 (a reading of this build; the pages'
+    kernels use bf16).  A token whose activations exceed fp16's range
+    (|x| up to ~4e5 here) is saturated and W4_DEV_FP16_RANGE is raised;
+    tokens whose activations lie mostly below 2^-14 (fp16 subnormals, absolute
+    step 2^-24) keep the layer's bound; every other token is unaffected."""
+    import torch
+    from helpers import bf16_bits_to_f64
+    name = "tiny"
+    cfg = wl.CONFIGS[name]
+    x_bits = wl.activations(cfg).copy()
+    xf = bf16_bits_to_f64(x_bits)
+    big, small = 3, [5, 6]
+    xf[big] *= 1e5
+    xf[small] *= 1e-4
+    x_bits = wl.f32_to_bf16_bits(xf.astype(np.float32))
+    assert np.abs(bf16_bits_to_f64(x_bits[big])).max() > 65504
+    assert np.mean(np.abs(bf16_bits_to_f64(x_bits[small])) < 2.0 ** -14) > 0.3
+    logits = wl.router_logits(cfg)
+    gu, dn = gpu_weights(name)
+    oids, ow = oracle.route(logits, cfg.k)
+    ids_d, w_d = torch.from_numpy(oids).cuda(), torch.from_numpy(ow).cuda()
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = lib.w4_moe_layer(x, ids_d, w_d, gu, dn, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & lib.W4_DEV_FP16_RANGE
+    ogu, odn = oracle_weights(cfg, range(cfg.E))
+    ref = oracle.moe_layer(x_bits, ogu, odn, oids, ow)
+    keep = np.array([t for t in range(cfg.M) if t != big])
+    err = rel_max_err(torch_bf16_to_f64(out)[keep], ref[keep])
+    print(f"activation range: other tokens max|gpu-oracle|/rms = {err:.3e}")
+    assert err <= LAYER_TOL
+    # the same batch without the out-of-range row raises nothing
+    x_ok = x.clone()
+    x_ok[big] = x[0]
+    status.zero_()
+    lib.w4_moe_layer(x_ok, ids_d, w_d, gu, dn, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0

@@ -110,7 +110,11 @@ def test_route_align_gather_matches_the_separate_calls(lib, name, bm):
     for key in ("sorted_ids", "block_expert", "expert_offsets", "num_padded"):
         assert torch.equal(al[key], ral[key])
     npad = int(ral["num_padded"].item())
-    assert torch.equal(xg[:npad].view(torch.int16), rxg[:npad].view(torch.int16))
+    # rows of padding slots are not written by either fused launch
+    real = ral["sorted_ids"][:npad] < cfg.A
+    used = cfg.d + 16 * ((cfg.d // 128 + 15) // 16)     # the rest of the sum block is not written
+    assert torch.equal(xg[:npad, :used][real].view(torch.int16),
+                       rxg[:npad, :used][real].view(torch.int16))
 
 
 @pytest.mark.parametrize("name", ["ragged", "layer256"])

@@ -3,26 +3,34 @@ run under random interleavings on the CPU, in the manner of
 test_dense_pipeline_protocol.py.
 
 Roles as the kernel writes them, with the kernel's constants: the TMA warp for
-codes and scales/zeros (5 code stages, 3 scale stages), the TMA warp for
+codes and scales/zeros (6 code stages, 2 or 3 scale stages), the TMA warp for
 activations (3 streamed slots, or 2 resident slots that hold a job's whole
-activation block), four MMA issuers (two A buffers each in tensor memory, two
-accumulator sets; their commits complete asynchronously in issue order per
-issuer), sixteen dequantisation warps (lane quarter x sub-chunk) and four
-epilogue warps.  Every wait is checked against the exact condition: the phase
-it stands for, counted from per-stage uses kept apart from the kernel's
-parity variables, has completed exactly when the parity test says so.  Unit
-lists mix jobs of 16 and 32 slots over several panels; contraction sizes
-cover gate_up (2816, streamed), down (704, resident) and short ones where an
-issuer has no sub-chunk (192, 384).
+activation block, the group-sum block included), two MMA issuers (issuer h
+takes ring h of three A buffers in tensor memory and has its own accumulator
+in each of two sets; each issuer's commits complete asynchronously in its
+issue order), eight dequantisation warps (lane quarter x half of each code
+stage; the half whose ring takes sub-chunk n_sub also produces the
+group-constant correction after its last sub-chunk of a unit) and four
+epilogue warps.  Every wait is checked against the exact condition:
+the phase it stands for, counted from per-stage uses kept apart from the
+kernel's parity variables, has completed exactly when the parity test says
+so.  Unit lists mix jobs of 16 and 32 slots over several panels; contraction
+sizes cover gate_up (2816, streamed), down (704, resident, a 64-code last
+sub-chunk) and short ones where one half has no sub-chunk in the last stage
+(384, 192).
 """
 import random
 
 import pytest
 
-ISSUERS, BUFS, SETS = 4, 2, 2
-STAGES_W, STAGES_B, STAGES_SZ = 5, 3, 3
-DQ_WARPS, EPI_WARPS = 16, 4
-CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 64, 32, 49152
+RINGS, RING_BUFS, SETS = 2, 3, 2
+STAGES_W, STAGES_B = 6, 3
+DQ_WARPS, EPI_WARPS = 8, 4
+CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 128, 32, 49152
+
+
+def sz_stages(G):
+    return 2 if G > 16 else 3
 
 
 class Bar:
@@ -42,33 +50,37 @@ def b_kcols(n):
 
 
 class Grouped:
-    def __init__(self, K, units, rng):
+    def __init__(self, K, units, rng, group=None):
         self.K, self.units, self.rng = K, units, rng
+        group = group or (128 if K % 128 == 0 and K > 704 else 64)
+        self.G = K // group
+        self.n_sz = sz_stages(self.G)
         self.n_kchunks = (K + CHUNK_K - 1) // CHUNK_K
-        self.n_sub = K // SUB_K
-        self.resident = K // 64 <= 256 and K * 2 * MAX_N <= RES_BYTES
+        self.n_sub = (K + SUB_K - 1) // SUB_K
+        self.resident = (K + 64) * 2 * MAX_N <= RES_BYTES
         B = lambda name, n, c: [Bar(f"{name}{i}", c) for i in range(n)]
         self.w_full, self.w_empty = B("w_full", STAGES_W, 1), B("w_empty", STAGES_W, DQ_WARPS)
         nb = 2 if self.resident else STAGES_B
-        self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, ISSUERS)
-        self.a_full = B("a_full", ISSUERS * BUFS, 4)
-        self.a_empty = B("a_empty", ISSUERS * BUFS, 1)
-        self.acc_full, self.acc_empty = B("acc_full", SETS, ISSUERS), B("acc_empty", SETS, EPI_WARPS)
-        self.sz_full, self.sz_empty = B("sz_full", STAGES_SZ, 1), B("sz_empty", STAGES_SZ, DQ_WARPS)
+        self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, 2)
+        self.a_full = B("a_full", RINGS * RING_BUFS, 4)
+        self.a_empty = B("a_empty", RINGS * RING_BUFS, 1)
+        self.acc_full, self.acc_empty = B("acc_full", SETS, 2), B("acc_empty", SETS, EPI_WARPS)
+        self.sz_full = B("sz_full", self.n_sz, 1)
+        self.sz_empty = B("sz_empty", self.n_sz, DQ_WARPS)
         self.copies = []
-        self.commits = [[] for _ in range(ISSUERS)]
+        self.commits = [[], []]
 
     # ---- roles; each wait carries (parity as the kernel computes it, the
     # phase index it stands for from independent use counts; -1: none yet)
     def tma_w(self):
         sa = szb = ph_a = ph_sz = 0
-        w_fill, sz_fill = [0] * STAGES_W, [0] * STAGES_SZ
+        w_fill, sz_fill = [0] * STAGES_W, [0] * self.n_sz
         for _job, _n in self.units:
             yield ("wait", self.sz_empty[szb], ph_sz ^ 1, sz_fill[szb] - 1)
             yield ("copy", self.sz_full[szb])
             sz_fill[szb] += 1
             szb += 1
-            if szb == STAGES_SZ:
+            if szb == self.n_sz:
                 szb, ph_sz = 0, ph_sz ^ 1
             for _ in range(self.n_kchunks):
                 yield ("wait", self.w_empty[sa], ph_a ^ 1, w_fill[sa] - 1)
@@ -94,7 +106,7 @@ class Grouped:
         sb = ph_b = 0
         fill = [0] * STAGES_B
         for _job, n in self.units:
-            for _ in range(0, self.K, 64 * b_kcols(n)):
+            for _ in range(0, self.K + 1, 64 * b_kcols(n)):     # blocks 0 .. K/64
                 yield ("wait", self.b_empty[sb], ph_b ^ 1, fill[sb] - 1)
                 yield ("copy", self.b_full[sb])
                 fill[sb] += 1
@@ -103,19 +115,19 @@ class Grouped:
                     sb, ph_b = 0, ph_b ^ 1
 
     def issuer(self, me):
-        a_slot = a_ph = 0
-        a_use = [0] * BUFS
+        ring_slot = ring_ph = 0
+        a_use = [0] * RING_BUFS
         acc_use, b_use = [0] * SETS, [0] * (2 if self.resident else STAGES_B)
         cur_job, res_slot, b_seq = None, 0, 0
 
         def issue():
-            nonlocal a_slot, a_ph
-            buf = me + ISSUERS * a_slot
-            yield ("wait", self.a_full[buf], a_ph, a_use[a_slot])
-            a_use[a_slot] += 1
-            a_slot += 1
-            if a_slot == BUFS:
-                a_slot, a_ph = 0, a_ph ^ 1
+            nonlocal ring_slot, ring_ph
+            buf = me * RING_BUFS + ring_slot
+            yield ("wait", self.a_full[buf], ring_ph, a_use[ring_slot])
+            a_use[ring_slot] += 1
+            ring_slot += 1
+            if ring_slot == RING_BUFS:
+                ring_slot, ring_ph = 0, ring_ph ^ 1
             yield ("commit", me, self.a_empty[buf])
 
         for n_unit, (job, n) in enumerate(self.units):
@@ -130,53 +142,60 @@ class Grouped:
                     b_use[res_slot] += 1
                     b_seq += 1
                     cur_job = job
-                for _j in range(me, self.n_sub, ISSUERS):
+                for _j in range(me, self.n_sub + 1, 2):      # the correction is j = n_sub
                     yield from issue()
             else:
-                kb_cap = 64 * b_kcols(n)
-                n_bslots = (self.K + kb_cap - 1) // kb_cap
+                kcols = b_kcols(n)
+                subs = kcols // 2
+                n_bslots = self.K // 64 // kcols + 1
                 for t in range(n_bslots):
                     sb = (b_seq + t) % STAGES_B
                     yield ("wait", self.b_full[sb], ((b_seq + t) // STAGES_B) & 1, b_use[sb])
                     b_use[sb] += 1
-                    j0 = t * (kb_cap // SUB_K)
-                    j1 = min(self.n_sub, j0 + kb_cap // SUB_K)
-                    j = j0 + ((me - j0) % ISSUERS + ISSUERS) % ISSUERS
-                    while j < j1:
+                    for _j in range(t * subs + me, min(self.n_sub, (t + 1) * subs), 2):
                         yield from issue()
-                        j += ISSUERS
+                    if t == n_bslots - 1 and self.n_sub % 2 == me:
+                        yield from issue()
                     yield ("commit", me, self.b_empty[sb])
                 b_seq += n_bslots
             yield ("commit", me, self.acc_full[st])
             acc_use[st] += 1
 
-    def dequant(self, sub):
+    def dequant(self, h):
         sa = szb = ph_a = ph_sz = 0
-        a_slot = a_ph = 0
-        w_use, sz_use, a_fill = [0] * STAGES_W, [0] * STAGES_SZ, [0] * BUFS
+        ring_slot = ring_ph = 0
+        w_use, sz_use, a_fill = [0] * STAGES_W, [0] * self.n_sz, [0] * RING_BUFS
         for _job, _n in self.units:
             yield ("wait", self.sz_full[szb], ph_sz, sz_use[szb])
             for kc in range(self.n_kchunks):
                 yield ("wait", self.w_full[sa], ph_a, w_use[sa])
                 w_use[sa] += 1
-                mine = kc * (CHUNK_K // SUB_K) + sub < self.n_sub
+                mine = 2 * kc + h < self.n_sub
                 yield ("arrive", self.w_empty[sa])
                 sa += 1
                 if sa == STAGES_W:
                     sa, ph_a = 0, ph_a ^ 1
                 if not mine:
                     continue
-                buf = sub + ISSUERS * a_slot
-                yield ("wait", self.a_empty[buf], a_ph ^ 1, a_fill[a_slot] - 1)
-                a_fill[a_slot] += 1
-                a_slot += 1
-                if a_slot == BUFS:
-                    a_slot, a_ph = 0, a_ph ^ 1
+                buf = h * RING_BUFS + ring_slot
+                yield ("wait", self.a_empty[buf], ring_ph ^ 1, a_fill[ring_slot] - 1)
+                a_fill[ring_slot] += 1
+                ring_slot += 1
+                if ring_slot == RING_BUFS:
+                    ring_slot, ring_ph = 0, ring_ph ^ 1
+                yield ("arrive", self.a_full[buf])
+            if self.n_sub % 2 == h:          # the correction sub-chunk
+                buf = h * RING_BUFS + ring_slot
+                yield ("wait", self.a_empty[buf], ring_ph ^ 1, a_fill[ring_slot] - 1)
+                a_fill[ring_slot] += 1
+                ring_slot += 1
+                if ring_slot == RING_BUFS:
+                    ring_slot, ring_ph = 0, ring_ph ^ 1
                 yield ("arrive", self.a_full[buf])
             yield ("arrive", self.sz_empty[szb])
             sz_use[szb] += 1
             szb += 1
-            if szb == STAGES_SZ:
+            if szb == self.n_sz:
                 szb, ph_sz = 0, ph_sz ^ 1
 
     def epilogue(self):
@@ -188,8 +207,8 @@ class Grouped:
             yield ("arrive", self.acc_empty[st])
 
     def run(self):
-        roles = [self.tma_w(), self.tma_b()] + [self.issuer(i) for i in range(ISSUERS)]
-        roles += [self.dequant(w // 4) for w in range(DQ_WARPS)]      # 4 lane quarters per sub
+        roles = [self.tma_w(), self.tma_b(), self.issuer(0), self.issuer(1)]
+        roles += [self.dequant(w // 4) for w in range(DQ_WARPS)]      # 4 lane quarters per half
         roles += [self.epilogue() for _ in range(EPI_WARPS)]
         nxt = [next(r, None) for r in roles]
         steps = 0
@@ -213,9 +232,9 @@ class Grouped:
                     choices.append(("role", i))
             if self.copies:
                 choices.append(("copy", None))
-            for k in range(ISSUERS):
-                if self.commits[k]:
-                    choices.append(("commit", k))
+            for q in range(2):
+                if self.commits[q]:
+                    choices.append(("commit", q))
             if not choices:
                 assert all(op is None for op in nxt), "deadlock: " + ", ".join(
                     f"{op[1].name} phase {op[3]}" for op in nxt if op is not None)
@@ -225,7 +244,7 @@ class Grouped:
                 self.copies.pop(self.rng.randrange(len(self.copies))).arrive()
                 continue
             if kind == "commit":
-                self.commits[i].pop(0).arrive()
+                self.commits[i].pop(0).arrive()   # an issuer's commits complete in order
                 continue
             op = nxt[i]
             if op[0] == "arrive":
@@ -249,7 +268,7 @@ def _units(rng, n_units):
     return units[:n_units]
 
 
-@pytest.mark.parametrize("K", [2816, 704, 384, 192])
+@pytest.mark.parametrize("K", [2816, 704, 384, 192, 320])
 @pytest.mark.parametrize("seed", range(12))
 def test_grouped_pipeline_protocol(K, seed):
     rng = random.Random(seed * 104729 + K)
@@ -260,8 +279,8 @@ def test_the_grouped_model_catches_a_broken_protocol():
     """A dequant warp that waits on its A buffer with the parity of the
     wrong slot must fail the checks."""
     class Broken(Grouped):
-        def dequant(self, sub):
-            for op in Grouped.dequant(self, sub):
+        def dequant(self, h):
+            for op in Grouped.dequant(self, h):
                 if op[0] == "wait" and op[1] in self.a_empty:
                     op = (op[0], op[1], 1, op[3])
                 yield op

@@ -24,6 +24,10 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 W4_DEV_BAD_EXPERT_ID = 0x1
 W4_DEV_PIPELINE_TIMEOUT = 0x2
 W4_DEV_TOO_MANY_JOBS = 0x4
+W4_DEV_FP16_RANGE = 0x8
+# xg and h rows end in one block of 64 columns of activation group sums, the
+# grouped GEMMs' input for the low parts of their dequantisation constants
+SUM_COLS = 64
 
 
 class W4Error(RuntimeError):
@@ -63,7 +67,7 @@ def load_library(path: str | None = None):
             "w4_moe_route": ([V, I, I, I, V, V, V], I),
             "w4_moe_align_capacity": ([I, I, I, I], I64),
             "w4_moe_align": ([V, I, I, I, I, V, V, V, V, V, V], I),
-            "w4_gather_activations": ([V, I, I, I, I, I, V, V, V, V], I),
+            "w4_gather_activations": ([V, I, I, I, I, I, V, V, V, V, V], I),
             "w4_moe_align_gather": ([V, V, I, I, I, I, I, V, V, V, V, V, V, V], I),
             "w4_moe_route_align_gather": ([V, V, I, I, I, I, I, V, V, V, V, V, V, V, V, V],
                                           I),
@@ -186,18 +190,21 @@ def w4_moe_align(topk_ids, E: int, block_m: int = 16, dev_status=None, out=None,
     return r
 
 
-def w4_gather_activations(x, align: dict, out=None, stream=None):
-    """x [M, d] bf16 -> xg [cap, d] fp16 in slot order and block order (zero
-    rows for padding slots; rows past num_padded are left untouched)."""
+def w4_gather_activations(x, align: dict, out=None, dev_status=None, stream=None):
+    """x [M, d] bf16 -> xg [cap, d + 64] fp16 in slot order: d values in block
+    order, then the sums of the groups of 128 (zero rows for padding slots;
+    rows past num_padded are left untouched).  Values beyond fp16's range
+    saturate and set W4_DEV_FP16_RANGE in dev_status."""
     import torch
-    _require_cuda(x, out)
+    _require_cuda(x, out, dev_status)
     M, d = x.shape
     cap = align["sorted_ids"].numel()
     if out is None:
-        out = torch.empty((cap, d), dtype=torch.float16, device=x.device)
+        out = torch.empty((cap, d + SUM_COLS), dtype=torch.float16, device=x.device)
     _check(load_library().w4_gather_activations(
         _ptr(x), M, d, align["k"], align["E"], align["block_m"], _ptr(align["sorted_ids"]),
-        _ptr(align["num_padded"]), _ptr(out), _stream(stream)), "w4_gather_activations")
+        _ptr(align["num_padded"]), _ptr(out), _ptr(dev_status), _stream(stream)),
+        "w4_gather_activations")
     return out
 
 
@@ -217,7 +224,7 @@ def w4_moe_align_gather(topk_ids, x, E: int, block_m: int = 16, dev_status=None,
                    num_padded=torch.empty(1, dtype=torch.int32, device=dev))
     out.update(M=M, k=k, E=E, block_m=block_m)
     if xg is None:
-        xg = torch.empty((cap, d), dtype=torch.float16, device=dev)
+        xg = torch.empty((cap, d + SUM_COLS), dtype=torch.float16, device=dev)
     _check(load_library().w4_moe_align_gather(
         _ptr(topk_ids), _ptr(x), M, d, k, E, block_m, _ptr(out["sorted_ids"]),
         _ptr(out["block_expert"]), _ptr(out["expert_offsets"]), _ptr(out["num_padded"]),
@@ -227,16 +234,17 @@ def w4_moe_align_gather(topk_ids, x, E: int, block_m: int = 16, dev_status=None,
 
 def w4_grouped_gemm_gate_up(xg, gu_q, gu_s, gu_z, align: dict, group: int = 128, h=None,
                             dev_status=None, stream=None):
-    """xg [cap, d] fp16 (from w4_gather_activations) -> h [cap, m] fp16 in block
-    order: gelu_tanh(gate) * up per alignment slot."""
+    """xg [cap, d + 64] fp16 (from w4_gather_activations) -> h [cap, m + 64]
+    fp16: m values in block order, gelu_tanh(gate) * up per alignment slot,
+    then the sums of every quarter (16 values) of each group of 64."""
     import torch
     _require_cuda(xg, gu_q, gu_s, gu_z, h, dev_status)
-    M, d = align["M"], xg.shape[1]
+    M, d = align["M"], xg.shape[1] - SUM_COLS
     E, two_m, _ = gu_q.shape
     m = two_m // 2
     cap = align["sorted_ids"].numel()
     if h is None:
-        h = torch.empty((cap, m), dtype=torch.float16, device=xg.device)
+        h = torch.empty((cap, m + SUM_COLS), dtype=torch.float16, device=xg.device)
     _check(load_library().w4_grouped_gemm_gate_up(
         _ptr(xg), M, d, m, E, align["k"], align["block_m"], _ptr(gu_q), _ptr(gu_s), _ptr(gu_z),
         group, _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(h),
@@ -258,7 +266,8 @@ def korder_to_natural(a):
 
 def w4_grouped_gemm_down(h, dn_q, dn_s, dn_z, align: dict, group: int = 64, y=None,
                          dev_status=None, stream=None):
-    """h [cap, m] fp16 -> y [M*k, d] fp32 (row = flat assignment index)."""
+    """h [cap, m + 64] fp16 (from w4_grouped_gemm_gate_up) -> y [M*k, d] fp32
+    (row = flat assignment index)."""
     import torch
     _require_cuda(h, dn_q, dn_s, dn_z, y, dev_status)
     E, d, half_m = dn_q.shape
@@ -334,7 +343,7 @@ def w4_moe_route_align_gather(logits, x, k: int, block_m: int = 16, dev_status=N
                    num_padded=torch.empty(1, dtype=torch.int32, device=dev))
     out.update(M=M, k=k, E=E, block_m=block_m)
     if xg is None:
-        xg = torch.empty((cap, d), dtype=torch.float16, device=dev)
+        xg = torch.empty((cap, d + SUM_COLS), dtype=torch.float16, device=dev)
     if ids is None:
         ids = torch.empty((M, k), dtype=torch.int32, device=dev)
     if weights is None:

@@ -70,6 +70,10 @@ int check_gemm_common(int M, int d, int m, int E, int k, int block_m, const void
     if (d % 128 || m % 64)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "need d %% 128 == 0 and m %% 64 == 0 (d=%d, m=%d)", d,
                     m);
+    if (d > 8192 || m > 1024)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE,
+                    "need d <= 8192 and m <= 1024: the group sums of xg and h fill at most one "
+                    "64-column block (d=%d, m=%d)", d, m);
     if (E > 1024 || k > E)
         return fail(W4_ERR_UNSUPPORTED_SHAPE, "need k <= E <= 1024");
     const int64_t A = static_cast<int64_t>(M) * k;
@@ -181,7 +185,7 @@ int w4_moe_align(const int32_t *topk_ids, int M, int k, int E, int block_m, int3
 
 int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int block_m,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          w4_stream_t stream)
+                          int32_t *dev_status, w4_stream_t stream)
 {
     if (!xg || !sorted_ids || !num_padded || (M > 0 && !x))
         return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
@@ -189,15 +193,18 @@ int w4_gather_activations(const uint16_t *x, int M, int d, int k, int E, int blo
         return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
     if (!valid_block_m(block_m))
         return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
-    if (d % 8)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "d must be a multiple of 8");
+    if (d % 128 || d > 8192)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE,
+                    "d must be a multiple of 128 and at most 8192 (its group sums fill one "
+                    "64-column block)");
     if (!aligned16(x) || !aligned16(xg) || !aligned4(sorted_ids) || !aligned4(num_padded))
         return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
     if (int rc = check_device())
         return rc;
     const int64_t cap = align_capacity(M, k, E, block_m);
     cudaError_t err =
-        w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg, as_stream(stream));
+        w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg, dev_status,
+                          as_stream(stream));
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "gather launch");
 }
 
@@ -213,8 +220,8 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
         return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
     if (!valid_block_m(block_m))
         return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
-    if (E > 1024 || d % 8)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need E <= 1024 and d %% 8 == 0");
+    if (E > 1024 || d % 128 || d > 8192)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need E <= 1024, d %% 128 == 0 and d <= 8192");
     if (!aligned16(x) || !aligned16(xg))
         return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
     const int64_t cap = align_capacity(M, k, E, block_m);
@@ -234,7 +241,7 @@ int w4_moe_align_gather(const int32_t *topk_ids, const uint16_t *x, int M, int d
         err = w4::launch_align(topk_ids, M, k, E, block_m, cap, sorted_ids, block_expert,
                                expert_offsets, num_padded, dev_status, as_stream(stream));
         if (err == cudaSuccess)
-            err = w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg,
+            err = w4::launch_gather(x, M, d, k, cap, sorted_ids, num_padded, xg, dev_status,
                                     as_stream(stream));
     }
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "align+gather launch");
@@ -259,8 +266,8 @@ int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int
         return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d d=%d k=%d E=%d", M, d, k, E);
     if (!valid_block_m(block_m))
         return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
-    if (d % 8)
-        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need d %% 8 == 0");
+    if (d % 128 || d > 8192)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need d %% 128 == 0 and d <= 8192");
     if (!aligned16(x) || !aligned16(xg))
         return fail(W4_ERR_MISALIGNED, "x and xg must be 16-byte aligned");
     if (int rc = check_device())
@@ -398,7 +405,8 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const fl
 
 // Workspace layout of w4_moe_layer (each piece 256-byte aligned):
 //   sorted_ids [cap] i32 | block_expert [cap/bm] i32 | expert_offsets [E+1] i32 |
-//   num_padded [1] i32 | xg [cap, d] fp16 | h [cap, m] fp16 | y [M*k, d] fp32
+//   num_padded [1] i32 | xg [cap, d + 64] fp16 | h [cap, m + 64] fp16 |
+//   y [M*k, d] fp32   (xg and h rows end in their 64-column group-sum block)
 namespace {
 struct LayerWs {
     size_t sorted, block, offs, npad, xg, h, y, total;
@@ -413,8 +421,8 @@ LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
     w.offs = up256(w.block + 4 * (cap / bm));
     w.npad = up256(w.offs + 4 * (static_cast<size_t>(E) + 1));
     w.xg = up256(w.npad + 4);
-    w.h = up256(w.xg + 2 * cap * static_cast<size_t>(d));
-    w.y = up256(w.h + 2 * cap * static_cast<size_t>(m));
+    w.h = up256(w.xg + 2 * cap * (static_cast<size_t>(d) + 64));
+    w.y = up256(w.h + 2 * cap * (static_cast<size_t>(m) + 64));
     w.total = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
     return w;
 }

@@ -11,45 +11,63 @@
 // with deq(W) = s_g * (q - z_g) for uint4 codes q packed two per byte and fp16
 // s, z per group of `group` elements along the contraction dim.
 //
-// Dequantisation.  Eight codes sit in one 32-bit word; ORing a masked pair
-// of nibbles into the mantissa of fp16 1024.0 gives 1024 + q (or 1024 + 16q
-// for the high nibbles) exactly; one HADD2 (or HFMA2 by 1/16) leaves q, and
-// one HFMA2 makes q * s + c with c = fp16(-z * s), a single rounding of the
-// product.  Per word that is one shift and four LOP3 on the integer pipe and
-// eight fp16 operations on the FMA pipe, which issue in parallel.
+// Dequantisation.  Eight codes sit in one 32-bit word (code i in bits
+// 4i..4i+3).  ANDing the word with 0x000F000F leaves codes 0 and 4 as the
+// bit patterns of two fp16 subnormals, q * 2^-24, exactly; 0x00F000F0 leaves
+// codes 1 and 5 as 16 q * 2^-24 (still subnormal: the first 10 bits of an
+// fp16 are its mantissa); the word shifted right by 8 gives codes 2, 6 and
+// 3, 7 the same way.  One HFMA2 per pair then forms
+//     A = q * S + C,  S = s * 2^(24 - c),  C = fp16(-s * z * 2^-c)
+// (S / 16 for the 16 q pairs): the product q * s * 2^-c is exact inside the
+// fused operation and A is rounded once, i.e. A = 2^-c * fp16(q s + fp16(-z s))
+// wherever that value is an fp16 normal.  c is a power-of-two exponent per
+// weight row, chosen from the row's largest scale so that every S of the row
+// is a finite fp16 (S <= 65504 needs s * 2^(24 - c) below 2^16); the epilogue
+// multiplies the row's fp32 accumulator by 2^c, which is exact.  So a weight
+// costs 5/8 integer and 4/8 fp16 operations: one shift and four LOP3 plus
+// four HFMA2 per eight codes.
 //
-// Design (one persistent CTA per SM, 26 warps, static round-robin schedule):
+// Group-constant correction.  Rounding C to fp16 leaves an error that is the
+// same for every weight of the group, so it adds up over the group as
+// (C_exact - C) * (sum of the group's activations) instead of averaging out.
+// The activation rows therefore end in a 64-column block of group sums (the
+// gather writes one per group of 128 of x, gate_up's epilogue one per
+// quarter of each group of 64 of h) and every unit ends with a correction
+// sub-chunk: per row the low parts C_lo = fp16(C_exact - C) (exact in fp32
+// before that rounding) as the A operand, one to four K = 16 MMAs against the
+// sum block.  The dequantised weight is then exact to its own fp16 rounding.
+//
+// Design (one persistent CTA of 16 warps per SM, static round-robin schedule):
 //   * A work unit is (job, panel).  A job is at most 32 consecutive slots of
 //     one expert; a panel is 128 weight rows (gate_up: 64 gate rows and the
 //     matching 64 up rows; down: 128 output rows).
 //   * Swap-AB: the 128 weight rows are the M = 128 operand, in tensor memory
 //     (written with tcgen05.st), the job's tokens are N (16 or 32).  B, the
 //     activations, is read by the tensor core from shared memory in the
-//     128-byte-swizzled K-major layout; one 3-D TMA copy fills a 32 KB slot.
-//   * A tcgen05.mma holds its issuing thread for ~100 cycles on this part
-//     whatever its size, so four issuer warps share the work: the unit's
-//     64-element sub-chunks go round-robin to them, each into its own fp32
-//     accumulator; the epilogue adds the four in a fixed order.
+//     128-byte-swizzled K-major layout; one 3-D TMA copy fills a slot.
+//   * Codes arrive by TMA in stages of 128 rows x 256 codes (two 64-row
+//     boxes).  Each stage is two 128-code sub-chunks; the dequant warp of a
+//     lane quarter and half h expands sub-chunk h of every stage for its 32
+//     rows into a 64-column A buffer of ring h (three buffers per ring).
+//   * Two issuer warps, one per ring, consume its sub-chunks in order, eight
+//     K = 16 MMAs each, into their own fp32 accumulators; the epilogue adds
+//     the two in a fixed order.  Two accumulator sets alternate per unit, so
+//     a unit's epilogue overlaps the next unit's MMAs.
 //   * Warp roles
-//       warps 0-3   tcgen05.mma issuers (one lane each).
-//       warps 4-7   epilogue (one TMEM lane quarter each).
-//       warps 8-23  dequant: four per lane quarter, one 64-code sub-chunk of
-//                   each 256-code chunk each (warps 8 + 4 i + q feed issuer i).
-//       warp 24     TMA: packed codes (128 rows x 256 codes per stage, two
-//                   64-row boxes, evict-first), per unit the scales, zeros
-//                   and activation group sums (bulk copies).
-//       warp 25     TMA: activation slots.
-//   * Tensor memory: columns 0-255 eight A sub-chunk buffers (64 codes, 32
-//     columns each), two per issuer, so every buffer has one producer group
-//     (the dequant warps of one half) and one consumer, both in order;
-//     columns 256-511 two sets of four 32-column accumulators, alternating
-//     per unit, so a unit's epilogue overlaps the next unit's MMAs.
-//   * Every barrier wait is at most one phase ahead of the barrier (each
-//     waiter waits on every phase of its barriers in order), which is what
-//     makes the parity waits exact.
+//       warp 0      tcgen05.mma issuer of ring 0 (converged, one elected lane
+//                   issues)
+//       warp 1      TMA: packed codes; per unit the scales and zeros
+//       warp 2      TMA: activation slots
+//       warp 3      tensor-memory allocation, then tcgen05.mma issuer of ring 1
+//       warps 4-7   epilogue (one TMEM lane quarter each)
+//       warps 8-15  dequant (warp 8 + 4 h + q: lane quarter q, half h)
+//   * Tensor memory (512 columns): A buffers at 64 (3 h + i), accumulators
+//     at 384 + 64 set + 32 issuer.
+//   * Every barrier has one producer group and one consumer group that take
+//     its phases in order, so a waiter is never two phases ahead and parity
+//     waits are exact (tests/test_grouped_pipeline_protocol.py models it).
 //   * Every output element is written once, by one thread, after a fixed
-//     sequence of MMAs and fixed-order sums: results are bit-identical run to
-//     run.
+//     sequence of MMAs: results are bit-identical run to run.
 //   * Every pipeline wait has a time limit; on expiry the CTA raises
 //     W4_DEV_PIPELINE_TIMEOUT, stops, drains its own copies and MMAs, frees
 //     its tensor memory and exits.
@@ -60,100 +78,38 @@
 #include "launch.h"
 #include "ptx.cuh"
 
-// Optional pipeline tracing (compile with -DW4_TRACE): CTA 0 records the SM
-// clock at sixteen points of its pipeline for its first 128 events of each;
-// the host reads them with w4_trace_read().  Compiled out by default.
-#ifdef W4_TRACE
-__device__ unsigned long long g_w4_trace[16][128];
-extern "C" int w4_trace_read(void *host)
-{
-    return static_cast<int>(cudaMemcpyFromSymbol(host, g_w4_trace, sizeof(g_w4_trace)));
-}
-#define W4_TRACE_POINT(row, idx)                                                     \
-    do {                                                                             \
-        if (blockIdx.x == 0 && (idx) < 128) {                                        \
-            unsigned long long c_;                                                   \
-            asm volatile("mov.u64 %0, %%clock64;" : "=l"(c_));                       \
-            g_w4_trace[row][idx] = c_;                                               \
-        }                                                                            \
-    } while (0)
-// First pipeline wait in the grid that ran out: block, warp, lane, barrier
-// index, parity, clock.
-__device__ unsigned long long g_w4_timeout[8];
-extern "C" int w4_timeout_read(void *host)
-{
-    return static_cast<int>(cudaMemcpyFromSymbol(host, g_w4_timeout, sizeof(g_w4_timeout)));
-}
-extern "C" int w4_timeout_reset(void)
-{
-    unsigned long long z[8] = {};
-    return static_cast<int>(cudaMemcpyToSymbol(g_w4_timeout, z, sizeof(z)));
-}
-// Per block and warp: the wait each warp gave up on (shared address | parity << 31).
-__device__ unsigned int g_w4_gaveup[256][32];
-extern "C" int w4_gaveup_read(void *host)
-{
-    return static_cast<int>(cudaMemcpyFromSymbol(host, g_w4_gaveup, sizeof(g_w4_gaveup)));
-}
-#define W4_TIMEOUT_RECORD(bar, parity, status)                                              \
-    do {                                                                                    \
-        if (blockIdx.x < 256)                                                               \
-            g_w4_gaveup[blockIdx.x][threadIdx.x >> 5] =                                     \
-                w4::smem_u32(bar) | (static_cast<unsigned>(parity) << 31);                  \
-        if ((status) && (*(volatile int32_t *)(status) & 2) &&                              \
-            atomicCAS(&g_w4_timeout[0], 0ull, 1ull) == 0ull) {                              \
-            g_w4_timeout[1] = blockIdx.x;                                                   \
-            g_w4_timeout[2] = threadIdx.x >> 5;                                             \
-            g_w4_timeout[3] = threadIdx.x & 31;                                             \
-            g_w4_timeout[4] = w4::smem_u32(bar);                                              \
-            g_w4_timeout[5] = (parity);                                                     \
-            unsigned long long c_;                                                          \
-            asm volatile("mov.u64 %0, %%clock64;" : "=l"(c_));                              \
-            g_w4_timeout[6] = c_;                                                           \
-        }                                                                                   \
-    } while (0)
-#else
-#define W4_TRACE_POINT(row, idx) ((void)0)
-#define W4_TIMEOUT_RECORD(bar, parity, status) ((void)0)
-#endif
-
 namespace w4 {
 
 namespace {
 
-constexpr int kIssuers = 4;                 // warps 0-3
-constexpr int kFirstEpiWarp = 4;            // warps 4-7
+constexpr int kWarpMma0 = 0;               // issuer of ring 0
+constexpr int kWarpTmaW = 1;
+constexpr int kWarpTmaB = 2;
+constexpr int kWarpMma1 = 3;               // issuer of ring 1; allocates tensor memory
+constexpr int kWarpAlloc = 3;
+constexpr int kFirstEpiWarp = 4;
 constexpr int kNumEpiWarps = 4;
-constexpr int kFirstDqWarp = 8;             // warps 8-15
-constexpr int kNumDqWarps = 16;            // warps 8-23
-constexpr int kWarpTmaW = 24;
-constexpr int kWarpTmaB = 25;
-constexpr int kNumWarps = 26;
+constexpr int kFirstDqWarp = 8;
+constexpr int kNumDqWarps = 8;
+constexpr int kNumWarps = 16;
 constexpr int kThreads = 32 * kNumWarps;
-constexpr int kStagesW = 5;                 // packed-code stages
-constexpr int kStagesB = 3;                 // activation slots
-constexpr int kStagesSZ = 3;                // per-unit scales, zeros, group sums
+constexpr int kRings = 2;                   // one per dequant half
+constexpr int kRingBufs = 3;                // A buffers per ring
+constexpr int kStagesW = 6;                 // packed-code stages
+constexpr int kStagesB = 3;                 // streamed activation slots
+constexpr int kMaxStagesSZ = 3;             // per-unit scales and zeros
 constexpr int kTileRows = 128;              // MMA M
 constexpr int kChunkK = 256;                // codes per row per stage
-constexpr int kSubK = 64;                   // codes per A sub-chunk
-constexpr int kMaxSubBufs = 12;             // A buffers in tensor memory (kIssuers x BUFS)
+constexpr int kSubK = 128;                  // codes per sub-chunk (one A buffer)
+constexpr int kSubCols = kSubK / 2;         // TMEM columns per A buffer
 constexpr int kStageWBytes = kTileRows * kChunkK / 2;   // 16 KB
 constexpr int kStageBBytes = 32768;
 constexpr int kResSlotBytes = kStagesB * kStageBBytes / 2;   // resident mode: 2 x 48 KB
 constexpr int kMaxN = 32;                   // slots per job
 constexpr uint32_t kTmemCols = 512;
-// Tensor memory: A buffer b at column 32 b (b = issuer + kIssuers * slot), then
-// the accumulators acc[set][issuer] at acc_col<BUFS> + 128 set + 32 issuer.
-// BUFS = 3 A buffers per issuer leave room for one accumulator set, BUFS = 2
-// for two (the next unit's MMAs need not wait for the epilogue).
-template <int BUFS>
-__host__ __device__ constexpr int acc_sets() { return BUFS >= 3 ? 1 : 2; }
-template <int BUFS>
-__host__ __device__ constexpr uint32_t acc_col() { return 32u * kIssuers * BUFS; }
-static_assert(acc_col<3>() + 128u * acc_sets<3>() <= kTmemCols, "tensor memory budget");
-static_assert(acc_col<2>() + 128u * acc_sets<2>() <= kTmemCols, "tensor memory budget");
-constexpr int kBufsGateUp = 2;
-constexpr int kBufsDown = 2;
+constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 384
+// accumulators: set s (alternating per unit), issuer i at kAccCol + 64 s + 32 i
+static_assert(kAccCol + 2 * 2 * kMaxN <= kTmemCols, "tensor memory budget");
 
 struct GemmArgs {
     CUtensorMap tmap_w;       // packed codes u8 [E*R rows, K/2 B], box 128 B x 64 rows, SW128
@@ -164,12 +120,15 @@ struct GemmArgs {
     const int32_t *expert_offsets;
     void *out;
     int32_t *dev_status;
-    int E, A, K, R, m_up, out_cols, group, group_shift, G, n_panels, n_kchunks, n_sub;
+    int E, A, K, R, m_up, out_cols, group_shift, G, n_panels, n_kchunks, n_sub, n_sz;
+    int n_corr_mma;           // K = 16 MMAs of the group-constant correction
+    int h_stride;             // gate_up: row length of h (m + 64: values, then group sums)
+    int h_groups;             // gate_up: groups of 64 along m (the down GEMM's groups)
     int early_schedule;       // the schedule may be read before the grid-dependency wait
-    int out_bf16;             // plain epilogue: bf16 rows instead of fp32
 };
 
-constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kMaxSubBufs + 2 + 2 + 2 * kStagesSZ + kIssuers;
+constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kRings * kRingBufs + 2 + 2 +
+                         2 * kMaxStagesSZ + 2;
 
 struct Bars {
     uint64_t *w_full, *w_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty,
@@ -185,12 +144,12 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
     r.b_full = r.w_empty + kStagesW;
     r.b_empty = r.b_full + kStagesB;
     r.a_full = r.b_empty + kStagesB;
-    r.a_empty = r.a_full + kMaxSubBufs;
-    r.acc_full = r.a_empty + kMaxSubBufs;
+    r.a_empty = r.a_full + kRings * kRingBufs;
+    r.acc_full = r.a_empty + kRings * kRingBufs;
     r.acc_empty = r.acc_full + 2;
     r.sz_full = r.acc_empty + 2;
-    r.sz_empty = r.sz_full + kStagesSZ;
-    r.drain = r.sz_empty + kStagesSZ;
+    r.sz_empty = r.sz_full + kMaxStagesSZ;
+    r.drain = r.sz_empty + kMaxStagesSZ;
     return r;
 }
 
@@ -199,14 +158,18 @@ struct SmemLayout {
     int sz_stride, total;
 };
 
-// One sz stage: s [128 rows][G] fp16, then z [128][G] fp16.
+// Scale/zero stages: s [128 rows][G] fp16, then z [128][G] fp16.  Three
+// stages when a unit's are small (down), two otherwise (gate_up: a unit is 11
+// code stages, so the copy of the next unit's scales is never waited for).
+__host__ __device__ inline int sz_stages(int G) { return G > 16 ? 2 : 3; }
+
 __host__ __device__ inline SmemLayout smem_layout(int G, int E)
 {
     SmemLayout L;
     L.off_b = kStagesW * kStageWBytes;
     L.sz_stride = ((kTileRows * G * 2 * 2) + 127) & ~127;
     L.off_sz = L.off_b + kStagesB * kStageBBytes;
-    L.off_bar = L.off_sz + kStagesSZ * L.sz_stride;
+    L.off_bar = L.off_sz + sz_stages(G) * L.sz_stride;
     L.off_misc = L.off_bar + kNumBars * 8;
     L.off_offs = L.off_misc + 16;
     L.off_jp = L.off_offs + (E + 1) * 4;
@@ -237,47 +200,30 @@ __device__ __forceinline__ Job decode_job(const int *jp, const int *offs, int E,
     return J;
 }
 
-// 64-code column blocks per activation slot for a job of n slots (32 KB).
+// 64-code column blocks per streamed activation slot for a job of n slots (32 KB).
 __host__ __device__ constexpr int b_kcols(int n) { return n == 16 ? 16 : 8; }
 
 // Resident mode: the activation block of a full job (kMaxN slots x K) fits
 // one of two 48 KB slots and is loaded once per job, not once per unit.
 __host__ __device__ constexpr bool b_fits_resident(int K)
 {
-    return K / 64 <= 256 && static_cast<int64_t>(K) * 2 * kMaxN <= kResSlotBytes;
+    return static_cast<int64_t>(K + 64) * 2 * kMaxN <= kResSlotBytes;   // with the sums block
 }
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// (a & MASK) | magic in one LOP3, the mask an immediate and the magic
-// constant in a register (two immediates would cost a second LOP3).
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t magic)
-{
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(magic));
-    return r;
-}
-
-// 8 codes (one word, code i in bits 4i..4i+3) -> 4 words of fp16 pairs
-// q * s + c in the block order (q0,q4) (q1,q5) (q2,q6) (q3,q7).  `magic` holds
-// fp16 1024.0 twice.
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2, uint32_t magic,
+// 8 codes (one word) -> 4 words of fp16 pairs A = q * S + C in the block
+// order (q0,q4) (q1,q5) (q2,q6) (q3,q7); the codes enter as fp16 subnormals
+// (q or 16 q times 2^-24), S16 = S / 16 serves the 16 q pairs.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 S, __half2 S16, __half2 C,
                                              uint32_t *o)
 {
-    const __half2 k1024 = u2h(magic);
-    const __half2 kSixteenth = u2h(0x2C002C00u);           // 1/16
-    const __half2 kMinus64 = u2h(0xD400D400u);             // -64
     const uint32_t w8 = w >> 8;
-    const __half2 q04 = __hsub2(u2h(and_or<0x000F000Fu>(w, magic)), k1024);
-    const __half2 q15 = __hfma2(u2h(and_or<0x00F000F0u>(w, magic)), kSixteenth, kMinus64);
-    const __half2 q26 = __hsub2(u2h(and_or<0x000F000Fu>(w8, magic)), k1024);
-    const __half2 q37 = __hfma2(u2h(and_or<0x00F000F0u>(w8, magic)), kSixteenth, kMinus64);
-    o[0] = h2u(__hfma2(q04, s2, c2));
-    o[1] = h2u(__hfma2(q15, s2, c2));
-    o[2] = h2u(__hfma2(q26, s2, c2));
-    o[3] = h2u(__hfma2(q37, s2, c2));
+    o[0] = h2u(__hfma2(u2h(w & 0x000F000Fu), S, C));
+    o[1] = h2u(__hfma2(u2h(w & 0x00F000F0u), S16, C));
+    o[2] = h2u(__hfma2(u2h(w8 & 0x000F000Fu), S, C));
+    o[3] = h2u(__hfma2(u2h(w8 & 0x00F000F0u), S16, C));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t saddr)
@@ -289,11 +235,45 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr)
     return v;
 }
 
-__device__ __forceinline__ float lds_half_as_float(uint32_t saddr)
+__device__ __forceinline__ uint32_t lds_u16(uint32_t saddr)
 {
     unsigned short h;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(saddr));
-    return __half2float(__ushort_as_half(h));
+    return h;
+}
+
+// The row exponent c from the largest |scale| bit pattern of the row (for
+// non-negative fp16 values the bit patterns order like the values): with f
+// the biased exponent of that scale, c = max(f, 1) - 6 makes every scale of
+// the row times 2^(24 - c) an fp16 of exponent at most 15, i.e. <= 65504.
+__device__ __forceinline__ int row_exponent(uint32_t smax_bits)
+{
+    const int f = min(static_cast<int>(smax_bits >> 10), 30);
+    return max(f, 1) - 6;
+}
+
+__device__ __forceinline__ float exp2i(int e)   // 2^e for -126 <= e <= 127, exact
+{
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// The dequant constants of one group: S, S / 16 and C (see dequant_word).
+struct GroupK {
+    __half2 S, S16, C;
+};
+
+__device__ __forceinline__ GroupK group_consts(uint32_t s_bits, uint32_t z_bits, float scale_s,
+                                               float scale_c)
+{
+    const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(s_bits)));
+    const float z = __half2float(__ushort_as_half(static_cast<unsigned short>(z_bits)));
+    GroupK g;
+    // power-of-two scalings of an fp16 value: exact
+    g.S = __float2half2_rn(s * scale_s);
+    g.S16 = __float2half2_rn(s * scale_s * 0.0625f);
+    // s * z is exact in fp32 (two 11-bit significands); one rounding to fp16
+    g.C = __float2half2_rn(-(s * z) * scale_c);
+    return g;
 }
 
 __device__ __forceinline__ float gelu_tanh(float v)
@@ -305,22 +285,16 @@ __device__ __forceinline__ float gelu_tanh(float v)
 // A bounded wait by every lane of a warp (each lane observes the phase
 // itself, which gives it acquire ordering); the vote keeps the warp's
 // control flow uniform if the wait ever times out.
-__device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity, int lane,
+__device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int32_t *status)
 {
-    const bool ok = mbar_wait_warp(bar, parity, abort_flag, status, kDevPipelineTimeout);
-    if (!ok && lane == 0)
-        W4_TIMEOUT_RECORD(bar, parity, status);
-    return ok;
+    return mbar_wait_warp(bar, parity, abort_flag, status, kDevPipelineTimeout);
 }
 
 __device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           int32_t *status)
 {
-    const bool ok = mbar_wait(bar, parity, abort_flag, status, kDevPipelineTimeout);
-    if (!ok)
-        W4_TIMEOUT_RECORD(bar, parity, status);
-    return ok;
+    return mbar_wait(bar, parity, abort_flag, status, kDevPipelineTimeout);
 }
 
 // bounded wait that ignores the abort flag (used only while draining)
@@ -345,11 +319,9 @@ __device__ __forceinline__ int tile_row(int q4, int lane)
 
 // RESIDENT: each job's activations are loaded once into one of two 48 KB
 // slots (contraction dim <= 768); otherwise they stream through 32 KB slots.
-template <bool GATE_UP, int BUFS, bool RESIDENT>
+template <bool GATE_UP, bool RESIDENT>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p)
 {
-    constexpr int kSets = acc_sets<BUFS>();
-    constexpr uint32_t kAccCol = acc_col<BUFS>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -366,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned full = 0xffffffffu;
     int32_t *status = p.dev_status;
+    const int n_sz = p.n_sz;
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
@@ -375,26 +348,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int i = 0; i < kStagesB; i++) {
             mbar_init(&bar.b_full[i], 1);
-            mbar_init(&bar.b_empty[i], kIssuers);
+            mbar_init(&bar.b_empty[i], 2);           // both issuers' commits
         }
-        for (int i = 0; i < kMaxSubBufs; i++) {
-            mbar_init(&bar.a_full[i], 4);            // the four lane quarters
+        for (int i = 0; i < kRings * kRingBufs; i++) {
+            mbar_init(&bar.a_full[i], 4);            // the four lane quarters of the ring
             mbar_init(&bar.a_empty[i], 1);           // the issuer's commit
         }
         for (int i = 0; i < 2; i++) {
-            mbar_init(&bar.acc_full[i], kIssuers);
+            mbar_init(&bar.acc_full[i], 2);          // both issuers' commits
             mbar_init(&bar.acc_empty[i], kNumEpiWarps);
         }
-        for (int i = 0; i < kStagesSZ; i++) {
+        for (int i = 0; i < kMaxStagesSZ; i++) {
             mbar_init(&bar.sz_full[i], 1);
             mbar_init(&bar.sz_empty[i], kNumDqWarps);
         }
-        for (int i = 0; i < kIssuers; i++)
-            mbar_init(&bar.drain[i], 1);
+        mbar_init(&bar.drain[0], 1);
+        mbar_init(&bar.drain[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == kWarpAlloc) {
         tmem_alloc(tmem_holder, kTmemCols);
         tmem_relinquish();
     }
@@ -440,128 +413,145 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t tmem = *tmem_holder;
     const int n_units = jp[p.E] * p.n_panels;
     const int K = p.K;
+    const int n_sub = p.n_sub;
+    // the last sub-chunk holds 64 codes when K is an odd multiple of 64
+    const bool half_tail = (K & (kSubK - 1)) != 0;
 
-    if (warp < kIssuers) {
-        // ------------------------------------------------------- MMA issuers
-        // Each issuer warp runs this loop converged (every value in it is
-        // warp-uniform) and one elected lane issues each tcgen05 instruction,
-        // which costs the warp far fewer cycles than issuing from a lone lane.
-        {
-            const int me = warp;
-            const uint32_t b_base = smem_u32(stage_b);
-            uint32_t b_seq = 0, n_unit = 0;
-            uint32_t a_slot = 0, a_ph = 0;   // this issuer's next A buffer and its phase
-            int n_tr = 0;
-            int cur_job = -1;       // resident mode: the job whose activations are held
-            uint32_t res_slot = 0;
-            bool ok = true;
-            // One 64-code sub-chunk: wait for its A buffer, four K=16 MMAs, and
-            // hand the buffer back when they complete.
-            auto issue = [&](uint32_t d_tmem, uint64_t bdesc, uint32_t idesc, bool first) -> bool {
-                const int buf = me + kIssuers * a_slot;
-                if (!warp_all_wait(&bar.a_full[buf], a_ph, lane, abort_flag, status))
-                    return false;
-                if (++a_slot == BUFS) {
-                    a_slot = 0;
-                    a_ph ^= 1;
-                }
-                tc_fence_after();
-                if (me == 0 && lane == 0)
-                    W4_TRACE_POINT(5, n_tr);
-                const uint32_t a_tmem = tmem + buf * 32;
-                // K steps of 16: +32 B in the swizzled row (+2 in the
-                // descriptor's address field), +8 columns of A
-                tc_mma_ts_elect(d_tmem, a_tmem, bdesc, idesc, first ? 0u : 1u);
-                tc_mma_ts_elect(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1u);
-                tc_mma_ts_elect(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1u);
-                tc_mma_ts_elect(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1u);
-                tc_commit_elect(&bar.a_empty[buf]);
-                if (me == 0 && lane == 0)
-                    W4_TRACE_POINT(6, n_tr);
-                n_tr++;
-                return true;
-            };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
-                const int job = u / p.n_panels;
-                const Job J = decode_job(jp, offs, p.E, job);
-                const uint32_t idesc = idesc_f16_f32(kTileRows, J.n);
-                const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
-                const int set = kSets == 1 ? 0 : (n_unit & 1);
-                const uint32_t acc_ph = (kSets == 1 ? n_unit : n_unit >> 1) & 1;
-                if (!warp_all_wait(&bar.acc_empty[set], acc_ph ^ 1, lane, abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + kAccCol + set * 128 + me * 32;
-                if constexpr (RESIDENT) {
-                    // the job's activations stay in one slot for all its units
-                    if (job != cur_job) {
-                        if (cur_job >= 0)
-                            tc_commit_elect(&bar.b_empty[res_slot]);
-                        res_slot = b_seq & 1;
-                        if (!warp_all_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, lane, abort_flag, status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        b_seq++;
-                        cur_job = job;
-                    }
-                    const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
-                    for (int j = me; j < p.n_sub; j += kIssuers) {
-                        if (!issue(d_tmem, sdesc_sw128(b_slot + static_cast<uint32_t>(j) * col_bytes),
-                                   idesc, j == me)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                } else {
-                    const int kb_cap = 64 * b_kcols(J.n);
-                    const int n_bslots = (K + kb_cap - 1) / kb_cap;
-                    bool first = true;
-                    for (int t = 0; t < n_bslots && ok; t++) {
-                        const int sb = (b_seq + t) % kStagesB;
-                        if (!warp_all_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, lane, abort_flag, status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t b_slot = b_base + sb * kStageBBytes;
-                        const int j0 = t * (kb_cap / kSubK);
-                        const int j1 = min(p.n_sub, j0 + kb_cap / kSubK);
-                        // my sub-chunks in this slot: j = me (mod kIssuers); sub-chunk
-                        // j - j0 of the slot is its (j - j0)-th 64-wide column block
-                        for (int j = j0 + ((me - j0) % kIssuers + kIssuers) % kIssuers; j < j1;
-                             j += kIssuers) {
-                            if (!issue(d_tmem,
-                                       sdesc_sw128(b_slot + static_cast<uint32_t>(j - j0) * col_bytes),
-                                       idesc, first)) {
-                                ok = false;
-                                break;
-                            }
-                            first = false;
-                        }
-                        if (!ok)
-                            break;
-                        tc_commit_elect(&bar.b_empty[sb]);
-                    }
-                    b_seq += n_bslots;
-                }
-                if (!ok)
-                    break;
-                tc_commit_elect(&bar.acc_full[set]);
+    if (warp == kWarpMma0 || warp == kWarpMma1) {
+        // ------------------------------------------------------ MMA issuers
+        // Issuer `me` takes the sub-chunks of ring me (j = me, me + 2, ...,
+        // and the correction when n_sub % 2 == me) into its own accumulator.
+        // The warp runs this loop converged (every value in it is
+        // warp-uniform, kept in registers) and one elected lane issues each
+        // tcgen05 instruction.
+        const int me = warp == kWarpMma0 ? 0 : 1;
+        const uint32_t b_base = smem_u32(stage_b);
+        uint32_t b_seq = 0, n_unit = 0;
+        uint32_t ring_slot = 0, ring_ph = 0;
+        int cur_job = -1;       // resident mode: the job whose activations are held
+        uint32_t res_slot = 0;
+        bool ok = true;
+        // Sub-chunk j of the unit (j % 2 == me): wait for its A buffer, 8 (or
+        // 4 for a 64-code tail) K = 16 MMAs, and hand the buffer back when
+        // they complete.  bdesc: descriptor of the sub-chunk's first 64-code
+        // column block; the second follows col_bytes later.  j == n_sub is
+        // the group-constant correction: n_corr_mma MMAs of the constants'
+        // low parts against the activations' group sums (one column block).
+        auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t col_bytes,
+                         uint32_t idesc) -> bool {
+            const int buf = me * kRingBufs + static_cast<int>(ring_slot);
+            if (!warp_all_wait(&bar.a_full[buf], ring_ph, abort_flag, status))
+                return false;
+            if (++ring_slot == kRingBufs) {
+                ring_slot = 0;
+                ring_ph ^= 1;
             }
-            // every MMA of this warp completes before tensor memory is freed
-            tc_commit_elect(&bar.drain[me]);
-            drain_wait(&bar.drain[me], 0);
+            tc_fence_after();
+            const uint32_t a_tmem = tmem + static_cast<uint32_t>(buf) * kSubCols;
+            const int n_mma = j == n_sub ? p.n_corr_mma : (half_tail && j == n_sub - 1) ? 4 : 8;
+            const uint64_t blk = col_bytes >> 4;
+            // this issuer's first sub-chunk of the unit starts its accumulator
+            const uint32_t acc0 = j == me ? 0u : 1u;
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                if (kk < n_mma)
+                    // K steps of 16: +32 B in the swizzled row (+2 in the
+                    // descriptor's address field), +8 columns of A
+                    tc_mma_ts_elect(d_tmem, a_tmem + 8 * kk,
+                                    bdesc + static_cast<uint64_t>(kk >> 2) * blk + 2 * (kk & 3),
+                                    idesc, kk == 0 ? acc0 : 1u);
+            }
+            tc_commit_elect(&bar.a_empty[buf]);
+            return true;
+        };
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
+            const int job = u / p.n_panels;
+            const Job J = decode_job(jp, offs, p.E, job);
+            const uint32_t idesc = idesc_f16_f32(kTileRows, J.n);
+            const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
+            const int set = n_unit & 1;
+            const uint32_t acc_ph = (n_unit >> 1) & 1;
+            if (!warp_all_wait(&bar.acc_empty[set], acc_ph ^ 1, abort_flag, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + kAccCol + set * (2 * kMaxN) + me * kMaxN;
+            if constexpr (RESIDENT) {
+                // the job's activations stay in one slot for all its units
+                if (job != cur_job) {
+                    if (cur_job >= 0)
+                        tc_commit_elect(&bar.b_empty[res_slot]);
+                    res_slot = b_seq & 1;
+                    if (!warp_all_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, abort_flag,
+                                       status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    b_seq++;
+                    cur_job = job;
+                }
+                const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
+                for (int j = me; j <= n_sub; j += 2) {
+                    // sub-chunk j reads column blocks 2j, 2j + 1; the
+                    // correction reads block K / 64 (the group sums)
+                    const uint32_t blk = j < n_sub ? 2u * j : static_cast<uint32_t>(K / 64);
+                    if (!issue(j, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), col_bytes,
+                               idesc)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            } else {
+                const int kcols = b_kcols(J.n);
+                const int subs_per_slot = kcols / 2;
+                // the last slot holds column block K / 64, the group sums
+                const int n_bslots = K / 64 / kcols + 1;
+                for (int t = 0; t < n_bslots && ok; t++) {
+                    const int sb = (b_seq + t) % kStagesB;
+                    if (!warp_all_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, abort_flag,
+                                       status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b_slot = b_base + sb * kStageBBytes;
+                    const int j0 = t * subs_per_slot;
+                    const int j1 = min(n_sub, j0 + subs_per_slot);
+                    // subs_per_slot is even, so j0 is; this issuer's are j0 + me, ...
+                    for (int j = j0 + me; j < j1; j += 2) {
+                        if (!issue(j, d_tmem, sdesc_sw128(b_slot + 2u * (j - j0) * col_bytes),
+                                   col_bytes, idesc)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (ok && t == n_bslots - 1 && (n_sub & 1) == me) {
+                        const uint32_t blk = static_cast<uint32_t>(K / 64 - t * kcols);
+                        if (!issue(n_sub, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), col_bytes,
+                                   idesc))
+                            ok = false;
+                    }
+                    if (!ok)
+                        break;
+                    tc_commit_elect(&bar.b_empty[sb]);
+                }
+                b_seq += n_bslots;
+            }
+            if (!ok)
+                break;
+            tc_commit_elect(&bar.acc_full[set]);
         }
+        // every MMA of this warp completes before tensor memory is freed
+        tc_commit_elect(&bar.drain[me]);
+        drain_wait(&bar.drain[me], 0);
         __syncwarp();
     } else if (warp == kWarpTmaW) {
-        // ----------------------------------- TMA: codes, scales/zeros, sums
+        // ------------------------------------------- TMA: codes, scales/zeros
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int sa = 0, szb = 0, n_tr = 0;
+            int sa = 0, szb = 0;
             uint32_t ph_a = 0, ph_sz = 0;
             uint32_t issued_a = 0, issue_ph_a = 0, issued_sz = 0, issue_ph_sz = 0;
             const uint32_t hb = 64u * p.G * 2;          // 64 rows of s (or z)
@@ -576,18 +566,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 {
                     uint8_t *dst = sz_base + szb * L.sz_stride;
                     mbar_arrive_expect_tx(&bar.sz_full[szb], 4 * hb);
-                    bulk_load(dst, p.sc + static_cast<int64_t>(row0) * p.G, hb, &bar.sz_full[szb],
-                              pol);
-                    bulk_load(dst + hb, p.sc + static_cast<int64_t>(row1) * p.G, hb,
-                              &bar.sz_full[szb], pol);
-                    bulk_load(dst + 2 * hb, p.zp + static_cast<int64_t>(row0) * p.G, hb,
-                              &bar.sz_full[szb], pol);
-                    bulk_load(dst + 3 * hb, p.zp + static_cast<int64_t>(row1) * p.G, hb,
-                              &bar.sz_full[szb], pol);
+                    bulk_load_nohint(dst, p.sc + static_cast<int64_t>(row0) * p.G, hb,
+                                     &bar.sz_full[szb]);
+                    bulk_load_nohint(dst + hb, p.sc + static_cast<int64_t>(row1) * p.G, hb,
+                                     &bar.sz_full[szb]);
+                    bulk_load_nohint(dst + 2 * hb, p.zp + static_cast<int64_t>(row0) * p.G, hb,
+                                     &bar.sz_full[szb]);
+                    bulk_load_nohint(dst + 3 * hb, p.zp + static_cast<int64_t>(row1) * p.G, hb,
+                                     &bar.sz_full[szb]);
                 }
                 issued_sz |= 1u << szb;
                 issue_ph_sz = (issue_ph_sz & ~(1u << szb)) | (ph_sz << szb);
-                if (++szb == kStagesSZ) {
+                if (++szb == n_sz) {
                     szb = 0;
                     ph_sz ^= 1;
                 }
@@ -596,8 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         ok = false;
                         break;
                     }
-                    W4_TRACE_POINT(0, n_tr);
-                    n_tr++;
                     uint8_t *dst = stage_w + sa * kStageWBytes;
                     mbar_arrive_expect_tx(&bar.w_full[sa], kStageWBytes);
                     tma_load_2d(dst, &p.tmap_w, kc * 128, row0, &bar.w_full[sa], pol);
@@ -615,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 for (int i = 0; i < kStagesW; i++)
                     if (issued_a >> i & 1u)
                         drain_wait(&bar.w_full[i], issue_ph_a >> i & 1u);
-                for (int i = 0; i < kStagesSZ; i++)
+                for (int i = 0; i < n_sz; i++)
                     if (issued_sz >> i & 1u)
                         drain_wait(&bar.sz_full[i], issue_ph_sz >> i & 1u);
             }
@@ -629,11 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             pdl_trigger();
         }
         if (lane == 0) {
-            int sb = 0, n_tr = 0;
+            int sb = 0;
             uint32_t ph_b = 0, issued_b = 0, issue_ph_b = 0;
             bool ok = true;
             if constexpr (RESIDENT) {
-                // one load per job into slot b_seq & 1, once the issuers have
+                // one load per job into slot b_seq & 1, once the issuer has
                 // released that slot's previous job
                 int cur_job = -1;
                 uint32_t b_seq = 0;
@@ -649,10 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         ok = false;
                         break;
                     }
-                    W4_TRACE_POINT(1, n_tr);
-                    n_tr++;
                     mbar_arrive_expect_tx(&bar.b_full[s],
-                                          static_cast<uint32_t>(J.n) * 128 * p.n_sub);
+                                          static_cast<uint32_t>(J.n) * 128 * (K / 64 + 1));
                     tma_load_3d(stage_b + s * kResSlotBytes, &p.tmap_b[J.n / 16 - 1], 0, J.start,
                                 0, &bar.b_full[s]);
                     issued_b |= 1u << s;
@@ -665,13 +651,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const CUtensorMap *map = &p.tmap_b[J.n / 16 - 1];
                     const int kcols = b_kcols(J.n);
                     const uint32_t bytes = static_cast<uint32_t>(J.n) * 128 * kcols;
-                    for (int k_lo = 0; k_lo < K; k_lo += 64 * kcols) {
+                    // column blocks 0 .. K / 64, the last one the group sums
+                    for (int k_lo = 0; k_lo <= K; k_lo += 64 * kcols) {
                         if (!lane_wait(&bar.b_empty[sb], ph_b ^ 1, abort_flag, status)) {
                             ok = false;
                             break;
                         }
-                        W4_TRACE_POINT(1, n_tr);
-                        n_tr++;
                         mbar_arrive_expect_tx(&bar.b_full[sb], bytes);
                         tma_load_3d(stage_b + sb * kStageBBytes, map, 0, J.start, k_lo / 64,
                                     &bar.b_full[sb]);
@@ -690,47 +675,51 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         drain_wait(&bar.b_full[i], issue_ph_b >> i & 1u);
         }
         __syncwarp();
-    } else if (warp >= kFirstDqWarp && warp < kFirstDqWarp + kNumDqWarps) {
+    } else if (warp >= kFirstDqWarp) {
         // ---------------------------------------------------------- dequant
-        // Warp (q4, sub) expands sub-chunk sub of every chunk for its 32 rows:
-        // sub-chunk j = 4 kc + sub goes to issuer sub, into that issuer's
-        // buffers sub and sub + 4, alternating.
+        // Warp (q4, h) expands sub-chunk h (codes 128 h .. 128 h + 127) of
+        // every stage for its 32 rows into the A buffers of ring h.
         const int q4 = warp & 3;
-        const int sub = (warp - kFirstDqWarp) >> 2;
+        const int h = (warp - kFirstDqWarp) >> 2;
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        int sa = 0, szb = 0, n_tr = 0;
-        uint32_t ph_a = 0, ph_sz = 0, n_unit = 0;
-        uint32_t a_slot = 0, a_ph = 0;   // next A buffer of issuer `sub`, and its phase
+        int sa = 0, szb = 0;
+        uint32_t ph_a = 0, ph_sz = 0;
+        uint32_t ring_slot = 0, ring_ph = 0;
         const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
-        const uint32_t code_off0 = static_cast<uint32_t>(row * 128 + (((2 * sub) ^ (row & 7)) << 4));
-        const uint32_t code_off1 =
-            static_cast<uint32_t>(row * 128 + (((2 * sub + 1) ^ (row & 7)) << 4));
-        uint32_t magic;   // fp16 1024.0 twice, kept in a register
-        asm("mov.b32 %0, 0x64006400;" : "=r"(magic));
+        // the four 16-byte chunks of this warp's half of a row, swizzled
+        uint32_t code_off[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            code_off[i] = static_cast<uint32_t>(row * 128 + (((4 * h + i) ^ (row & 7)) << 4));
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
-            if (!warp_all_wait(&bar.sz_full[szb], ph_sz, lane, abort_flag, status))
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            if (!warp_all_wait(&bar.sz_full[szb], ph_sz, abort_flag, status))
                 break;
             const uint32_t s_addr = sz_base_s + szb * L.sz_stride + 2 * row * p.G;
+            const uint32_t z_addr = s_addr + 2 * kTileRows * p.G;
+            uint32_t smax = 0;
+            for (int g = 0; g < p.G; g++)
+                smax = max(smax, lds_u16(s_addr + 2 * g) & 0x7FFFu);
+            const int c = row_exponent(smax);
+            const float scale_s = exp2i(24 - c), scale_c = exp2i(-c);
             for (int kc = 0; kc < p.n_kchunks; kc++) {
-                if (!warp_all_wait(&bar.w_full[sa], ph_a, lane, abort_flag, status)) {
+                if (!warp_all_wait(&bar.w_full[sa], ph_a, abort_flag, status)) {
                     ok = false;
                     break;
                 }
-                if (warp == kFirstDqWarp && lane == 0)
-                    W4_TRACE_POINT(2, n_tr);
-                const int j = kc * (kChunkK / kSubK) + sub;   // sub-chunk in unit
-                const bool mine = j < p.n_sub;
+                const int j = 2 * kc + h;                 // sub-chunk of the unit
+                const bool mine = j < n_sub;
+                const bool tail = mine && half_tail && j == n_sub - 1;   // 64 codes
                 const uint32_t rp = stage_w_s + sa * kStageWBytes;
-                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-                float sf = 0.0f, zf = 0.0f;
+                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0, v3 = v0;
                 if (mine) {
-                    w0 = lds128(rp + code_off0);
-                    w1 = lds128(rp + code_off1);
-                    const uint32_t g = static_cast<uint32_t>(j * kSubK) >> p.group_shift;
-                    sf = lds_half_as_float(s_addr + 2 * g);
-                    zf = lds_half_as_float(s_addr + 2 * (kTileRows * p.G + g));
+                    v0 = lds128(rp + code_off[0]);
+                    v1 = lds128(rp + code_off[1]);
+                    if (!tail) {
+                        v2 = lds128(rp + code_off[2]);
+                        v3 = lds128(rp + code_off[3]);
+                    }
                 }
                 __syncwarp();
                 mbar_arrive_elect(&bar.w_empty[sa]);
@@ -740,47 +729,113 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 if (!mine)
                     continue;
-                const int buf = sub + kIssuers * a_slot;
-                if (!warp_all_wait(&bar.a_empty[buf], a_ph ^ 1, lane, abort_flag, status)) {
+                // groups of the two 64-code halves (the same group for g128)
+                const uint32_t g0 = static_cast<uint32_t>(j * kSubK) >> p.group_shift;
+                const uint32_t g1 = static_cast<uint32_t>(j * kSubK + 64) >> p.group_shift;
+                const GroupK k0 =
+                    group_consts(lds_u16(s_addr + 2 * g0), lds_u16(z_addr + 2 * g0), scale_s, scale_c);
+                uint32_t o[32];
+                dequant_word(v0.x, k0.S, k0.S16, k0.C, &o[0]);
+                dequant_word(v0.y, k0.S, k0.S16, k0.C, &o[4]);
+                dequant_word(v0.z, k0.S, k0.S16, k0.C, &o[8]);
+                dequant_word(v0.w, k0.S, k0.S16, k0.C, &o[12]);
+                dequant_word(v1.x, k0.S, k0.S16, k0.C, &o[16]);
+                dequant_word(v1.y, k0.S, k0.S16, k0.C, &o[20]);
+                dequant_word(v1.z, k0.S, k0.S16, k0.C, &o[24]);
+                dequant_word(v1.w, k0.S, k0.S16, k0.C, &o[28]);
+                const int buf = h * kRingBufs + static_cast<int>(ring_slot);
+                if (!warp_all_wait(&bar.a_empty[buf], ring_ph ^ 1, abort_flag, status)) {
                     ok = false;
                     break;
                 }
-                if (++a_slot == BUFS) {
-                    a_slot = 0;
-                    a_ph ^= 1;
+                if (++ring_slot == kRingBufs) {
+                    ring_slot = 0;
+                    ring_ph ^= 1;
                 }
-                if (warp == kFirstDqWarp && lane == 0)
-                    W4_TRACE_POINT(4, n_tr);
                 tc_fence_after();
-                const __half2 s2 = __float2half2_rn(sf);
-                const __half2 c2 = __float2half2_rn(-zf * sf);
-                uint32_t o[32];
-                dequant_word(w0.x, s2, c2, magic, &o[0]);
-                dequant_word(w0.y, s2, c2, magic, &o[4]);
-                dequant_word(w0.z, s2, c2, magic, &o[8]);
-                dequant_word(w0.w, s2, c2, magic, &o[12]);
-                dequant_word(w1.x, s2, c2, magic, &o[16]);
-                dequant_word(w1.y, s2, c2, magic, &o[20]);
-                dequant_word(w1.z, s2, c2, magic, &o[24]);
-                dequant_word(w1.w, s2, c2, magic, &o[28]);
-                if (warp == kFirstDqWarp && lane == 0)
-                    W4_TRACE_POINT(8, n_tr);
-                tmem_st_32x32b_x32(tmem + lane_base + buf * 32, o);
+                const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
+                tmem_st_32x32b_x32(a_col, o);
+                if (!tail) {
+                    const GroupK k1 = g1 == g0 ? k0
+                                               : group_consts(lds_u16(s_addr + 2 * g1),
+                                                              lds_u16(z_addr + 2 * g1), scale_s,
+                                                              scale_c);
+                    uint32_t o2[32];
+                    dequant_word(v2.x, k1.S, k1.S16, k1.C, &o2[0]);
+                    dequant_word(v2.y, k1.S, k1.S16, k1.C, &o2[4]);
+                    dequant_word(v2.z, k1.S, k1.S16, k1.C, &o2[8]);
+                    dequant_word(v2.w, k1.S, k1.S16, k1.C, &o2[12]);
+                    dequant_word(v3.x, k1.S, k1.S16, k1.C, &o2[16]);
+                    dequant_word(v3.y, k1.S, k1.S16, k1.C, &o2[20]);
+                    dequant_word(v3.z, k1.S, k1.S16, k1.C, &o2[24]);
+                    dequant_word(v3.w, k1.S, k1.S16, k1.C, &o2[28]);
+                    tmem_st_32x32b_x32(a_col + 32, o2);
+                }
                 tmem_wait_st();
-                if (warp == kFirstDqWarp && lane == 0)
-                    W4_TRACE_POINT(14, n_tr);
                 tc_fence_before();
                 __syncwarp();
                 mbar_arrive_elect(&bar.a_full[buf]);
-                if (warp == kFirstDqWarp && lane == 0)
-                    W4_TRACE_POINT(3, n_tr);
-                n_tr++;
             }
             if (!ok)
                 break;
+            if ((n_sub & 1) == h) {
+                // The correction sub-chunk: C = -s z 2^-c rounded to fp16 (the
+                // constant of every dequantised weight of the group) leaves
+                // the part C_lo = fp16(C_exact - C).  The activations carry
+                // one (xg) or four (h) sum columns per group, so contraction
+                // index k of the correction belongs to group k or k / 4;
+                // column i of MMA step t holds k = 16 t + 2 i, 16 t + 2 i + 1;
+                // zero past the last group.
+                const int buf = h * kRingBufs + static_cast<int>(ring_slot);
+                // gate_up: word i of step t holds groups 16 t + 2 i, + 1;
+                // down (four sum columns per group): both halves of words
+                // 2 i' and 2 i' + 1 of step t hold group 4 t + i'
+                constexpr int kRep = GATE_UP ? 1 : 4;
+                uint32_t cw[4][8];
+#pragma unroll
+                for (int t = 0; t < 4; t++)
+#pragma unroll
+                    for (int gi = 0; gi < 16 / kRep; gi++) {
+                        const int g = (16 / kRep) * t + gi;
+                        uint32_t lo = 0;
+                        if (t < p.n_corr_mma && g < p.G) {
+                            const float sv = __half2float(__ushort_as_half(
+                                static_cast<unsigned short>(lds_u16(s_addr + 2 * g))));
+                            const float zv = __half2float(__ushort_as_half(
+                                static_cast<unsigned short>(lds_u16(z_addr + 2 * g))));
+                            const float cx = -(sv * zv) * scale_c;      // exact
+                            const float chi = __half2float(__float2half_rn(cx));
+                            lo = __half_as_ushort(__float2half_rn(cx - chi));   // cx - chi exact
+                        }
+                        if constexpr (kRep == 1) {
+                            if (gi & 1)
+                                cw[t][gi >> 1] |= lo << 16;
+                            else
+                                cw[t][gi >> 1] = lo;
+                        } else {
+                            cw[t][2 * gi] = cw[t][2 * gi + 1] = lo | (lo << 16);
+                        }
+                    }
+                if (!warp_all_wait(&bar.a_empty[buf], ring_ph ^ 1, abort_flag, status))
+                    break;
+                if (++ring_slot == kRingBufs) {
+                    ring_slot = 0;
+                    ring_ph ^= 1;
+                }
+                tc_fence_after();
+                const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
+#pragma unroll
+                for (int t = 0; t < 4; t++)
+                    if (t < p.n_corr_mma)
+                        tmem_st_32x32b_x8(a_col + 8 * t, cw[t]);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                mbar_arrive_elect(&bar.a_full[buf]);
+            }
             __syncwarp();
             mbar_arrive_elect(&bar.sz_empty[szb]);
-            if (++szb == kStagesSZ) {
+            if (++szb == n_sz) {
                 szb = 0;
                 ph_sz ^= 1;
             }
@@ -788,8 +843,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kNumEpiWarps) {
         // ---------------------------------------------------------- epilogue
         const int q4 = warp & 3;
+        const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        const int n_acc = min(kIssuers, p.n_sub);
         // gate_up: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
         // the gate lane finishes even slots, the up lane odd ones
         const bool is_gate = lane < 16;
@@ -798,93 +853,100 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, n_unit++) {
             const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
             const int pnl = u % p.n_panels;
-            const int set = kSets == 1 ? 0 : (n_unit & 1);
-            const uint32_t acc_ph = (kSets == 1 ? n_unit : n_unit >> 1) & 1;
-            // down: the assignment of every slot of the job, fetched early
-            int my_a = -1;
-            if constexpr (!GATE_UP)
-                my_a = lane < J.n ? __ldg(p.sorted_ids + J.start + lane) : -1;
-            if (!warp_all_wait(&bar.acc_full[set], acc_ph, lane, abort_flag, status))
+            const int set = n_unit & 1;
+            const uint32_t acc_ph = (n_unit >> 1) & 1;
+            // this lane's weight row, for its exponent (the same rule as the
+            // dequant warps, from the same scales, read here from global
+            // memory while the unit's MMAs run)
+            const int64_t grow =
+                GATE_UP ? static_cast<int64_t>(J.e) * p.R + (row < 64 ? 0 : p.m_up) + pnl * 64 +
+                              (row & 63)
+                        : static_cast<int64_t>(J.e) * p.R + pnl * 128 + row;
+            uint32_t smax = 0;
+            for (int g = 0; g < p.G; g++)
+                smax = max(smax, static_cast<uint32_t>(__ldg(p.sc + grow * p.G + g)) & 0x7FFFu);
+            const float factor = exp2i(row_exponent(smax));
+            // the assignment of every slot of the job, fetched early (gate_up:
+            // padding slots get zero rows; down: rows go to y by assignment)
+            const int my_a = lane < J.n ? __ldg(p.sorted_ids + J.start + lane) : -1;
+            if (!warp_all_wait(&bar.acc_full[set], acc_ph, abort_flag, status))
                 break;
-            if (warp == kFirstEpiWarp && lane == 0)
-                W4_TRACE_POINT(10, n_unit);
             tc_fence_after();
-            // Per block of 8 slots: the issuers' accumulators, added in a fixed
-            // order (issuers without a sub-chunk in this unit never wrote
-            // theirs), then the outputs.  The set goes back to the issuers as
-            // soon as its last block is in registers.
-            const uint32_t acc = tmem + lane_base + kAccCol + set * 128;
-            const int n_blk = J.n / 8;
+            float v[kMaxN];
+            {
+                // the two issuers' accumulators, added in a fixed order
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kAccCol + set * (2 * kMaxN), r0);
+                tmem_ld_32x32b_x32(tmem + lane_base + kAccCol + set * (2 * kMaxN) + kMaxN, r1);
 #pragma unroll
-            for (int b = 0; b < kMaxN / 8; b++) {
-                if (b >= n_blk)
-                    break;
-                float v[8];
-                {
-                    uint32_t r[32];
-                    tmem_ld_4x_32x32b_x8(acc + 8 * b, acc + 32 + 8 * b, acc + 64 + 8 * b,
-                                         acc + 96 + 8 * b, r);
+                for (int i = 0; i < kMaxN; i++)
+                    v[i] = (__uint_as_float(r0[i]) + __uint_as_float(r1[i])) * factor;
+            }
+            tc_fence_before();
+            __syncwarp();
+            mbar_arrive_elect(&bar.acc_empty[set]);
+            if constexpr (GATE_UP) {
+                // h of this panel: 64 intermediates = group pnl of the down
+                // GEMM's contraction; this warp holds 16 of them and also
+                // writes their sum (of the fp16 values) to sum column
+                // 4 pnl + q4 of the row, the down GEMM's correction input
+                uint16_t *hout = reinterpret_cast<uint16_t *>(p.out);
+                const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);
+                bool range = false;
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        float t = __uint_as_float(r[i]);
-                        if (n_acc > 1)
-                            t += __uint_as_float(r[8 + i]);
-                        if (n_acc > 2)
-                            t += __uint_as_float(r[16 + i]);
-                        if (n_acc > 3)
-                            t += __uint_as_float(r[24 + i]);
-                        v[i] = t;
+                for (int i = 0; i < kMaxN; i += 2) {
+                    if (i >= J.n)
+                        break;
+                    const float send = is_gate ? v[i + 1] : v[i];
+                    const float recv = __shfl_xor_sync(full, send, 16);
+                    const float gv = is_gate ? v[i] : recv;
+                    const float uv = is_gate ? recv : v[i + 1];
+                    const int si = i + (is_gate ? 0 : 1);
+                    const int a = __shfl_sync(full, my_a, si);
+                    const bool real = static_cast<unsigned>(a) < static_cast<unsigned>(p.A);
+                    const float hv = gelu_tanh(gv) * uv;
+                    range |= real && !(fabsf(hv) <= 65504.0f);
+                    const uint16_t hq = real ? static_cast<uint16_t>(f16x2_sat(hv, 0.0f)) : 0;
+                    uint16_t *hrow = hout + (J.start + si) * static_cast<int64_t>(p.h_stride);
+                    hrow[pos] = hq;
+                    // lanes 0-15 sum slot i, lanes 16-31 slot i + 1 (fixed tree)
+                    float part = __half2float(__ushort_as_half(hq));
+                    part += __shfl_xor_sync(full, part, 8);
+                    part += __shfl_xor_sync(full, part, 4);
+                    part += __shfl_xor_sync(full, part, 2);
+                    part += __shfl_xor_sync(full, part, 1);
+                    if ((lane & 15) == 0) {
+                        range |= !(fabsf(part) <= 65504.0f);
+                        hrow[p.out_cols + 4 * pnl + q4] =
+                            static_cast<uint16_t>(f16x2_sat(part, 0.0f));
+                        if (pnl == 0)   // sum columns past the last group, read by the
+                                        // correction's last MMA step: zero
+                            for (int c = 4 * p.h_groups + q4; c < 16 * ((p.h_groups + 3) / 4);
+                                 c += 4)
+                                hrow[p.out_cols + c] = 0;
                     }
                 }
-                if (b == n_blk - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    mbar_arrive_elect(&bar.acc_empty[set]);
-                }
-                if constexpr (GATE_UP) {
-                    __half *hout = reinterpret_cast<__half *>(p.out);
-                    const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);
+                if (__any_sync(full, range) && lane == 0 && status)
+                    atomicOr(status, kDevFp16Range);
+            } else {
+                float *yout = reinterpret_cast<float *>(p.out);
+                const int col = pnl * 128 + row;
 #pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const float send = is_gate ? v[i + 1] : v[i];
-                        const float recv = __shfl_xor_sync(full, send, 16);
-                        const float gv = is_gate ? v[i] : recv;
-                        const float uv = is_gate ? recv : v[i + 1];
-                        const int64_t slot = J.start + 8 * b + i + (is_gate ? 0 : 1);
-                        hout[slot * p.out_cols + pos] = __ushort_as_half(
-                            static_cast<uint16_t>(f16x2_sat(gelu_tanh(gv) * uv, 0.0f)));
-                    }
-                } else {
-                    const int col = pnl * 128 + 32 * q4 + lane;
-                    if (p.out_bf16) {
-                        uint16_t *bout = reinterpret_cast<uint16_t *>(p.out);
-#pragma unroll
-                        for (int i = 0; i < 8; i++) {
-                            const int a = __shfl_sync(full, my_a, 8 * b + i);
-                            if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
-                                bout[static_cast<int64_t>(a) * p.out_cols + col] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
-                        }
-                    } else {
-                        float *yout = reinterpret_cast<float *>(p.out);
-#pragma unroll
-                        for (int i = 0; i < 8; i++) {
-                            const int a = __shfl_sync(full, my_a, 8 * b + i);
-                            if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
-                                yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
-                        }
-                    }
+                for (int i = 0; i < kMaxN; i++) {
+                    if (i >= J.n)
+                        break;
+                    const int a = __shfl_sync(full, my_a, i);
+                    if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
+                        yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
                 }
             }
-            if (warp == kFirstEpiWarp && lane == 0)
-                W4_TRACE_POINT(11, n_unit);
         }
     }
 
     // --------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kWarpAlloc) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -980,14 +1042,24 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.R = q.R;
     a.m_up = q.gate_up ? q.R / 2 : 0;
     a.out_cols = q.out_cols;
-    a.group = q.group;
     a.group_shift = q.group == 128 ? 7 : 6;
     a.G = q.K / q.group;
     a.n_panels = q.gate_up ? (q.R / 2) / 64 : q.R / 128;
     a.n_kchunks = (q.K + kChunkK - 1) / kChunkK;
-    a.n_sub = q.K / kSubK;
+    a.n_sub = (q.K + kSubK - 1) / kSubK;
+    a.n_sz = sz_stages(a.G);
+    // the activation rows end in one 64-column block of group sums: xg one
+    // per group of 128, h one per quarter (16 intermediates) of each group of 64
+    const int corr_rep = q.gate_up ? 1 : 4;
+    if (a.G * corr_rep > 64) {
+        *why = q.gate_up ? "gate_up contraction dim too large for its group sums (d <= 8192)"
+                         : "down contraction dim too large for its group sums (m <= 1024)";
+        return cudaErrorInvalidValue;
+    }
+    a.n_corr_mma = (a.G * corr_rep + 15) / 16;
+    a.h_stride = q.gate_up ? q.R / 2 + 64 : 0;
+    a.h_groups = q.gate_up ? (q.R / 2) / 64 : 0;
     a.early_schedule = q.early_schedule ? 1 : 0;
-    a.out_bf16 = q.out_bf16 ? 1 : 0;
     const bool resident = !q.gate_up && b_fits_resident(q.K);
 
     const SmemLayout L = smem_layout(a.G, a.E);
@@ -1015,16 +1087,16 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     }
     for (int i = 0; i < 2; i++) {
         const int rows = 16 * (i + 1);
-        const int kcols = resident ? q.K / 64 : b_kcols(rows);
-        if (!encode_act(encode, &a.tmap_b[i], q.act, q.cap, q.K, rows, kcols)) {
+        const int kcols = resident ? q.K / 64 + 1 : b_kcols(rows);
+        if (!encode_act(encode, &a.tmap_b[i], q.act, q.cap, q.K + 64, rows, kcols)) {
             *why = "cuTensorMapEncodeTiled rejected the activation tensor";
             return cudaErrorInvalidValue;
         }
     }
 
-    auto kern = q.gate_up ? grouped_gemm_kernel<true, kBufsGateUp, false>
-                : resident ? grouped_gemm_kernel<false, kBufsDown, true>
-                           : grouped_gemm_kernel<false, kBufsDown, false>;
+    auto kern = q.gate_up ? grouped_gemm_kernel<true, false>
+                : resident ? grouped_gemm_kernel<false, true>
+                           : grouped_gemm_kernel<false, false>;
     const int which = q.gate_up ? 2 : (resident ? 1 : 0);
     if (!di.attr_set[which]) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

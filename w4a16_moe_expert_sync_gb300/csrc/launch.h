@@ -14,6 +14,7 @@ namespace w4 {
 constexpr int32_t kDevBadExpertId = 0x1;
 constexpr int32_t kDevPipelineTimeout = 0x2;
 constexpr int32_t kDevTooManyJobs = 0x4;
+constexpr int32_t kDevFp16Range = 0x8;
 
 cudaError_t launch_quantize(const float *W, int64_t rows, int K, int group, uint8_t *q,
                             uint16_t *s, uint16_t *z, cudaStream_t stream);
@@ -30,7 +31,7 @@ cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, i
 // for slots below *num_padded.
 cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          cudaStream_t stream);
+                          int32_t *dev_status, cudaStream_t stream);
 
 // Alignment and gather in one launch (every CTA aligns in shared memory).
 size_t align_gather_smem_bytes(int M, int k, int E, int num_sms);
@@ -82,9 +83,6 @@ struct GroupedGemmProblem {
     // down may then read its schedule, and stream its weights, before its
     // grid-dependency wait.  Activations are read only after that wait.
     bool early_schedule = false;
-    // plain (down) epilogue only: write bf16 rows instead of fp32 ones (no
-    // entry point sets it at present: the dense linear has its own kernel)
-    bool out_bf16 = false;
 };
 
 // The dense W4A16 GEMM (dense_gemm.cu): y [M, N] bf16 = xg [Mpad, K] fp16

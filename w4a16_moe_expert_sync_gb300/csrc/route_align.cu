@@ -340,26 +340,100 @@ __global__ void __launch_bounds__(kAlignWarps * 32, 1)
                 dev_status, nullptr, ids_sm, &offs, &total);
 }
 
+// bf16 bit patterns of magnitude >= 65536 (and inf, NaN) do not fit fp16's
+// finite range: any of the eight in a 16-byte chunk?
+__device__ __forceinline__ bool bf16x8_out_of_f16_range(uint4 v)
+{
+    auto big = [](uint32_t w) {
+        return (w & 0x7FFFu) >= 0x4780u || ((w >> 16) & 0x7FFFu) >= 0x4780u;
+    };
+    return big(v.x) || big(v.y) || big(v.z) || big(v.w);
+}
+
+// The gathered rows (xg) are d fp16 values in block order followed by one
+// 64-column block of group sums: column d + g holds the sum of the fp16
+// values of group g (128 consecutive elements), columns from d/128 up to the
+// next multiple of 16 hold zero.  The grouped GEMM multiplies them by the
+// low parts of its dequantisation constants (grouped_gemm.cu).
+constexpr int kXGroup = 128;
+__host__ __device__ inline int64_t xg_stride(int d) { return static_cast<int64_t>(d) + 64; }
+
+// Sum of the eight fp16 values of a converted chunk, reduced over the 16
+// lanes that hold the 16 chunks of one group (lanes 16i .. 16i + 15 with
+// consecutive chunk indices; all 16 call together), in a fixed order.
+__device__ __forceinline__ float group_sum16(uint4 o)
+{
+    const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+        s += __low2float(h) + __high2float(h);
+    }
+    const unsigned mask = 0xFFFFu << (threadIdx.x & 16);
+    s += __shfl_xor_sync(mask, s, 1);
+    s += __shfl_xor_sync(mask, s, 2);
+    s += __shfl_xor_sync(mask, s, 4);
+    s += __shfl_xor_sync(mask, s, 8);
+    return s;
+}
+
+// The sum-block column written by the thread of chunk c8 of a row: its
+// group's sum (c8 % 16 == 0, column d + c8 / 16) or a zero column (c8 in
+// [d/128, 16 ceil(d/2048))); -1 for neither.  *value gets the fp16 bits.
+__device__ __forceinline__ int sum_column(int c8, int d, float gsum, uint16_t *value,
+                                          bool *range)
+{
+    const int G = d / kXGroup;
+    if ((c8 & 15) == 0) {
+        *range |= !(fabsf(gsum) <= 65504.0f);
+        *value = static_cast<uint16_t>(f16x2_sat(gsum, 0.0f));
+        return d + c8 / 16;
+    }
+    if (c8 >= G && c8 < 16 * ((G + 15) / 16)) {
+        *value = 0;
+        return d + c8;
+    }
+    return -1;
+}
+
 // Standalone gather: xg[slot] = x[token of slot] (fp16, block order), zero
-// for padding slots, for every slot below num_padded.
+// for padding slots, for every slot below num_padded; activations outside
+// fp16's finite range set W4_DEV_FP16_RANGE.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t *__restrict__ x, int d, int k,
                                                      int A, const int32_t *__restrict__ sorted_ids,
                                                      const int32_t *__restrict__ num_padded,
-                                                     uint16_t *__restrict__ xg)
+                                                     uint16_t *__restrict__ xg,
+                                                     int32_t *__restrict__ dev_status)
 {
     const int c8n = d / 8;
+    const int64_t ld = xg_stride(d);
     const int64_t total = static_cast<int64_t>(__ldg(num_padded)) * c8n;
+    bool range = false;
+    // c8n is a multiple of 16: the 16 lanes of a group take the chunks of one
+    // group of one row together
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t slot = i / c8n;
         const int c8 = static_cast<int>(i - slot * c8n);
         const int a = __ldg(sorted_ids + slot);
         uint4 o = make_uint4(0, 0, 0, 0);
-        if (static_cast<unsigned>(a) < static_cast<unsigned>(A))
-            o = bf16x8_to_f16_korder(__ldg(
-                reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(a / k) * d + 8 * c8)));
-        *reinterpret_cast<uint4 *>(xg + slot * d + 8 * c8) = o;
+        if (static_cast<unsigned>(a) < static_cast<unsigned>(A)) {
+            const uint4 raw = __ldg(
+                reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(a / k) * d + 8 * c8));
+            range |= bf16x8_out_of_f16_range(raw);
+            o = bf16x8_to_f16_korder(raw);
+        }
+        uint16_t *row = xg + slot * ld;
+        *reinterpret_cast<uint4 *>(row + 8 * c8) = o;
+        const float gsum = group_sum16(o);
+        uint16_t v;
+        const int col = sum_column(c8, d, gsum, &v, &range);
+        if (col >= 0)
+            row[col] = v;
     }
+    if (__any_sync(0xffffffffu, range) && (threadIdx.x & 31) == 0 && dev_status)
+        atomicOr(dev_status, kDevFp16Range);
 }
 
 // The alignment of M tokens to a single expert with one slot each (the dense
@@ -406,17 +480,20 @@ cudaError_t launch_identity_align_gather(const uint16_t *x, int M, int d, int pa
 // Fused alignment + gather (with ROUTE, router + alignment + gather from the
 // logits: every CTA routes every token into shared memory first, with the
 // same arithmetic as route_kernel, and writes ids and weights of its own
-// tokens).  Every CTA computes the alignment in its own
-// shared memory (so no CTA waits for another) and writes its share of the
-// alignment outputs.  CTA b copies the rows of tokens [b*tpc, (b+1)*tpc) to
-// the slots of their k assignments (each x row is read once; the first
-// kAheadTok x kAheadCols 16-byte chunks of a thread are loaded before the
-// alignment so that their latency overlaps it) and zeroes the padding slots
-// of experts b, b + G, ...
+// tokens).  CTA b owns tokens [b*tpc, (b+1)*tpc), i.e. assignments
+// [own0, own1).  It needs the alignment only for those: the padded offsets
+// (from every expert's count) and, for each owned assignment, its rank among
+// the assignments of its expert (the count of that expert's assignments
+// before own0, plus its rank among the owned ones).  So every CTA counts all
+// ids with shared-memory atomics, keeping apart those before own0, scans the
+// padded counts, places its own assignments (one warp, in order) and copies
+// its tokens' rows to their k slots.  The grid's threads write the padding
+// slots and block owners one expert each.  The rows of padding slots in xg
+// are not written: the GEMMs' outputs for those slots are discarded or
+// zeroed.  The first kAheadTok x kAheadCols 16-byte chunks of a thread's rows
+// are loaded before the counting so that their latency overlaps it.
 constexpr int kAheadTok = 2, kAheadCols = 2;
 
-// 16 warps: the alignment is bound by its instruction count, which splits
-// evenly over the warps; fewer warps leave the SM idle, more add scan work.
 __host__ __device__ inline int align_gather_threads(int E) { return E <= 512 ? 512 : (E + 31) / 32 * 32; }
 
 constexpr int kRouteEpl = 4;    // the fused router: E <= 128
@@ -435,12 +512,17 @@ __global__ void __launch_bounds__(1024, 1)
     pdl_wait();
     pdl_trigger();
     const int A = M * k;
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    int *pos = sm + align_smem_bytes(E, nthr >> 5) / sizeof(int);   // [tpc * k]
-    int *ids_sm = A <= kAlignStagedIds ? pos + tpc * k : nullptr;    // [A]
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned full = 0xffffffffu;
+    int *cnt = sm;                  // [E] assignments per expert
+    int *pre = cnt + E;             // [E] ... of them before own0
+    int *offs = pre + E;            // [E+1] padded offsets
+    int *pos = offs + E + 1;        // [tpc * k] slot of each owned assignment, -1 if skipped
+    int *ids_sm = pos + tpc * k;    // [A] (ROUTE only)
     const int c8n = d / 8;
     const int t0 = min(M, static_cast<int>(blockIdx.x) * tpc), t1 = min(M, t0 + tpc);
     const int ntok = t1 - t0;
+    const int own0 = t0 * k, own1 = t1 * k;
     // chunk c8 of this CTA's token tl is xr[tl * c8n + c8]
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0) * d);
     uint4 ahead[kAheadTok][kAheadCols];   // raw bf16: converted after the alignment
@@ -451,10 +533,14 @@ __global__ void __launch_bounds__(1024, 1)
             const int c8 = tid + r * nthr;
             ahead[tl][r] = tl < ntok && c8 < c8n ? __ldg(xr + tl * c8n + c8) : make_uint4(0, 0, 0, 0);
         }
+    for (int i = tid; i < E; i += nthr) {
+        cnt[i] = 0;
+        pre[i] = 0;
+    }
     if constexpr (ROUTE) {
-        // every token's top-k into shared memory (ids_sm is always there on
-        // this path), this CTA's tokens also to ids_out / w_out
-        const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+        // every token's top-k into shared memory, this CTA's tokens also to
+        // ids_out / w_out
+        const int nw = nthr >> 5;
         for (int t = warp; t < M; t += nw) {
             int id;
             float w;
@@ -467,18 +553,91 @@ __global__ void __launch_bounds__(1024, 1)
                 }
             }
         }
-        __syncthreads();
     }
-    int *offs, *total;
-    align_block(ROUTE ? nullptr : ids, A, E, bm, cap, t0 * k, t1 * k, sorted_ids, block_expert,
-                offsets, num_padded, dev_status, pos, ids_sm, &offs, &total);
     __syncthreads();
+    auto id_at = [&](int a) { return ROUTE ? ids_sm[a] : __ldg(ids + a); };
+
+    // counts: every valid id, and separately those before own0
+    bool bad = false;
+    for (int a = tid; a < A; a += nthr) {
+        const int e = id_at(a);
+        if (e >= 0 && e < E) {
+            atomicAdd(&cnt[e], 1);
+            if (a < own0)
+                atomicAdd(&pre[e], 1);
+        } else {
+            bad = true;
+        }
+    }
+    if (blockIdx.x == 0 && __any_sync(full, bad) && lane == 0 && dev_status)
+        atomicOr(dev_status, kDevBadExpertId);
+    __syncthreads();
+
+    // padded offsets: exclusive scan of ceil(count / bm) * bm (warp 0)
+    if (warp == 0) {
+        int base = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int padded = e < E ? (cnt[e] + bm - 1) / bm * bm : 0;
+            int inc = padded;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(full, inc, o);
+                if (lane >= o)
+                    inc += v;
+            }
+            if (e < E)
+                offs[e] = base + inc - padded;
+            base += __shfl_sync(full, inc, 31);
+        }
+        if (lane == 0)
+            offs[E] = base;
+    }
+    __syncthreads();
+
+    // stable placement of the owned assignments, in order (warp 0): rank =
+    // the expert's assignments before own0 + those before it in [own0, a)
+    if (warp == 0) {
+        const int nbits = 32 - __clz(max(E - 1, 1));
+        const unsigned lt_mask = (1u << lane) - 1u;
+        for (int base = own0; base < own1; base += 32) {
+            const int a = base + lane;
+            const int e = a < own1 ? id_at(a) : -1;
+            const bool valid = a < own1 && e >= 0 && e < E;
+            const unsigned grp = match_key(e, nbits, valid);
+            const int slot = valid ? offs[e] + pre[e] + __popc(grp & lt_mask) : -1;
+            __syncwarp();
+            if (valid && lane == __ffs(grp) - 1)
+                pre[e] += __popc(grp);
+            __syncwarp();
+            if (a < own1) {
+                pos[a - own0] = slot;
+                if (valid)
+                    sorted_ids[slot] = a;
+            }
+        }
+    }
+    __syncthreads();
+
+    // this CTA's rows to the slots of their assignments, in fp16 block order
+    bool range = false;
+    const int64_t ld = xg_stride(d);
+    // (the 16 lanes of a group always call this together: c8n is a multiple
+    // of 16 and each loop below gives a lane's group one chunk range)
     auto put = [&](int tl, int c8, uint4 raw) {
+        range |= bf16x8_out_of_f16_range(raw);
         const uint4 o = bf16x8_to_f16_korder(raw);
+        const float gsum = group_sum16(o);
+        uint16_t v;
+        const int col = sum_column(c8, d, gsum, &v, &range);
         for (int j = 0; j < k; j++) {
             const int slot = pos[tl * k + j];
-            if (slot >= 0)
-                *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(slot) * d + 8 * c8) = o;
+            if (slot >= 0) {
+                uint16_t *row = xg + static_cast<int64_t>(slot) * ld;
+                *reinterpret_cast<uint4 *>(row + 8 * c8) = o;
+                if (col >= 0)
+                    row[col] = v;
+            }
         }
     };
 #pragma unroll
@@ -492,15 +651,28 @@ __global__ void __launch_bounds__(1024, 1)
     for (int tl = 0; tl < ntok; tl++)
         for (int c8 = tid + (tl < kAheadTok ? kAheadCols * nthr : 0); c8 < c8n; c8 += nthr)
             put(tl, c8, __ldg(xr + tl * c8n + c8));
-    // padding rows: row sl of the padded range belongs to CTA sl mod grid; the
-    // warps of a CTA take the experts in turn
-    const int G = gridDim.x, b = blockIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = warp; e < E; e += nthr >> 5) {
-        const int s0 = offs[e] + total[e], s1 = offs[e + 1];
-        for (int sl = s0 + (b - s0 % G + G) % G; sl < s1; sl += G)
-            for (int c8 = lane; c8 < c8n; c8 += 32)
-                *reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(sl) * d + 8 * c8) =
-                    make_uint4(0, 0, 0, 0);
+    if (__any_sync(full, range) && lane == 0 && dev_status)
+        atomicOr(dev_status, kDevFp16Range);
+
+    // padding slots and block owners, one expert per thread of the grid; the
+    // slots past the last expert; offsets and num_padded from CTA 0
+    const int gtid = blockIdx.x * nthr + tid, gstride = gridDim.x * nthr;
+    for (int e = gtid; e < E; e += gstride) {
+        for (int sl = offs[e] + cnt[e]; sl < offs[e + 1]; sl++)
+            sorted_ids[sl] = A;
+        for (int b = offs[e] / bm; b < offs[e + 1] / bm; b++)
+            block_expert[b] = e;
+    }
+    const int npad = offs[E];
+    for (int sl = npad + gtid; sl < cap; sl += gstride)
+        sorted_ids[sl] = A;
+    for (int b = npad / bm + gtid; b < cap / bm; b += gstride)
+        block_expert[b] = -1;
+    if (blockIdx.x == 0) {
+        for (int i = tid; i <= E; i += nthr)
+            offsets[i] = offs[i];
+        if (tid == 0)
+            num_padded[0] = npad;
     }
 }
 
@@ -527,12 +699,12 @@ cudaError_t launch_align(const int32_t *ids, int M, int k, int E, int block_m, i
 
 cudaError_t launch_gather(const uint16_t *x, int M, int d, int k, int64_t cap,
                           const int32_t *sorted_ids, const int32_t *num_padded, uint16_t *xg,
-                          cudaStream_t stream)
+                          int32_t *dev_status, cudaStream_t stream)
 {
     const int64_t total = cap * (d / 8);
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 4096));
     gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, d, k, M * k, sorted_ids,
-                                                                      num_padded, xg);
+                                                                      num_padded, xg, dev_status);
     return cudaGetLastError();
 }
 
@@ -548,9 +720,13 @@ size_t align_gather_smem_bytes(int M, int k, int E, int num_sms)
 {
     int grid, tpc;
     align_gather_grid(M, num_sms, &grid, &tpc);
-    const int64_t A = static_cast<int64_t>(M) * k;
-    return align_smem_bytes(E, align_gather_threads(E) / 32) +
-           sizeof(int) * (static_cast<size_t>(tpc) * k + (A <= kAlignStagedIds ? A : 0));
+    // counts, counts before own0, offsets, owned slots (+ every id with the router)
+    return sizeof(int) * (3 * static_cast<size_t>(E) + 1 + static_cast<size_t>(tpc) * k);
+}
+
+static size_t route_align_gather_smem_bytes(int M, int k, int E, int num_sms)
+{
+    return align_gather_smem_bytes(M, k, E, num_sms) + sizeof(int) * static_cast<size_t>(M) * k;
 }
 
 cudaError_t launch_align_gather(const int32_t *ids, int M, int k, int E, int block_m, int64_t cap,
@@ -580,7 +756,7 @@ bool route_align_gather_fits(int M, int k, int E, int num_sms)
     // (measured: 22.5 us against 17.4 us at 32 tokens, 26.8 against 15.3 at 64).
     return E <= 32 * kRouteEpl && M <= align_gather_threads(E) / 32 &&
            static_cast<int64_t>(M) * k <= kAlignStagedIds &&
-           align_gather_smem_bytes(M, k, E, num_sms) <= 200 * 1024;
+           route_align_gather_smem_bytes(M, k, E, num_sms) <= 200 * 1024;
 }
 
 cudaError_t launch_route_align_gather(const float *logits, int M, int k, int E, int block_m,
@@ -592,7 +768,7 @@ cudaError_t launch_route_align_gather(const float *logits, int M, int k, int E, 
 {
     if (!route_align_gather_fits(M, k, E, num_sms))
         return cudaErrorInvalidValue;
-    const size_t smem = align_gather_smem_bytes(M, k, E, num_sms);
+    const size_t smem = route_align_gather_smem_bytes(M, k, E, num_sms);
     cudaError_t err = set_align_smem(reinterpret_cast<const void *>(moe_align_gather_kernel<true>));
     if (err != cudaSuccess)
         return err;
