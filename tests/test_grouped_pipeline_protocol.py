@@ -5,13 +5,15 @@ test_dense_pipeline_protocol.py.
 Roles as the kernel writes them, with the kernel's constants: the TMA warp for
 codes and scales/zeros (6 code stages, 2 or 3 scale stages), the TMA warp for
 activations (3 streamed slots, or 2 resident slots that hold a job's whole
-activation block, the group-sum block included), two MMA issuers (issuer h
-takes ring h of three A buffers in tensor memory and has its own accumulator
-in each of two sets; each issuer's commits complete asynchronously in its
-issue order), eight dequantisation warps (lane quarter x half of each code
-stage; the half whose ring takes sub-chunk n_sub also produces the
-group-constant correction after its last sub-chunk of a unit) and four
-epilogue warps.  Every wait is checked against the exact condition:
+activation block, the group-sum block included), four MMA issuers (issuer
+2h + p takes half p of every A buffer of ring h, two buffers per ring in
+tensor memory; each has its own accumulator in each of two sets; each
+issuer's commits complete asynchronously in its issue order), eight
+dequantisation warps (lane quarter x half of each code stage, pipelined by
+one item: a buffer's two halves are handed over only after the warp's next
+item has been loaded and computed; the half whose ring takes sub-chunk n_sub
+also produces the group-constant correction after its last sub-chunk of a
+unit) and four epilogue warps.  Every wait is checked against the exact condition:
 the phase it stands for, counted from per-stage uses kept apart from the
 kernel's parity variables, has completed exactly when the parity test says
 so.  Unit lists mix jobs of 16 and 32 slots over several panels; contraction
@@ -23,7 +25,7 @@ import random
 
 import pytest
 
-RINGS, RING_BUFS, SETS = 2, 3, 2
+RINGS, RING_BUFS, SETS, ISSUERS = 2, 2, 2, 4
 STAGES_W, STAGES_B = 6, 3
 DQ_WARPS, EPI_WARPS = 8, 4
 CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 128, 32, 49152
@@ -57,18 +59,20 @@ class Grouped:
         self.n_sz = sz_stages(self.G)
         self.n_kchunks = (K + CHUNK_K - 1) // CHUNK_K
         self.n_sub = (K + SUB_K - 1) // SUB_K
+        tail = K % SUB_K != 0
+        self.corr_ring = (self.n_sub - 1) % 2 if tail else self.n_sub % 2
         self.resident = (K + 64) * 2 * MAX_N <= RES_BYTES
         B = lambda name, n, c: [Bar(f"{name}{i}", c) for i in range(n)]
         self.w_full, self.w_empty = B("w_full", STAGES_W, 1), B("w_empty", STAGES_W, DQ_WARPS)
         nb = 2 if self.resident else STAGES_B
-        self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, 2)
-        self.a_full = B("a_full", RINGS * RING_BUFS, 4)
-        self.a_empty = B("a_empty", RINGS * RING_BUFS, 1)
-        self.acc_full, self.acc_empty = B("acc_full", SETS, 2), B("acc_empty", SETS, EPI_WARPS)
+        self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, ISSUERS)
+        self.a_full = B("a_full", 2 * RINGS * RING_BUFS, 4)        # [buffer][half]
+        self.a_empty = B("a_empty", RINGS * RING_BUFS, 2)
+        self.acc_full, self.acc_empty = B("acc_full", SETS, ISSUERS), B("acc_empty", SETS, EPI_WARPS)
         self.sz_full = B("sz_full", self.n_sz, 1)
         self.sz_empty = B("sz_empty", self.n_sz, DQ_WARPS)
         self.copies = []
-        self.commits = [[], []]
+        self.commits = [[] for _ in range(ISSUERS)]
 
     # ---- roles; each wait carries (parity as the kernel computes it, the
     # phase index it stands for from independent use counts; -1: none yet)
@@ -115,6 +119,7 @@ class Grouped:
                     sb, ph_b = 0, ph_b ^ 1
 
     def issuer(self, me):
+        ring, part = me >> 1, me & 1
         ring_slot = ring_ph = 0
         a_use = [0] * RING_BUFS
         acc_use, b_use = [0] * SETS, [0] * (2 if self.resident else STAGES_B)
@@ -122,8 +127,8 @@ class Grouped:
 
         def issue():
             nonlocal ring_slot, ring_ph
-            buf = me * RING_BUFS + ring_slot
-            yield ("wait", self.a_full[buf], ring_ph, a_use[ring_slot])
+            buf = ring * RING_BUFS + ring_slot
+            yield ("wait", self.a_full[2 * buf + part], ring_ph, a_use[ring_slot])
             a_use[ring_slot] += 1
             ring_slot += 1
             if ring_slot == RING_BUFS:
@@ -142,7 +147,9 @@ class Grouped:
                     b_use[res_slot] += 1
                     b_seq += 1
                     cur_job = job
-                for _j in range(me, self.n_sub + 1, 2):      # the correction is j = n_sub
+                for _j in range(ring, self.n_sub, 2):
+                    yield from issue()
+                if ring == self.corr_ring:                   # the correction
                     yield from issue()
             else:
                 kcols = b_kcols(n)
@@ -152,9 +159,9 @@ class Grouped:
                     sb = (b_seq + t) % STAGES_B
                     yield ("wait", self.b_full[sb], ((b_seq + t) // STAGES_B) & 1, b_use[sb])
                     b_use[sb] += 1
-                    for _j in range(t * subs + me, min(self.n_sub, (t + 1) * subs), 2):
+                    for _j in range(t * subs + ring, min(self.n_sub, (t + 1) * subs), 2):
                         yield from issue()
-                    if t == n_bslots - 1 and self.n_sub % 2 == me:
+                    if t == n_bslots - 1 and ring == self.corr_ring:
                         yield from issue()
                     yield ("commit", me, self.b_empty[sb])
                 b_seq += n_bslots
@@ -162,9 +169,30 @@ class Grouped:
             acc_use[st] += 1
 
     def dequant(self, h):
+        # pipelined by one item: a buffer is handed over (both halves) only
+        # after the next item of the same warp has been loaded and computed
         sa = szb = ph_a = ph_sz = 0
         ring_slot = ring_ph = 0
         w_use, sz_use, a_fill = [0] * STAGES_W, [0] * self.n_sz, [0] * RING_BUFS
+        pend = None
+
+        def flush():
+            nonlocal pend
+            if pend is not None:
+                yield ("arrive", self.a_full[2 * pend])
+                yield ("arrive", self.a_full[2 * pend + 1])
+                pend = None
+
+        def claim():
+            nonlocal ring_slot, ring_ph, pend
+            buf = h * RING_BUFS + ring_slot
+            yield ("wait", self.a_empty[buf], ring_ph ^ 1, a_fill[ring_slot] - 1)
+            a_fill[ring_slot] += 1
+            ring_slot += 1
+            if ring_slot == RING_BUFS:
+                ring_slot, ring_ph = 0, ring_ph ^ 1
+            pend = buf
+
         for _job, _n in self.units:
             yield ("wait", self.sz_full[szb], ph_sz, sz_use[szb])
             for kc in range(self.n_kchunks):
@@ -177,26 +205,17 @@ class Grouped:
                     sa, ph_a = 0, ph_a ^ 1
                 if not mine:
                     continue
-                buf = h * RING_BUFS + ring_slot
-                yield ("wait", self.a_empty[buf], ring_ph ^ 1, a_fill[ring_slot] - 1)
-                a_fill[ring_slot] += 1
-                ring_slot += 1
-                if ring_slot == RING_BUFS:
-                    ring_slot, ring_ph = 0, ring_ph ^ 1
-                yield ("arrive", self.a_full[buf])
-            if self.n_sub % 2 == h:          # the correction sub-chunk
-                buf = h * RING_BUFS + ring_slot
-                yield ("wait", self.a_empty[buf], ring_ph ^ 1, a_fill[ring_slot] - 1)
-                a_fill[ring_slot] += 1
-                ring_slot += 1
-                if ring_slot == RING_BUFS:
-                    ring_slot, ring_ph = 0, ring_ph ^ 1
-                yield ("arrive", self.a_full[buf])
+                yield from flush()
+                yield from claim()
+            if self.corr_ring == h:          # the correction sub-chunk
+                yield from flush()
+                yield from claim()
             yield ("arrive", self.sz_empty[szb])
             sz_use[szb] += 1
             szb += 1
             if szb == self.n_sz:
                 szb, ph_sz = 0, ph_sz ^ 1
+        yield from flush()
 
     def epilogue(self):
         use = [0] * SETS
@@ -207,7 +226,7 @@ class Grouped:
             yield ("arrive", self.acc_empty[st])
 
     def run(self):
-        roles = [self.tma_w(), self.tma_b(), self.issuer(0), self.issuer(1)]
+        roles = [self.tma_w(), self.tma_b()] + [self.issuer(i) for i in range(ISSUERS)]
         roles += [self.dequant(w // 4) for w in range(DQ_WARPS)]      # 4 lane quarters per half
         roles += [self.epilogue() for _ in range(EPI_WARPS)]
         nxt = [next(r, None) for r in roles]
@@ -232,7 +251,7 @@ class Grouped:
                     choices.append(("role", i))
             if self.copies:
                 choices.append(("copy", None))
-            for q in range(2):
+            for q in range(ISSUERS):
                 if self.commits[q]:
                     choices.append(("commit", q))
             if not choices:
@@ -268,7 +287,7 @@ def _units(rng, n_units):
     return units[:n_units]
 
 
-@pytest.mark.parametrize("K", [2816, 704, 384, 192, 320])
+@pytest.mark.parametrize("K", [2816, 704, 384, 192, 320, 128, 64])
 @pytest.mark.parametrize("seed", range(12))
 def test_grouped_pipeline_protocol(K, seed):
     rng = random.Random(seed * 104729 + K)

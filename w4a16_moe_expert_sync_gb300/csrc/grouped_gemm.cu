@@ -48,21 +48,24 @@
 //   * Codes arrive by TMA in stages of 128 rows x 256 codes (two 64-row
 //     boxes).  Each stage is two 128-code sub-chunks; the dequant warp of a
 //     lane quarter and half h expands sub-chunk h of every stage for its 32
-//     rows into a 64-column A buffer of ring h (three buffers per ring).
-//   * Two issuer warps, one per ring, consume its sub-chunks in order, eight
-//     K = 16 MMAs each, into their own fp32 accumulators; the epilogue adds
-//     the two in a fixed order.  Two accumulator sets alternate per unit, so
-//     a unit's epilogue overlaps the next unit's MMAs.
+//     rows into a 64-column A buffer of ring h (two buffers per ring).
+//   * Four issuer warps, one per SM sub-partition: issuer 2 h + p takes the
+//     64-code half p of every sub-chunk of ring h (four K = 16 MMAs, one
+//     commit) into its own fp32 accumulator; the dequant warps hand over
+//     each half as soon as it is in tensor memory.  A thread issues an MMA
+//     every ~55 cycles at best and a commit costs it ~150, so one issuer per
+//     ring cannot keep up.  The epilogue adds the four accumulators in a
+//     fixed order.  Two accumulator sets alternate per unit, so a unit's
+//     epilogue overlaps the next unit's MMAs.
 //   * Warp roles
-//       warp 0      tcgen05.mma issuer of ring 0 (converged, one elected lane
-//                   issues)
-//       warp 1      TMA: packed codes; per unit the scales and zeros
-//       warp 2      TMA: activation slots
-//       warp 3      tensor-memory allocation, then tcgen05.mma issuer of ring 1
+//       warps 0-3   tcgen05.mma issuers (converged, one elected lane issues);
+//                   warp 0 also allocates tensor memory
 //       warps 4-7   epilogue (one TMEM lane quarter each)
 //       warps 8-15  dequant (warp 8 + 4 h + q: lane quarter q, half h)
-//   * Tensor memory (512 columns): A buffers at 64 (3 h + i), accumulators
-//     at 384 + 64 set + 32 issuer.
+//       warp 16     TMA: packed codes; per unit the scales and zeros
+//       warp 17     TMA: activation slots
+//   * Tensor memory (512 columns): A buffers at 64 (2 h + i), accumulators
+//     at 256 + 128 set + 32 issuer.
 //   * Every barrier has one producer group and one consumer group that take
 //     its phases in order, so a waiter is never two phases ahead and parity
 //     waits are exact (tests/test_grouped_pipeline_protocol.py models it).
@@ -82,19 +85,18 @@ namespace w4 {
 
 namespace {
 
-constexpr int kWarpMma0 = 0;               // issuer of ring 0
-constexpr int kWarpTmaW = 1;
-constexpr int kWarpTmaB = 2;
-constexpr int kWarpMma1 = 3;               // issuer of ring 1; allocates tensor memory
-constexpr int kWarpAlloc = 3;
+constexpr int kNumIssuers = 4;              // warps 0-3: issuer 2 h + p takes half p of ring h
+constexpr int kWarpAlloc = 0;               // tensor-memory allocation (an issuer)
+constexpr int kWarpTmaW = 16;
+constexpr int kWarpTmaB = 17;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kFirstDqWarp = 8;
 constexpr int kNumDqWarps = 8;
-constexpr int kNumWarps = 16;
+constexpr int kNumWarps = 18;
 constexpr int kThreads = 32 * kNumWarps;
 constexpr int kRings = 2;                   // one per dequant half
-constexpr int kRingBufs = 3;                // A buffers per ring
+constexpr int kRingBufs = 2;                // A buffers per ring
 constexpr int kStagesW = 6;                 // packed-code stages
 constexpr int kStagesB = 3;                 // streamed activation slots
 constexpr int kMaxStagesSZ = 3;             // per-unit scales and zeros
@@ -107,9 +109,11 @@ constexpr int kStageBBytes = 32768;
 constexpr int kResSlotBytes = kStagesB * kStageBBytes / 2;   // resident mode: 2 x 48 KB
 constexpr int kMaxN = 32;                   // slots per job
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 384
-// accumulators: set s (alternating per unit), issuer i at kAccCol + 64 s + 32 i
-static_assert(kAccCol + 2 * 2 * kMaxN <= kTmemCols, "tensor memory budget");
+constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 256
+// Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 128 set
+// + 32 i, the set alternating per unit.
+constexpr int kChains = kNumIssuers;
+static_assert(kAccCol + 2 * kChains * kMaxN <= kTmemCols, "tensor memory budget");
 
 struct GemmArgs {
     CUtensorMap tmap_w;       // packed codes u8 [E*R rows, K/2 B], box 128 B x 64 rows, SW128
@@ -124,11 +128,13 @@ struct GemmArgs {
     int n_corr_mma;           // K = 16 MMAs of the group-constant correction
     int h_stride;             // gate_up: row length of h (m + 64: values, then group sums)
     int h_groups;             // gate_up: groups of 64 along m (the down GEMM's groups)
+    int acc_mask;             // issuers (accumulators) that receive MMAs in every unit
+    int corr_ring;            // the ring that carries the correction sub-chunk
     int early_schedule;       // the schedule may be read before the grid-dependency wait
 };
 
-constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kRings * kRingBufs + 2 + 2 +
-                         2 * kMaxStagesSZ + 2;
+constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 3 * kRings * kRingBufs + 2 + 2 +
+                         2 * kMaxStagesSZ + kNumIssuers;
 
 struct Bars {
     uint64_t *w_full, *w_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty,
@@ -143,8 +149,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
     r.w_empty = r.w_full + kStagesW;
     r.b_full = r.w_empty + kStagesW;
     r.b_empty = r.b_full + kStagesB;
-    r.a_full = r.b_empty + kStagesB;
-    r.a_empty = r.a_full + kRings * kRingBufs;
+    r.a_full = r.b_empty + kStagesB;                 // [buffer][half]
+    r.a_empty = r.a_full + 2 * kRings * kRingBufs;
     r.acc_full = r.a_empty + kRings * kRingBufs;
     r.acc_empty = r.acc_full + 2;
     r.sz_full = r.acc_empty + 2;
@@ -348,22 +354,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int i = 0; i < kStagesB; i++) {
             mbar_init(&bar.b_full[i], 1);
-            mbar_init(&bar.b_empty[i], 2);           // both issuers' commits
+            mbar_init(&bar.b_empty[i], kNumIssuers);   // every issuer's commit
         }
         for (int i = 0; i < kRings * kRingBufs; i++) {
-            mbar_init(&bar.a_full[i], 4);            // the four lane quarters of the ring
-            mbar_init(&bar.a_empty[i], 1);           // the issuer's commit
+            mbar_init(&bar.a_full[2 * i], 4);        // the four lane quarters, half 0
+            mbar_init(&bar.a_full[2 * i + 1], 4);    // ... half 1
+            mbar_init(&bar.a_empty[i], 2);           // the ring's two issuers' commits
         }
         for (int i = 0; i < 2; i++) {
-            mbar_init(&bar.acc_full[i], 2);          // both issuers' commits
+            mbar_init(&bar.acc_full[i], kNumIssuers);
             mbar_init(&bar.acc_empty[i], kNumEpiWarps);
         }
         for (int i = 0; i < kMaxStagesSZ; i++) {
             mbar_init(&bar.sz_full[i], 1);
             mbar_init(&bar.sz_empty[i], kNumDqWarps);
         }
-        mbar_init(&bar.drain[0], 1);
-        mbar_init(&bar.drain[1], 1);
+        for (int i = 0; i < kNumIssuers; i++)
+            mbar_init(&bar.drain[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -417,51 +424,55 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // the last sub-chunk holds 64 codes when K is an odd multiple of 64
     const bool half_tail = (K & (kSubK - 1)) != 0;
 
-    if (warp == kWarpMma0 || warp == kWarpMma1) {
+    if (warp < kNumIssuers) {
         // ------------------------------------------------------ MMA issuers
-        // Issuer `me` takes the sub-chunks of ring me (j = me, me + 2, ...,
-        // and the correction when n_sub % 2 == me) into its own accumulator.
-        // The warp runs this loop converged (every value in it is
-        // warp-uniform, kept in registers) and one elected lane issues each
-        // tcgen05 instruction.
-        const int me = warp == kWarpMma0 ? 0 : 1;
+        // Issuer me = 2 h + p takes K steps 4p .. 4p + 3 (one 64-code half)
+        // of every sub-chunk of ring h (j = h, h + 2, ...; then the
+        // correction, "j = n_sub", when h is the correction's ring) into its
+        // own accumulator.
+        // A thread issues one MMA per ~55 cycles and a commit costs it ~150,
+        // so four issuers, one per SM sub-partition, share the work.  The
+        // warp runs this loop converged (every value in it is warp-uniform,
+        // kept in registers) and one elected lane issues each tcgen05
+        // instruction.
+        const int me = warp;
+        const int ring = me >> 1, part = me & 1;
         const uint32_t b_base = smem_u32(stage_b);
         uint32_t b_seq = 0, n_unit = 0;
         uint32_t ring_slot = 0, ring_ph = 0;
         int cur_job = -1;       // resident mode: the job whose activations are held
         uint32_t res_slot = 0;
         bool ok = true;
-        // Sub-chunk j of the unit (j % 2 == me): wait for its A buffer, 8 (or
-        // 4 for a 64-code tail) K = 16 MMAs, and hand the buffer back when
-        // they complete.  bdesc: descriptor of the sub-chunk's first 64-code
-        // column block; the second follows col_bytes later.  j == n_sub is
-        // the group-constant correction: n_corr_mma MMAs of the constants'
-        // low parts against the activations' group sums (one column block).
+        bool started = false;   // has this unit's first MMA gone (accumulate from then on)?
+        // Sub-chunk j of the unit (j % 2 == ring): wait for its half `part`,
+        // issue that half's K = 16 MMAs (up to 4; none for the second half
+        // of a 64-code tail or of the correction), and release the buffer
+        // (the ring's two issuers both commit).  bdesc: descriptor of the
+        // sub-chunk's first 64-code column block; the second follows
+        // col_bytes later.  j == n_sub is the group-constant correction:
+        // n_corr_mma MMAs of the constants' low parts against the
+        // activations' group sums (one column block).
         auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t col_bytes,
                          uint32_t idesc) -> bool {
-            const int buf = me * kRingBufs + static_cast<int>(ring_slot);
-            if (!warp_all_wait(&bar.a_full[buf], ring_ph, abort_flag, status))
+            const int buf = ring * kRingBufs + static_cast<int>(ring_slot);
+            // operands first, then the wait, then one issue sequence
+            const int n_all = j == n_sub ? p.n_corr_mma : (half_tail && j == n_sub - 1) ? 4 : 8;
+            const int n_mma = min(max(n_all - 4 * part, 0), 4);
+            const uint32_t a_tmem =
+                tmem + static_cast<uint32_t>(buf) * kSubCols + 32u * static_cast<uint32_t>(part);
+            // K steps of 16: +32 B in the swizzled row (+2 in the descriptor's
+            // address field); half `part` starts at column block `part`
+            const uint64_t b = bdesc + static_cast<uint64_t>(part) * (col_bytes >> 4);
+            if (!warp_all_wait(&bar.a_full[2 * buf + part], ring_ph, abort_flag, status))
                 return false;
             if (++ring_slot == kRingBufs) {
                 ring_slot = 0;
                 ring_ph ^= 1;
             }
             tc_fence_after();
-            const uint32_t a_tmem = tmem + static_cast<uint32_t>(buf) * kSubCols;
-            const int n_mma = j == n_sub ? p.n_corr_mma : (half_tail && j == n_sub - 1) ? 4 : 8;
-            const uint64_t blk = col_bytes >> 4;
-            // this issuer's first sub-chunk of the unit starts its accumulator
-            const uint32_t acc0 = j == me ? 0u : 1u;
-#pragma unroll
-            for (int kk = 0; kk < 8; kk++) {
-                if (kk < n_mma)
-                    // K steps of 16: +32 B in the swizzled row (+2 in the
-                    // descriptor's address field), +8 columns of A
-                    tc_mma_ts_elect(d_tmem, a_tmem + 8 * kk,
-                                    bdesc + static_cast<uint64_t>(kk >> 2) * blk + 2 * (kk & 3),
-                                    idesc, kk == 0 ? acc0 : 1u);
-            }
-            tc_commit_elect(&bar.a_empty[buf]);
+            tc_mma4_ts_commit_elect(d_tmem, a_tmem, b, b + 2, b + 4, b + 6, idesc, n_mma,
+                                    started ? 1u : 0u, &bar.a_empty[buf]);
+            started = started || n_mma > 0;
             return true;
         };
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -476,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + kAccCol + set * (2 * kMaxN) + me * kMaxN;
+            const uint32_t d_tmem = tmem + kAccCol + set * (kChains * kMaxN) + me * kMaxN;
+            started = false;
             if constexpr (RESIDENT) {
                 // the job's activations stay in one slot for all its units
                 if (job != cur_job) {
@@ -493,16 +505,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     cur_job = job;
                 }
                 const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
-                for (int j = me; j <= n_sub; j += 2) {
-                    // sub-chunk j reads column blocks 2j, 2j + 1; the
-                    // correction reads block K / 64 (the group sums)
-                    const uint32_t blk = j < n_sub ? 2u * j : static_cast<uint32_t>(K / 64);
-                    if (!issue(j, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), col_bytes,
+                for (int j = ring; j < n_sub; j += 2) {
+                    // sub-chunk j reads column blocks 2j, 2j + 1
+                    if (!issue(j, d_tmem, sdesc_sw128(b_slot + 2u * j * col_bytes), col_bytes,
                                idesc)) {
                         ok = false;
                         break;
                     }
                 }
+                // the correction reads block K / 64 (the group sums)
+                if (ok && ring == p.corr_ring &&
+                    !issue(n_sub, d_tmem,
+                           sdesc_sw128(b_slot + static_cast<uint32_t>(K / 64) * col_bytes),
+                           col_bytes, idesc))
+                    ok = false;
             } else {
                 const int kcols = b_kcols(J.n);
                 const int subs_per_slot = kcols / 2;
@@ -519,15 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint32_t b_slot = b_base + sb * kStageBBytes;
                     const int j0 = t * subs_per_slot;
                     const int j1 = min(n_sub, j0 + subs_per_slot);
-                    // subs_per_slot is even, so j0 is; this issuer's are j0 + me, ...
-                    for (int j = j0 + me; j < j1; j += 2) {
+                    // subs_per_slot is even, so j0 is; this ring's are j0 + ring, ...
+                    for (int j = j0 + ring; j < j1; j += 2) {
                         if (!issue(j, d_tmem, sdesc_sw128(b_slot + 2u * (j - j0) * col_bytes),
                                    col_bytes, idesc)) {
                             ok = false;
                             break;
                         }
                     }
-                    if (ok && t == n_bslots - 1 && (n_sub & 1) == me) {
+                    if (ok && t == n_bslots - 1 && ring == p.corr_ring) {
                         const uint32_t blk = static_cast<uint32_t>(K / 64 - t * kcols);
                         if (!issue(n_sub, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), col_bytes,
                                    idesc))
@@ -675,10 +691,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         drain_wait(&bar.b_full[i], issue_ph_b >> i & 1u);
         }
         __syncwarp();
-    } else if (warp >= kFirstDqWarp) {
+    } else if (warp >= kFirstDqWarp && warp < kFirstDqWarp + kNumDqWarps) {
         // ---------------------------------------------------------- dequant
         // Warp (q4, h) expands sub-chunk h (codes 128 h .. 128 h + 127) of
-        // every stage for its 32 rows into the A buffers of ring h.
+        // every stage for its 32 rows into the A buffers of ring h.  The
+        // loop is pipelined by one item: the tensor-memory stores of item i
+        // are waited for (and item i handed to the issuers) only after item
+        // i + 1 has been loaded and computed, so the store latency overlaps
+        // that work.
         const int q4 = warp & 3;
         const int h = (warp - kFirstDqWarp) >> 2;
         const int row = tile_row<GATE_UP>(q4, lane);
@@ -686,12 +706,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         int sa = 0, szb = 0;
         uint32_t ph_a = 0, ph_sz = 0;
         uint32_t ring_slot = 0, ring_ph = 0;
+        int pend_buf = -1;      // buffer whose stores are in flight, not yet handed over
         const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
         // the four 16-byte chunks of this warp's half of a row, swizzled
         uint32_t code_off[4];
 #pragma unroll
         for (int i = 0; i < 4; i++)
             code_off[i] = static_cast<uint32_t>(row * 128 + (((4 * h + i) ^ (row & 7)) << 4));
+        // wait for the pending stores and hand their buffer (both halves) over
+        auto flush = [&]() {
+            if (pend_buf >= 0) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                mbar_arrive_elect(&bar.a_full[2 * pend_buf]);
+                mbar_arrive_elect(&bar.a_full[2 * pend_buf + 1]);
+                pend_buf = -1;
+            }
+        };
+        // the next free buffer of this ring (its previous MMAs complete)
+        auto claim = [&](int *buf) -> bool {
+            *buf = h * kRingBufs + static_cast<int>(ring_slot);
+            if (!warp_all_wait(&bar.a_empty[*buf], ring_ph ^ 1, abort_flag, status))
+                return false;
+            if (++ring_slot == kRingBufs) {
+                ring_slot = 0;
+                ring_ph ^= 1;
+            }
+            tc_fence_after();
+            return true;
+        };
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             if (!warp_all_wait(&bar.sz_full[szb], ph_sz, abort_flag, status))
@@ -734,6 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t g1 = static_cast<uint32_t>(j * kSubK + 64) >> p.group_shift;
                 const GroupK k0 =
                     group_consts(lds_u16(s_addr + 2 * g0), lds_u16(z_addr + 2 * g0), scale_s, scale_c);
+                const GroupK k1 = g1 == g0 ? k0
+                                           : group_consts(lds_u16(s_addr + 2 * g1),
+                                                          lds_u16(z_addr + 2 * g1), scale_s, scale_c);
                 uint32_t o[32];
                 dequant_word(v0.x, k0.S, k0.S16, k0.C, &o[0]);
                 dequant_word(v0.y, k0.S, k0.S16, k0.C, &o[4]);
@@ -743,42 +790,31 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 dequant_word(v1.y, k0.S, k0.S16, k0.C, &o[20]);
                 dequant_word(v1.z, k0.S, k0.S16, k0.C, &o[24]);
                 dequant_word(v1.w, k0.S, k0.S16, k0.C, &o[28]);
-                const int buf = h * kRingBufs + static_cast<int>(ring_slot);
-                if (!warp_all_wait(&bar.a_empty[buf], ring_ph ^ 1, abort_flag, status)) {
+                flush();            // the previous item's stores, issued one item ago
+                int buf;
+                if (!claim(&buf)) {
                     ok = false;
                     break;
                 }
-                if (++ring_slot == kRingBufs) {
-                    ring_slot = 0;
-                    ring_ph ^= 1;
-                }
-                tc_fence_after();
                 const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
                 tmem_st_32x32b_x32(a_col, o);
-                if (!tail) {
-                    const GroupK k1 = g1 == g0 ? k0
-                                               : group_consts(lds_u16(s_addr + 2 * g1),
-                                                              lds_u16(z_addr + 2 * g1), scale_s,
-                                                              scale_c);
-                    uint32_t o2[32];
-                    dequant_word(v2.x, k1.S, k1.S16, k1.C, &o2[0]);
-                    dequant_word(v2.y, k1.S, k1.S16, k1.C, &o2[4]);
-                    dequant_word(v2.z, k1.S, k1.S16, k1.C, &o2[8]);
-                    dequant_word(v2.w, k1.S, k1.S16, k1.C, &o2[12]);
-                    dequant_word(v3.x, k1.S, k1.S16, k1.C, &o2[16]);
-                    dequant_word(v3.y, k1.S, k1.S16, k1.C, &o2[20]);
-                    dequant_word(v3.z, k1.S, k1.S16, k1.C, &o2[24]);
-                    dequant_word(v3.w, k1.S, k1.S16, k1.C, &o2[28]);
-                    tmem_st_32x32b_x32(a_col + 32, o2);
+                if (!tail) {        // (a 64-code tail has no second half: its issuer only commits)
+                    // o was read by the store at issue and is free again
+                    dequant_word(v2.x, k1.S, k1.S16, k1.C, &o[0]);
+                    dequant_word(v2.y, k1.S, k1.S16, k1.C, &o[4]);
+                    dequant_word(v2.z, k1.S, k1.S16, k1.C, &o[8]);
+                    dequant_word(v2.w, k1.S, k1.S16, k1.C, &o[12]);
+                    dequant_word(v3.x, k1.S, k1.S16, k1.C, &o[16]);
+                    dequant_word(v3.y, k1.S, k1.S16, k1.C, &o[20]);
+                    dequant_word(v3.z, k1.S, k1.S16, k1.C, &o[24]);
+                    dequant_word(v3.w, k1.S, k1.S16, k1.C, &o[28]);
+                    tmem_st_32x32b_x32(a_col + 32, o);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                mbar_arrive_elect(&bar.a_full[buf]);
+                pend_buf = buf;
             }
             if (!ok)
                 break;
-            if ((n_sub & 1) == h) {
+            if (p.corr_ring == h) {
                 // The correction sub-chunk: C = -s z 2^-c rounded to fp16 (the
                 // constant of every dequantised weight of the group) leaves
                 // the part C_lo = fp16(C_exact - C).  The activations carry
@@ -786,7 +822,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 // index k of the correction belongs to group k or k / 4;
                 // column i of MMA step t holds k = 16 t + 2 i, 16 t + 2 i + 1;
                 // zero past the last group.
-                const int buf = h * kRingBufs + static_cast<int>(ring_slot);
                 // gate_up: word i of step t holds groups 16 t + 2 i, + 1;
                 // down (four sum columns per group): both halves of words
                 // 2 i' and 2 i' + 1 of step t hold group 4 t + i'
@@ -816,22 +851,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                             cw[t][2 * gi] = cw[t][2 * gi + 1] = lo | (lo << 16);
                         }
                     }
-                if (!warp_all_wait(&bar.a_empty[buf], ring_ph ^ 1, abort_flag, status))
+                flush();
+                int buf;
+                if (!claim(&buf))
                     break;
-                if (++ring_slot == kRingBufs) {
-                    ring_slot = 0;
-                    ring_ph ^= 1;
-                }
-                tc_fence_after();
                 const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
 #pragma unroll
                 for (int t = 0; t < 4; t++)
-                    if (t < p.n_corr_mma)
+                    if (t < p.n_corr_mma)       // the correction's MMAs are all in half 0
                         tmem_st_32x32b_x8(a_col + 8 * t, cw[t]);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                mbar_arrive_elect(&bar.a_full[buf]);
+                pend_buf = buf;
             }
             __syncwarp();
             mbar_arrive_elect(&bar.sz_empty[szb]);
@@ -840,6 +869,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 ph_sz ^= 1;
             }
         }
+        if (ok)
+            flush();
     } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kNumEpiWarps) {
         // ---------------------------------------------------------- epilogue
         const int q4 = warp & 3;
@@ -874,13 +905,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tc_fence_after();
             float v[kMaxN];
             {
-                // the two issuers' accumulators, added in a fixed order
-                uint32_t r0[32], r1[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kAccCol + set * (2 * kMaxN), r0);
-                tmem_ld_32x32b_x32(tmem + lane_base + kAccCol + set * (2 * kMaxN) + kMaxN, r1);
+                // the accumulator chains that received MMAs, added in a fixed order
 #pragma unroll
                 for (int i = 0; i < kMaxN; i++)
-                    v[i] = (__uint_as_float(r0[i]) + __uint_as_float(r1[i])) * factor;
+                    v[i] = 0.0f;
+#pragma unroll
+                for (int c = 0; c < kChains; c++) {
+                    if (!(p.acc_mask >> c & 1))
+                        continue;
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(
+                        tmem + lane_base + kAccCol + set * (kChains * kMaxN) + c * kMaxN, r);
+#pragma unroll
+                    for (int i = 0; i < kMaxN; i++)
+                        v[i] += __uint_as_float(r[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < kMaxN; i++)
+                    v[i] *= factor;
             }
             tc_fence_before();
             __syncwarp();
@@ -1057,6 +1099,21 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         return cudaErrorInvalidValue;
     }
     a.n_corr_mma = (a.G * corr_rep + 15) / 16;
+    {
+        // the correction goes to the ring of a 64-code tail (which has the
+        // lighter load), else to the ring whose turn follows the last
+        // sub-chunk; issuer 2 h + p gets K steps 4p .. 4p + 3 of the
+        // sub-chunks of ring h, and the correction's are all in half 0
+        const bool tail = (q.K % kSubK) != 0;
+        a.corr_ring = tail ? (a.n_sub - 1) & 1 : a.n_sub & 1;
+        a.acc_mask = 1 << (2 * a.corr_ring);
+        for (int j = 0; j < a.n_sub; j++) {
+            const int n = (tail && j == a.n_sub - 1) ? 4 : 8;
+            a.acc_mask |= 1 << (2 * (j & 1));
+            if (n >= 5)
+                a.acc_mask |= 1 << (2 * (j & 1) + 1);
+        }
+    }
     a.h_stride = q.gate_up ? q.R / 2 + 64 : 0;
     a.h_groups = q.gate_up ? (q.R / 2) / 64 : 0;
     a.early_schedule = q.early_schedule ? 1 : 0;

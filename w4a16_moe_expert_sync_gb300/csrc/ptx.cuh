@@ -349,6 +349,39 @@ __device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
+// Up to four MMAs (A in tensor memory, B from shared memory, one D) and a
+// commit of this thread's tcgen05 work to `bar`, all from one elected lane of
+// a converged warp: MMA t is issued when t < n, with a_tmem + 8 t and
+// b_desc + b_step[t]; the first adds to D only when `accumulate` is set, the
+// others always.  One elect and one issue sequence for the group keeps the
+// per-MMA cost of the issuing warp low.
+__device__ __forceinline__ void tc_mma4_ts_commit_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                        uint64_t b0, uint64_t b1, uint64_t b2,
+                                                        uint64_t b3, uint32_t idesc, int n,
+                                                        uint32_t accumulate, uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, q0, q1, q2, q3, acc, on;\n\t"
+        ".reg .b32 a1, a2, a3;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+        "setp.ne.b32 acc, %7, 0;\n\t"
+        "setp.eq.b32 on, %7, %7;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.gt.and.s32 q0, %8, 0, e;\n\t"
+        "setp.gt.and.s32 q1, %8, 1, e;\n\t"
+        "setp.gt.and.s32 q2, %8, 2, e;\n\t"
+        "setp.gt.and.s32 q3, %8, 3, e;\n\t"
+        "@q0 tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %6, acc;\n\t"
+        "@q1 tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %6, on;\n\t"
+        "@q2 tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %6, on;\n\t"
+        "@q3 tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %6, on;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(accumulate), "r"(n),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit_elect(uint64_t *bar)
 {
     asm volatile(
