@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 7
+#define W4MOE_ABI_VERSION 8
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -235,7 +235,10 @@ int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int
  * fp32), multiplied on the tensor cores (tcgen05, fp16 x fp16 -> fp32), and
  * the part of -z * s lost to its fp16 rounding is added back through the
  * group sums; h is rounded to fp16 with saturation at +-65504.
- * Requires d % 128 == 0, d <= 8192, m % 64 == 0, m <= 1024, group == 128.
+ * Requires d % 128 == 0, d <= 8192, m % 64 == 0, m <= 1024, group == 128,
+ * and that a unit's scales and zeros fit shared memory beside the code and
+ * activation stages: d up to about 3840 at E = 128 (2944 at E = 1024);
+ * W4_ERR_UNSUPPORTED_SHAPE beyond, before anything is launched.
  * dev_status may be NULL.
  * ------------------------------------------------------------------------ */
 int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
@@ -283,15 +286,57 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids,
                                uint16_t *out, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * w4_grouped_gemm_down_combine -- w4_grouped_gemm_down with
+ * w4_moe_combine_fixed_order folded into its epilogue: one launch for both
+ * ("dg-w4-kernels" -- Grouped MoE: one fused launch; "Inference: Making every
+ *  denoising pass fast" -- Quantisation alone leaves a sparse execution
+ *  problem: the fixed-order, atomics-free reduction of a token's outputs).
+ *
+ *   h, dn_q/dn_s/dn_z, sorted_ids, expert_offsets, y   as w4_grouped_gemm_down
+ *                  (y is still written: it holds the terms of the combine)
+ *   topk_ids/topk_weights [M, k]   as w4_moe_combine_fixed_order
+ *   counters       [M, d/128] int32, set by w4_moe_combine_prepare with
+ *                  the same topk_ids, M, k, E, d and out (earlier on the
+ *                  stream, after any earlier use of the same counters);
+ *                  consumed by this call
+ *   out            [M, d] bf16 out, 8-byte aligned: bit-identical to
+ *                  w4_grouped_gemm_down followed by
+ *                  w4_moe_combine_fixed_order
+ * Once a CTA has stored the 128 y columns of one panel of an assignment it
+ * counts an arrival on the (token, 128-column panel) counter; the warp
+ * whose arrival completes it computes those 128 columns of out[t] from the
+ * token's k rows of y in assignment order (the combine's fp32 fma chain),
+ * so no element of out is written twice and none depends on arrival order.  The
+ * counter atomics are the only atomics; they decide who combines, never
+ * what.  Same requirements as w4_grouped_gemm_down.
+ * ------------------------------------------------------------------------ */
+int w4_grouped_gemm_down_combine(const uint16_t *h, int M, int d, int m, int E, int k,
+                                 int block_m, const uint8_t *dn_q, const uint16_t *dn_s,
+                                 const uint16_t *dn_z, int group, const int32_t *sorted_ids,
+                                 const int32_t *expert_offsets, const int32_t *topk_ids,
+                                 const float *topk_weights, int32_t *counters, float *y,
+                                 uint16_t *out, int32_t *dev_status, w4_stream_t stream);
+
+/* w4_moe_combine_prepare -- sets the counters of w4_grouped_gemm_down_combine:
+ * counters[t, p, q] = k - (number of ids of token t inside [0, E)), and
+ * writes the zero out row of every token with no such id (the combine of no
+ * terms).  topk_ids [M, k], counters [M, d/128] int32, out [M, d] bf16
+ * (8-byte aligned).  Requires d % 128 == 0.  One launch. */
+int w4_moe_combine_prepare(const int32_t *topk_ids, int M, int k, int E, int d,
+                           int32_t *counters, uint16_t *out, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * w4_moe_layer -- the whole routed-expert layer: alignment fused with the
- * activation gather, gate_up + activation, down, fixed-order combine, as
- * four launches on one stream
+ * activation gather, gate_up + activation (which also sets the combine's
+ * counters, as w4_moe_combine_prepare), down with the fixed-order combine
+ * folded in (w4_grouped_gemm_down_combine), as three launches on one stream
  * ("dg-w4-kernels" -- Grouped MoE: out = fused_moe_w4_v2(hidden, experts,
  *  topk_ids, topk_weights)).
  *
  * workspace: caller-owned device buffer of at least
  * w4_moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds the
- * alignment outputs, the gathered activations, h and y.  Its contents on return are the intermediates
+ * alignment outputs, the gathered activations, h, y and the combine's
+ * counters.  Its contents on return are the intermediates
  * of this call (layout: see the implementation; not part of the ABI).
  * Same shape rules as the individual calls; dev_status may be NULL.
  * ------------------------------------------------------------------------ */
@@ -445,6 +490,19 @@ int w4_fused_entropy(const float *logits, int M, int64_t V, float *entropy, void
 int w4_gumbel_argmax_sample(const float *logits, int M, int64_t V, uint64_t seed,
                             uint64_t offset, int64_t *sample, int64_t *argmax, void *workspace,
                             size_t workspace_bytes, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_test_pipeline_hooks -- a test hook of the grouped GEMMs (not for
+ * production use): for later w4_grouped_gemm_gate_up / _down / _down_combine
+ * calls and the layer's GEMMs made from the calling thread, every pipeline
+ * wait gives up after wait_limit_ns (0: back to the default of one second)
+ * and, if withhold_first_scales is nonzero, each CTA withholds the copy of
+ * its first unit's scales and zeros, so that its waits run out: the kernel
+ * then sets W4_DEV_PIPELINE_TIMEOUT, lets its own copies land, drains its
+ * MMAs, frees its tensor memory and exits, leaving its outputs incomplete
+ * and the context usable.  Returns W4_OK.
+ * ------------------------------------------------------------------------ */
+int w4_test_pipeline_hooks(uint64_t wait_limit_ns, int withhold_first_scales);
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,7 @@ def test_header_compiles_as_plain_c():
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4_abi_version() == 7
+    assert clib.w4_abi_version() == 8
     assert clib.w4_status_string(0) == b"W4_OK"
     assert clib.w4_status_string(2) == b"W4_ERR_UNSUPPORTED_SHAPE"
     assert clib.w4_status_string(99) == b"W4_ERR_UNKNOWN"
@@ -78,6 +78,20 @@ def test_argument_validation_without_launching(clib):
     # down group must be 64
     dargs = [fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake, None, None]
     assert clib.w4_grouped_gemm_down(*dargs) == 2
+    # down with the folded combine: NULL counters, misaligned out, then the
+    # down checks; the counter preparation needs d % 128 == 0
+    cargs = [fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 64, fake, fake, fake, fake, None,
+             fake, fake, None, None]
+    assert clib.w4_grouped_gemm_down_combine(*cargs) == 1
+    cargs[15] = fake
+    cargs[17] = P(0x10004)
+    assert clib.w4_grouped_gemm_down_combine(*cargs) == 3
+    cargs[17] = fake
+    cargs[10] = 128
+    assert clib.w4_grouped_gemm_down_combine(*cargs) == 2
+    assert clib.w4_moe_combine_prepare(fake, 4, 2, 8, 200, fake, fake, None) == 2
+    assert clib.w4_moe_combine_prepare(None, 4, 2, 8, 256, fake, fake, None) == 1
+    assert clib.w4_moe_combine_prepare(fake, 4, 2, 8, 256, fake, P(0x10002), None) == 3
     # gather: d must be a multiple of 8
     assert clib.w4_gather_activations(fake, 4, 252, 2, 8, 16, fake, fake, fake, None, None) == 2
     # workspace too small

@@ -207,3 +207,28 @@ def test_layer_activation_range_is_flagged(lib):
     lib.w4_moe_layer(x_ok, ids_d, w_d, gu, dn, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+def test_layer_rejects_shapes_beyond_shared_memory_before_launching(lib):
+    """gate_up with d = 5120 (40 groups of 128) needs more shared memory for a
+    unit's scales and zeros than an SM has: the layer is rejected with
+    W4_ERR_UNSUPPORTED_SHAPE before its first launch, so out keeps its
+    contents."""
+    import torch
+    M, d, m, E, k = 4, 5120, 128, 8, 2
+    x = torch.zeros((M, d), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((M, k), dtype=torch.int32, device="cuda")
+    ids[:, 1] = 1
+    w = torch.full((M, k), 0.5, dtype=torch.float32, device="cuda")
+    gu = (torch.zeros((E, 2 * m, d // 2), dtype=torch.uint8, device="cuda"),
+          torch.zeros((E, 2 * m, d // 128), dtype=torch.float16, device="cuda"),
+          torch.zeros((E, 2 * m, d // 128), dtype=torch.float16, device="cuda"))
+    dn = (torch.zeros((E, d, m // 2), dtype=torch.uint8, device="cuda"),
+          torch.zeros((E, d, m // 64), dtype=torch.float16, device="cuda"),
+          torch.zeros((E, d, m // 64), dtype=torch.float16, device="cuda"))
+    out = torch.full((M, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.W4Error) as e:
+        lib.w4_moe_layer(x, ids, w, gu, dn, out=out)
+    assert e.value.status == 2 and "shared memory" in str(e.value)
+    torch.cuda.synchronize()
+    assert bool((out == 3.0).all())

@@ -2,37 +2,53 @@
 run under random interleavings on the CPU, in the manner of
 test_dense_pipeline_protocol.py.
 
-Roles as the kernel writes them, with the kernel's constants: the TMA warp for
-codes and scales/zeros (6 code stages, 2 or 3 scale stages), the TMA warp for
+Roles as the kernel writes them, with the kernel's constants: the two TMA
+threads for codes (one per parity of the stage sequence, 6 code stages in
+all; the parity-0 one also issues the 2 or 3 scale/zero stages), the TMA
+warp for
 activations (3 streamed slots, or 2 resident slots that hold a job's whole
-activation block, the group-sum block included), four MMA issuers (issuer
-2h + p takes half p of every A buffer of ring h, two buffers per ring in
-tensor memory; each has its own accumulator in each of two sets; each
-issuer's commits complete asynchronously in its issue order), eight
-dequantisation warps (lane quarter x half of each code stage, pipelined by
-one item: a buffer's two halves are handed over only after the warp's next
-item has been loaded and computed; the half whose ring takes sub-chunk n_sub
-also produces the group-constant correction after its last sub-chunk of a
-unit) and four epilogue warps.  Every wait is checked against the exact condition:
-the phase it stands for, counted from per-stage uses kept apart from the
-kernel's parity variables, has completed exactly when the parity test says
-so.  Unit lists mix jobs of 16 and 32 slots over several panels; contraction
-sizes cover gate_up (2816, streamed), down (704, resident, a 64-code last
-sub-chunk) and short ones where one half has no sub-chunk in the last stage
-(384, 192).
+activation block, the group-sum block included), four MMA issuers (issuer r
+takes ring r: one A buffer in tensor memory and its own accumulator in each
+of two sets; each issuer's commits complete asynchronously in its issue
+order), sixteen dequantisation warps (lane quarter x ring; ring 2 gp + h
+takes half h of the stages whose index in the CTA's stage sequence has
+parity gp, so a warp skips the other stages; ring 1 or 3, half 1 of the
+parity the unit's first stage does not have, also produces the unit's
+group-constant correction), four epilogue warps (which also read the row
+scales the dequant warps publish per unit), and the warp of the combine
+folded into the down GEMM (one phase of y_full per unit).  Every wait is
+checked against the exact condition: the phase it stands for, counted from
+per-stage uses kept apart from the kernel's parity variables, has completed
+exactly when the parity test says so.  Unit lists mix jobs of 16 and 32 slots over several panels; contraction
+sizes cover gate_up (2816, streamed, 11 stages per unit: the rings' parities
+alternate from unit to unit), down (704, resident, a 64-code last sub-chunk)
+and short ones (384, 192, 320, 128, 64).
 """
 import random
 
 import pytest
 
-RINGS, RING_BUFS, SETS, ISSUERS = 2, 2, 2, 4
-STAGES_W, STAGES_B = 6, 3
-DQ_WARPS, EPI_WARPS = 8, 4
+RINGS, SETS, ISSUERS = 4, 2, 4
+# code stages (16 KB) and streamed activation slots (32 KB); resident mode
+# has the same code stages and two job slots
+STAGES_W_STREAMED, STAGES_W_RESIDENT, STAGES_B = 6, 6, 3
+STAGE_B_BYTES = 32768
+DQ_WARPS, EPI_WARPS = 16, 4
 CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 128, 32, 49152
+ROW_SCALE_SETS = 4
+COMB_WARPS, Y_SETS = 1, 4
 
 
 def sz_stages(G):
     return 2 if G > 16 else 3
+
+
+def unit_ring(gp0, j):
+    return 2 * ((gp0 + (j >> 1)) & 1) + (j & 1)
+
+
+def corr_ring(gp0, n_kchunks):
+    return 2 * (gp0 ^ 1) + 1
 
 
 class Bar:
@@ -48,7 +64,7 @@ class Bar:
 
 
 def b_kcols(n):
-    return 16 if n == 16 else 8
+    return STAGE_B_BYTES // (n * 128)
 
 
 class Grouped:
@@ -59,40 +75,43 @@ class Grouped:
         self.n_sz = sz_stages(self.G)
         self.n_kchunks = (K + CHUNK_K - 1) // CHUNK_K
         self.n_sub = (K + SUB_K - 1) // SUB_K
-        tail = K % SUB_K != 0
-        self.corr_ring = (self.n_sub - 1) % 2 if tail else self.n_sub % 2
         self.resident = (K + 64) * 2 * MAX_N <= RES_BYTES
+        self.stages_w = STAGES_W_RESIDENT if self.resident else STAGES_W_STREAMED
         B = lambda name, n, c: [Bar(f"{name}{i}", c) for i in range(n)]
-        self.w_full, self.w_empty = B("w_full", STAGES_W, 1), B("w_empty", STAGES_W, DQ_WARPS)
+        self.w_full = B("w_full", self.stages_w, 1)
+        self.w_empty = B("w_empty", self.stages_w, DQ_WARPS // 2)
         nb = 2 if self.resident else STAGES_B
         self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, ISSUERS)
-        self.a_full = B("a_full", 2 * RINGS * RING_BUFS, 4)        # [buffer][half]
-        self.a_empty = B("a_empty", RINGS * RING_BUFS, 2)
+        self.a_full = B("a_full", RINGS, 4)
+        self.a_empty = B("a_empty", RINGS, 1)
         self.acc_full, self.acc_empty = B("acc_full", SETS, ISSUERS), B("acc_empty", SETS, EPI_WARPS)
+        # the folded combine (down): epilogue -> combine warps, one phase per unit
+        self.y_full, self.y_empty = B("y_full", Y_SETS, EPI_WARPS), B("y_empty", Y_SETS, COMB_WARPS)
         self.sz_full = B("sz_full", self.n_sz, 1)
         self.sz_empty = B("sz_empty", self.n_sz, DQ_WARPS)
+        # row-scale tables (dequant -> epilogue), one entry per lane quarter
+        self.row_scale = [[None] * 4 for _ in range(ROW_SCALE_SETS)]
         self.copies = []
         self.commits = [[] for _ in range(ISSUERS)]
 
-    # ---- roles; each wait carries (parity as the kernel computes it, the
-    # phase index it stands for from independent use counts; -1: none yet)
-    def tma_w(self):
-        sa = szb = ph_a = ph_sz = 0
-        w_fill, sz_fill = [0] * STAGES_W, [0] * self.n_sz
-        for _job, _n in self.units:
-            yield ("wait", self.sz_empty[szb], ph_sz ^ 1, sz_fill[szb] - 1)
-            yield ("copy", self.sz_full[szb])
-            sz_fill[szb] += 1
-            szb += 1
-            if szb == self.n_sz:
-                szb, ph_sz = 0, ph_sz ^ 1
-            for _ in range(self.n_kchunks):
-                yield ("wait", self.w_empty[sa], ph_a ^ 1, w_fill[sa] - 1)
+    def tma_w(self, gp):
+        """The code stages of parity gp of the CTA's stage sequence, unit by
+        unit; the parity-0 thread issues each unit's scales and zeros before
+        the unit's stages."""
+        w_fill, sz_fill = [0] * self.stages_w, [0] * self.n_sz
+        for n in range(len(self.units)):
+            if gp == 0:
+                szb = n % self.n_sz
+                yield ("wait", self.sz_empty[szb], ((n // self.n_sz) & 1) ^ 1, sz_fill[szb] - 1)
+                yield ("copy", self.sz_full[szb])
+                sz_fill[szb] += 1
+            gs0 = n * self.n_kchunks
+            for kc in range(0 if (gs0 & 1) == gp else 1, self.n_kchunks, 2):
+                g = gs0 + kc
+                sa = g % self.stages_w
+                yield ("wait", self.w_empty[sa], ((g // self.stages_w) & 1) ^ 1, w_fill[sa] - 1)
                 yield ("copy", self.w_full[sa])
                 w_fill[sa] += 1
-                sa += 1
-                if sa == STAGES_W:
-                    sa, ph_a = 0, ph_a ^ 1
 
     def tma_b(self):
         if self.resident:
@@ -119,24 +138,20 @@ class Grouped:
                     sb, ph_b = 0, ph_b ^ 1
 
     def issuer(self, me):
-        ring, part = me >> 1, me & 1
-        ring_slot = ring_ph = 0
-        a_use = [0] * RING_BUFS
+        a_use = 0
         acc_use, b_use = [0] * SETS, [0] * (2 if self.resident else STAGES_B)
         cur_job, res_slot, b_seq = None, 0, 0
 
-        def issue():
-            nonlocal ring_slot, ring_ph
-            buf = ring * RING_BUFS + ring_slot
-            yield ("wait", self.a_full[2 * buf + part], ring_ph, a_use[ring_slot])
-            a_use[ring_slot] += 1
-            ring_slot += 1
-            if ring_slot == RING_BUFS:
-                ring_slot, ring_ph = 0, ring_ph ^ 1
-            yield ("commit", me, self.a_empty[buf])
+        def issue(j):
+            nonlocal a_use
+            yield ("wait", self.a_full[me], a_use & 1, a_use)
+            a_use += 1
+            yield ("commit", me, self.a_empty[me])
 
         for n_unit, (job, n) in enumerate(self.units):
             st, acc_ph = n_unit & 1, (n_unit >> 1) & 1
+            gp0 = (n_unit * self.n_kchunks) & 1
+            corr = corr_ring(gp0, self.n_kchunks)
             yield ("wait", self.acc_empty[st], acc_ph ^ 1, acc_use[st] - 1)
             if self.resident:
                 if job != cur_job:
@@ -147,10 +162,11 @@ class Grouped:
                     b_use[res_slot] += 1
                     b_seq += 1
                     cur_job = job
-                for _j in range(ring, self.n_sub, 2):
-                    yield from issue()
-                if ring == self.corr_ring:                   # the correction
-                    yield from issue()
+                for j in range(self.n_sub):
+                    if unit_ring(gp0, j) == me:
+                        yield from issue(j)
+                if me == corr:
+                    yield from issue(self.n_sub)
             else:
                 kcols = b_kcols(n)
                 subs = kcols // 2
@@ -159,76 +175,82 @@ class Grouped:
                     sb = (b_seq + t) % STAGES_B
                     yield ("wait", self.b_full[sb], ((b_seq + t) // STAGES_B) & 1, b_use[sb])
                     b_use[sb] += 1
-                    for _j in range(t * subs + ring, min(self.n_sub, (t + 1) * subs), 2):
-                        yield from issue()
-                    if t == n_bslots - 1 and ring == self.corr_ring:
-                        yield from issue()
+                    for j in range(t * subs, min(self.n_sub, (t + 1) * subs)):
+                        if unit_ring(gp0, j) == me:
+                            yield from issue(j)
+                    if t == n_bslots - 1 and me == corr:
+                        yield from issue(self.n_sub)
                     yield ("commit", me, self.b_empty[sb])
                 b_seq += n_bslots
             yield ("commit", me, self.acc_full[st])
             acc_use[st] += 1
 
-    def dequant(self, h):
-        # pipelined by one item: a buffer is handed over (both halves) only
-        # after the next item of the same warp has been loaded and computed
-        sa = szb = ph_a = ph_sz = 0
-        ring_slot = ring_ph = 0
-        w_use, sz_use, a_fill = [0] * STAGES_W, [0] * self.n_sz, [0] * RING_BUFS
-        pend = None
+    @staticmethod
+    def stage_parity(g, kc):
+        """Rings by the stage's index in the CTA's stage sequence."""
+        return g & 1
 
-        def flush():
-            nonlocal pend
-            if pend is not None:
-                yield ("arrive", self.a_full[2 * pend])
-                yield ("arrive", self.a_full[2 * pend + 1])
-                pend = None
+    def dequant(self, r, q=0):
+        gp, h = r >> 1, r & 1
+        szb = ph_sz = 0
+        sz_use = [0] * self.n_sz
+        w_use = [0] * self.stages_w
+        a_fill = 0
 
-        def claim():
-            nonlocal ring_slot, ring_ph, pend
-            buf = h * RING_BUFS + ring_slot
-            yield ("wait", self.a_empty[buf], ring_ph ^ 1, a_fill[ring_slot] - 1)
-            a_fill[ring_slot] += 1
-            ring_slot += 1
-            if ring_slot == RING_BUFS:
-                ring_slot, ring_ph = 0, ring_ph ^ 1
-            pend = buf
+        def fill_buffer(first):
+            nonlocal a_fill
+            yield ("wait", self.a_empty[r], (a_fill & 1) ^ 1, a_fill - 1)
+            a_fill += 1
+            if first:
+                yield ("rs_write", n_unit, q)
+            yield ("arrive", self.a_full[r])
 
-        for _job, _n in self.units:
+        for n_unit, _u in enumerate(self.units):
             yield ("wait", self.sz_full[szb], ph_sz, sz_use[szb])
+            gs0 = n_unit * self.n_kchunks
             for kc in range(self.n_kchunks):
-                yield ("wait", self.w_full[sa], ph_a, w_use[sa])
-                w_use[sa] += 1
-                mine = 2 * kc + h < self.n_sub
-                yield ("arrive", self.w_empty[sa])
-                sa += 1
-                if sa == STAGES_W:
-                    sa, ph_a = 0, ph_a ^ 1
-                if not mine:
+                g = gs0 + kc
+                if self.stage_parity(g, kc) != gp:
                     continue
-                yield from flush()
-                yield from claim()
-            if self.corr_ring == h:          # the correction sub-chunk
-                yield from flush()
-                yield from claim()
+                sa = g % self.stages_w
+                yield ("wait", self.w_full[sa], (g // self.stages_w) & 1, w_use[sa])
+                w_use[sa] += 1
+                yield ("arrive", self.w_empty[sa])
+                if 2 * kc + h >= self.n_sub:
+                    continue
+                yield from fill_buffer(2 * kc + h == 0)
+            if r == corr_ring(gs0 & 1, self.n_kchunks):
+                yield from fill_buffer(False)
             yield ("arrive", self.sz_empty[szb])
             sz_use[szb] += 1
             szb += 1
             if szb == self.n_sz:
                 szb, ph_sz = 0, ph_sz ^ 1
-        yield from flush()
 
-    def epilogue(self):
+    def epilogue(self, q=0):
         use = [0] * SETS
         for n_unit, _u in enumerate(self.units):
             st = n_unit & 1
             yield ("wait", self.acc_full[st], (n_unit >> 1) & 1, use[st])
             use[st] += 1
+            yield ("rs_read", n_unit, q)
             yield ("arrive", self.acc_empty[st])
+            ys = n_unit % Y_SETS
+            yield ("wait", self.y_empty[ys], ((n_unit // Y_SETS) & 1) ^ 1, n_unit // Y_SETS - 1)
+            yield ("arrive", self.y_full[ys])
+
+    def combine(self):
+        for n_unit, _u in enumerate(self.units):
+            ys = n_unit % Y_SETS
+            yield ("wait", self.y_full[ys], (n_unit // Y_SETS) & 1, n_unit // Y_SETS)
+            yield ("arrive", self.y_empty[ys])
 
     def run(self):
-        roles = [self.tma_w(), self.tma_b()] + [self.issuer(i) for i in range(ISSUERS)]
-        roles += [self.dequant(w // 4) for w in range(DQ_WARPS)]      # 4 lane quarters per half
-        roles += [self.epilogue() for _ in range(EPI_WARPS)]
+        roles = [self.tma_w(0), self.tma_w(1), self.tma_b()]
+        roles += [self.issuer(i) for i in range(ISSUERS)]
+        roles += [self.dequant(w // 4, w % 4) for w in range(DQ_WARPS)]   # 4 lane quarters per ring
+        roles += [self.epilogue(q) for q in range(EPI_WARPS)]
+        roles += [self.combine() for _ in range(COMB_WARPS)]
         nxt = [next(r, None) for r in roles]
         steps = 0
         while True:
@@ -270,6 +292,12 @@ class Grouped:
                 op[1].arrive()
             elif op[0] == "copy":
                 self.copies.append(op[1])
+            elif op[0] == "rs_write":
+                self.row_scale[op[1] % ROW_SCALE_SETS][op[2]] = op[1]
+            elif op[0] == "rs_read":
+                got = self.row_scale[op[1] % ROW_SCALE_SETS][op[2]]
+                assert got == op[1], f"row scales of unit {op[1]} read as unit {got}'s"
+
             elif op[0] == "commit":
                 self.commits[op[1]].append(op[2])
             nxt[i] = next(roles[i], None)
@@ -295,11 +323,11 @@ def test_grouped_pipeline_protocol(K, seed):
 
 
 def test_the_grouped_model_catches_a_broken_protocol():
-    """A dequant warp that waits on its A buffer with the parity of the
-    wrong slot must fail the checks."""
+    """A dequant warp that waits on its A buffer with a fixed parity must
+    fail the checks."""
     class Broken(Grouped):
-        def dequant(self, h):
-            for op in Grouped.dequant(self, h):
+        def dequant(self, r, q=0):
+            for op in Grouped.dequant(self, r, q):
                 if op[0] == "wait" and op[1] in self.a_empty:
                     op = (op[0], op[1], 1, op[3])
                 yield op
@@ -308,6 +336,47 @@ def test_the_grouped_model_catches_a_broken_protocol():
         rng = random.Random(seed)
         try:
             Broken(704, _units(rng, 6), rng).run()
-        except AssertionError:
+        except AssertionError as e:
+            assert "parity test" in str(e)
             failures += 1
+    assert failures > 0
+
+
+def test_the_grouped_model_catches_rings_by_stage_within_unit():
+    """Assigning stages to rings by their index within the unit instead of
+    in the CTA's stage sequence breaks the parity waits when a unit has an
+    odd number of stages (gate_up: 11): a warp would skip phases of its
+    stage slots."""
+    class Broken(Grouped):
+        @staticmethod
+        def stage_parity(g, kc):
+            return kc & 1                          # the broken rule
+    failures = 0
+    for seed in range(10):
+        rng = random.Random(seed)
+        try:
+            Broken(2816, _units(rng, 4), rng).run()
+        except AssertionError as e:
+            # a skipped phase shows as a wrong parity test or as a deadlock
+            assert "parity test" in str(e) or "deadlock" in str(e)
+            failures += 1
+    assert failures > 0
+
+
+def test_the_grouped_model_catches_a_short_row_scale_table():
+    """With two row-scale tables instead of four, the dequant warps of unit
+    n + 2 can overwrite unit n's before its epilogue reads it."""
+    global ROW_SCALE_SETS
+    saved, ROW_SCALE_SETS = ROW_SCALE_SETS, 2
+    failures = 0
+    try:
+        for seed in range(40):
+            rng = random.Random(seed)
+            try:
+                Grouped(704, _units(rng, 7), rng).run()
+            except AssertionError as e:
+                assert "row scales" in str(e)
+                failures += 1
+    finally:
+        ROW_SCALE_SETS = saved
     assert failures > 0

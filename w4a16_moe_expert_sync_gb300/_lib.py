@@ -74,6 +74,10 @@ def load_library(path: str | None = None):
             "w4_grouped_gemm_gate_up": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_grouped_gemm_down": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V], I),
             "w4_moe_combine_fixed_order": ([V, V, V, I, I, I, I, V, V], I),
+            "w4_grouped_gemm_down_combine": ([V, I, I, I, I, I, I, V, V, V, I, V, V, V, V, V, V,
+                                              V, V, V], I),
+            "w4_moe_combine_prepare": ([V, I, I, I, I, V, V, V], I),
+            "w4_test_pipeline_hooks": ([U64, I], I),
             "w4_moe_layer_workspace_size": ([I, I, I, I, I, I], SZ),
             "w4_moe_layer": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V, SZ, V, V,
                               V], I),
@@ -296,14 +300,53 @@ def w4_moe_combine_fixed_order(y, topk_ids, topk_weights, E: int, out=None, stre
     return out
 
 
+def w4_moe_combine_prepare(topk_ids, E: int, d: int, counters=None, out=None, stream=None):
+    """The counters [M, d/128] int32 of w4_grouped_gemm_down_combine (and
+    the zero out rows of tokens with no valid expert id); returns
+    (counters, out)."""
+    import torch
+    _require_cuda(topk_ids, counters, out)
+    M, k = topk_ids.shape
+    if counters is None:
+        counters = torch.empty((M, d // 128), dtype=torch.int32, device=topk_ids.device)
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=topk_ids.device)
+    _check(load_library().w4_moe_combine_prepare(
+        _ptr(topk_ids), M, k, E, d, _ptr(counters), _ptr(out), _stream(stream)),
+        "w4_moe_combine_prepare")
+    return counters, out
+
+
+def w4_grouped_gemm_down_combine(h, dn_q, dn_s, dn_z, align: dict, topk_ids, topk_weights,
+                                 counters, out, group: int = 64, y=None, dev_status=None,
+                                 stream=None):
+    """w4_grouped_gemm_down with the fixed-order combine folded in: out
+    [M, d] bf16 (prepared with w4_moe_combine_prepare, which set counters);
+    returns (y, out)."""
+    import torch
+    _require_cuda(h, dn_q, dn_s, dn_z, topk_ids, topk_weights, counters, out, y, dev_status)
+    E, d, half_m = dn_q.shape
+    m = half_m * 2
+    M, k = align["M"], align["k"]
+    if y is None:
+        y = torch.empty((M * k, d), dtype=torch.float32, device=h.device)
+    _check(load_library().w4_grouped_gemm_down_combine(
+        _ptr(h), M, d, m, E, k, align["block_m"], _ptr(dn_q), _ptr(dn_s), _ptr(dn_z), group,
+        _ptr(align["sorted_ids"]), _ptr(align["expert_offsets"]), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(counters), _ptr(y), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "w4_grouped_gemm_down_combine")
+    return y, out
+
+
 def w4_moe_layer_workspace_size(M, d, m, E, k, block_m=16) -> int:
     return int(load_library().w4_moe_layer_workspace_size(M, d, m, E, k, block_m))
 
 
 def w4_moe_layer(x, topk_ids, topk_weights, gu, dn, block_m: int = 16, gu_group: int = 128,
                  dn_group: int = 64, workspace=None, out=None, dev_status=None, stream=None):
-    """The whole routed-expert layer (align, gate_up + activation, down,
-    fixed-order combine) as four launches on the current stream."""
+    """The whole routed-expert layer (align+gather, gate_up + activation,
+    down with the fixed-order combine folded in) as three launches on the
+    current stream."""
     import torch
     gu_q, gu_s, gu_z = gu
     dn_q, dn_s, dn_z = dn

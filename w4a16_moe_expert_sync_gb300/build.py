@@ -13,7 +13,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libw4moe.so")
 SOURCES = ["api.cu", "quantize.cu", "route_align.cu", "combine.cu", "grouped_gemm.cu",
            "static_scratch.cu", "rmsnorm.cu", "sampler.cu", "dense_gemm.cu"]
-HEADERS = ["launch.h", "ptx.cuh", "korder.cuh"]
+HEADERS = ["launch.h", "ptx.cuh", "korder.cuh", "combine_fold.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -8,6 +8,14 @@
 #include "../../include/w4moe.h"
 #include "launch.h"
 
+namespace w4 {
+PipelineTestHooks &pipeline_test_hooks()
+{
+    thread_local PipelineTestHooks hooks;
+    return hooks;
+}
+}  // namespace w4
+
 namespace {
 
 thread_local char g_detail[512] = "";
@@ -289,10 +297,23 @@ int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int
                                expert_offsets, num_padded, xg, dev_status, stream);
 }
 
-int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
-                            const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
-                            int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
-                            uint16_t *h, int32_t *dev_status, w4_stream_t stream)
+}  // extern "C"
+
+namespace {
+// The layer's combine folded into the GEMMs (w4_moe_layer only; comb_cnt
+// NULL elsewhere): see GroupedGemmProblem.
+struct FoldedCombine {
+    const int32_t *topk_ids = nullptr;
+    const float *topk_w = nullptr;
+    int32_t *cnt = nullptr;
+    uint16_t *out = nullptr;
+};
+
+int grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
+                         const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                         int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
+                         uint16_t *h, int32_t *dev_status, w4_stream_t stream,
+                         const FoldedCombine &fc)
 {
     if (int rc = check_gemm_common(M, d, m, E, k, block_m, xg, gu_q, gu_s, gu_z, sorted_ids,
                                    expert_offsets, h))
@@ -319,6 +340,12 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int 
     p.group = group;
     p.out_cols = m;
     p.cap = align_capacity(M, k, E, block_m);
+    p.topk_ids = fc.topk_ids;
+    p.comb_cnt = fc.cnt;
+    p.comb_out = fc.out;
+    p.comb_d = d;
+    p.wait_ns = w4::pipeline_test_hooks().wait_ns;
+    p.test_withhold_sz = w4::pipeline_test_hooks().withhold_sz;
     if (M == 0)
         return W4_OK;
     const char *why = nullptr;
@@ -328,15 +355,13 @@ int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int 
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "gate_up launch");
 }
 
-}  // extern "C"
-
-namespace {
 // early_schedule: see GroupedGemmProblem (set only by w4_moe_layer, where the
 // alignment is two launches back and gate_up waits for it before triggering)
 int grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
                       const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
                       const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
-                      int32_t *dev_status, w4_stream_t stream, bool early_schedule)
+                      int32_t *dev_status, w4_stream_t stream, bool early_schedule,
+                      const FoldedCombine &fc)
 {
     if (int rc = check_gemm_common(M, d, m, E, k, block_m, h, dn_q, dn_s, dn_z, sorted_ids,
                                    expert_offsets, y))
@@ -364,6 +389,13 @@ int grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int 
     p.out_cols = d;
     p.cap = align_capacity(M, k, E, block_m);
     p.early_schedule = early_schedule;
+    p.topk_ids = fc.topk_ids;
+    p.topk_w = fc.topk_w;
+    p.comb_cnt = fc.cnt;
+    p.comb_out = fc.out;
+    p.comb_d = d;
+    p.wait_ns = w4::pipeline_test_hooks().wait_ns;
+    p.test_withhold_sz = w4::pipeline_test_hooks().withhold_sz;
     if (M == 0)
         return W4_OK;
     const char *why = nullptr;
@@ -376,13 +408,75 @@ int grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int 
 
 extern "C" {
 
+int w4_grouped_gemm_gate_up(const uint16_t *xg, int M, int d, int m, int E, int k, int block_m,
+                            const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z,
+                            int group, const int32_t *sorted_ids, const int32_t *expert_offsets,
+                            uint16_t *h, int32_t *dev_status, w4_stream_t stream)
+{
+    return grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, group, sorted_ids,
+                                expert_offsets, h, dev_status, stream, FoldedCombine{});
+}
+
 int w4_grouped_gemm_down(const uint16_t *h, int M, int d, int m, int E, int k, int block_m,
                          const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int group,
                          const int32_t *sorted_ids, const int32_t *expert_offsets, float *y,
                          int32_t *dev_status, w4_stream_t stream)
 {
     return grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, group, sorted_ids,
-                             expert_offsets, y, dev_status, stream, false);
+                             expert_offsets, y, dev_status, stream, false, FoldedCombine{});
+}
+
+int w4_grouped_gemm_down_combine(const uint16_t *h, int M, int d, int m, int E, int k,
+                                 int block_m, const uint8_t *dn_q, const uint16_t *dn_s,
+                                 const uint16_t *dn_z, int group, const int32_t *sorted_ids,
+                                 const int32_t *expert_offsets, const int32_t *topk_ids,
+                                 const float *topk_weights, int32_t *counters, float *y,
+                                 uint16_t *out, int32_t *dev_status, w4_stream_t stream)
+{
+    if (M > 0 && (!topk_ids || !topk_weights || !counters || !out))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) || !aligned4(topk_ids) ||
+        !aligned4(topk_weights) || !aligned4(counters))
+        return fail(W4_ERR_MISALIGNED, "out must be 8-byte and topk_ids, topk_weights and "
+                                       "counters 4-byte aligned");
+    FoldedCombine fc;
+    fc.topk_ids = topk_ids;
+    fc.topk_w = topk_weights;
+    fc.cnt = counters;
+    fc.out = out;
+    return grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, group, sorted_ids,
+                             expert_offsets, y, dev_status, stream, false, fc);
+}
+
+int w4_test_pipeline_hooks(uint64_t wait_limit_ns, int withhold_first_scales)
+{
+    w4::PipelineTestHooks &h = w4::pipeline_test_hooks();
+    h.wait_ns = wait_limit_ns ? wait_limit_ns : 1000000000ull;
+    h.withhold_sz = withhold_first_scales != 0;
+    return W4_OK;
+}
+
+int w4_moe_combine_prepare(const int32_t *topk_ids, int M, int k, int E, int d,
+                           int32_t *counters, uint16_t *out, w4_stream_t stream)
+{
+    if (M > 0 && (!topk_ids || !counters || !out))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 0 || k <= 0 || d <= 0 || E <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes M=%d k=%d d=%d E=%d", M, k, d, E);
+    if (d % 128)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "d must be a multiple of 128 (got %d)", d);
+    if (static_cast<int64_t>(M) * k >= (1ll << 31) || static_cast<int64_t>(M) * d >= (1ll << 31))
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "M * k and M * d must be below 2^31");
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) || !aligned4(topk_ids) || !aligned4(counters))
+        return fail(W4_ERR_MISALIGNED, "out must be 8-byte and topk_ids and counters 4-byte "
+                                       "aligned");
+    if (M == 0)
+        return W4_OK;
+    if (int rc = check_device())
+        return rc;
+    cudaError_t err = w4::launch_combine_prepare(topk_ids, M, k, E, d, counters, out,
+                                                 as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "combine prepare launch");
 }
 
 int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const float *topk_weights,
@@ -403,13 +497,16 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const fl
     return err == cudaSuccess ? W4_OK : cuda_fail(err, "combine launch");
 }
 
+}  // extern "C"
+
 // Workspace layout of w4_moe_layer (each piece 256-byte aligned):
 //   sorted_ids [cap] i32 | block_expert [cap/bm] i32 | expert_offsets [E+1] i32 |
 //   num_padded [1] i32 | xg [cap, d + 64] fp16 | h [cap, m + 64] fp16 |
-//   y [M*k, d] fp32   (xg and h rows end in their 64-column group-sum block)
+//   y [M*k, d] fp32 | combine counters [M, d/128] i32
+//   (xg and h rows end in their 64-column group-sum block)
 namespace {
 struct LayerWs {
-    size_t sorted, block, offs, npad, xg, h, y, total;
+    size_t sorted, block, offs, npad, xg, h, y, cnt, total;
 };
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
@@ -423,10 +520,68 @@ LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
     w.xg = up256(w.npad + 4);
     w.h = up256(w.xg + 2 * cap * (static_cast<size_t>(d) + 64));
     w.y = up256(w.h + 2 * cap * (static_cast<size_t>(m) + 64));
-    w.total = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
+    w.cnt = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
+    w.total = up256(w.cnt + 4 * static_cast<size_t>(M) * (d / 128));
     return w;
 }
+
+// The checks of the layer's GEMM and combine arguments, made before its
+// first launch (the workspace pieces stand in for the intermediates).
+int check_layer(int M, int d, int m, int E, int k, int block_m, const uint8_t *gu_q,
+                const uint16_t *gu_s, const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
+                const uint16_t *dn_s, const uint16_t *dn_z, int dn_group, const uint8_t *ws,
+                const LayerWs &L, const float *topk_weights, const uint16_t *out)
+{
+    if (int rc = check_gemm_common(M, d, m, E, k, block_m, ws + L.xg, gu_q, gu_s, gu_z,
+                                   ws + L.sorted, ws + L.offs, ws + L.h))
+        return rc;
+    if (int rc = check_gemm_common(M, d, m, E, k, block_m, ws + L.h, dn_q, dn_s, dn_z,
+                                   ws + L.sorted, ws + L.offs, ws + L.y))
+        return rc;
+    if (gu_group != 128 || dn_group != 64)
+        return fail(W4_ERR_UNSUPPORTED_SHAPE, "need gate_up group 128 and down group 64 (got %d, %d)",
+                    gu_group, dn_group);
+    if (int rc = check_device())
+        return rc;
+    if (!w4::grouped_gemm_fits(true, d, gu_group, E) || !w4::grouped_gemm_fits(false, m, dn_group, E))
+        return fail(W4_ERR_UNSUPPORTED_SHAPE,
+                    "the grouped GEMMs' scale/zero stages do not fit shared memory (d=%d, m=%d, "
+                    "E=%d; gate_up takes d up to about 3840 at E = 128)", d, m, E);
+    if (M > 0 && (!out || !topk_weights))
+        return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) || !aligned4(topk_weights))
+        return fail(W4_ERR_MISALIGNED, "out must be 8-byte and topk_weights 4-byte aligned");
+    return W4_OK;
+}
+
+// gate_up (which also sets the combine counters) and down with the combine
+// folded into its epilogue: the layer's launches after alignment+gather
+int layer_gemms(const int32_t *topk_ids, const float *topk_weights, int M,
+                int d, int m, int E, int k, int block_m, const uint8_t *gu_q,
+                const uint16_t *gu_s, const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
+                const uint16_t *dn_s, const uint16_t *dn_z, int dn_group, uint8_t *ws,
+                const LayerWs &L, uint16_t *out, int32_t *dev_status, w4_stream_t stream)
+{
+    const int32_t *sorted = reinterpret_cast<const int32_t *>(ws + L.sorted);
+    const int32_t *offs = reinterpret_cast<const int32_t *>(ws + L.offs);
+    const uint16_t *xg = reinterpret_cast<const uint16_t *>(ws + L.xg);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    float *y = reinterpret_cast<float *>(ws + L.y);
+    FoldedCombine fc;
+    fc.topk_ids = topk_ids;
+    fc.topk_w = topk_weights;
+    fc.cnt = reinterpret_cast<int32_t *>(ws + L.cnt);
+    fc.out = out;
+    int rc = grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group, sorted,
+                                  offs, h, dev_status, stream, fc);
+    if (rc)
+        return rc;
+    return grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs,
+                             y, dev_status, stream, true, fc);
+}
 }  // namespace
+
+extern "C" {
 
 size_t w4_moe_layer_workspace_size(int M, int d, int m, int E, int k, int block_m)
 {
@@ -451,28 +606,22 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(W4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (int rc = check_layer(M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group, dn_q, dn_s, dn_z,
+                             dn_group, ws, L, topk_weights, out))
+        return rc;
     int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
     int32_t *block = reinterpret_cast<int32_t *>(ws + L.block);
     int32_t *offs = reinterpret_cast<int32_t *>(ws + L.offs);
     int32_t *npad = reinterpret_cast<int32_t *>(ws + L.npad);
     uint16_t *xg = reinterpret_cast<uint16_t *>(ws + L.xg);
-    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    float *y = reinterpret_cast<float *>(ws + L.y);
     // alignment and the activation gather share one launch
     if (int rc0 = w4_moe_align_gather(topk_ids, x, M, d, k, E, block_m, sorted, block, offs, npad,
                                       xg, dev_status, stream))
         return rc0;
     if (M == 0)
         return W4_OK;
-    int rc = w4_grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
-                                     sorted, offs, h, dev_status, stream);
-    if (rc)
-        return rc;
-    rc = grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs, y,
-                           dev_status, stream, true);
-    if (rc)
-        return rc;
-    return w4_moe_combine_fixed_order(y, topk_ids, topk_weights, M, k, d, E, out, stream);
+    return layer_gemms(topk_ids, topk_weights, M, d, m, E, k, block_m, gu_q, gu_s, gu_z,
+                       gu_group, dn_q, dn_s, dn_z, dn_group, ws, L, out, dev_status, stream);
 }
 
 int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int d, int m, int E,
@@ -493,13 +642,14 @@ int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int 
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(W4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (int rc = check_layer(M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group, dn_q, dn_s, dn_z,
+                             dn_group, ws, L, topk_weights, out))
+        return rc;
     int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
     int32_t *block = reinterpret_cast<int32_t *>(ws + L.block);
     int32_t *offs = reinterpret_cast<int32_t *>(ws + L.offs);
     int32_t *npad = reinterpret_cast<int32_t *>(ws + L.npad);
     uint16_t *xg = reinterpret_cast<uint16_t *>(ws + L.xg);
-    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    float *y = reinterpret_cast<float *>(ws + L.y);
     // router, alignment and activation gather share one launch
     if (int rc0 = w4_moe_route_align_gather(logits, x, M, d, k, E, block_m, topk_ids,
                                             topk_weights, sorted, block, offs, npad, xg,
@@ -507,15 +657,8 @@ int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int 
         return rc0;
     if (M == 0)
         return W4_OK;
-    int rc = w4_grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
-                                     sorted, offs, h, dev_status, stream);
-    if (rc)
-        return rc;
-    rc = grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs, y,
-                           dev_status, stream, true);
-    if (rc)
-        return rc;
-    return w4_moe_combine_fixed_order(y, topk_ids, topk_weights, M, k, d, E, out, stream);
+    return layer_gemms(topk_ids, topk_weights, M, d, m, E, k, block_m, gu_q, gu_s, gu_z,
+                       gu_group, dn_q, dn_s, dn_z, dn_group, ws, L, out, dev_status, stream);
 }
 
 }  // extern "C"

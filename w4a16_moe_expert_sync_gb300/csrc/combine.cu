@@ -10,6 +10,7 @@
 // the result is bit-identical from run to run.
 #include <cuda_bf16.h>
 
+#include "combine_fold.cuh"
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -76,6 +77,30 @@ cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, i
     const int64_t blocks = (n + threads - 1) / threads;
     return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
                       y, ids, w, M, k, d, E, out);
+}
+
+// The counters of the combine folded into the down GEMM (combine_fold.cuh),
+// one warp per token, for callers that run the down GEMM with the combine
+// on their own (the layer sets them in its gate_up launch instead).
+__global__ void __launch_bounds__(256) combine_prepare_kernel(const int32_t *__restrict__ ids,
+                                                              int M, int k, int E, int d,
+                                                              int32_t *__restrict__ cnt,
+                                                              uint16_t *__restrict__ out)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t < M)
+        fold_prepare_token(t, threadIdx.x & 31, ids, k, E, d, cnt, out);
+}
+
+cudaError_t launch_combine_prepare(const int32_t *ids, int M, int k, int E, int d, int32_t *cnt,
+                                   uint16_t *out, cudaStream_t stream)
+{
+    if (M == 0)
+        return cudaSuccess;
+    return launch_pdl(combine_prepare_kernel, dim3(static_cast<unsigned>((M + 7) / 8)), dim3(256),
+                      0, stream, ids, M, k, E, d, cnt, out);
 }
 
 }  // namespace w4

@@ -37,35 +37,40 @@
 // before that rounding) as the A operand, one to four K = 16 MMAs against the
 // sum block.  The dequantised weight is then exact to its own fp16 rounding.
 //
-// Design (one persistent CTA of 16 warps per SM, static round-robin schedule):
+// Design (one persistent CTA of 28 warps per SM, static round-robin schedule):
 //   * A work unit is (job, panel).  A job is at most 32 consecutive slots of
 //     one expert; a panel is 128 weight rows (gate_up: 64 gate rows and the
 //     matching 64 up rows; down: 128 output rows).
 //   * Swap-AB: the 128 weight rows are the M = 128 operand, in tensor memory
 //     (written with tcgen05.st), the job's tokens are N (16 or 32).  B, the
 //     activations, is read by the tensor core from shared memory in the
-//     128-byte-swizzled K-major layout; one 3-D TMA copy fills a slot.
+//     128-byte-swizzled K-major layout; 3-D TMA copies fill its slots (or, for
+//     down, one copy per job fills a resident slot).
 //   * Codes arrive by TMA in stages of 128 rows x 256 codes (two 64-row
-//     boxes).  Each stage is two 128-code sub-chunks; the dequant warp of a
-//     lane quarter and half h expands sub-chunk h of every stage for its 32
-//     rows into a 64-column A buffer of ring h (two buffers per ring).
-//   * Four issuer warps, one per SM sub-partition: issuer 2 h + p takes the
-//     64-code half p of every sub-chunk of ring h (four K = 16 MMAs, one
-//     commit) into its own fp32 accumulator; the dequant warps hand over
-//     each half as soon as it is in tensor memory.  A thread issues an MMA
-//     every ~55 cycles at best and a commit costs it ~150, so one issuer per
-//     ring cannot keep up.  The epilogue adds the four accumulators in a
-//     fixed order.  Two accumulator sets alternate per unit, so a unit's
-//     epilogue overlaps the next unit's MMAs.
+//     boxes), evict-first in L2.  A stage is two 128-code sub-chunks.  Ring
+//     r = 2 gp + h (one 64-column A buffer in tensor memory) takes sub-chunk
+//     h of the stages whose index in the CTA's stage sequence has parity gp;
+//     the four dequant warps of ring r (one per lane quarter) expand it.
+//   * Four issuer warps, one per SM sub-partition: issuer r issues ring r's
+//     eight K = 16 MMAs per fill as two fused issue blocks, the second with
+//     the commit that releases the buffer, into its own fp32 accumulator
+//     ("chain").  The epilogue adds the chains in a fixed order.  Two
+//     accumulator sets alternate per unit, so a unit's epilogue overlaps the
+//     next unit's MMAs.  Ring 1 or 3 also carries the unit's correction.
 //   * Warp roles
 //       warps 0-3   tcgen05.mma issuers (converged, one elected lane issues);
 //                   warp 0 also allocates tensor memory
 //       warps 4-7   epilogue (one TMEM lane quarter each)
-//       warps 8-15  dequant (warp 8 + 4 h + q: lane quarter q, half h)
-//       warp 16     TMA: packed codes; per unit the scales and zeros
-//       warp 17     TMA: activation slots
-//   * Tensor memory (512 columns): A buffers at 64 (2 h + i), accumulators
-//     at 256 + 128 set + 32 issuer.
+//       warps 8-23  dequant (warp 8 + 4 r + q: lane quarter q, ring r)
+//       warp 24     TMA: per unit the scales and zeros, and the code stages
+//                   of parity 0 of the CTA's stage sequence
+//       warp 27     TMA: the code stages of parity 1
+//       warp 25     TMA: activation slots
+//       warp 26     the combine folded into down (combine_fold.cuh): gate_up
+//                   sets the counters, down counts y panels; every warp
+//                   combines the tokens its CTA completed after the last unit
+//   * Tensor memory (512 columns): A buffers at 64 r, accumulators at
+//     256 + 128 set + 32 chain.
 //   * Every barrier has one producer group and one consumer group that take
 //     its phases in order, so a waiter is never two phases ahead and parity
 //     waits are exact (tests/test_grouped_pipeline_protocol.py models it).
@@ -77,6 +82,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "combine_fold.cuh"
 #include "korder.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -85,18 +91,25 @@ namespace w4 {
 
 namespace {
 
-constexpr int kNumIssuers = 4;              // warps 0-3: issuer 2 h + p takes half p of ring h
+constexpr int kNumIssuers = 4;              // warps 0-3: issuer r takes ring r
 constexpr int kWarpAlloc = 0;               // tensor-memory allocation (an issuer)
-constexpr int kWarpTmaW = 16;
-constexpr int kWarpTmaB = 17;
+constexpr int kWarpTmaW = 24;              // scales/zeros and parity-0 code stages
+constexpr int kWarpTmaW1 = 27;             // parity-1 code stages
+constexpr int kWarpTmaB = 25;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kFirstDqWarp = 8;
-constexpr int kNumDqWarps = 8;
-constexpr int kNumWarps = 18;
+constexpr int kNumDqWarps = 16;            // warp 8 + 4 r + q: lane quarter q, ring r
+constexpr int kWarpComb = 26;               // the folded combine (and its counters)
+constexpr int kNumWarps = 28;
+// y_full / y_empty: epilogue -> combine warps, one phase per unit, four sets
+constexpr int kYSets = 4;
 constexpr int kThreads = 32 * kNumWarps;
-constexpr int kRings = 2;                   // one per dequant half
-constexpr int kRingBufs = 2;                // A buffers per ring
+// Ring r = 2 gp + h holds sub-chunk h of the stages whose global index (in
+// the CTA's stage sequence) has parity gp, so every dequant warp works on
+// every other stage and has two stages' time for each of its sub-chunks.
+constexpr int kRings = 4;
+constexpr int kRingBufs = 1;                // A buffers per ring
 constexpr int kStagesW = 6;                 // packed-code stages
 constexpr int kStagesB = 3;                 // streamed activation slots
 constexpr int kMaxStagesSZ = 3;             // per-unit scales and zeros
@@ -113,7 +126,17 @@ constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 256
 // Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 128 set
 // + 32 i, the set alternating per unit.
 constexpr int kChains = kNumIssuers;
+// Row scales 2^c handed from the dequant warps to the epilogue, one table
+// per unit for the last four units: the dequant warp of sub-chunk 0 writes
+// unit n's after claiming its ring buffer, whose previous MMAs (unit >= n - 2)
+// waited for the epilogue of unit n - 4 to release its accumulators, which
+// it does after reading its table.
+constexpr int kRowScaleSets = 4;
+// The (token, panel) combines a down CTA completes, kept until its last unit
+// (a longer list is combined as it overflows).
+constexpr int kCombListCap = 1024;
 static_assert(kAccCol + 2 * kChains * kMaxN <= kTmemCols, "tensor memory budget");
+static_assert(kStagesW % 2 == 0, "a dequant warp must see every phase of its stage slots");
 
 struct GemmArgs {
     CUtensorMap tmap_w;       // packed codes u8 [E*R rows, K/2 B], box 128 B x 64 rows, SW128
@@ -128,17 +151,32 @@ struct GemmArgs {
     int n_corr_mma;           // K = 16 MMAs of the group-constant correction
     int h_stride;             // gate_up: row length of h (m + 64: values, then group sums)
     int h_groups;             // gate_up: groups of 64 along m (the down GEMM's groups)
-    int acc_mask;             // issuers (accumulators) that receive MMAs in every unit
-    int corr_ring;            // the ring that carries the correction sub-chunk
+    int acc_mask[2];          // issuers (accumulators) with MMAs in a unit whose first
+                              // stage has global index parity 0 / 1
     int early_schedule;       // the schedule may be read before the grid-dependency wait
+    // The layer's combine, folded into the down GEMM (comb_cnt non-null):
+    // counters [M][d/128 panels][4 lane quarters], set by the gate_up launch
+    // before it (to k minus the token's valid assignments; it also zeroes
+    // the out rows of tokens with none) and counted up by the down
+    // epilogue; the warp that completes a counter writes those 32 columns
+    // of out.
+    const int32_t *topk_ids;  // [M, k]
+    const float *topk_w;      // [M, k]
+    int32_t *comb_cnt;
+    uint16_t *comb_out;       // [M, d] bf16
+    int M, k, comb_d;
+    // test hooks: the pipeline wait limit (ns), and whether the first unit's
+    // scale/zero copy is withheld (so that the waits run out)
+    uint64_t wait_ns;
+    int test_withhold_sz;
 };
 
-constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 3 * kRings * kRingBufs + 2 + 2 +
-                         2 * kMaxStagesSZ + kNumIssuers;
+constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kRings * kRingBufs + 2 + 2 +
+                         2 * kMaxStagesSZ + kNumIssuers + 2 * kYSets;
 
 struct Bars {
     uint64_t *w_full, *w_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty,
-        *sz_full, *sz_empty, *drain;
+        *sz_full, *sz_empty, *drain, *y_full, *y_empty;
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t *base)
@@ -149,18 +187,20 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
     r.w_empty = r.w_full + kStagesW;
     r.b_full = r.w_empty + kStagesW;
     r.b_empty = r.b_full + kStagesB;
-    r.a_full = r.b_empty + kStagesB;                 // [buffer][half]
-    r.a_empty = r.a_full + 2 * kRings * kRingBufs;
+    r.a_full = r.b_empty + kStagesB;
+    r.a_empty = r.a_full + kRings * kRingBufs;
     r.acc_full = r.a_empty + kRings * kRingBufs;
     r.acc_empty = r.acc_full + 2;
     r.sz_full = r.acc_empty + 2;
     r.sz_empty = r.sz_full + kMaxStagesSZ;
     r.drain = r.sz_empty + kMaxStagesSZ;
+    r.y_full = r.drain + kNumIssuers;
+    r.y_empty = r.y_full + kYSets;
     return r;
 }
 
 struct SmemLayout {
-    int off_b, off_sz, off_bar, off_misc, off_offs, off_jp;
+    int off_b, off_sz, off_bar, off_misc, off_offs, off_jp, off_rs, off_cl;
     int sz_stride, total;
 };
 
@@ -169,7 +209,7 @@ struct SmemLayout {
 // code stages, so the copy of the next unit's scales is never waited for).
 __host__ __device__ inline int sz_stages(int G) { return G > 16 ? 2 : 3; }
 
-__host__ __device__ inline SmemLayout smem_layout(int G, int E)
+__host__ __device__ inline SmemLayout smem_layout(int G, int E, bool gate_up)
 {
     SmemLayout L;
     L.off_b = kStagesW * kStageWBytes;
@@ -179,7 +219,10 @@ __host__ __device__ inline SmemLayout smem_layout(int G, int E)
     L.off_misc = L.off_bar + kNumBars * 8;
     L.off_offs = L.off_misc + 16;
     L.off_jp = L.off_offs + (E + 1) * 4;
-    L.total = L.off_jp + (E + 1) * 4;
+    L.off_rs = (L.off_jp + (E + 1) * 4 + 15) & ~15;
+    L.off_cl = L.off_rs + kRowScaleSets * kTileRows * 4;
+    // down: the combine list (its count in the misc words)
+    L.total = L.off_cl + (gate_up ? 0 : kCombListCap * 4);
     return L;
 }
 
@@ -206,8 +249,8 @@ __device__ __forceinline__ Job decode_job(const int *jp, const int *offs, int E,
     return J;
 }
 
-// 64-code column blocks per streamed activation slot for a job of n slots (32 KB).
-__host__ __device__ constexpr int b_kcols(int n) { return n == 16 ? 16 : 8; }
+// 64-code column blocks per streamed activation slot for a job of n slots.
+__host__ __device__ constexpr int b_kcols(int n) { return kStageBBytes / (n * 128); }
 
 // Resident mode: the activation block of a full job (kMaxN slots x K) fits
 // one of two 48 KB slots and is loaded once per job, not once per unit.
@@ -258,6 +301,23 @@ __device__ __forceinline__ int row_exponent(uint32_t smax_bits)
     return max(f, 1) - 6;
 }
 
+// The largest |scale| bit pattern among the G scales of a row in shared
+// memory at s_addr, sixteen independent loads at a time.
+__device__ __forceinline__ uint32_t row_smax(uint32_t s_addr, int G)
+{
+    uint32_t smax = 0;
+    for (int g0 = 0; g0 < G; g0 += 16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            v[i] = g0 + i < G ? lds_u16(s_addr + 2 * (g0 + i)) : 0u;
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            smax = max(smax, v[i] & 0x7FFFu);
+    }
+    return smax;
+}
+
 __device__ __forceinline__ float exp2i(int e)   // 2^e for -126 <= e <= 127, exact
 {
     return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
@@ -291,16 +351,23 @@ __device__ __forceinline__ float gelu_tanh(float v)
 // A bounded wait by every lane of a warp (each lane observes the phase
 // itself, which gives it acquire ordering); the vote keeps the warp's
 // control flow uniform if the wait ever times out.
-__device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity,
-                                              volatile int *abort_flag, int32_t *status)
+// What a pipeline wait needs besides its barrier: the CTA's abort flag, the
+// device status word and the time limit (one second unless a test shortens it).
+struct WaitCtx {
+    volatile int *abort_flag;
+    int32_t *status;
+    uint64_t limit_ns;
+};
+
+__device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity, const WaitCtx &wc)
 {
-    return mbar_wait_warp(bar, parity, abort_flag, status, kDevPipelineTimeout);
+    return mbar_wait_warp(bar, parity, wc.abort_flag, wc.status, kDevPipelineTimeout,
+                          wc.limit_ns);
 }
 
-__device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status)
+__device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, const WaitCtx &wc)
 {
-    return mbar_wait(bar, parity, abort_flag, status, kDevPipelineTimeout);
+    return mbar_wait(bar, parity, wc.abort_flag, wc.status, kDevPipelineTimeout, wc.limit_ns);
 }
 
 // bounded wait that ignores the abort flag (used only while draining)
@@ -310,6 +377,24 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
     while (!mbar_try_wait(bar, parity))
         if (global_timer_ns() - t0 > 200000000ull)
             return;
+}
+
+// The ring of the unit's sub-chunk j (in stage j / 2, half j % 2) when the
+// unit's first stage has global index parity gp0.
+__host__ __device__ __forceinline__ int unit_ring(int gp0, int j)
+{
+    return 2 * ((gp0 + (j >> 1)) & 1) + (j & 1);
+}
+
+// The ring that carries the unit's correction sub-chunk: half 1 of the
+// stages of the other parity than the unit's first stage.  Those are never
+// more than the first stage's parity has (one fewer when the unit has an odd
+// number of stages), and their half 1 is the one a 64-code tail leaves idle,
+// so no ring gets more than its share of the unit's fills.
+__host__ __device__ __forceinline__ int corr_ring(int gp0, int n_kchunks)
+{
+    (void)n_kchunks;
+    return 2 * (gp0 ^ 1) + 1;
 }
 
 // Tile row (0..127 of the stage) held by lane `lane` of a warp of TMEM lane
@@ -323,6 +408,97 @@ __device__ __forceinline__ int tile_row(int q4, int lane)
         return 32 * q4 + lane;
 }
 
+// ------------------------------------------------- the combine, folded in
+// out[t, pnl*128 .. +128] = bf16(sum over j = 0..k-1 in order of w_j y_j) by
+// one warp (four columns per lane): the fp32 chain acc = fma(w_j, y_j, acc)
+// from 0 over the token's valid assignments, rounded once, as the standalone
+// combine computes it, so the result does not depend on which CTA completed
+// the counter.  The y rows of all k assignments are loaded at once (rows of
+// invalid ids are loaded but unused); y is read from L2 (written in this
+// launch by other CTAs).
+__device__ __forceinline__ void combine_panel(const GemmArgs &p, int t, int pnl, int lane)
+{
+    const unsigned full = 0xffffffffu;
+    const int col = pnl * 128 + 4 * lane;
+    const float *y = reinterpret_cast<const float *>(p.out);
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    for (int j0 = 0; j0 < p.k; j0 += 8) {
+        // ids and weights of 8 assignments on lanes 0-7, their y rows on all
+        const int jl = j0 + (lane & 7);
+        const int64_t aj = static_cast<int64_t>(t) * p.k + jl;
+        const int e = jl < p.k ? __ldg(p.topk_ids + aj) : -1;
+        const float wv = jl < p.k ? __ldg(p.topk_w + aj) : 0.0f;
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+            v[u] = j0 + u < p.k ? __ldcg(reinterpret_cast<const float4 *>(
+                                      y + (static_cast<int64_t>(t) * p.k + j0 + u) * p.comb_d +
+                                      col))
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const unsigned vmask = __ballot_sync(full, e >= 0 && e < p.E) & 0xFFu;
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const float wj = __shfl_sync(full, wv, u);
+            if (vmask >> u & 1u) {
+                a0 = fmaf(wj, v[u].x, a0);
+                a1 = fmaf(wj, v[u].y, a1);
+                a2 = fmaf(wj, v[u].z, a2);
+                a3 = fmaf(wj, v[u].w, a3);
+            }
+        }
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a0, a1);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(a2, a3);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p.comb_out + static_cast<int64_t>(t) * p.comb_d + col) = pk;
+}
+
+// (down, the combine warp) After the epilogue has stored unit (J, pnl)'s y
+// columns (ordered before this warp by the y_full barrier): one arrival per
+// valid slot of the job on its token's counter of panel pnl (lane i for
+// slot i).  The arrivals are release atomics at gpu scope,
+// which publish the unit's y stores to the CTA that completes the counter;
+// a warp that completed counters acquires the other CTAs' stores with an
+// acquire-release fence.  Completed (token, panel) pairs go to the CTA's
+// list, combined after its last unit (or here, past the list's capacity).
+__device__ __forceinline__ void combine_count(const GemmArgs &p, const Job &J, int pnl, int lane,
+                                              int *list, int *count)
+{
+    const unsigned full = 0xffffffffu;
+    int t = -1;
+    bool last = false;
+    if (lane < J.n) {
+        const int a = __ldg(p.sorted_ids + J.start + lane);
+        if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A)) {
+            t = a / p.k;
+            last = atom_add_release_gpu(p.comb_cnt + fold_counter_index(t, p.n_panels, pnl), 1) ==
+                   p.k - 1;
+        }
+    }
+    unsigned done = __ballot_sync(full, last);
+    if (!done)
+        return;
+    fence_acq_rel_gpu();
+    int slot = 0;
+    if (lane == 0)
+        slot = atomicAdd(count, __popc(done));
+    slot = __shfl_sync(full, slot, 0);
+    while (done) {
+        const int src = __ffs(done) - 1;
+        done &= done - 1;
+        const int tt = __shfl_sync(full, t, src);
+        if (slot < kCombListCap) {
+            if (lane == 0)
+                list[slot] = tt * p.n_panels + pnl;
+        } else {
+            combine_panel(p, tt, pnl, lane);
+        }
+        slot++;
+    }
+}
+
 // RESIDENT: each job's activations are loaded once into one of two 48 KB
 // slots (contraction dim <= 768); otherwise they stream through 32 KB slots.
 template <bool GATE_UP, bool RESIDENT>
@@ -331,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const SmemLayout L = smem_layout(p.G, p.E);
+    const SmemLayout L = smem_layout(p.G, p.E, GATE_UP);
     uint8_t *stage_w = smem;
     uint8_t *stage_b = smem + L.off_b;
     uint8_t *sz_base = smem + L.off_sz;
@@ -339,27 +515,31 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.off_misc + 4);
     int *offs = reinterpret_cast<int *>(smem + L.off_offs);
+    // 2^c per weight row for the last kRowScaleSets units (dequant -> epilogue)
+    float *row_scale = reinterpret_cast<float *>(smem + L.off_rs);
+    int *comb_list = reinterpret_cast<int *>(smem + L.off_cl);
+    int *comb_count = reinterpret_cast<int *>(smem + L.off_misc) + 2;
     int *jp = reinterpret_cast<int *>(smem + L.off_jp);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned full = 0xffffffffu;
     int32_t *status = p.dev_status;
+    const WaitCtx wc{abort_flag, status, p.wait_ns};
     const int n_sz = p.n_sz;
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
         for (int i = 0; i < kStagesW; i++) {
             mbar_init(&bar.w_full[i], 1);
-            mbar_init(&bar.w_empty[i], kNumDqWarps);
+            mbar_init(&bar.w_empty[i], kNumDqWarps / 2);   // the two rings of its parity
         }
         for (int i = 0; i < kStagesB; i++) {
             mbar_init(&bar.b_full[i], 1);
             mbar_init(&bar.b_empty[i], kNumIssuers);   // every issuer's commit
         }
         for (int i = 0; i < kRings * kRingBufs; i++) {
-            mbar_init(&bar.a_full[2 * i], 4);        // the four lane quarters, half 0
-            mbar_init(&bar.a_full[2 * i + 1], 4);    // ... half 1
-            mbar_init(&bar.a_empty[i], 2);           // the ring's two issuers' commits
+            mbar_init(&bar.a_full[i], 4);            // the ring's four lane quarters
+            mbar_init(&bar.a_empty[i], 1);           // the ring's issuer's commit
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&bar.acc_full[i], kNumIssuers);
@@ -371,7 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int i = 0; i < kNumIssuers; i++)
             mbar_init(&bar.drain[i], 1);
+        for (int i = 0; i < kYSets; i++) {
+            mbar_init(&bar.y_full[i], kNumEpiWarps);
+            mbar_init(&bar.y_empty[i], 1);
+        }
         *abort_flag = 0;
+        *comb_count = 0;
         fence_mbar_init();
     }
     if (warp == kWarpAlloc) {
@@ -426,53 +611,43 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     if (warp < kNumIssuers) {
         // ------------------------------------------------------ MMA issuers
-        // Issuer me = 2 h + p takes K steps 4p .. 4p + 3 (one 64-code half)
-        // of every sub-chunk of ring h (j = h, h + 2, ...; then the
-        // correction, "j = n_sub", when h is the correction's ring) into its
-        // own accumulator.
-        // A thread issues one MMA per ~55 cycles and a commit costs it ~150,
-        // so four issuers, one per SM sub-partition, share the work.  The
-        // warp runs this loop converged (every value in it is warp-uniform,
-        // kept in registers) and one elected lane issues each tcgen05
-        // instruction.
+        // Issuer r takes the sub-chunks of ring r (the unit's sub-chunk j is
+        // in ring unit_ring(j)), eight K = 16 MMAs each as two issue blocks,
+        // then the correction when r is the unit's correction ring, into its
+        // own accumulator.  A thread issues an MMA every ~28-55 cycles at
+        // best and a commit costs it more, so four issuers, one per SM
+        // sub-partition, share the work.  The warp runs this loop converged
+        // (every value in it is warp-uniform, kept in registers) and one
+        // elected lane issues each tcgen05 instruction.
         const int me = warp;
-        const int ring = me >> 1, part = me & 1;
         const uint32_t b_base = smem_u32(stage_b);
         uint32_t b_seq = 0, n_unit = 0;
-        uint32_t ring_slot = 0, ring_ph = 0;
+        uint32_t a_ph = 0;      // phase of this ring's (single) A buffer
         int cur_job = -1;       // resident mode: the job whose activations are held
         uint32_t res_slot = 0;
         bool ok = true;
         bool started = false;   // has this unit's first MMA gone (accumulate from then on)?
-        // Sub-chunk j of the unit (j % 2 == ring): wait for its half `part`,
-        // issue that half's K = 16 MMAs (up to 4; none for the second half
-        // of a 64-code tail or of the correction), and release the buffer
-        // (the ring's two issuers both commit).  bdesc: descriptor of the
-        // sub-chunk's first 64-code column block; the second follows
-        // col_bytes later.  j == n_sub is the group-constant correction:
-        // n_corr_mma MMAs of the constants' low parts against the
-        // activations' group sums (one column block).
+        // Sub-chunk j: wait for the ring's buffer, issue its MMAs (8; 4 for a
+        // 64-code tail; n_corr_mma for the correction, j == n_sub) and
+        // release the buffer.  bdesc: descriptor of the sub-chunk's first
+        // 64-code column block; the second follows col_bytes later.
         auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t col_bytes,
                          uint32_t idesc) -> bool {
-            const int buf = ring * kRingBufs + static_cast<int>(ring_slot);
-            // operands first, then the wait, then one issue sequence
             const int n_all = j == n_sub ? p.n_corr_mma : (half_tail && j == n_sub - 1) ? 4 : 8;
-            const int n_mma = min(max(n_all - 4 * part, 0), 4);
-            const uint32_t a_tmem =
-                tmem + static_cast<uint32_t>(buf) * kSubCols + 32u * static_cast<uint32_t>(part);
+            const uint32_t a_tmem = tmem + static_cast<uint32_t>(me) * kSubCols;
             // K steps of 16: +32 B in the swizzled row (+2 in the descriptor's
-            // address field); half `part` starts at column block `part`
-            const uint64_t b = bdesc + static_cast<uint64_t>(part) * (col_bytes >> 4);
-            if (!warp_all_wait(&bar.a_full[2 * buf + part], ring_ph, abort_flag, status))
+            // address field), +8 columns of A; the second block of four starts
+            // at the next 64-code column block
+            const uint64_t b1 = bdesc + (col_bytes >> 4);
+            if (!warp_all_wait(&bar.a_full[me], a_ph, wc))
                 return false;
-            if (++ring_slot == kRingBufs) {
-                ring_slot = 0;
-                ring_ph ^= 1;
-            }
+            a_ph ^= 1;
             tc_fence_after();
-            tc_mma4_ts_commit_elect(d_tmem, a_tmem, b, b + 2, b + 4, b + 6, idesc, n_mma,
-                                    started ? 1u : 0u, &bar.a_empty[buf]);
-            started = started || n_mma > 0;
+            tc_mma4_ts_elect(d_tmem, a_tmem, bdesc, bdesc + 2, bdesc + 4, bdesc + 6, idesc,
+                             min(n_all, 4), started ? 1u : 0u);
+            started = true;
+            tc_mma4_ts_commit_elect(d_tmem, a_tmem + 32, b1, b1 + 2, b1 + 4, b1 + 6, idesc,
+                                    max(n_all - 4, 0), 1u, &bar.a_empty[me]);
             return true;
         };
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -482,7 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
             const int set = n_unit & 1;
             const uint32_t acc_ph = (n_unit >> 1) & 1;
-            if (!warp_all_wait(&bar.acc_empty[set], acc_ph ^ 1, abort_flag, status)) {
+            const int gp0 = (n_unit * p.n_kchunks) & 1;   // parity of the unit's first stage
+            const int corr = corr_ring(gp0, p.n_kchunks);
+            if (!warp_all_wait(&bar.acc_empty[set], acc_ph ^ 1, wc)) {
                 ok = false;
                 break;
             }
@@ -495,8 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     if (cur_job >= 0)
                         tc_commit_elect(&bar.b_empty[res_slot]);
                     res_slot = b_seq & 1;
-                    if (!warp_all_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, abort_flag,
-                                       status)) {
+                    if (!warp_all_wait(&bar.b_full[res_slot], (b_seq >> 1) & 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -505,16 +681,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     cur_job = job;
                 }
                 const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
-                for (int j = ring; j < n_sub; j += 2) {
+                for (int j = 0; j < n_sub && ok; j++)
                     // sub-chunk j reads column blocks 2j, 2j + 1
-                    if (!issue(j, d_tmem, sdesc_sw128(b_slot + 2u * j * col_bytes), col_bytes,
-                               idesc)) {
+                    if (unit_ring(gp0, j) == me &&
+                        !issue(j, d_tmem, sdesc_sw128(b_slot + 2u * j * col_bytes), col_bytes,
+                               idesc))
                         ok = false;
-                        break;
-                    }
-                }
                 // the correction reads block K / 64 (the group sums)
-                if (ok && ring == p.corr_ring &&
+                if (ok && me == corr &&
                     !issue(n_sub, d_tmem,
                            sdesc_sw128(b_slot + static_cast<uint32_t>(K / 64) * col_bytes),
                            col_bytes, idesc))
@@ -526,8 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const int n_bslots = K / 64 / kcols + 1;
                 for (int t = 0; t < n_bslots && ok; t++) {
                     const int sb = (b_seq + t) % kStagesB;
-                    if (!warp_all_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, abort_flag,
-                                       status)) {
+                    if (!warp_all_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -535,15 +708,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint32_t b_slot = b_base + sb * kStageBBytes;
                     const int j0 = t * subs_per_slot;
                     const int j1 = min(n_sub, j0 + subs_per_slot);
-                    // subs_per_slot is even, so j0 is; this ring's are j0 + ring, ...
-                    for (int j = j0 + ring; j < j1; j += 2) {
-                        if (!issue(j, d_tmem, sdesc_sw128(b_slot + 2u * (j - j0) * col_bytes),
-                                   col_bytes, idesc)) {
+                    for (int j = j0; j < j1 && ok; j++)
+                        if (unit_ring(gp0, j) == me &&
+                            !issue(j, d_tmem, sdesc_sw128(b_slot + 2u * (j - j0) * col_bytes),
+                                   col_bytes, idesc))
                             ok = false;
-                            break;
-                        }
-                    }
-                    if (ok && t == n_bslots - 1 && ring == p.corr_ring) {
+                    if (ok && t == n_bslots - 1 && me == corr) {
                         const uint32_t blk = static_cast<uint32_t>(K / 64 - t * kcols);
                         if (!issue(n_sub, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), col_bytes,
                                    idesc))
@@ -563,23 +733,31 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tc_commit_elect(&bar.drain[me]);
         drain_wait(&bar.drain[me], 0);
         __syncwarp();
-    } else if (warp == kWarpTmaW) {
+    } else if (warp == kWarpTmaW || warp == kWarpTmaW1) {
         // ------------------------------------------- TMA: codes, scales/zeros
+        // Two producer threads, one per parity gp of the CTA's stage sequence:
+        // stage g goes to slot g % kStagesW, so a parity owns every other
+        // slot, only its own dequant warps free them, and a parity whose
+        // warps run ahead is never held back by the other's slower ones.
+        // The parity-0 thread also issues each unit's scales and zeros
+        // before the unit's stages.
         if (lane == 0) {
+            const int gp = warp == kWarpTmaW ? 0 : 1;
             const uint64_t pol = l2_policy_evict_first();
-            int sa = 0, szb = 0;
-            uint32_t ph_a = 0, ph_sz = 0;
-            uint32_t issued_a = 0, issue_ph_a = 0, issued_sz = 0, issue_ph_sz = 0;
             const uint32_t hb = 64u * p.G * 2;          // 64 rows of s (or z)
+            uint32_t issued_a = 0, issue_ph_a = 0, issued_sz = 0, issue_ph_sz = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            int n_unit = 0;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
                 const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
                 const int pnl = u % p.n_panels;
                 const int row0 = J.e * p.R + pnl * (GATE_UP ? 64 : 128);
                 const int row1 = GATE_UP ? row0 + p.m_up : row0 + 64;
-                if (!lane_wait(&bar.sz_empty[szb], ph_sz ^ 1, abort_flag, status))
-                    break;
-                {
+                if (gp == 0 && !(p.test_withhold_sz && n_unit == 0)) {
+                    const int szb = n_unit % n_sz;
+                    const uint32_t ph = (n_unit / n_sz) & 1;
+                    if (!lane_wait(&bar.sz_empty[szb], ph ^ 1, wc))
+                        break;
                     uint8_t *dst = sz_base + szb * L.sz_stride;
                     mbar_arrive_expect_tx(&bar.sz_full[szb], 4 * hb);
                     bulk_load_nohint(dst, p.sc + static_cast<int64_t>(row0) * p.G, hb,
@@ -590,29 +768,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                      &bar.sz_full[szb]);
                     bulk_load_nohint(dst + 3 * hb, p.zp + static_cast<int64_t>(row1) * p.G, hb,
                                      &bar.sz_full[szb]);
+                    issued_sz |= 1u << szb;
+                    issue_ph_sz = (issue_ph_sz & ~(1u << szb)) | (ph << szb);
                 }
-                issued_sz |= 1u << szb;
-                issue_ph_sz = (issue_ph_sz & ~(1u << szb)) | (ph_sz << szb);
-                if (++szb == n_sz) {
-                    szb = 0;
-                    ph_sz ^= 1;
-                }
-                for (int kc = 0; kc < p.n_kchunks; kc++) {
-                    if (!lane_wait(&bar.w_empty[sa], ph_a ^ 1, abort_flag, status)) {
+                const int gs0 = n_unit * p.n_kchunks;
+                for (int kc = (gs0 & 1) == gp ? 0 : 1; kc < p.n_kchunks; kc += 2) {
+                    const int g = gs0 + kc;
+                    const int sa = g % kStagesW;
+                    const uint32_t ph = (g / kStagesW) & 1;
+                    if (!lane_wait(&bar.w_empty[sa], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
                     uint8_t *dst = stage_w + sa * kStageWBytes;
                     mbar_arrive_expect_tx(&bar.w_full[sa], kStageWBytes);
                     tma_load_2d(dst, &p.tmap_w, kc * 128, row0, &bar.w_full[sa], pol);
-                    tma_load_2d(dst + kStageWBytes / 2, &p.tmap_w, kc * 128, row1, &bar.w_full[sa],
-                                pol);
+                    tma_load_2d(dst + kStageWBytes / 2, &p.tmap_w, kc * 128, row1,
+                                &bar.w_full[sa], pol);
                     issued_a |= 1u << sa;
-                    issue_ph_a = (issue_ph_a & ~(1u << sa)) | (ph_a << sa);
-                    if (++sa == kStagesW) {
-                        sa = 0;
-                        ph_a ^= 1;
-                    }
+                    issue_ph_a = (issue_ph_a & ~(1u << sa)) | (ph << sa);
                 }
             }
             if (*abort_flag) {   // let our own copies land before the CTA exits
@@ -649,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const Job J = decode_job(jp, offs, p.E, job);
                     const int s = b_seq & 1;
                     const uint32_t ph = (b_seq >> 1) & 1;
-                    if (!lane_wait(&bar.b_empty[s], ph ^ 1, abort_flag, status)) {
+                    if (!lane_wait(&bar.b_empty[s], ph ^ 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -669,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint32_t bytes = static_cast<uint32_t>(J.n) * 128 * kcols;
                     // column blocks 0 .. K / 64, the last one the group sums
                     for (int k_lo = 0; k_lo <= K; k_lo += 64 * kcols) {
-                        if (!lane_wait(&bar.b_empty[sb], ph_b ^ 1, abort_flag, status)) {
+                        if (!lane_wait(&bar.b_empty[sb], ph_b ^ 1, wc)) {
                             ok = false;
                             break;
                         }
@@ -693,128 +867,121 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
     } else if (warp >= kFirstDqWarp && warp < kFirstDqWarp + kNumDqWarps) {
         // ---------------------------------------------------------- dequant
-        // Warp (q4, h) expands sub-chunk h (codes 128 h .. 128 h + 127) of
-        // every stage for its 32 rows into the A buffers of ring h.  The
-        // loop is pipelined by one item: the tensor-memory stores of item i
-        // are waited for (and item i handed to the issuers) only after item
-        // i + 1 has been loaded and computed, so the store latency overlaps
-        // that work.
+        // Warp (q4, r), r = 2 gp + h: for every stage whose global index has
+        // parity gp, expands sub-chunk h (codes 128 h .. 128 h + 127) for its
+        // 32 rows into ring r's A buffer.  The other stages it skips (the
+        // other two rings take them), so each of its sub-chunks has two
+        // stages' time.  The stage count is even, so a warp touches only the stage
+        // slots of its parity, and every phase of them.
         const int q4 = warp & 3;
-        const int h = (warp - kFirstDqWarp) >> 2;
+        const int r = (warp - kFirstDqWarp) >> 2;
+        const int gp = r >> 1, h = r & 1;
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        int sa = 0, szb = 0;
-        uint32_t ph_a = 0, ph_sz = 0;
-        uint32_t ring_slot = 0, ring_ph = 0;
-        int pend_buf = -1;      // buffer whose stores are in flight, not yet handed over
+        const uint32_t a_col0 = tmem + lane_base + static_cast<uint32_t>(r) * kSubCols;
+        int szb = 0;
+        uint32_t ph_sz = 0, a_ph = 0, n_unit = 0;
         const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
-        // the four 16-byte chunks of this warp's half of a row, swizzled
-        uint32_t code_off[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-            code_off[i] = static_cast<uint32_t>(row * 128 + (((4 * h + i) ^ (row & 7)) << 4));
-        // wait for the pending stores and hand their buffer (both halves) over
-        auto flush = [&]() {
-            if (pend_buf >= 0) {
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                mbar_arrive_elect(&bar.a_full[2 * pend_buf]);
-                mbar_arrive_elect(&bar.a_full[2 * pend_buf + 1]);
-                pend_buf = -1;
-            }
-        };
-        // the next free buffer of this ring (its previous MMAs complete)
-        auto claim = [&](int *buf) -> bool {
-            *buf = h * kRingBufs + static_cast<int>(ring_slot);
-            if (!warp_all_wait(&bar.a_empty[*buf], ring_ph ^ 1, abort_flag, status))
+        // this warp's half of a row: 16-byte chunks 4 h .. 4 h + 3, swizzled
+        const uint32_t row_off = static_cast<uint32_t>(row * 128);
+        const uint32_t sw = static_cast<uint32_t>(row & 7);
+        // claim the ring's buffer (its previous MMAs complete)
+        auto claim = [&]() -> bool {
+            if (!warp_all_wait(&bar.a_empty[r], a_ph ^ 1, wc))
                 return false;
-            if (++ring_slot == kRingBufs) {
-                ring_slot = 0;
-                ring_ph ^= 1;
-            }
+            a_ph ^= 1;
             tc_fence_after();
             return true;
         };
+        auto hand_over = [&]() {
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            mbar_arrive_elect(&bar.a_full[r]);
+        };
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            if (!warp_all_wait(&bar.sz_full[szb], ph_sz, abort_flag, status))
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
+            if (!warp_all_wait(&bar.sz_full[szb], ph_sz, wc))
                 break;
+            const int gs0 = static_cast<int>(n_unit) * p.n_kchunks;   // the unit's first stage
             const uint32_t s_addr = sz_base_s + szb * L.sz_stride + 2 * row * p.G;
             const uint32_t z_addr = s_addr + 2 * kTileRows * p.G;
-            uint32_t smax = 0;
-            for (int g = 0; g < p.G; g++)
-                smax = max(smax, lds_u16(s_addr + 2 * g) & 0x7FFFu);
-            const int c = row_exponent(smax);
+            const int c = row_exponent(row_smax(s_addr, p.G));
             const float scale_s = exp2i(24 - c), scale_c = exp2i(-c);
             for (int kc = 0; kc < p.n_kchunks; kc++) {
-                if (!warp_all_wait(&bar.w_full[sa], ph_a, abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
+                const int g = gs0 + kc;
+                if ((g & 1) != gp)
+                    continue;
+                const int sa = g % kStagesW;
                 const int j = 2 * kc + h;                 // sub-chunk of the unit
                 const bool mine = j < n_sub;
                 const bool tail = mine && half_tail && j == n_sub - 1;   // 64 codes
-                const uint32_t rp = stage_w_s + sa * kStageWBytes;
+                // groups of the two 64-code halves (the same group for g128),
+                // their constants from the unit's scale stage before the codes
+                // arrive
+                const uint32_t g0 = static_cast<uint32_t>(j * kSubK) >> p.group_shift;
+                const uint32_t g1 = static_cast<uint32_t>(j * kSubK + 64) >> p.group_shift;
+                GroupK k0{};
+                if (mine)
+                    k0 = group_consts(lds_u16(s_addr + 2 * g0), lds_u16(z_addr + 2 * g0), scale_s,
+                                      scale_c);
+                if (!warp_all_wait(&bar.w_full[sa], (g / kStagesW) & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rp = stage_w_s + sa * kStageWBytes + row_off;
                 uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0, v3 = v0;
                 if (mine) {
-                    v0 = lds128(rp + code_off[0]);
-                    v1 = lds128(rp + code_off[1]);
+                    v0 = lds128(rp + (((4 * h + 0) ^ sw) << 4));
+                    v1 = lds128(rp + (((4 * h + 1) ^ sw) << 4));
                     if (!tail) {
-                        v2 = lds128(rp + code_off[2]);
-                        v3 = lds128(rp + code_off[3]);
+                        v2 = lds128(rp + (((4 * h + 2) ^ sw) << 4));
+                        v3 = lds128(rp + (((4 * h + 3) ^ sw) << 4));
                     }
                 }
                 __syncwarp();
                 mbar_arrive_elect(&bar.w_empty[sa]);
-                if (++sa == kStagesW) {
-                    sa = 0;
-                    ph_a ^= 1;
-                }
                 if (!mine)
                     continue;
-                // groups of the two 64-code halves (the same group for g128)
-                const uint32_t g0 = static_cast<uint32_t>(j * kSubK) >> p.group_shift;
-                const uint32_t g1 = static_cast<uint32_t>(j * kSubK + 64) >> p.group_shift;
-                const GroupK k0 =
-                    group_consts(lds_u16(s_addr + 2 * g0), lds_u16(z_addr + 2 * g0), scale_s, scale_c);
-                const GroupK k1 = g1 == g0 ? k0
-                                           : group_consts(lds_u16(s_addr + 2 * g1),
-                                                          lds_u16(z_addr + 2 * g1), scale_s, scale_c);
-                uint32_t o[32];
+                uint32_t o[16];
                 dequant_word(v0.x, k0.S, k0.S16, k0.C, &o[0]);
                 dequant_word(v0.y, k0.S, k0.S16, k0.C, &o[4]);
                 dequant_word(v0.z, k0.S, k0.S16, k0.C, &o[8]);
                 dequant_word(v0.w, k0.S, k0.S16, k0.C, &o[12]);
-                dequant_word(v1.x, k0.S, k0.S16, k0.C, &o[16]);
-                dequant_word(v1.y, k0.S, k0.S16, k0.C, &o[20]);
-                dequant_word(v1.z, k0.S, k0.S16, k0.C, &o[24]);
-                dequant_word(v1.w, k0.S, k0.S16, k0.C, &o[28]);
-                flush();            // the previous item's stores, issued one item ago
-                int buf;
-                if (!claim(&buf)) {
+                if (!claim()) {
                     ok = false;
                     break;
                 }
-                const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
-                tmem_st_32x32b_x32(a_col, o);
-                if (!tail) {        // (a 64-code tail has no second half: its issuer only commits)
-                    // o was read by the store at issue and is free again
+                if (j == 0)
+                    row_scale[(n_unit & (kRowScaleSets - 1)) * kTileRows + row] = exp2i(c);
+                // o is read by each store at issue and is free again after it
+                tmem_st_32x32b_x16(a_col0, o);
+                dequant_word(v1.x, k0.S, k0.S16, k0.C, &o[0]);
+                dequant_word(v1.y, k0.S, k0.S16, k0.C, &o[4]);
+                dequant_word(v1.z, k0.S, k0.S16, k0.C, &o[8]);
+                dequant_word(v1.w, k0.S, k0.S16, k0.C, &o[12]);
+                tmem_st_32x32b_x16(a_col0 + 16, o);
+                if (!tail) {        // (a 64-code tail has no second half)
+                    const GroupK k1 = g1 == g0 ? k0
+                                               : group_consts(lds_u16(s_addr + 2 * g1),
+                                                              lds_u16(z_addr + 2 * g1), scale_s,
+                                                              scale_c);
                     dequant_word(v2.x, k1.S, k1.S16, k1.C, &o[0]);
                     dequant_word(v2.y, k1.S, k1.S16, k1.C, &o[4]);
                     dequant_word(v2.z, k1.S, k1.S16, k1.C, &o[8]);
                     dequant_word(v2.w, k1.S, k1.S16, k1.C, &o[12]);
-                    dequant_word(v3.x, k1.S, k1.S16, k1.C, &o[16]);
-                    dequant_word(v3.y, k1.S, k1.S16, k1.C, &o[20]);
-                    dequant_word(v3.z, k1.S, k1.S16, k1.C, &o[24]);
-                    dequant_word(v3.w, k1.S, k1.S16, k1.C, &o[28]);
-                    tmem_st_32x32b_x32(a_col + 32, o);
+                    tmem_st_32x32b_x16(a_col0 + 32, o);
+                    dequant_word(v3.x, k1.S, k1.S16, k1.C, &o[0]);
+                    dequant_word(v3.y, k1.S, k1.S16, k1.C, &o[4]);
+                    dequant_word(v3.z, k1.S, k1.S16, k1.C, &o[8]);
+                    dequant_word(v3.w, k1.S, k1.S16, k1.C, &o[12]);
+                    tmem_st_32x32b_x16(a_col0 + 48, o);
                 }
-                pend_buf = buf;
+                hand_over();
             }
             if (!ok)
                 break;
-            if (p.corr_ring == h) {
+            if (r == corr_ring(gs0 & 1, p.n_kchunks)) {
                 // The correction sub-chunk: C = -s z 2^-c rounded to fp16 (the
                 // constant of every dequantised weight of the group) leaves
                 // the part C_lo = fp16(C_exact - C).  The activations carry
@@ -826,41 +993,42 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 // down (four sum columns per group): both halves of words
                 // 2 i' and 2 i' + 1 of step t hold group 4 t + i'
                 constexpr int kRep = GATE_UP ? 1 : 4;
-                uint32_t cw[4][8];
+                if (!claim())
+                    break;
 #pragma unroll
-                for (int t = 0; t < 4; t++)
+                for (int t = 0; t < 4; t++) {
+                    if (t >= p.n_corr_mma)
+                        break;
+                    // the step's groups: all loads first (independent), then the math
+                    constexpr int kNg = 16 / kRep;
+                    uint32_t sb[kNg], zb[kNg];
 #pragma unroll
-                    for (int gi = 0; gi < 16 / kRep; gi++) {
-                        const int g = (16 / kRep) * t + gi;
-                        uint32_t lo = 0;
-                        if (t < p.n_corr_mma && g < p.G) {
-                            const float sv = __half2float(__ushort_as_half(
-                                static_cast<unsigned short>(lds_u16(s_addr + 2 * g))));
-                            const float zv = __half2float(__ushort_as_half(
-                                static_cast<unsigned short>(lds_u16(z_addr + 2 * g))));
-                            const float cx = -(sv * zv) * scale_c;      // exact
-                            const float chi = __half2float(__float2half_rn(cx));
-                            lo = __half_as_ushort(__float2half_rn(cx - chi));   // cx - chi exact
-                        }
+                    for (int gi = 0; gi < kNg; gi++) {
+                        const int g = kNg * t + gi;
+                        sb[gi] = g < p.G ? lds_u16(s_addr + 2 * g) : 0u;
+                        zb[gi] = g < p.G ? lds_u16(z_addr + 2 * g) : 0u;
+                    }
+                    uint32_t cw[8];
+#pragma unroll
+                    for (int gi = 0; gi < kNg; gi++) {
+                        const float sv = __half2float(__ushort_as_half(static_cast<unsigned short>(sb[gi])));
+                        const float zv = __half2float(__ushort_as_half(static_cast<unsigned short>(zb[gi])));
+                        const float cx = -(sv * zv) * scale_c;          // exact
+                        const float chi = __half2float(__float2half_rn(cx));
+                        // cx - chi is exact; zero past the last group (s = z = 0)
+                        const uint32_t lo = __half_as_ushort(__float2half_rn(cx - chi));
                         if constexpr (kRep == 1) {
                             if (gi & 1)
-                                cw[t][gi >> 1] |= lo << 16;
+                                cw[gi >> 1] |= lo << 16;
                             else
-                                cw[t][gi >> 1] = lo;
+                                cw[gi >> 1] = lo;
                         } else {
-                            cw[t][2 * gi] = cw[t][2 * gi + 1] = lo | (lo << 16);
+                            cw[2 * gi] = cw[2 * gi + 1] = lo | (lo << 16);
                         }
                     }
-                flush();
-                int buf;
-                if (!claim(&buf))
-                    break;
-                const uint32_t a_col = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
-#pragma unroll
-                for (int t = 0; t < 4; t++)
-                    if (t < p.n_corr_mma)       // the correction's MMAs are all in half 0
-                        tmem_st_32x32b_x8(a_col + 8 * t, cw[t]);
-                pend_buf = buf;
+                    tmem_st_32x32b_x8(a_col0 + 8 * t, cw);
+                }
+                hand_over();
             }
             __syncwarp();
             mbar_arrive_elect(&bar.sz_empty[szb]);
@@ -869,8 +1037,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 ph_sz ^= 1;
             }
         }
-        if (ok)
-            flush();
     } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kNumEpiWarps) {
         // ---------------------------------------------------------- epilogue
         const int q4 = warp & 3;
@@ -886,101 +1052,133 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int pnl = u % p.n_panels;
             const int set = n_unit & 1;
             const uint32_t acc_ph = (n_unit >> 1) & 1;
-            // this lane's weight row, for its exponent (the same rule as the
-            // dequant warps, from the same scales, read here from global
-            // memory while the unit's MMAs run)
-            const int64_t grow =
-                GATE_UP ? static_cast<int64_t>(J.e) * p.R + (row < 64 ? 0 : p.m_up) + pnl * 64 +
-                              (row & 63)
-                        : static_cast<int64_t>(J.e) * p.R + pnl * 128 + row;
-            uint32_t smax = 0;
-            for (int g = 0; g < p.G; g++)
-                smax = max(smax, static_cast<uint32_t>(__ldg(p.sc + grow * p.G + g)) & 0x7FFFu);
-            const float factor = exp2i(row_exponent(smax));
             // the assignment of every slot of the job, fetched early (gate_up:
             // padding slots get zero rows; down: rows go to y by assignment)
             const int my_a = lane < J.n ? __ldg(p.sorted_ids + J.start + lane) : -1;
-            if (!warp_all_wait(&bar.acc_full[set], acc_ph, abort_flag, status))
+            if (!warp_all_wait(&bar.acc_full[set], acc_ph, wc))
                 break;
             tc_fence_after();
-            float v[kMaxN];
-            {
-                // the accumulator chains that received MMAs, added in a fixed order
+            // 2^c of this lane's weight row, published by the dequant warps
+            const float factor = row_scale[(n_unit & (kRowScaleSets - 1)) * kTileRows + row];
+            const int mask = p.acc_mask[(n_unit * p.n_kchunks) & 1];
+            uint16_t *hout = reinterpret_cast<uint16_t *>(p.out);
+            float *yout = reinterpret_cast<float *>(p.out);
+            const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);    // gate_up
+            bool range = false;
+            // two passes of 16 slots (one for a 16-slot job)
+#pragma unroll 1
+            for (int half = 0; half < 2; half++) {
+                if (half * 16 >= J.n)
+                    break;
+                float v[16];
+                {
+                    // the accumulators that received MMAs, added in a fixed order
 #pragma unroll
-                for (int i = 0; i < kMaxN; i++)
-                    v[i] = 0.0f;
+                    for (int i = 0; i < 16; i++)
+                        v[i] = 0.0f;
 #pragma unroll
-                for (int c = 0; c < kChains; c++) {
-                    if (!(p.acc_mask >> c & 1))
-                        continue;
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(
-                        tmem + lane_base + kAccCol + set * (kChains * kMaxN) + c * kMaxN, r);
+                    for (int c = 0; c < kChains; c++) {
+                        if (!(mask >> c & 1))
+                            continue;
+                        uint32_t rr[16];
+                        tmem_ld_32x32b_x16(tmem + lane_base + kAccCol + set * (kChains * kMaxN) +
+                                               c * kMaxN + 16 * half,
+                                           rr);
 #pragma unroll
-                    for (int i = 0; i < kMaxN; i++)
-                        v[i] += __uint_as_float(r[i]);
+                        for (int i = 0; i < 16; i++)
+                            v[i] += __uint_as_float(rr[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        v[i] *= factor;
                 }
+                if (half * 16 + 16 >= J.n) {   // the set's last read: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    mbar_arrive_elect(&bar.acc_empty[set]);
+                }
+                if constexpr (GATE_UP) {
+                    // h of this panel: 64 intermediates = group pnl of the down
+                    // GEMM's contraction; this warp holds 16 of them and also
+                    // writes their sum (of the fp16 values) to sum column
+                    // 4 pnl + q4 of the row, the down GEMM's correction input
 #pragma unroll
-                for (int i = 0; i < kMaxN; i++)
-                    v[i] *= factor;
-            }
-            tc_fence_before();
-            __syncwarp();
-            mbar_arrive_elect(&bar.acc_empty[set]);
-            if constexpr (GATE_UP) {
-                // h of this panel: 64 intermediates = group pnl of the down
-                // GEMM's contraction; this warp holds 16 of them and also
-                // writes their sum (of the fp16 values) to sum column
-                // 4 pnl + q4 of the row, the down GEMM's correction input
-                uint16_t *hout = reinterpret_cast<uint16_t *>(p.out);
-                const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);
-                bool range = false;
+                    for (int i = 0; i < 16; i += 2) {
+                        const float send = is_gate ? v[i + 1] : v[i];
+                        const float recv = __shfl_xor_sync(full, send, 16);
+                        const float gv = is_gate ? v[i] : recv;
+                        const float uv = is_gate ? recv : v[i + 1];
+                        const int si = 16 * half + i + (is_gate ? 0 : 1);
+                        const int a = __shfl_sync(full, my_a, si);
+                        const bool real = static_cast<unsigned>(a) < static_cast<unsigned>(p.A);
+                        const float hv = gelu_tanh(gv) * uv;
+                        range |= real && !(fabsf(hv) <= 65504.0f);
+                        const uint16_t hq = real ? static_cast<uint16_t>(f16x2_sat(hv, 0.0f)) : 0;
+                        uint16_t *hrow = hout + (J.start + si) * static_cast<int64_t>(p.h_stride);
+                        hrow[pos] = hq;
+                        // lanes 0-15 sum slot i, lanes 16-31 slot i + 1 (fixed tree)
+                        float part = __half2float(__ushort_as_half(hq));
+                        part += __shfl_xor_sync(full, part, 8);
+                        part += __shfl_xor_sync(full, part, 4);
+                        part += __shfl_xor_sync(full, part, 2);
+                        part += __shfl_xor_sync(full, part, 1);
+                        if ((lane & 15) == 0) {
+                            range |= !(fabsf(part) <= 65504.0f);
+                            hrow[p.out_cols + 4 * pnl + q4] =
+                                static_cast<uint16_t>(f16x2_sat(part, 0.0f));
+                            if (pnl == 0)   // sum columns past the last group, read by
+                                            // the correction's last MMA step: zero
+                                for (int c = 4 * p.h_groups + q4;
+                                     c < 16 * ((p.h_groups + 3) / 4); c += 4)
+                                    hrow[p.out_cols + c] = 0;
+                        }
+                    }
+                } else {
+                    const int col = pnl * 128 + row;
 #pragma unroll
-                for (int i = 0; i < kMaxN; i += 2) {
-                    if (i >= J.n)
-                        break;
-                    const float send = is_gate ? v[i + 1] : v[i];
-                    const float recv = __shfl_xor_sync(full, send, 16);
-                    const float gv = is_gate ? v[i] : recv;
-                    const float uv = is_gate ? recv : v[i + 1];
-                    const int si = i + (is_gate ? 0 : 1);
-                    const int a = __shfl_sync(full, my_a, si);
-                    const bool real = static_cast<unsigned>(a) < static_cast<unsigned>(p.A);
-                    const float hv = gelu_tanh(gv) * uv;
-                    range |= real && !(fabsf(hv) <= 65504.0f);
-                    const uint16_t hq = real ? static_cast<uint16_t>(f16x2_sat(hv, 0.0f)) : 0;
-                    uint16_t *hrow = hout + (J.start + si) * static_cast<int64_t>(p.h_stride);
-                    hrow[pos] = hq;
-                    // lanes 0-15 sum slot i, lanes 16-31 slot i + 1 (fixed tree)
-                    float part = __half2float(__ushort_as_half(hq));
-                    part += __shfl_xor_sync(full, part, 8);
-                    part += __shfl_xor_sync(full, part, 4);
-                    part += __shfl_xor_sync(full, part, 2);
-                    part += __shfl_xor_sync(full, part, 1);
-                    if ((lane & 15) == 0) {
-                        range |= !(fabsf(part) <= 65504.0f);
-                        hrow[p.out_cols + 4 * pnl + q4] =
-                            static_cast<uint16_t>(f16x2_sat(part, 0.0f));
-                        if (pnl == 0)   // sum columns past the last group, read by the
-                                        // correction's last MMA step: zero
-                            for (int c = 4 * p.h_groups + q4; c < 16 * ((p.h_groups + 3) / 4);
-                                 c += 4)
-                                hrow[p.out_cols + c] = 0;
+                    for (int i = 0; i < 16; i++) {
+                        const int a = __shfl_sync(full, my_a, 16 * half + i);
+                        if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
+                            yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
                     }
                 }
+            }
+            if constexpr (!GATE_UP) {
+                if (p.comb_cnt) {
+                    // this unit's y columns are stored: hand the unit to the
+                    // combine warps (one phase of y_full per unit)
+                    const int ys = static_cast<int>(n_unit % kYSets);
+                    if (!warp_all_wait(&bar.y_empty[ys], ((n_unit / kYSets) & 1) ^ 1,
+                                       wc))
+                        break;
+                    __syncwarp();
+                    mbar_arrive_elect(&bar.y_full[ys]);
+                }
+            }
+            if constexpr (GATE_UP) {
                 if (__any_sync(full, range) && lane == 0 && status)
                     atomicOr(status, kDevFp16Range);
-            } else {
-                float *yout = reinterpret_cast<float *>(p.out);
-                const int col = pnl * 128 + row;
-#pragma unroll
-                for (int i = 0; i < kMaxN; i++) {
-                    if (i >= J.n)
-                        break;
-                    const int a = __shfl_sync(full, my_a, i);
-                    if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
-                        yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
-                }
+            }
+        }
+    } else if (warp == kWarpComb && p.comb_cnt) {
+        // ------------------------------------------------- the folded combine
+        if constexpr (GATE_UP) {
+            // the counters, before the down launch that counts them
+            for (int t = blockIdx.x; t < p.M; t += gridDim.x)
+                fold_prepare_token(t, lane, p.topk_ids, p.k, p.E, p.comb_d, p.comb_cnt,
+                                   p.comb_out);
+        } else {
+            if (p.early_schedule)
+                pdl_wait();       // the counters are the preceding kernel's output
+            uint32_t n_unit = 0;
+            for (int u = blockIdx.x; u < n_units; u += gridDim.x, n_unit++) {
+                const int ys = static_cast<int>(n_unit % kYSets);
+                if (!warp_all_wait(&bar.y_full[ys], (n_unit / kYSets) & 1, wc))
+                    break;
+                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                combine_count(p, J, u % p.n_panels, lane, comb_list, comb_count);
+                __syncwarp();
+                mbar_arrive_elect(&bar.y_empty[ys]);
             }
         }
     }
@@ -991,6 +1189,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (warp == kWarpAlloc) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if constexpr (!GATE_UP) {
+        // the CTA's completed combines, one (token, panel) per warp at a time
+        if (p.comb_cnt && !*abort_flag) {
+            const int n = min(*comb_count, kCombListCap);
+            for (int i = warp; i < n; i += kNumWarps)
+                combine_panel(p, comb_list[i] / p.n_panels, comb_list[i] % p.n_panels, lane);
+        }
     }
 }
 
@@ -1063,6 +1269,17 @@ bool encode_act(EncodeTiledFn encode, CUtensorMap *map, const void *base, int64_
 
 }  // namespace
 
+bool grouped_gemm_fits(bool gate_up, int K, int group, int E)
+{
+    if (group <= 0 || K % group != 0)
+        return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    const SmemLayout L = smem_layout(K / group, E, gate_up);
+    return static_cast<size_t>(L.total) + 1024 <= static_cast<size_t>(device_info(dev).smem_optin);
+}
+
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream,
                                 const char **why)
 {
@@ -1099,27 +1316,28 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         return cudaErrorInvalidValue;
     }
     a.n_corr_mma = (a.G * corr_rep + 15) / 16;
-    {
-        // the correction goes to the ring of a 64-code tail (which has the
-        // lighter load), else to the ring whose turn follows the last
-        // sub-chunk; issuer 2 h + p gets K steps 4p .. 4p + 3 of the
-        // sub-chunks of ring h, and the correction's are all in half 0
-        const bool tail = (q.K % kSubK) != 0;
-        a.corr_ring = tail ? (a.n_sub - 1) & 1 : a.n_sub & 1;
-        a.acc_mask = 1 << (2 * a.corr_ring);
-        for (int j = 0; j < a.n_sub; j++) {
-            const int n = (tail && j == a.n_sub - 1) ? 4 : 8;
-            a.acc_mask |= 1 << (2 * (j & 1));
-            if (n >= 5)
-                a.acc_mask |= 1 << (2 * (j & 1) + 1);
-        }
+    // the accumulators (issuers) that receive MMAs in a unit, for either
+    // parity of its first stage's global index
+    for (int gp0 = 0; gp0 < 2; gp0++) {
+        a.acc_mask[gp0] = 1 << corr_ring(gp0, a.n_kchunks);
+        for (int j = 0; j < a.n_sub; j++)
+            a.acc_mask[gp0] |= 1 << unit_ring(gp0, j);
     }
     a.h_stride = q.gate_up ? q.R / 2 + 64 : 0;
     a.h_groups = q.gate_up ? (q.R / 2) / 64 : 0;
     a.early_schedule = q.early_schedule ? 1 : 0;
+    a.topk_ids = q.topk_ids;
+    a.topk_w = q.topk_w;
+    a.comb_cnt = q.comb_cnt;
+    a.comb_out = q.comb_out;
+    a.M = q.M;
+    a.k = q.k;
+    a.comb_d = q.comb_d;
+    a.wait_ns = q.wait_ns;
+    a.test_withhold_sz = q.test_withhold_sz ? 1 : 0;
     const bool resident = !q.gate_up && b_fits_resident(q.K);
 
-    const SmemLayout L = smem_layout(a.G, a.E);
+    const SmemLayout L = smem_layout(a.G, a.E, q.gate_up);
     const size_t smem = static_cast<size_t>(L.total) + 1024;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);

@@ -62,6 +62,10 @@ cudaError_t launch_identity_align_gather(const uint16_t *x, int M, int d, int pa
                                          cudaStream_t stream);
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int M, int k,
                            int d, int E, uint16_t *out, cudaStream_t stream);
+// Sets the counters [M, d/128] of the combine folded into the down GEMM
+// and zeroes the out rows of tokens without a valid expert id.
+cudaError_t launch_combine_prepare(const int32_t *ids, int M, int k, int E, int d, int32_t *cnt,
+                                   uint16_t *out, cudaStream_t stream);
 
 // Grouped W4A16 GEMM (tcgen05).  gate_up=true: xg fp16 -> h fp16 with the
 // gated activation; gate_up=false: h fp16 -> y fp32.
@@ -83,7 +87,28 @@ struct GroupedGemmProblem {
     // down may then read its schedule, and stream its weights, before its
     // grid-dependency wait.  Activations are read only after that wait.
     bool early_schedule = false;
+    // The layer's fixed-order combine folded into the down launch (both
+    // launches get comb_cnt; NULL: neither does anything of it).  gate_up
+    // sets the counters [M][comb_d/128] and zeroes the out rows of tokens
+    // without a valid expert id; down writes out [M, comb_d] bf16 =
+    // sum_j w_j y_j (bit-identical to launch_combine) as tokens complete.
+    const int32_t *topk_ids = nullptr;   // [M, k]
+    const float *topk_w = nullptr;       // [M, k] (down)
+    int32_t *comb_cnt = nullptr;
+    uint16_t *comb_out = nullptr;
+    int comb_d = 0;
+    // test hooks (w4_test_pipeline_hooks): the pipeline wait limit, and
+    // withholding the first unit's scale/zero copy so that waits run out
+    uint64_t wait_ns = 1000000000ull;
+    bool test_withhold_sz = false;
 };
+
+// The test hooks of the calling thread, applied to its grouped GEMM launches.
+struct PipelineTestHooks {
+    uint64_t wait_ns = 1000000000ull;
+    bool withhold_sz = false;
+};
+PipelineTestHooks &pipeline_test_hooks();
 
 // The dense W4A16 GEMM (dense_gemm.cu): y [M, N] bf16 = xg [Mpad, K] fp16
 // (block order, rows past M zero) . deq(W)^T, W [N, K/2] u8 with s, z
@@ -102,6 +127,11 @@ bool dense_gemm_supported(int M, int N, int K, int group);
 int dense_gemm_splits(int M, int N, int K);
 size_t dense_gemm_partial_bytes(int M, int N, int K);
 cudaError_t launch_dense_gemm(const DenseGemmProblem &p, cudaStream_t stream, const char **why);
+
+// Whether the grouped GEMM's shared memory (code, activation and scale/zero
+// stages, schedule) fits the current device for contraction dim K with
+// this group and expert count; launch_grouped_gemm rejects what does not.
+bool grouped_gemm_fits(bool gate_up, int K, int group, int E);
 
 // Returns cudaSuccess, or an error; *why receives a static description when
 // the problem is rejected before launch (shape or resource limits).

@@ -22,6 +22,26 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// ------------------------------------------------- gpu-scope synchronisation
+// atomicAdd with release semantics at gpu scope: this thread's earlier
+// writes, and those ordered before it by CTA-scope synchronisation, are
+// visible to a thread that reads the new value and then acquires.
+__device__ __forceinline__ int atom_add_release_gpu(int *addr, int v)
+{
+    int old;
+    asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(addr), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Acquire-release fence at gpu scope (the acquire side of the above).
+__device__ __forceinline__ void fence_acq_rel_gpu()
+{
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
@@ -215,6 +235,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Prefetch of one 2-D tile (the tensor map's box at x, y) from global memory
+// into L2; no shared memory, no completion.  Coordinates as tma_load_2d.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Prefetch of `bytes` (a multiple of 16) at the 16-byte aligned src into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled TMA load without a cache hint.
 __device__ __forceinline__ void tma_load_2d_nohint(void *dst, const CUtensorMap *map, int x, int y,
                                                    uint64_t *bar)
@@ -346,6 +382,30 @@ __device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Up to four MMAs as in tc_mma4_ts_commit_elect, without the commit.
+__device__ __forceinline__ void tc_mma4_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                                 uint64_t b1, uint64_t b2, uint64_t b3,
+                                                 uint32_t idesc, int n, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, q0, q1, q2, q3, acc, on;\n\t"
+        ".reg .b32 a1, a2, a3;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+        "setp.ne.b32 acc, %7, 0;\n\t"
+        "setp.eq.b32 on, %7, %7;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.gt.and.s32 q0, %8, 0, e;\n\t"
+        "setp.gt.and.s32 q1, %8, 1, e;\n\t"
+        "setp.gt.and.s32 q2, %8, 2, e;\n\t"
+        "setp.gt.and.s32 q3, %8, 3, e;\n\t"
+        "@q0 tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %6, acc;\n\t"
+        "@q1 tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %6, on;\n\t"
+        "@q2 tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %6, on;\n\t"
+        "@q3 tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %6, on;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(accumulate), "r"(n)
         : "memory");
 }
 
