@@ -14,9 +14,8 @@ order), sixteen dequantisation warps (lane quarter x ring; ring 2 gp + h
 takes half h of the stages whose index in the CTA's stage sequence has
 parity gp, so a warp skips the other stages; ring 1 or 3, half 1 of the
 parity the unit's first stage does not have, also produces the unit's
-group-constant correction), four epilogue warps (which also read the row
-scales the dequant warps publish per unit), and the warp of the combine
-folded into the down GEMM (one phase of y_full per unit).  Every wait is
+group-constant correction) and four epilogue warps (which also read the row
+scales the dequant warps publish per unit).  Every wait is
 checked against the exact condition: the phase it stands for, counted from
 per-stage uses kept apart from the kernel's parity variables, has completed
 exactly when the parity test says so.  Unit lists mix jobs of 16 and 32 slots over several panels; contraction
@@ -36,7 +35,6 @@ STAGE_B_BYTES = 32768
 DQ_WARPS, EPI_WARPS = 16, 4
 CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 128, 32, 49152
 ROW_SCALE_SETS = 4
-COMB_WARPS, Y_SETS = 1, 4
 
 
 def sz_stages(G):
@@ -85,8 +83,6 @@ class Grouped:
         self.a_full = B("a_full", RINGS, 4)
         self.a_empty = B("a_empty", RINGS, 1)
         self.acc_full, self.acc_empty = B("acc_full", SETS, ISSUERS), B("acc_empty", SETS, EPI_WARPS)
-        # the folded combine (down): epilogue -> combine warps, one phase per unit
-        self.y_full, self.y_empty = B("y_full", Y_SETS, EPI_WARPS), B("y_empty", Y_SETS, COMB_WARPS)
         self.sz_full = B("sz_full", self.n_sz, 1)
         self.sz_empty = B("sz_empty", self.n_sz, DQ_WARPS)
         # row-scale tables (dequant -> epilogue), one entry per lane quarter
@@ -235,22 +231,12 @@ class Grouped:
             use[st] += 1
             yield ("rs_read", n_unit, q)
             yield ("arrive", self.acc_empty[st])
-            ys = n_unit % Y_SETS
-            yield ("wait", self.y_empty[ys], ((n_unit // Y_SETS) & 1) ^ 1, n_unit // Y_SETS - 1)
-            yield ("arrive", self.y_full[ys])
-
-    def combine(self):
-        for n_unit, _u in enumerate(self.units):
-            ys = n_unit % Y_SETS
-            yield ("wait", self.y_full[ys], (n_unit // Y_SETS) & 1, n_unit // Y_SETS)
-            yield ("arrive", self.y_empty[ys])
 
     def run(self):
         roles = [self.tma_w(0), self.tma_w(1), self.tma_b()]
         roles += [self.issuer(i) for i in range(ISSUERS)]
         roles += [self.dequant(w // 4, w % 4) for w in range(DQ_WARPS)]   # 4 lane quarters per ring
         roles += [self.epilogue(q) for q in range(EPI_WARPS)]
-        roles += [self.combine() for _ in range(COMB_WARPS)]
         nxt = [next(r, None) for r in roles]
         steps = 0
         while True:

@@ -66,9 +66,10 @@
 //                   of parity 0 of the CTA's stage sequence
 //       warp 27     TMA: the code stages of parity 1
 //       warp 25     TMA: activation slots
-//       warp 26     the combine folded into down (combine_fold.cuh): gate_up
-//                   sets the counters, down counts y panels; every warp
-//                   combines the tokens its CTA completed after the last unit
+//       warp 26     gate_up: sets the counters of the combine folded into
+//                   down (combine_fold.cuh); in down, after its last unit,
+//                   every warp of the CTA counts the CTA's y panels and
+//                   combines the (token, panel) pairs it completed
 //   * Tensor memory (512 columns): A buffers at 64 r, accumulators at
 //     256 + 128 set + 32 chain.
 //   * Every barrier has one producer group and one consumer group that take
@@ -100,10 +101,8 @@ constexpr int kFirstEpiWarp = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kFirstDqWarp = 8;
 constexpr int kNumDqWarps = 16;            // warp 8 + 4 r + q: lane quarter q, ring r
-constexpr int kWarpComb = 26;               // the folded combine (and its counters)
+constexpr int kWarpComb = 26;               // gate_up: sets the folded combine's counters
 constexpr int kNumWarps = 28;
-// y_full / y_empty: epilogue -> combine warps, one phase per unit, four sets
-constexpr int kYSets = 4;
 constexpr int kThreads = 32 * kNumWarps;
 // Ring r = 2 gp + h holds sub-chunk h of the stages whose global index (in
 // the CTA's stage sequence) has parity gp, so every dequant warp works on
@@ -172,11 +171,11 @@ struct GemmArgs {
 };
 
 constexpr int kNumBars = 2 * kStagesW + 2 * kStagesB + 2 * kRings * kRingBufs + 2 + 2 +
-                         2 * kMaxStagesSZ + kNumIssuers + 2 * kYSets;
+                         2 * kMaxStagesSZ + kNumIssuers;
 
 struct Bars {
     uint64_t *w_full, *w_empty, *b_full, *b_empty, *a_full, *a_empty, *acc_full, *acc_empty,
-        *sz_full, *sz_empty, *drain, *y_full, *y_empty;
+        *sz_full, *sz_empty, *drain;
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t *base)
@@ -194,8 +193,6 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base)
     r.sz_full = r.acc_empty + 2;
     r.sz_empty = r.sz_full + kMaxStagesSZ;
     r.drain = r.sz_empty + kMaxStagesSZ;
-    r.y_full = r.drain + kNumIssuers;
-    r.y_empty = r.y_full + kYSets;
     return r;
 }
 
@@ -284,6 +281,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u16(uint32_t saddr)
 {
     unsigned short h;
@@ -302,9 +306,23 @@ __device__ __forceinline__ int row_exponent(uint32_t smax_bits)
 }
 
 // The largest |scale| bit pattern among the G scales of a row in shared
-// memory at s_addr, sixteen independent loads at a time.
+// memory at s_addr: for even G two scales per 32-bit load and a packed
+// 16-bit max, else sixteen independent 16-bit loads at a time.
 __device__ __forceinline__ uint32_t row_smax(uint32_t s_addr, int G)
 {
+    if ((G & 1) == 0) {
+        uint32_t m2 = 0;
+        for (int g0 = 0; g0 < G; g0 += 16) {
+            uint32_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                v[i] = g0 + 2 * i < G ? lds_u32(s_addr + 2 * (g0 + 2 * i)) : 0u;
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                m2 = __vmaxu2(m2, v[i] & 0x7FFF7FFFu);
+        }
+        return max(m2 & 0xFFFFu, m2 >> 16);
+    }
     uint32_t smax = 0;
     for (int g0 = 0; g0 < G; g0 += 16) {
         uint32_t v[16];
@@ -342,10 +360,16 @@ __device__ __forceinline__ GroupK group_consts(uint32_t s_bits, uint32_t z_bits,
     return g;
 }
 
+// gelu_tanh(v) = 0.5 v (1 + tanh(u)), u = sqrt(2/pi) (v + 0.044715 v^3),
+// evaluated as v / (1 + e^(-2u)) (the same function: 1 + tanh(u) =
+// 2 / (1 + e^(-2u))) with the fast exponential and division, a relative
+// error of a few units of fp32 against the fp16 rounding of h that
+// follows; e^(-2u) = inf for large negative v gives the limit -0.
 __device__ __forceinline__ float gelu_tanh(float v)
 {
     const float c = 0.7978845608028654f;   // sqrt(2/pi)
-    return 0.5f * v * (1.0f + tanhf(c * (v + 0.044715f * v * v * v)));
+    const float u = c * fmaf(0.044715f * v, v * v, v);
+    return __fdividef(v, 1.0f + __expf(-2.0f * u));
 }
 
 // A bounded wait by every lane of a warp (each lane observes the phase
@@ -455,14 +479,12 @@ __device__ __forceinline__ void combine_panel(const GemmArgs &p, int t, int pnl,
     *reinterpret_cast<uint2 *>(p.comb_out + static_cast<int64_t>(t) * p.comb_d + col) = pk;
 }
 
-// (down, the combine warp) After the epilogue has stored unit (J, pnl)'s y
-// columns (ordered before this warp by the y_full barrier): one arrival per
-// valid slot of the job on its token's counter of panel pnl (lane i for
-// slot i).  The arrivals are release atomics at gpu scope,
-// which publish the unit's y stores to the CTA that completes the counter;
-// a warp that completed counters acquires the other CTAs' stores with an
-// acquire-release fence.  Completed (token, panel) pairs go to the CTA's
-// list, combined after its last unit (or here, past the list's capacity).
+// (down, after the CTA's last unit and a fence that released its y stores)
+// One arrival per valid slot of unit (J, pnl) on its token's counter of
+// panel pnl (lane i for slot i); a warp that completed counters acquires
+// the other CTAs' y stores with an acquire-release fence.  Completed
+// (token, panel) pairs go to the CTA's list (or, past its capacity, are
+// combined here).
 __device__ __forceinline__ void combine_count(const GemmArgs &p, const Job &J, int pnl, int lane,
                                               int *list, int *count)
 {
@@ -473,8 +495,7 @@ __device__ __forceinline__ void combine_count(const GemmArgs &p, const Job &J, i
         const int a = __ldg(p.sorted_ids + J.start + lane);
         if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A)) {
             t = a / p.k;
-            last = atom_add_release_gpu(p.comb_cnt + fold_counter_index(t, p.n_panels, pnl), 1) ==
-                   p.k - 1;
+            last = atomicAdd(p.comb_cnt + fold_counter_index(t, p.n_panels, pnl), 1) == p.k - 1;
         }
     }
     unsigned done = __ballot_sync(full, last);
@@ -551,10 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int i = 0; i < kNumIssuers; i++)
             mbar_init(&bar.drain[i], 1);
-        for (int i = 0; i < kYSets; i++) {
-            mbar_init(&bar.y_full[i], kNumEpiWarps);
-            mbar_init(&bar.y_empty[i], 1);
-        }
         *abort_flag = 0;
         *comb_count = 0;
         fence_mbar_init();
@@ -1143,43 +1160,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                 }
             }
-            if constexpr (!GATE_UP) {
-                if (p.comb_cnt) {
-                    // this unit's y columns are stored: hand the unit to the
-                    // combine warps (one phase of y_full per unit)
-                    const int ys = static_cast<int>(n_unit % kYSets);
-                    if (!warp_all_wait(&bar.y_empty[ys], ((n_unit / kYSets) & 1) ^ 1,
-                                       wc))
-                        break;
-                    __syncwarp();
-                    mbar_arrive_elect(&bar.y_full[ys]);
-                }
-            }
             if constexpr (GATE_UP) {
                 if (__any_sync(full, range) && lane == 0 && status)
                     atomicOr(status, kDevFp16Range);
             }
         }
     } else if (warp == kWarpComb && p.comb_cnt) {
-        // ------------------------------------------------- the folded combine
+        // ------------------------------------ the folded combine's counters
         if constexpr (GATE_UP) {
-            // the counters, before the down launch that counts them
+            // set before the down launch that counts them
             for (int t = blockIdx.x; t < p.M; t += gridDim.x)
                 fold_prepare_token(t, lane, p.topk_ids, p.k, p.E, p.comb_d, p.comb_cnt,
                                    p.comb_out);
-        } else {
-            if (p.early_schedule)
-                pdl_wait();       // the counters are the preceding kernel's output
-            uint32_t n_unit = 0;
-            for (int u = blockIdx.x; u < n_units; u += gridDim.x, n_unit++) {
-                const int ys = static_cast<int>(n_unit % kYSets);
-                if (!warp_all_wait(&bar.y_full[ys], (n_unit / kYSets) & 1, wc))
-                    break;
-                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
-                combine_count(p, J, u % p.n_panels, lane, comb_list, comb_count);
-                __syncwarp();
-                mbar_arrive_elect(&bar.y_empty[ys]);
-            }
         }
     }
 
@@ -1191,8 +1183,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tmem_dealloc(tmem, kTmemCols);
     }
     if constexpr (!GATE_UP) {
-        // the CTA's completed combines, one (token, panel) per warp at a time
         if (p.comb_cnt && !*abort_flag) {
+            if (p.early_schedule)
+                pdl_wait();        // the counters are the preceding kernel's output
+            // Every y store of this CTA is done (the barrier above); each
+            // thread's fence then releases them to the CTA that completes a
+            // counter.  One arrival per valid slot of each of the CTA's
+            // units on its token's counter of the unit's panel (a warp per
+            // unit, a lane per slot); completed (token, panel) pairs go to the
+            // CTA's list (or are combined at once past its capacity).
+            fence_acq_rel_gpu();
+            for (int n = warp; n * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x) < n_units;
+                 n += kNumWarps) {
+                const int u = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
+                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                combine_count(p, J, u % p.n_panels, lane, comb_list, comb_count);
+            }
+            __syncthreads();
+            // the CTA's completed combines, one (token, panel) per warp at a time
             const int n = min(*comb_count, kCombListCap);
             for (int i = warp; i < n; i += kNumWarps)
                 combine_panel(p, comb_list[i] / p.n_panels, comb_list[i] % p.n_panels, lane);

@@ -23,20 +23,10 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 }
 
 // ------------------------------------------------- gpu-scope synchronisation
-// atomicAdd with release semantics at gpu scope: this thread's earlier
-// writes, and those ordered before it by CTA-scope synchronisation, are
-// visible to a thread that reads the new value and then acquires.
-__device__ __forceinline__ int atom_add_release_gpu(int *addr, int v)
-{
-    int old;
-    asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(addr), "r"(v)
-                 : "memory");
-    return old;
-}
-
-// Acquire-release fence at gpu scope (the acquire side of the above).
+// Acquire-release fence at gpu scope: releases this thread's earlier writes
+// (and those ordered before it by CTA-scope synchronisation) to a thread
+// that reads a later write of this thread and then acquires, and acquires
+// what such a write published.
 __device__ __forceinline__ void fence_acq_rel_gpu()
 {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
