@@ -3,8 +3,8 @@
 
 One step = one pass of the whole layer over one batch: token-to-expert
 alignment with the activation gather, grouped gate_up GEMM with the gated
-activation, grouped down GEMM with the fixed-order combine folded into its
-epilogue (three launches of libw4moe.so on one stream).  The
+activation, grouped down GEMM, fixed-order combine (four launches of
+libw4moe.so on one stream, each a programmatic dependent of the one before).  The
 workload is one 256-token canvas at the pages' layer shape: M=256, d=2816,
 m=704, E=128, top-8, uint4 weights with fp16 scale/zero (groups of 128 for
 gate_up, 64 for down), bf16 activations; inputs are seeded synthetic tensors
@@ -407,22 +407,18 @@ def time_configs(args, gu, dn, dev, status):
         al, xg = w4.w4_moe_align_gather(ids, x, c.E, args.block_m, dev_status=status)
         h = w4.w4_grouped_gemm_gate_up(xg, *gu, al, dev_status=status)
         y = w4.w4_grouped_gemm_down(h, *dn, al, dev_status=status)
-        counters = torch.empty((c.M, c.d // 128), dtype=torch.int32, device=dev)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         gsum = [0.0, 0.0]
         for i in range(12):
             ev[0].record()
             w4.w4_grouped_gemm_gate_up(xg, *gu, al, h=h, dev_status=status)
             ev[1].record()
-            w4.w4_moe_combine_prepare(ids, c.E, c.d, counters=counters, out=out)
+            w4.w4_grouped_gemm_down(h, *dn, al, y=y, dev_status=status)
             ev[2].record()
-            w4.w4_grouped_gemm_down_combine(h, *dn, al, ids, w, counters, out, y=y,
-                                            dev_status=status)
-            ev[3].record()
             torch.cuda.synchronize()
             if i >= 2:
                 gsum[0] += ev[0].elapsed_time(ev[1]) / 10
-                gsum[1] += ev[2].elapsed_time(ev[3]) / 10
+                gsum[1] += ev[1].elapsed_time(ev[2]) / 10
         nbytes = layer_alg_bytes(c.M, c.d, c.m, c.k, touched)
         flops = c.M * c.k * 2.0 * 3 * c.m * c.d
         res[name] = {"M": c.M, "routing": c.routing, "touched_experts": touched,
@@ -455,9 +451,8 @@ def run_gpu(args, cfg, world, rank, local):
     ws = torch.empty(w4.w4_moe_layer_workspace_size(cfg.M, cfg.d, cfg.m, cfg.E, cfg.k, bm),
                      dtype=torch.uint8, device=dev)
 
-    # one step = one w4_moe_layer call: its three launches (align+gather,
-    # gate_up, down with the combine folded in) go out back to back on one
-    # stream, each a
+    # one step = one w4_moe_layer call: its four launches (align+gather,
+    # gate_up, down, combine) go out back to back on one stream, each a
     # programmatic dependent of the one before
     def layer():
         w4.w4_moe_layer(x, ids, w, gu, dn, block_m=bm, workspace=ws, out=out, dev_status=status)
@@ -496,20 +491,15 @@ def run_gpu(args, cfg, world, rank, local):
     # per-kernel times: the same launches through the binding's entry
     # points of the same names, events between them (which serialises the
     # launches: no overlap of one kernel's start with the previous one's end)
-    counters = torch.empty((cfg.M, cfg.d // 128), dtype=torch.int32, device=dev)
-
     def step_split(ev):
         ev[0].record()
         w4.w4_moe_align_gather(ids, x, cfg.E, bm, dev_status=status, out=al, xg=xg)
         ev[1].record()
         w4.w4_grouped_gemm_gate_up(xg, *gu, al, h=h, dev_status=status)
         ev[2].record()
-        # the layer sets the counters inside its gate_up launch; here the
-        # standalone preparation launch stands in for that
-        w4.w4_moe_combine_prepare(ids, cfg.E, cfg.d, counters=counters, out=out)
+        w4.w4_grouped_gemm_down(h, *dn, al, y=y, dev_status=status)
         ev[3].record()
-        w4.w4_grouped_gemm_down_combine(h, *dn, al, ids, w, counters, out, y=y,
-                                        dev_status=status)
+        w4.w4_moe_combine_fixed_order(y, ids, w, cfg.E, out=out)
         ev[4].record()
 
     n_split = max(3, min(args.steps, 300))
@@ -519,8 +509,7 @@ def run_gpu(args, cfg, world, rank, local):
     torch.cuda.synchronize()
     evs = evs[3:]
     per_kernel = {name: [e[i].elapsed_time(e[i + 1]) for e in evs]
-                  for i, name in enumerate(("align_gather", "gate_up", "combine_prepare",
-                                            "down_combine"))}
+                  for i, name in enumerate(("align_gather", "gate_up", "down", "combine"))}
     serial_ms = statistics.fmean(e[0].elapsed_time(e[4]) for e in evs)
 
     # ---------------------------------------------------------------- e2e
@@ -559,8 +548,7 @@ def run_gpu(args, cfg, world, rank, local):
         e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms,
-               "api": "w4_moe_layer (one C-ABI call: align+gather, gate_up, down with the "
-                      "combine folded in) "
+               "api": "w4_moe_layer (one C-ABI call: align+gather, gate_up, down, combine) "
                       "with pinned-host inputs copied in and the output copied out each step"}
         if not torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16)):
             raise RuntimeError("e2e output copy mismatch")
@@ -595,7 +583,7 @@ def run_gpu(args, cfg, world, rank, local):
                            f"{n_split} steps after the timed region",
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": sampler.summary() if sampler else None,
         "timed_region_wall_s": t_wall,
         "precision": "uint4 weights dequantised to fp16 in registers (q*s + fp16(-z*s), one "
@@ -607,8 +595,7 @@ def run_gpu(args, cfg, world, rank, local):
         line["configs_note"] = ("the other configurations of the layer, each with its own "
                                 "activations and routing and the layer256 packed weights: "
                                 "back-to-back w4_moe_layer calls (50, or 20 at M=2048); "
-                                "gate_up and down (with the combine folded in) from a "
-                                "serialised pass; fractions of the "
+                                "gate_up and down from a serialised pass; fractions of the "
                                 "measured HBM and bf16 peaks")
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(cfg, args.cpu_tokens).items()

@@ -237,7 +237,7 @@ int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int
  * group sums; h is rounded to fp16 with saturation at +-65504.
  * Requires d % 128 == 0, d <= 8192, m % 64 == 0, m <= 1024, group == 128,
  * and that a unit's scales and zeros fit shared memory beside the code and
- * activation stages: d up to about 3840 at E = 128 (2944 at E = 1024);
+ * activation stages: d up to about 3584 at E = 128 (2688 at E = 1024);
  * W4_ERR_UNSUPPORTED_SHAPE beyond, before anything is launched.
  * dev_status may be NULL.
  * ------------------------------------------------------------------------ */
@@ -302,13 +302,17 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids,
  *   out            [M, d] bf16 out, 8-byte aligned: bit-identical to
  *                  w4_grouped_gemm_down followed by
  *                  w4_moe_combine_fixed_order
- * Once a CTA has stored the 128 y columns of one panel of an assignment it
- * counts an arrival on the (token, 128-column panel) counter; the warp
- * whose arrival completes it computes those 128 columns of out[t] from the
- * token's k rows of y in assignment order (the combine's fp32 fma chain),
- * so no element of out is written twice and none depends on arrival order.  The
+ * After its last unit each CTA counts one arrival per slot of each of its
+ * units on the (token, 128-column panel) counter; the warp whose arrival
+ * completes a counter computes those 128 columns of out[t] from the token's
+ * k rows of y in assignment order (the combine's fp32 fma chain), so no
+ * element of out is written twice and none depends on arrival order.  The
  * counter atomics are the only atomics; they decide who combines, never
- * what.  Same requirements as w4_grouped_gemm_down.
+ * what.  The counting and the combines run after each CTA's last unit, so
+ * the CTAs that finish last take most of them: one launch fewer than down
+ * followed by w4_moe_combine_fixed_order, but at M = 256, d = 2816, top-8
+ * about 13 us slower per layer, which is why w4_moe_layer does not use it.
+ * Same requirements as w4_grouped_gemm_down.
  * ------------------------------------------------------------------------ */
 int w4_grouped_gemm_down_combine(const uint16_t *h, int M, int d, int m, int E, int k,
                                  int block_m, const uint8_t *dn_q, const uint16_t *dn_s,
@@ -327,16 +331,15 @@ int w4_moe_combine_prepare(const int32_t *topk_ids, int M, int k, int E, int d,
 
 /* --------------------------------------------------------------------------
  * w4_moe_layer -- the whole routed-expert layer: alignment fused with the
- * activation gather, gate_up + activation (which also sets the combine's
- * counters, as w4_moe_combine_prepare), down with the fixed-order combine
- * folded in (w4_grouped_gemm_down_combine), as three launches on one stream
+ * activation gather, gate_up + activation, down, fixed-order combine, as
+ * four launches on one stream (each a programmatic dependent of the one
+ * before, so their starts and ends overlap)
  * ("dg-w4-kernels" -- Grouped MoE: out = fused_moe_w4_v2(hidden, experts,
  *  topk_ids, topk_weights)).
  *
  * workspace: caller-owned device buffer of at least
  * w4_moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds the
- * alignment outputs, the gathered activations, h, y and the combine's
- * counters.  Its contents on return are the intermediates
+ * alignment outputs, the gathered activations, h and y.  Its contents on return are the intermediates
  * of this call (layout: see the implementation; not part of the ABI).
  * Same shape rules as the individual calls; dev_status may be NULL.
  * ------------------------------------------------------------------------ */

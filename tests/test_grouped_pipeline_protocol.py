@@ -7,14 +7,14 @@ threads for codes (one per parity of the stage sequence, 6 code stages in
 all; the parity-0 one also issues the 2 or 3 scale/zero stages), the TMA
 warp for
 activations (3 streamed slots, or 2 resident slots that hold a job's whole
-activation block, the group-sum block included), four MMA issuers (issuer r
-takes ring r: one A buffer in tensor memory and its own accumulator in each
-of two sets; each issuer's commits complete asynchronously in its issue
-order), sixteen dequantisation warps (lane quarter x ring; ring 2 gp + h
-takes half h of the stages whose index in the CTA's stage sequence has
-parity gp, so a warp skips the other stages; ring 1 or 3, half 1 of the
-parity the unit's first stage does not have, also produces the unit's
-group-constant correction) and four epilogue warps (which also read the row
+activation block, the group-sum block included), two MMA issuers (issuer r
+takes ring r: three A buffers in tensor memory that take the ring's fills
+in turn, and its own accumulator in each of two sets; each issuer's commits
+complete asynchronously in its issue order), sixteen dequantisation warps
+(lane quarter x ring x half; ring gp takes both halves of the stages whose
+index in the CTA's stage sequence has parity gp, so a warp skips the other
+stages; the ring of the parity the unit's first stage does not have also
+takes the unit's group-constant correction, made by its half-1 warps) and four epilogue warps (which also read the row
 scales the dequant warps publish per unit).  Every wait is
 checked against the exact condition: the phase it stands for, counted from
 per-stage uses kept apart from the kernel's parity variables, has completed
@@ -27,14 +27,14 @@ import random
 
 import pytest
 
-RINGS, SETS, ISSUERS = 4, 2, 4
+RINGS, RING_BUFS, SETS, ISSUERS = 2, 3, 2, 2
 # code stages (16 KB) and streamed activation slots (32 KB); resident mode
 # has the same code stages and two job slots
 STAGES_W_STREAMED, STAGES_W_RESIDENT, STAGES_B = 6, 6, 3
 STAGE_B_BYTES = 32768
 DQ_WARPS, EPI_WARPS = 16, 4
 CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 128, 32, 49152
-ROW_SCALE_SETS = 4
+ROW_SCALE_SETS = 8
 
 
 def sz_stages(G):
@@ -42,11 +42,11 @@ def sz_stages(G):
 
 
 def unit_ring(gp0, j):
-    return 2 * ((gp0 + (j >> 1)) & 1) + (j & 1)
+    return (gp0 + (j >> 1)) & 1
 
 
 def corr_ring(gp0, n_kchunks):
-    return 2 * (gp0 ^ 1) + 1
+    return gp0 ^ 1
 
 
 class Bar:
@@ -80,8 +80,9 @@ class Grouped:
         self.w_empty = B("w_empty", self.stages_w, DQ_WARPS // 2)
         nb = 2 if self.resident else STAGES_B
         self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, ISSUERS)
-        self.a_full = B("a_full", RINGS, 4)
-        self.a_empty = B("a_empty", RINGS, 1)
+        # ring r's buffer b is a_full / a_empty [r * RING_BUFS + b]
+        self.a_full = B("a_full", RINGS * RING_BUFS, 4)
+        self.a_empty = B("a_empty", RINGS * RING_BUFS, 1)
         self.acc_full, self.acc_empty = B("acc_full", SETS, ISSUERS), B("acc_empty", SETS, EPI_WARPS)
         self.sz_full = B("sz_full", self.n_sz, 1)
         self.sz_empty = B("sz_empty", self.n_sz, DQ_WARPS)
@@ -134,15 +135,16 @@ class Grouped:
                     sb, ph_b = 0, ph_b ^ 1
 
     def issuer(self, me):
-        a_use = 0
+        fill = 0
         acc_use, b_use = [0] * SETS, [0] * (2 if self.resident else STAGES_B)
         cur_job, res_slot, b_seq = None, 0, 0
 
         def issue(j):
-            nonlocal a_use
-            yield ("wait", self.a_full[me], a_use & 1, a_use)
-            a_use += 1
-            yield ("commit", me, self.a_empty[me])
+            nonlocal fill
+            buf = me * RING_BUFS + fill % RING_BUFS
+            yield ("wait", self.a_full[buf], (fill // RING_BUFS) & 1, fill // RING_BUFS)
+            fill += 1
+            yield ("commit", me, self.a_empty[buf])
 
         for n_unit, (job, n) in enumerate(self.units):
             st, acc_ph = n_unit & 1, (n_unit >> 1) & 1
@@ -187,19 +189,21 @@ class Grouped:
         return g & 1
 
     def dequant(self, r, q=0):
+        """Warp (q, gp, h) with r = 2 gp + h: half h of ring gp's stages; both
+        halves count every fill of the ring (and the correction, made by the
+        half-1 warps)."""
         gp, h = r >> 1, r & 1
         szb = ph_sz = 0
         sz_use = [0] * self.n_sz
         w_use = [0] * self.stages_w
-        a_fill = 0
+        fill = 0
 
-        def fill_buffer(first):
-            nonlocal a_fill
-            yield ("wait", self.a_empty[r], (a_fill & 1) ^ 1, a_fill - 1)
-            a_fill += 1
+        def fill_buffer(f, first):
+            buf = gp * RING_BUFS + f % RING_BUFS
+            yield ("wait", self.a_empty[buf], ((f // RING_BUFS) & 1) ^ 1, f // RING_BUFS - 1)
             if first:
                 yield ("rs_write", n_unit, q)
-            yield ("arrive", self.a_full[r])
+            yield ("arrive", self.a_full[buf])
 
         for n_unit, _u in enumerate(self.units):
             yield ("wait", self.sz_full[szb], ph_sz, sz_use[szb])
@@ -209,14 +213,19 @@ class Grouped:
                 if self.stage_parity(g, kc) != gp:
                     continue
                 sa = g % self.stages_w
+                my_fill = fill + (1 if h and 2 * kc < self.n_sub else 0)
+                fill += (2 * kc < self.n_sub) + (2 * kc + 1 < self.n_sub)
                 yield ("wait", self.w_full[sa], (g // self.stages_w) & 1, w_use[sa])
                 w_use[sa] += 1
                 yield ("arrive", self.w_empty[sa])
                 if 2 * kc + h >= self.n_sub:
                     continue
-                yield from fill_buffer(2 * kc + h == 0)
-            if r == corr_ring(gs0 & 1, self.n_kchunks):
-                yield from fill_buffer(False)
+                yield from fill_buffer(my_fill, 2 * kc + h == 0)
+            if gp == corr_ring(gs0 & 1, self.n_kchunks):
+                corr_fill = fill
+                fill += 1
+                if h == 1:
+                    yield from fill_buffer(corr_fill, False)
             yield ("arrive", self.sz_empty[szb])
             sz_use[szb] += 1
             szb += 1
@@ -350,7 +359,7 @@ def test_the_grouped_model_catches_rings_by_stage_within_unit():
 
 
 def test_the_grouped_model_catches_a_short_row_scale_table():
-    """With two row-scale tables instead of four, the dequant warps of unit
+    """With two row-scale tables instead of eight, the dequant warps of unit
     n + 2 can overwrite unit n's before its epilogue reads it."""
     global ROW_SCALE_SETS
     saved, ROW_SCALE_SETS = ROW_SCALE_SETS, 2

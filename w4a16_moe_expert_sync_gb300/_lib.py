@@ -345,8 +345,7 @@ def w4_moe_layer_workspace_size(M, d, m, E, k, block_m=16) -> int:
 def w4_moe_layer(x, topk_ids, topk_weights, gu, dn, block_m: int = 16, gu_group: int = 128,
                  dn_group: int = 64, workspace=None, out=None, dev_status=None, stream=None):
     """The whole routed-expert layer (align+gather, gate_up + activation,
-    down with the fixed-order combine folded in) as three launches on the
-    current stream."""
+    down, fixed-order combine) as four launches on the current stream."""
     import torch
     gu_q, gu_s, gu_z = gu
     dn_q, dn_s, dn_z = dn

@@ -502,11 +502,11 @@ int w4_moe_combine_fixed_order(const float *y, const int32_t *topk_ids, const fl
 // Workspace layout of w4_moe_layer (each piece 256-byte aligned):
 //   sorted_ids [cap] i32 | block_expert [cap/bm] i32 | expert_offsets [E+1] i32 |
 //   num_padded [1] i32 | xg [cap, d + 64] fp16 | h [cap, m + 64] fp16 |
-//   y [M*k, d] fp32 | combine counters [M, d/128] i32
+//   y [M*k, d] fp32
 //   (xg and h rows end in their 64-column group-sum block)
 namespace {
 struct LayerWs {
-    size_t sorted, block, offs, npad, xg, h, y, cnt, total;
+    size_t sorted, block, offs, npad, xg, h, y, total;
 };
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
@@ -520,8 +520,7 @@ LayerWs layer_ws(int M, int d, int m, int E, int k, int bm)
     w.xg = up256(w.npad + 4);
     w.h = up256(w.xg + 2 * cap * (static_cast<size_t>(d) + 64));
     w.y = up256(w.h + 2 * cap * (static_cast<size_t>(m) + 64));
-    w.cnt = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
-    w.total = up256(w.cnt + 4 * static_cast<size_t>(M) * (d / 128));
+    w.total = up256(w.y + 4 * static_cast<size_t>(M) * k * d);
     return w;
 }
 
@@ -546,7 +545,7 @@ int check_layer(int M, int d, int m, int E, int k, int block_m, const uint8_t *g
     if (!w4::grouped_gemm_fits(true, d, gu_group, E) || !w4::grouped_gemm_fits(false, m, dn_group, E))
         return fail(W4_ERR_UNSUPPORTED_SHAPE,
                     "the grouped GEMMs' scale/zero stages do not fit shared memory (d=%d, m=%d, "
-                    "E=%d; gate_up takes d up to about 3840 at E = 128)", d, m, E);
+                    "E=%d; gate_up takes d up to about 3584 at E = 128)", d, m, E);
     if (M > 0 && (!out || !topk_weights))
         return fail(W4_ERR_INVALID_ARG, "NULL pointer argument");
     if ((reinterpret_cast<uintptr_t>(out) & 7u) || !aligned4(topk_weights))
@@ -567,17 +566,23 @@ int layer_gemms(const int32_t *topk_ids, const float *topk_weights, int M,
     const uint16_t *xg = reinterpret_cast<const uint16_t *>(ws + L.xg);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
     float *y = reinterpret_cast<float *>(ws + L.y);
-    FoldedCombine fc;
-    fc.topk_ids = topk_ids;
-    fc.topk_w = topk_weights;
-    fc.cnt = reinterpret_cast<int32_t *>(ws + L.cnt);
-    fc.out = out;
+    // The combine runs as its own launch: folded into the down GEMM
+    // (w4_grouped_gemm_down_combine) the completed tokens gather on the CTAs
+    // that finish last and their y reads (23 MB at M = 256, d = 2816, top-8)
+    // run in those CTAs' tails, which measured ~13 us slower per layer than
+    // the standalone fixed-order combine, which reads the same bytes with the
+    // whole GPU and overlaps its start with the down GEMM's end.
     int rc = grouped_gemm_gate_up(xg, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group, sorted,
-                                  offs, h, dev_status, stream, fc);
+                                  offs, h, dev_status, stream, FoldedCombine{});
     if (rc)
         return rc;
-    return grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs,
-                             y, dev_status, stream, true, fc);
+    rc = grouped_gemm_down(h, M, d, m, E, k, block_m, dn_q, dn_s, dn_z, dn_group, sorted, offs, y,
+                           dev_status, stream, true, FoldedCombine{});
+    if (rc)
+        return rc;
+    cudaError_t err = w4::launch_combine(y, topk_ids, topk_weights, M, k, d, E, out,
+                                         as_stream(stream));
+    return err == cudaSuccess ? W4_OK : cuda_fail(err, "combine launch");
 }
 }  // namespace
 

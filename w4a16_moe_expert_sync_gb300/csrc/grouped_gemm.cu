@@ -48,20 +48,23 @@
 //     down, one copy per job fills a resident slot).
 //   * Codes arrive by TMA in stages of 128 rows x 256 codes (two 64-row
 //     boxes), evict-first in L2.  A stage is two 128-code sub-chunks.  Ring
-//     r = 2 gp + h (one 64-column A buffer in tensor memory) takes sub-chunk
-//     h of the stages whose index in the CTA's stage sequence has parity gp;
-//     the four dequant warps of ring r (one per lane quarter) expand it.
-//   * Four issuer warps, one per SM sub-partition: issuer r issues ring r's
-//     eight K = 16 MMAs per fill as two fused issue blocks, the second with
-//     the commit that releases the buffer, into its own fp32 accumulator
-//     ("chain").  The epilogue adds the chains in a fixed order.  Two
-//     accumulator sets alternate per unit, so a unit's epilogue overlaps the
-//     next unit's MMAs.  Ring 1 or 3 also carries the unit's correction.
+//     gp (three 64-column A buffers in tensor memory, taken in turn) takes
+//     both sub-chunks of the stages whose index in the CTA's stage sequence
+//     has parity gp; eight dequant warps per ring (lane quarter x half of the
+//     stage) expand them.
+//   * Two issuer warps: issuer r issues each of ring r's fills as eight
+//     K = 16 MMAs in two fused issue blocks, the second with the commit that
+//     frees the buffer, into its own fp32 accumulator ("chain").  The
+//     epilogue adds the chains in a fixed order.  Two accumulator sets
+//     alternate per unit, so a unit's epilogue overlaps the next unit's
+//     MMAs.  The ring of the parity the unit's first stage does not have
+//     also carries the unit's correction.
 //   * Warp roles
-//       warps 0-3   tcgen05.mma issuers (converged, one elected lane issues);
-//                   warp 0 also allocates tensor memory
+//       warps 0-1   tcgen05.mma issuers (converged, one elected lane issues);
+//                   warp 0 also allocates tensor memory; warps 2-3 idle
 //       warps 4-7   epilogue (one TMEM lane quarter each)
-//       warps 8-23  dequant (warp 8 + 4 r + q: lane quarter q, ring r)
+//       warps 8-23  dequant (warp 8 + 8 gp + 4 h + q: lane quarter q, ring
+//                   gp, half h of the ring's stages)
 //       warp 24     TMA: per unit the scales and zeros, and the code stages
 //                   of parity 0 of the CTA's stage sequence
 //       warp 27     TMA: the code stages of parity 1
@@ -70,8 +73,8 @@
 //                   down (combine_fold.cuh); in down, after its last unit,
 //                   every warp of the CTA counts the CTA's y panels and
 //                   combines the (token, panel) pairs it completed
-//   * Tensor memory (512 columns): A buffers at 64 r, accumulators at
-//     256 + 128 set + 32 chain.
+//   * Tensor memory (512 columns): A buffers at 64 (3 gp + b), accumulators
+//     at 384 + 64 set + 32 chain.
 //   * Every barrier has one producer group and one consumer group that take
 //     its phases in order, so a waiter is never two phases ahead and parity
 //     waits are exact (tests/test_grouped_pipeline_protocol.py models it).
@@ -92,7 +95,7 @@ namespace w4 {
 
 namespace {
 
-constexpr int kNumIssuers = 4;              // warps 0-3: issuer r takes ring r
+constexpr int kNumIssuers = 2;              // warps 0-1: issuer r takes ring r (warps 2-3 idle)
 constexpr int kWarpAlloc = 0;               // tensor-memory allocation (an issuer)
 constexpr int kWarpTmaW = 24;              // scales/zeros and parity-0 code stages
 constexpr int kWarpTmaW1 = 27;             // parity-1 code stages
@@ -100,15 +103,17 @@ constexpr int kWarpTmaB = 25;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kFirstDqWarp = 8;
-constexpr int kNumDqWarps = 16;            // warp 8 + 4 r + q: lane quarter q, ring r
+constexpr int kNumDqWarps = 16;            // warp 8 + 8 gp + 4 h + q
 constexpr int kWarpComb = 26;               // gate_up: sets the folded combine's counters
 constexpr int kNumWarps = 28;
 constexpr int kThreads = 32 * kNumWarps;
-// Ring r = 2 gp + h holds sub-chunk h of the stages whose global index (in
-// the CTA's stage sequence) has parity gp, so every dequant warp works on
-// every other stage and has two stages' time for each of its sub-chunks.
-constexpr int kRings = 4;
-constexpr int kRingBufs = 1;                // A buffers per ring
+// Ring gp takes both sub-chunks of the stages whose global index (in the
+// CTA's stage sequence) has parity gp, in stage order, into its three A
+// buffers in turn, so every dequant warp works on every other stage and has
+// two stages' time for each of its sub-chunks, and a ring's warps fill its
+// next buffers while the tensor core still reads the last.
+constexpr int kRings = 2;
+constexpr int kRingBufs = 3;                // A buffers per ring
 constexpr int kStagesW = 6;                 // packed-code stages
 constexpr int kStagesB = 3;                 // streamed activation slots
 constexpr int kMaxStagesSZ = 3;             // per-unit scales and zeros
@@ -121,16 +126,19 @@ constexpr int kStageBBytes = 32768;
 constexpr int kResSlotBytes = kStagesB * kStageBBytes / 2;   // resident mode: 2 x 48 KB
 constexpr int kMaxN = 32;                   // slots per job
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 256
-// Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 128 set
+constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 384
+// Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 64 set
 // + 32 i, the set alternating per unit.
 constexpr int kChains = kNumIssuers;
 // Row scales 2^c handed from the dequant warps to the epilogue, one table
-// per unit for the last four units: the dequant warp of sub-chunk 0 writes
-// unit n's after claiming its ring buffer, whose previous MMAs (unit >= n - 2)
-// waited for the epilogue of unit n - 4 to release its accumulators, which
-// it does after reading its table.
-constexpr int kRowScaleSets = 4;
+// per unit for the last eight units.  The dequant warps of sub-chunk 0 write
+// unit n's after claiming their buffer, i.e. after the MMAs of the ring's
+// fill three fills earlier; every unit gives each ring at least one fill
+// (sub-chunk 0 to one ring, the correction to the other), so those MMAs
+// belong to unit n - 3 or later and waited for the epilogue of unit n - 5 to
+// release its accumulators, which it does after reading its table: the
+// table of unit n - 8 is free.
+constexpr int kRowScaleSets = 8;
 // The (token, panel) combines a down CTA completes, kept until its last unit
 // (a longer list is combined as it overflows).
 constexpr int kCombListCap = 1024;
@@ -407,18 +415,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 // unit's first stage has global index parity gp0.
 __host__ __device__ __forceinline__ int unit_ring(int gp0, int j)
 {
-    return 2 * ((gp0 + (j >> 1)) & 1) + (j & 1);
+    return (gp0 + (j >> 1)) & 1;
 }
 
-// The ring that carries the unit's correction sub-chunk: half 1 of the
-// stages of the other parity than the unit's first stage.  Those are never
-// more than the first stage's parity has (one fewer when the unit has an odd
-// number of stages), and their half 1 is the one a 64-code tail leaves idle,
-// so no ring gets more than its share of the unit's fills.
+// The ring that carries the unit's correction sub-chunk (made by its half-1
+// warps, after the ring's last sub-chunk of the unit): the parity other than
+// the unit's first stage's, which never has more stages than that one.
 __host__ __device__ __forceinline__ int corr_ring(int gp0, int n_kchunks)
 {
     (void)n_kchunks;
-    return 2 * (gp0 ^ 1) + 1;
+    return gp0 ^ 1;
 }
 
 // Tile row (0..127 of the stage) held by lane `lane` of a warp of TMEM lane
@@ -628,18 +634,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     if (warp < kNumIssuers) {
         // ------------------------------------------------------ MMA issuers
-        // Issuer r takes the sub-chunks of ring r (the unit's sub-chunk j is
-        // in ring unit_ring(j)), eight K = 16 MMAs each as two issue blocks,
+        // Issuer r takes the fills of ring r in order: the unit's sub-chunks
+        // j in ring unit_ring(j), eight K = 16 MMAs each as two issue blocks,
         // then the correction when r is the unit's correction ring, into its
-        // own accumulator.  A thread issues an MMA every ~28-55 cycles at
-        // best and a commit costs it more, so four issuers, one per SM
-        // sub-partition, share the work.  The warp runs this loop converged
-        // (every value in it is warp-uniform, kept in registers) and one
-        // elected lane issues each tcgen05 instruction.
+        // own accumulator.  The warp runs this loop converged (every value in
+        // it is warp-uniform, kept in registers) and one elected lane issues
+        // each tcgen05 instruction.
         const int me = warp;
         const uint32_t b_base = smem_u32(stage_b);
         uint32_t b_seq = 0, n_unit = 0;
-        uint32_t a_ph = 0;      // phase of this ring's (single) A buffer
+        uint32_t fill = 0;      // fills of this ring so far: buffer fill % kRingBufs
         int cur_job = -1;       // resident mode: the job whose activations are held
         uint32_t res_slot = 0;
         bool ok = true;
@@ -651,20 +655,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t col_bytes,
                          uint32_t idesc) -> bool {
             const int n_all = j == n_sub ? p.n_corr_mma : (half_tail && j == n_sub - 1) ? 4 : 8;
-            const uint32_t a_tmem = tmem + static_cast<uint32_t>(me) * kSubCols;
+            const int buf = me * kRingBufs + static_cast<int>(fill % kRingBufs);
+            const uint32_t a_tmem = tmem + static_cast<uint32_t>(buf) * kSubCols;
             // K steps of 16: +32 B in the swizzled row (+2 in the descriptor's
             // address field), +8 columns of A; the second block of four starts
             // at the next 64-code column block
             const uint64_t b1 = bdesc + (col_bytes >> 4);
-            if (!warp_all_wait(&bar.a_full[me], a_ph, wc))
+            if (!warp_all_wait(&bar.a_full[buf], (fill / kRingBufs) & 1, wc))
                 return false;
-            a_ph ^= 1;
+            fill++;
             tc_fence_after();
             tc_mma4_ts_elect(d_tmem, a_tmem, bdesc, bdesc + 2, bdesc + 4, bdesc + 6, idesc,
                              min(n_all, 4), started ? 1u : 0u);
             started = true;
             tc_mma4_ts_commit_elect(d_tmem, a_tmem + 32, b1, b1 + 2, b1 + 4, b1 + 6, idesc,
-                                    max(n_all - 4, 0), 1u, &bar.a_empty[me]);
+                                    max(n_all - 4, 0), 1u, &bar.a_empty[buf]);
             return true;
         };
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -884,37 +889,40 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
     } else if (warp >= kFirstDqWarp && warp < kFirstDqWarp + kNumDqWarps) {
         // ---------------------------------------------------------- dequant
-        // Warp (q4, r), r = 2 gp + h: for every stage whose global index has
-        // parity gp, expands sub-chunk h (codes 128 h .. 128 h + 127) for its
-        // 32 rows into ring r's A buffer.  The other stages it skips (the
-        // other two rings take them), so each of its sub-chunks has two
-        // stages' time.  The stage count is even, so a warp touches only the stage
-        // slots of its parity, and every phase of them.
+        // Warp (q4, gp, h): for every stage whose global index has parity
+        // gp, expands sub-chunk h (codes 128 h .. 128 h + 127) for its 32
+        // rows into ring gp's next A buffer.  The other stages it skips (the
+        // other ring takes them), so each of its sub-chunks has two stages'
+        // time.  The stage count is even, so a warp touches only the stage
+        // slots of its parity, and every phase of them.  Both halves' warps
+        // count all of the ring's fills, so they agree on every buffer.
         const int q4 = warp & 3;
-        const int r = (warp - kFirstDqWarp) >> 2;
-        const int gp = r >> 1, h = r & 1;
+        const int gp = (warp - kFirstDqWarp) >> 3, h = ((warp - kFirstDqWarp) >> 2) & 1;
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        const uint32_t a_col0 = tmem + lane_base + static_cast<uint32_t>(r) * kSubCols;
+        uint32_t a_col0 = 0;    // the claimed buffer (this warp's lane quarter)
+        uint32_t fill = 0;      // fills of ring gp so far
         int szb = 0;
-        uint32_t ph_sz = 0, a_ph = 0, n_unit = 0;
+        uint32_t ph_sz = 0, n_unit = 0;
         const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
         // this warp's half of a row: 16-byte chunks 4 h .. 4 h + 3, swizzled
         const uint32_t row_off = static_cast<uint32_t>(row * 128);
         const uint32_t sw = static_cast<uint32_t>(row & 7);
-        // claim the ring's buffer (its previous MMAs complete)
-        auto claim = [&]() -> bool {
-            if (!warp_all_wait(&bar.a_empty[r], a_ph ^ 1, wc))
+        // claim the buffer of the ring's fill f (the MMAs of fill f - 3 in it
+        // complete) and hand it over once written
+        auto claim = [&](uint32_t f) -> bool {
+            const int buf = gp * kRingBufs + static_cast<int>(f % kRingBufs);
+            if (!warp_all_wait(&bar.a_empty[buf], ((f / kRingBufs) & 1) ^ 1, wc))
                 return false;
-            a_ph ^= 1;
             tc_fence_after();
+            a_col0 = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
             return true;
         };
-        auto hand_over = [&]() {
+        auto hand_over = [&](uint32_t f) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            mbar_arrive_elect(&bar.a_full[r]);
+            mbar_arrive_elect(&bar.a_full[gp * kRingBufs + static_cast<int>(f % kRingBufs)]);
         };
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -932,6 +940,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const int sa = g % kStagesW;
                 const int j = 2 * kc + h;                 // sub-chunk of the unit
                 const bool mine = j < n_sub;
+                // the ring's fill of this sub-chunk: the stage's half 0 first
+                const uint32_t my_fill = fill + (h && 2 * kc < n_sub ? 1u : 0u);
+                fill += (2 * kc < n_sub ? 1u : 0u) + (2 * kc + 1 < n_sub ? 1u : 0u);
                 const bool tail = mine && half_tail && j == n_sub - 1;   // 64 codes
                 // groups of the two 64-code halves (the same group for g128),
                 // their constants from the unit's scale stage before the codes
@@ -965,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 dequant_word(v0.y, k0.S, k0.S16, k0.C, &o[4]);
                 dequant_word(v0.z, k0.S, k0.S16, k0.C, &o[8]);
                 dequant_word(v0.w, k0.S, k0.S16, k0.C, &o[12]);
-                if (!claim()) {
+                if (!claim(my_fill)) {
                     ok = false;
                     break;
                 }
@@ -994,11 +1005,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     dequant_word(v3.w, k1.S, k1.S16, k1.C, &o[12]);
                     tmem_st_32x32b_x16(a_col0 + 48, o);
                 }
-                hand_over();
+                hand_over(my_fill);
             }
             if (!ok)
                 break;
-            if (r == corr_ring(gs0 & 1, p.n_kchunks)) {
+            // the correction: a fill of its ring (counted by both halves'
+            // warps), made by the half-1 warps
+            const bool corr_here = gp == corr_ring(gs0 & 1, p.n_kchunks);
+            const uint32_t corr_fill = fill;
+            if (corr_here)
+                fill++;
+            if (corr_here && h == 1) {
                 // The correction sub-chunk: C = -s z 2^-c rounded to fp16 (the
                 // constant of every dequantised weight of the group) leaves
                 // the part C_lo = fp16(C_exact - C).  The activations carry
@@ -1010,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 // down (four sum columns per group): both halves of words
                 // 2 i' and 2 i' + 1 of step t hold group 4 t + i'
                 constexpr int kRep = GATE_UP ? 1 : 4;
-                if (!claim())
+                if (!claim(corr_fill))
                     break;
 #pragma unroll
                 for (int t = 0; t < 4; t++) {
@@ -1045,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                     tmem_st_32x32b_x8(a_col0 + 8 * t, cw);
                 }
-                hand_over();
+                hand_over(corr_fill);
             }
             __syncwarp();
             mbar_arrive_elect(&bar.sz_empty[szb]);
