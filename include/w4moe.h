@@ -70,6 +70,10 @@ typedef enum {
                                          activation) lay outside fp16's finite
                                          range and was saturated to +-65504:
                                          the GEMMs' operands are fp16           */
+#define W4_DEV_OUT_OF_BOUNDS 0x10     /* a range check of a data-dependent
+                                         global store failed and the store was
+                                         skipped (only in a library built with
+                                         -DW4_CHECK_BOUNDS, a test build)       */
 
 /* Human-readable name of a w4_status value (static string). */
 const char *w4_status_string(int status);

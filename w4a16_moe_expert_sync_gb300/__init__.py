@@ -9,7 +9,8 @@ synthetic workloads (``workloads``) used by the tests and the benchmark.
     ids, w = w4.w4_moe_route(logits, k=8)
     out = w4.w4_moe_layer(x_bf16, ids, w, (gu_q, gu_s, gu_z), (dn_q, dn_s, dn_z))
 """
-from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_FP16_RANGE, W4_DEV_PIPELINE_TIMEOUT,
+from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_FP16_RANGE, W4_DEV_OUT_OF_BOUNDS,
+                   W4_DEV_PIPELINE_TIMEOUT,
                    W4_DEV_TOO_MANY_JOBS,
                    W4Error, header_functions, korder_to_natural, load_library,
                    w4_gather_activations, w4_grouped_gemm_down, w4_moe_align_gather,
@@ -31,5 +32,5 @@ __all__ = [
     "w4_moe_route_align_gather", "w4_moe_layer_from_logits", "w4_rmsnorm", "w4_sample_logits",
     "w4_sample_logits_workspace_size", "w4_fused_entropy", "w4_gumbel_argmax_sample",
     "w4_w4a16_linear", "w4_w4a16_linear_workspace_size",
-    "W4_DEV_BAD_EXPERT_ID", "W4_DEV_FP16_RANGE", "W4_DEV_PIPELINE_TIMEOUT", "W4_DEV_TOO_MANY_JOBS",
+    "W4_DEV_BAD_EXPERT_ID", "W4_DEV_FP16_RANGE", "W4_DEV_OUT_OF_BOUNDS", "W4_DEV_PIPELINE_TIMEOUT", "W4_DEV_TOO_MANY_JOBS",
 ]

@@ -25,6 +25,7 @@ W4_DEV_BAD_EXPERT_ID = 0x1
 W4_DEV_PIPELINE_TIMEOUT = 0x2
 W4_DEV_TOO_MANY_JOBS = 0x4
 W4_DEV_FP16_RANGE = 0x8
+W4_DEV_OUT_OF_BOUNDS = 0x10
 # xg and h rows end in one block of 64 columns of activation group sums, the
 # grouped GEMMs' input for the low parts of their dequantisation constants
 SUM_COLS = 64

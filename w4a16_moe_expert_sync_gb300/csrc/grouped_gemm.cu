@@ -86,6 +86,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "checks.cuh"
 #include "combine_fold.cuh"
 #include "korder.cuh"
 #include "launch.h"
@@ -172,6 +173,7 @@ struct GemmArgs {
     int32_t *comb_cnt;
     uint16_t *comb_out;       // [M, d] bf16
     int M, k, comb_d;
+    int64_t cap;              // alignment slots (rows of xg / h)
     // test hooks: the pipeline wait limit (ns), and whether the first unit's
     // scale/zero copy is withheld (so that the waits run out)
     uint64_t wait_ns;
@@ -482,7 +484,8 @@ __device__ __forceinline__ void combine_panel(const GemmArgs &p, int t, int pnl,
     uint2 pk;
     pk.x = *reinterpret_cast<const uint32_t *>(&lo);
     pk.y = *reinterpret_cast<const uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(p.comb_out + static_cast<int64_t>(t) * p.comb_d + col) = pk;
+    if (W4_IN_BOUNDS(t < p.M && col + 4 <= p.comb_d, p.dev_status))
+        *reinterpret_cast<uint2 *>(p.comb_out + static_cast<int64_t>(t) * p.comb_d + col) = pk;
 }
 
 // (down, after the CTA's last unit and a fence that released its y stores)
@@ -1149,22 +1152,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         range |= real && !(fabsf(hv) <= 65504.0f);
                         const uint16_t hq = real ? static_cast<uint16_t>(f16x2_sat(hv, 0.0f)) : 0;
                         uint16_t *hrow = hout + (J.start + si) * static_cast<int64_t>(p.h_stride);
-                        hrow[pos] = hq;
+                        const bool row_ok = W4_IN_BOUNDS(J.start + si < p.cap, status);
+                        if (row_ok && W4_IN_BOUNDS(pos < p.h_stride, status))
+                            hrow[pos] = hq;
                         // lanes 0-15 sum slot i, lanes 16-31 slot i + 1 (fixed tree)
                         float part = __half2float(__ushort_as_half(hq));
                         part += __shfl_xor_sync(full, part, 8);
                         part += __shfl_xor_sync(full, part, 4);
                         part += __shfl_xor_sync(full, part, 2);
                         part += __shfl_xor_sync(full, part, 1);
-                        if ((lane & 15) == 0) {
+                        if ((lane & 15) == 0 && row_ok) {
                             range |= !(fabsf(part) <= 65504.0f);
-                            hrow[p.out_cols + 4 * pnl + q4] =
-                                static_cast<uint16_t>(f16x2_sat(part, 0.0f));
+                            if (W4_IN_BOUNDS(p.out_cols + 4 * pnl + q4 < p.h_stride, status))
+                                hrow[p.out_cols + 4 * pnl + q4] =
+                                    static_cast<uint16_t>(f16x2_sat(part, 0.0f));
                             if (pnl == 0)   // sum columns past the last group, read by
                                             // the correction's last MMA step: zero
                                 for (int c = 4 * p.h_groups + q4;
                                      c < 16 * ((p.h_groups + 3) / 4); c += 4)
-                                    hrow[p.out_cols + c] = 0;
+                                    if (W4_IN_BOUNDS(p.out_cols + c < p.h_stride, status))
+                                        hrow[p.out_cols + c] = 0;
                         }
                     }
                 } else {
@@ -1172,7 +1179,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
                         const int a = __shfl_sync(full, my_a, 16 * half + i);
-                        if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A))
+                        if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A) &&
+                            W4_IN_BOUNDS(col < p.out_cols, status))
                             yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
                     }
                 }
@@ -1358,6 +1366,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.M = q.M;
     a.k = q.k;
     a.comb_d = q.comb_d;
+    a.cap = q.cap;
     a.wait_ns = q.wait_ns;
     a.test_withhold_sz = q.test_withhold_sz ? 1 : 0;
     const bool resident = !q.gate_up && b_fits_resident(q.K);

@@ -15,6 +15,8 @@ constexpr int32_t kDevBadExpertId = 0x1;
 constexpr int32_t kDevPipelineTimeout = 0x2;
 constexpr int32_t kDevTooManyJobs = 0x4;
 constexpr int32_t kDevFp16Range = 0x8;
+// kDevOutOfBounds = 0x10 (checks.cuh): a store failed its range check
+// (only in the W4_CHECK_BOUNDS build)
 
 cudaError_t launch_quantize(const float *W, int64_t rows, int K, int group, uint8_t *q,
                             uint16_t *s, uint16_t *z, cudaStream_t stream);

@@ -29,6 +29,7 @@
 #include <cfloat>
 
 #include "korder.cuh"
+#include "checks.cuh"
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -293,7 +294,7 @@ __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int
             hist[warp * E + e] += __popc(grp);
         __syncwarp();
         if (a < a1 && a >= own0 && a < own1) {   // lanes past a1 are another warp's
-            if (sorted_ids && valid)
+            if (sorted_ids && valid && W4_IN_BOUNDS(pos < cap, dev_status))
                 sorted_ids[pos] = a;
             if (pos_sm)
                 pos_sm[a - own0] = valid ? pos : -1;
@@ -306,9 +307,11 @@ __device__ __forceinline__ void align_block(const int32_t *__restrict__ ids, int
         const int gtid = blockIdx.x * blockDim.x + tid, gstride = gridDim.x * blockDim.x;
         for (int e = gtid; e < E; e += gstride) {
             for (int sl = offs[e] + total[e]; sl < offs[e + 1]; sl++)
-                sorted_ids[sl] = A;
+                if (W4_IN_BOUNDS(sl < cap, dev_status))
+                    sorted_ids[sl] = A;
             for (int b = offs[e] / bm; b < offs[e + 1] / bm; b++)
-                block_expert[b] = e;
+                if (W4_IN_BOUNDS(b < cap / bm, dev_status))
+                    block_expert[b] = e;
         }
         const int npad = offs[E];
         for (int sl = npad + gtid; sl < cap; sl += gstride)
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__(1024, 1)
             __syncwarp();
             if (a < own1) {
                 pos[a - own0] = slot;
-                if (valid)
+                if (valid && W4_IN_BOUNDS(slot < cap, dev_status))
                     sorted_ids[slot] = a;
             }
         }
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(1024, 1)
         const int col = sum_column(c8, d, gsum, &v, &range);
         for (int j = 0; j < k; j++) {
             const int slot = pos[tl * k + j];
-            if (slot >= 0) {
+            if (slot >= 0 && W4_IN_BOUNDS(slot < cap, dev_status)) {
                 uint16_t *row = xg + static_cast<int64_t>(slot) * ld;
                 *reinterpret_cast<uint4 *>(row + 8 * c8) = o;
                 if (col >= 0)
@@ -659,9 +662,11 @@ __global__ void __launch_bounds__(1024, 1)
     const int gtid = blockIdx.x * nthr + tid, gstride = gridDim.x * nthr;
     for (int e = gtid; e < E; e += gstride) {
         for (int sl = offs[e] + cnt[e]; sl < offs[e + 1]; sl++)
-            sorted_ids[sl] = A;
+            if (W4_IN_BOUNDS(sl < cap, dev_status))
+                sorted_ids[sl] = A;
         for (int b = offs[e] / bm; b < offs[e + 1] / bm; b++)
-            block_expert[b] = e;
+            if (W4_IN_BOUNDS(b < cap / bm, dev_status))
+                block_expert[b] = e;
     }
     const int npad = offs[E];
     for (int sl = npad + gtid; sl < cap; sl += gstride)
