@@ -157,9 +157,10 @@ def test_gemm_weight_rows_with_mixed_scales(lib):
 # oracle by its own fp16 rounding (h: 2^-10 |h| covers it with the rounding of
 # its gate and up inputs) plus TAU of the rms.  The TAU terms bound the
 # compute error before that rounding.  Error model: every dequantised weight
-# is rounded to fp16 once (relative <= 2^-11) and every group constant -z*s
-# once more, a per-group offset multiplied by the group's activation sum;
-# together ~5e-4 rms relative error in g and u.  h = gelu(g) u turns it into
+# is rounded to fp16 once (relative <= 2^-11); the rounding of each group's
+# constant -z*s, a per-group offset that the group's activation sum would
+# multiply, is added back by the correction MMAs; ~5e-4 rms relative error
+# in g and u.  h = gelu(g) u turns it into
 # ~9e-4 rms of h (the error of g is scaled by |u|, a heavy-tailed factor),
 # which the down contraction passes on to y as ~1e-3 rms.  The largest of
 # ~10^6 such errors lies near 6 (y) to 10 (h) of those rms: observed at
