@@ -3,37 +3,36 @@ run under random interleavings on the CPU, in the manner of
 test_dense_pipeline_protocol.py.
 
 Roles as the kernel writes them, with the kernel's constants: the two TMA
-threads for codes (one per parity of the stage sequence, 6 code stages in
-all; the parity-0 one also issues the 2 or 3 scale/zero stages), the TMA
-warp for
-activations (3 streamed slots, or 2 resident slots that hold a job's whole
-activation block, the group-sum block included), two MMA issuers (issuer r
-takes ring r: three A buffers in tensor memory that take the ring's fills
-in turn, and its own accumulator in each of two sets; each issuer's commits
-complete asynchronously in its issue order), sixteen dequantisation warps
-(lane quarter x ring x half; ring gp takes both halves of the stages whose
-index in the CTA's stage sequence has parity gp, so a warp skips the other
-stages; the ring of the parity the unit's first stage does not have also
-takes the unit's group-constant correction, made by its half-1 warps) and four epilogue warps (which also read the row
-scales the dequant warps publish per unit).  Every wait is
-checked against the exact condition: the phase it stands for, counted from
-per-stage uses kept apart from the kernel's parity variables, has completed
-exactly when the parity test says so.  Unit lists mix jobs of 16 and 32 slots over several panels; contraction
-sizes cover gate_up (2816, streamed, 11 stages per unit: the rings' parities
-alternate from unit to unit), down (704, resident, a 64-code last sub-chunk)
-and short ones (384, 192, 320, 128, 64).
+threads for codes (one per parity of the CTA's stage sequence, 6 code stages
+in all; the parity-0 one also issues the 2 or 3 scale/zero stages), the TMA
+warp for activations (3 streamed slots, or 2 resident slots that hold a
+job's whole activation block, the group-sum block included), four MMA
+issuers (issuer r takes ring r: two A buffers in tensor memory that take the
+ring's fills in turn, and its own accumulator in each of two sets; each
+issuer's commits complete asynchronously in its issue order), sixteen
+dequantisation warps (lane quarter x ring; ring r takes 64-code slice r of
+every stage, i.e. the unit's blocks j with j % 4 == r, and ring
+(blocks + unit) % 4 also takes the unit's group-constant correction) and
+four epilogue warps (which also read the row scales the ring-0 dequant
+warps publish per unit).  Every wait is checked against the exact
+condition: the phase it stands for, counted from per-stage uses kept apart
+from the kernel's parity variables, has completed exactly when the parity
+test says so.  Unit lists mix jobs of 16 and 32 slots over several panels;
+contraction sizes cover gate_up (2816, streamed, 11 stages per unit), down
+(704, resident, a last stage with three of its four slices) and short ones
+(384, 192, 320, 128, 64).
 """
 import random
 
 import pytest
 
-RINGS, RING_BUFS, SETS, ISSUERS = 2, 3, 2, 2
+RINGS, RING_BUFS, SETS, ISSUERS = 4, 2, 2, 4
 # code stages (16 KB) and streamed activation slots (32 KB); resident mode
 # has the same code stages and two job slots
 STAGES_W_STREAMED, STAGES_W_RESIDENT, STAGES_B = 6, 6, 3
 STAGE_B_BYTES = 32768
 DQ_WARPS, EPI_WARPS = 16, 4
-CHUNK_K, SUB_K, MAX_N, RES_BYTES = 256, 128, 32, 49152
+CHUNK_K, SLICE_K, MAX_N, RES_BYTES = 256, 64, 32, 49152
 ROW_SCALE_SETS = 8
 
 
@@ -41,12 +40,12 @@ def sz_stages(G):
     return 2 if G > 16 else 3
 
 
-def unit_ring(gp0, j):
-    return (gp0 + (j >> 1)) & 1
+def block_ring(j):
+    return j & (RINGS - 1)
 
 
-def corr_ring(gp0, n_kchunks):
-    return gp0 ^ 1
+def corr_ring(n_unit, n_blocks):
+    return (n_blocks + n_unit) & (RINGS - 1)
 
 
 class Bar:
@@ -72,12 +71,12 @@ class Grouped:
         self.G = K // group
         self.n_sz = sz_stages(self.G)
         self.n_kchunks = (K + CHUNK_K - 1) // CHUNK_K
-        self.n_sub = (K + SUB_K - 1) // SUB_K
+        self.n_blocks = K // SLICE_K
         self.resident = (K + 64) * 2 * MAX_N <= RES_BYTES
         self.stages_w = STAGES_W_RESIDENT if self.resident else STAGES_W_STREAMED
         B = lambda name, n, c: [Bar(f"{name}{i}", c) for i in range(n)]
         self.w_full = B("w_full", self.stages_w, 1)
-        self.w_empty = B("w_empty", self.stages_w, DQ_WARPS // 2)
+        self.w_empty = B("w_empty", self.stages_w, DQ_WARPS)
         nb = 2 if self.resident else STAGES_B
         self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, ISSUERS)
         # ring r's buffer b is a_full / a_empty [r * RING_BUFS + b]
@@ -103,8 +102,10 @@ class Grouped:
                 yield ("copy", self.sz_full[szb])
                 sz_fill[szb] += 1
             gs0 = n * self.n_kchunks
-            for kc in range(0 if (gs0 & 1) == gp else 1, self.n_kchunks, 2):
+            for kc in range(self.n_kchunks):
                 g = gs0 + kc
+                if self.stage_parity(g, kc) != gp:
+                    continue
                 sa = g % self.stages_w
                 yield ("wait", self.w_empty[sa], ((g // self.stages_w) & 1) ^ 1, w_fill[sa] - 1)
                 yield ("copy", self.w_full[sa])
@@ -138,8 +139,9 @@ class Grouped:
         fill = 0
         acc_use, b_use = [0] * SETS, [0] * (2 if self.resident else STAGES_B)
         cur_job, res_slot, b_seq = None, 0, 0
+        nb = self.n_blocks
 
-        def issue(j):
+        def issue():
             nonlocal fill
             buf = me * RING_BUFS + fill % RING_BUFS
             yield ("wait", self.a_full[buf], (fill // RING_BUFS) & 1, fill // RING_BUFS)
@@ -148,8 +150,7 @@ class Grouped:
 
         for n_unit, (job, n) in enumerate(self.units):
             st, acc_ph = n_unit & 1, (n_unit >> 1) & 1
-            gp0 = (n_unit * self.n_kchunks) & 1
-            corr = corr_ring(gp0, self.n_kchunks)
+            corr = corr_ring(n_unit, nb)
             yield ("wait", self.acc_empty[st], acc_ph ^ 1, acc_use[st] - 1)
             if self.resident:
                 if job != cur_job:
@@ -160,24 +161,22 @@ class Grouped:
                     b_use[res_slot] += 1
                     b_seq += 1
                     cur_job = job
-                for j in range(self.n_sub):
-                    if unit_ring(gp0, j) == me:
-                        yield from issue(j)
+                for j in range(me, nb, RINGS):
+                    yield from issue()
                 if me == corr:
-                    yield from issue(self.n_sub)
+                    yield from issue()
             else:
                 kcols = b_kcols(n)
-                subs = kcols // 2
-                n_bslots = self.K // 64 // kcols + 1
+                n_bslots = nb // kcols + 1
                 for t in range(n_bslots):
                     sb = (b_seq + t) % STAGES_B
                     yield ("wait", self.b_full[sb], ((b_seq + t) // STAGES_B) & 1, b_use[sb])
                     b_use[sb] += 1
-                    for j in range(t * subs, min(self.n_sub, (t + 1) * subs)):
-                        if unit_ring(gp0, j) == me:
-                            yield from issue(j)
+                    for j in range(t * kcols, min(nb, (t + 1) * kcols)):
+                        if block_ring(j) == me:
+                            yield from issue()
                     if t == n_bslots - 1 and me == corr:
-                        yield from issue(self.n_sub)
+                        yield from issue()
                     yield ("commit", me, self.b_empty[sb])
                 b_seq += n_bslots
             yield ("commit", me, self.acc_full[st])
@@ -185,47 +184,42 @@ class Grouped:
 
     @staticmethod
     def stage_parity(g, kc):
-        """Rings by the stage's index in the CTA's stage sequence."""
+        """Code producers by the stage's index in the CTA's stage sequence."""
         return g & 1
 
     def dequant(self, r, q=0):
-        """Warp (q, gp, h) with r = 2 gp + h: half h of ring gp's stages; both
-        halves count every fill of the ring (and the correction, made by the
-        half-1 warps)."""
-        gp, h = r >> 1, r & 1
+        """Warp (q, r): slice r of every stage (block 4 kc + r of the unit),
+        then the correction when r is the unit's correction ring."""
         szb = ph_sz = 0
         sz_use = [0] * self.n_sz
         w_use = [0] * self.stages_w
         fill = 0
 
-        def fill_buffer(f, first):
-            buf = gp * RING_BUFS + f % RING_BUFS
-            yield ("wait", self.a_empty[buf], ((f // RING_BUFS) & 1) ^ 1, f // RING_BUFS - 1)
+        def fill_buffer(first):
+            nonlocal fill
+            buf = r * RING_BUFS + fill % RING_BUFS
+            yield ("wait", self.a_empty[buf], ((fill // RING_BUFS) & 1) ^ 1,
+                   fill // RING_BUFS - 1)
             if first:
                 yield ("rs_write", n_unit, q)
             yield ("arrive", self.a_full[buf])
+            fill += 1
 
         for n_unit, _u in enumerate(self.units):
             yield ("wait", self.sz_full[szb], ph_sz, sz_use[szb])
             gs0 = n_unit * self.n_kchunks
             for kc in range(self.n_kchunks):
                 g = gs0 + kc
-                if self.stage_parity(g, kc) != gp:
-                    continue
                 sa = g % self.stages_w
-                my_fill = fill + (1 if h and 2 * kc < self.n_sub else 0)
-                fill += (2 * kc < self.n_sub) + (2 * kc + 1 < self.n_sub)
+                j = 4 * kc + r
                 yield ("wait", self.w_full[sa], (g // self.stages_w) & 1, w_use[sa])
                 w_use[sa] += 1
                 yield ("arrive", self.w_empty[sa])
-                if 2 * kc + h >= self.n_sub:
+                if j >= self.n_blocks:
                     continue
-                yield from fill_buffer(my_fill, 2 * kc + h == 0)
-            if gp == corr_ring(gs0 & 1, self.n_kchunks):
-                corr_fill = fill
-                fill += 1
-                if h == 1:
-                    yield from fill_buffer(corr_fill, False)
+                yield from fill_buffer(j == 0)
+            if r == corr_ring(n_unit, self.n_blocks):
+                yield from fill_buffer(False)
             yield ("arrive", self.sz_empty[szb])
             sz_use[szb] += 1
             szb += 1
@@ -337,11 +331,11 @@ def test_the_grouped_model_catches_a_broken_protocol():
     assert failures > 0
 
 
-def test_the_grouped_model_catches_rings_by_stage_within_unit():
-    """Assigning stages to rings by their index within the unit instead of
-    in the CTA's stage sequence breaks the parity waits when a unit has an
-    odd number of stages (gate_up: 11): a warp would skip phases of its
-    stage slots."""
+def test_the_grouped_model_catches_producers_by_stage_within_unit():
+    """Splitting the code stages between the two producer threads by their
+    index within the unit instead of in the CTA's stage sequence breaks the
+    parity waits when a unit has an odd number of stages (gate_up: 11): both
+    threads would fill the same stage slots."""
     class Broken(Grouped):
         @staticmethod
         def stage_parity(g, kc):
@@ -359,8 +353,8 @@ def test_the_grouped_model_catches_rings_by_stage_within_unit():
 
 
 def test_the_grouped_model_catches_a_short_row_scale_table():
-    """With two row-scale tables instead of eight, the dequant warps of unit
-    n + 2 can overwrite unit n's before its epilogue reads it."""
+    """With two row-scale tables instead of eight, the ring-0 dequant warps
+    of unit n + 2 can overwrite unit n's before its epilogue reads it."""
     global ROW_SCALE_SETS
     saved, ROW_SCALE_SETS = ROW_SCALE_SETS, 2
     failures = 0

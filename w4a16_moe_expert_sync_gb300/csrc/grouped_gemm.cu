@@ -47,24 +47,21 @@
 //     128-byte-swizzled K-major layout; 3-D TMA copies fill its slots (or, for
 //     down, one copy per job fills a resident slot).
 //   * Codes arrive by TMA in stages of 128 rows x 256 codes (two 64-row
-//     boxes), evict-first in L2.  A stage is two 128-code sub-chunks.  Ring
-//     gp (three 64-column A buffers in tensor memory, taken in turn) takes
-//     both sub-chunks of the stages whose index in the CTA's stage sequence
-//     has parity gp; eight dequant warps per ring (lane quarter x half of the
-//     stage) expand them.
-//   * Two issuer warps: issuer r issues each of ring r's fills as eight
-//     K = 16 MMAs in two fused issue blocks, the second with the commit that
-//     frees the buffer, into its own fp32 accumulator ("chain").  The
-//     epilogue adds the chains in a fixed order.  Two accumulator sets
-//     alternate per unit, so a unit's epilogue overlaps the next unit's
-//     MMAs.  The ring of the parity the unit's first stage does not have
-//     also carries the unit's correction.
+//     boxes), evict-first in L2.  A stage is four 64-code slices (the unit's
+//     blocks 4 kc .. 4 kc + 3).  Ring r (two 32-column A buffers in tensor
+//     memory, taken in turn) takes slice r of every stage; four dequant
+//     warps per ring (one per lane quarter) expand it.
+//   * Four issuer warps: issuer r issues each of ring r's fills as four
+//     K = 16 MMAs and the commit that frees the buffer, in one issue block,
+//     into its own fp32 accumulator ("chain").  The epilogue adds the chains
+//     in a fixed order.  Two accumulator sets alternate per unit, so a
+//     unit's epilogue overlaps the next unit's MMAs.  The unit's correction
+//     goes to ring (blocks + unit) % 4, after that ring's last block.
 //   * Warp roles
-//       warps 0-1   tcgen05.mma issuers (converged, one elected lane issues);
-//                   warp 0 also allocates tensor memory; warps 2-3 idle
+//       warps 0-3   tcgen05.mma issuers (converged, one elected lane issues);
+//                   warp 0 also allocates tensor memory
 //       warps 4-7   epilogue (one TMEM lane quarter each)
-//       warps 8-23  dequant (warp 8 + 8 gp + 4 h + q: lane quarter q, ring
-//                   gp, half h of the ring's stages)
+//       warps 8-23  dequant (warp 8 + 4 r + q: lane quarter q, ring r)
 //       warp 24     TMA: per unit the scales and zeros, and the code stages
 //                   of parity 0 of the CTA's stage sequence
 //       warp 27     TMA: the code stages of parity 1
@@ -73,8 +70,8 @@
 //                   down (combine_fold.cuh); in down, after its last unit,
 //                   every warp of the CTA counts the CTA's y panels and
 //                   combines the (token, panel) pairs it completed
-//   * Tensor memory (512 columns): A buffers at 64 (3 gp + b), accumulators
-//     at 384 + 64 set + 32 chain.
+//   * Tensor memory (512 columns): A buffers at 32 (2 r + b), accumulators
+//     at 256 + 128 set + 32 chain.
 //   * Every barrier has one producer group and one consumer group that take
 //     its phases in order, so a waiter is never two phases ahead and parity
 //     waits are exact (tests/test_grouped_pipeline_protocol.py models it).
@@ -96,7 +93,7 @@ namespace w4 {
 
 namespace {
 
-constexpr int kNumIssuers = 2;              // warps 0-1: issuer r takes ring r (warps 2-3 idle)
+constexpr int kNumIssuers = 4;              // warps 0-3: issuer r takes ring r
 constexpr int kWarpAlloc = 0;               // tensor-memory allocation (an issuer)
 constexpr int kWarpTmaW = 24;              // scales/zeros and parity-0 code stages
 constexpr int kWarpTmaW1 = 27;             // parity-1 code stages
@@ -104,41 +101,39 @@ constexpr int kWarpTmaB = 25;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kFirstDqWarp = 8;
-constexpr int kNumDqWarps = 16;            // warp 8 + 8 gp + 4 h + q
+constexpr int kNumDqWarps = 16;            // warp 8 + 4 r + q: lane quarter q, ring r
 constexpr int kWarpComb = 26;               // gate_up: sets the folded combine's counters
 constexpr int kNumWarps = 28;
 constexpr int kThreads = 32 * kNumWarps;
-// Ring gp takes both sub-chunks of the stages whose global index (in the
-// CTA's stage sequence) has parity gp, in stage order, into its three A
-// buffers in turn, so every dequant warp works on every other stage and has
-// two stages' time for each of its sub-chunks, and a ring's warps fill its
-// next buffers while the tensor core still reads the last.
-constexpr int kRings = 2;
-constexpr int kRingBufs = 3;                // A buffers per ring
+// Ring r takes slice r (codes 64 r .. 64 r + 63) of every stage into its
+// two A buffers in turn: all sixteen dequant warps work on every stage, so a
+// stage is free as soon as each has read its slice, and a ring's four warps
+// fill one buffer while the tensor core reads the other.
+constexpr int kRings = 4;
+constexpr int kRingBufs = 2;                // A buffers per ring
 constexpr int kStagesW = 6;                 // packed-code stages
 constexpr int kStagesB = 3;                 // streamed activation slots
 constexpr int kMaxStagesSZ = 3;             // per-unit scales and zeros
 constexpr int kTileRows = 128;              // MMA M
 constexpr int kChunkK = 256;                // codes per row per stage
-constexpr int kSubK = 128;                  // codes per sub-chunk (one A buffer)
-constexpr int kSubCols = kSubK / 2;         // TMEM columns per A buffer
+constexpr int kSliceK = 64;                 // codes per fill (one A buffer)
+constexpr int kFillCols = kSliceK / 2;      // TMEM columns per A buffer
 constexpr int kStageWBytes = kTileRows * kChunkK / 2;   // 16 KB
 constexpr int kStageBBytes = 32768;
 constexpr int kResSlotBytes = kStagesB * kStageBBytes / 2;   // resident mode: 2 x 48 KB
 constexpr int kMaxN = 32;                   // slots per job
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = kRings * kRingBufs * kSubCols;  // 384
-// Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 64 set
+constexpr uint32_t kAccCol = kRings * kRingBufs * kFillCols;  // 256
+// Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 128 set
 // + 32 i, the set alternating per unit.
 constexpr int kChains = kNumIssuers;
 // Row scales 2^c handed from the dequant warps to the epilogue, one table
-// per unit for the last eight units.  The dequant warps of sub-chunk 0 write
-// unit n's after claiming their buffer, i.e. after the MMAs of the ring's
-// fill three fills earlier; every unit gives each ring at least one fill
-// (sub-chunk 0 to one ring, the correction to the other), so those MMAs
-// belong to unit n - 3 or later and waited for the epilogue of unit n - 5 to
-// release its accumulators, which it does after reading its table: the
-// table of unit n - 8 is free.
+// per unit for the last eight units.  The ring-0 dequant warps write unit n's
+// after claiming the buffer of its block 0, i.e. after the MMAs of ring 0's
+// fill two fills earlier; every unit gives ring 0 at least one fill (block
+// 0), so those MMAs belong to unit n - 2 or later and waited for the
+// epilogue of unit n - 4 to release its accumulators, which it does after
+// reading its table: the table of unit n - 8 is free.
 constexpr int kRowScaleSets = 8;
 // The (token, panel) combines a down CTA completes, kept until its last unit
 // (a longer list is combined as it overflows).
@@ -155,12 +150,12 @@ struct GemmArgs {
     const int32_t *expert_offsets;
     void *out;
     int32_t *dev_status;
-    int E, A, K, R, m_up, out_cols, group_shift, G, n_panels, n_kchunks, n_sub, n_sz;
+    int E, A, K, R, m_up, out_cols, group_shift, G, n_panels, n_kchunks, n_blocks, n_sz;
     int n_corr_mma;           // K = 16 MMAs of the group-constant correction
     int h_stride;             // gate_up: row length of h (m + 64: values, then group sums)
     int h_groups;             // gate_up: groups of 64 along m (the down GEMM's groups)
-    int acc_mask[2];          // issuers (accumulators) with MMAs in a unit whose first
-                              // stage has global index parity 0 / 1
+    int acc_mask[4];          // issuers (accumulators) with MMAs in the CTA's unit n,
+                              // by n % 4 (the correction's ring rotates)
     int early_schedule;       // the schedule may be read before the grid-dependency wait
     // The layer's combine, folded into the down GEMM (comb_cnt non-null):
     // counters [M][d/128 panels][4 lane quarters], set by the gate_up launch
@@ -413,20 +408,15 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
             return;
 }
 
-// The ring of the unit's sub-chunk j (in stage j / 2, half j % 2) when the
-// unit's first stage has global index parity gp0.
-__host__ __device__ __forceinline__ int unit_ring(int gp0, int j)
-{
-    return (gp0 + (j >> 1)) & 1;
-}
+// The ring of the unit's 64-code block j (slice j % 4 of stage j / 4).
+__host__ __device__ __forceinline__ int block_ring(int j) { return j & (kRings - 1); }
 
-// The ring that carries the unit's correction sub-chunk (made by its half-1
-// warps, after the ring's last sub-chunk of the unit): the parity other than
-// the unit's first stage's, which never has more stages than that one.
-__host__ __device__ __forceinline__ int corr_ring(int gp0, int n_kchunks)
+// The ring that carries the correction fill of the CTA's unit n (after the
+// ring's last block of the unit): the ring the next block would go to,
+// turned by one per unit, so that over four units every ring takes one.
+__host__ __device__ __forceinline__ int corr_ring(int n_unit, int n_blocks)
 {
-    (void)n_kchunks;
-    return gp0 ^ 1;
+    return (n_blocks + n_unit) & (kRings - 1);
 }
 
 // Tile row (0..127 of the stage) held by lane `lane` of a warp of TMEM lane
@@ -561,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (tid == 0) {
         for (int i = 0; i < kStagesW; i++) {
             mbar_init(&bar.w_full[i], 1);
-            mbar_init(&bar.w_empty[i], kNumDqWarps / 2);   // the two rings of its parity
+            mbar_init(&bar.w_empty[i], kNumDqWarps);   // every dequant warp
         }
         for (int i = 0; i < kStagesB; i++) {
             mbar_init(&bar.b_full[i], 1);
@@ -631,18 +621,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t tmem = *tmem_holder;
     const int n_units = jp[p.E] * p.n_panels;
     const int K = p.K;
-    const int n_sub = p.n_sub;
-    // the last sub-chunk holds 64 codes when K is an odd multiple of 64
-    const bool half_tail = (K & (kSubK - 1)) != 0;
+    const int n_blocks = p.n_blocks;     // 64-code blocks along K
 
     if (warp < kNumIssuers) {
         // ------------------------------------------------------ MMA issuers
-        // Issuer r takes the fills of ring r in order: the unit's sub-chunks
-        // j in ring unit_ring(j), eight K = 16 MMAs each as two issue blocks,
-        // then the correction when r is the unit's correction ring, into its
-        // own accumulator.  The warp runs this loop converged (every value in
-        // it is warp-uniform, kept in registers) and one elected lane issues
-        // each tcgen05 instruction.
+        // Issuer r takes the fills of ring r in order: the unit's blocks j
+        // with block_ring(j) == r, four K = 16 MMAs and the commit that frees
+        // the buffer as one issue block each, then the correction when r is
+        // the unit's correction ring, into its own accumulator.  Four issuers,
+        // one per SM sub-partition.  The warp runs this loop converged (every
+        // value in it is warp-uniform, kept in registers) and one elected
+        // lane issues each tcgen05 instruction.
         const int me = warp;
         const uint32_t b_base = smem_u32(stage_b);
         uint32_t b_seq = 0, n_unit = 0;
@@ -651,28 +640,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         uint32_t res_slot = 0;
         bool ok = true;
         bool started = false;   // has this unit's first MMA gone (accumulate from then on)?
-        // Sub-chunk j: wait for the ring's buffer, issue its MMAs (8; 4 for a
-        // 64-code tail; n_corr_mma for the correction, j == n_sub) and
-        // release the buffer.  bdesc: descriptor of the sub-chunk's first
-        // 64-code column block; the second follows col_bytes later.
-        auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t col_bytes,
-                         uint32_t idesc) -> bool {
-            const int n_all = j == n_sub ? p.n_corr_mma : (half_tail && j == n_sub - 1) ? 4 : 8;
+        // Block j (j == n_blocks: the correction): wait for the ring's next
+        // buffer, issue its MMAs (four; n_corr_mma for the correction) with B
+        // at the descriptor bdesc of the block's 64-code column block, and
+        // release the buffer.
+        auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t idesc) -> bool {
+            const int n_mma = j == n_blocks ? p.n_corr_mma : 4;
             const int buf = me * kRingBufs + static_cast<int>(fill % kRingBufs);
-            const uint32_t a_tmem = tmem + static_cast<uint32_t>(buf) * kSubCols;
-            // K steps of 16: +32 B in the swizzled row (+2 in the descriptor's
-            // address field), +8 columns of A; the second block of four starts
-            // at the next 64-code column block
-            const uint64_t b1 = bdesc + (col_bytes >> 4);
+            const uint32_t a_tmem = tmem + static_cast<uint32_t>(buf) * kFillCols;
             if (!warp_all_wait(&bar.a_full[buf], (fill / kRingBufs) & 1, wc))
                 return false;
             fill++;
             tc_fence_after();
-            tc_mma4_ts_elect(d_tmem, a_tmem, bdesc, bdesc + 2, bdesc + 4, bdesc + 6, idesc,
-                             min(n_all, 4), started ? 1u : 0u);
+            // K steps of 16: +32 B in the swizzled row (+2 in the descriptor's
+            // address field), +8 columns of A
+            tc_mma4_ts_commit_elect(d_tmem, a_tmem, bdesc, bdesc + 2, bdesc + 4, bdesc + 6, idesc,
+                                    n_mma, started ? 1u : 0u, &bar.a_empty[buf]);
             started = true;
-            tc_mma4_ts_commit_elect(d_tmem, a_tmem + 32, b1, b1 + 2, b1 + 4, b1 + 6, idesc,
-                                    max(n_all - 4, 0), 1u, &bar.a_empty[buf]);
             return true;
         };
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -682,8 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
             const int set = n_unit & 1;
             const uint32_t acc_ph = (n_unit >> 1) & 1;
-            const int gp0 = (n_unit * p.n_kchunks) & 1;   // parity of the unit's first stage
-            const int corr = corr_ring(gp0, p.n_kchunks);
+            const int corr = corr_ring(static_cast<int>(n_unit), n_blocks);
             if (!warp_all_wait(&bar.acc_empty[set], acc_ph ^ 1, wc)) {
                 ok = false;
                 break;
@@ -706,23 +689,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     cur_job = job;
                 }
                 const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
-                for (int j = 0; j < n_sub && ok; j++)
-                    // sub-chunk j reads column blocks 2j, 2j + 1
-                    if (unit_ring(gp0, j) == me &&
-                        !issue(j, d_tmem, sdesc_sw128(b_slot + 2u * j * col_bytes), col_bytes,
+                for (int j = me; j < n_blocks && ok; j += kRings)
+                    if (!issue(j, d_tmem, sdesc_sw128(b_slot + static_cast<uint32_t>(j) * col_bytes),
                                idesc))
                         ok = false;
-                // the correction reads block K / 64 (the group sums)
+                // the correction reads block n_blocks (the group sums)
                 if (ok && me == corr &&
-                    !issue(n_sub, d_tmem,
-                           sdesc_sw128(b_slot + static_cast<uint32_t>(K / 64) * col_bytes),
-                           col_bytes, idesc))
+                    !issue(n_blocks, d_tmem,
+                           sdesc_sw128(b_slot + static_cast<uint32_t>(n_blocks) * col_bytes),
+                           idesc))
                     ok = false;
             } else {
                 const int kcols = b_kcols(J.n);
-                const int subs_per_slot = kcols / 2;
-                // the last slot holds column block K / 64, the group sums
-                const int n_bslots = K / 64 / kcols + 1;
+                // the last slot holds column block n_blocks, the group sums
+                const int n_bslots = n_blocks / kcols + 1;
                 for (int t = 0; t < n_bslots && ok; t++) {
                     const int sb = (b_seq + t) % kStagesB;
                     if (!warp_all_wait(&bar.b_full[sb], ((b_seq + t) / kStagesB) & 1, wc)) {
@@ -731,17 +711,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                     tc_fence_after();
                     const uint32_t b_slot = b_base + sb * kStageBBytes;
-                    const int j0 = t * subs_per_slot;
-                    const int j1 = min(n_sub, j0 + subs_per_slot);
+                    const int j0 = t * kcols;
+                    const int j1 = min(n_blocks, j0 + kcols);
                     for (int j = j0; j < j1 && ok; j++)
-                        if (unit_ring(gp0, j) == me &&
-                            !issue(j, d_tmem, sdesc_sw128(b_slot + 2u * (j - j0) * col_bytes),
-                                   col_bytes, idesc))
+                        if (block_ring(j) == me &&
+                            !issue(j, d_tmem,
+                                   sdesc_sw128(b_slot + static_cast<uint32_t>(j - j0) * col_bytes),
+                                   idesc))
                             ok = false;
                     if (ok && t == n_bslots - 1 && me == corr) {
-                        const uint32_t blk = static_cast<uint32_t>(K / 64 - t * kcols);
-                        if (!issue(n_sub, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), col_bytes,
-                                   idesc))
+                        const uint32_t blk = static_cast<uint32_t>(n_blocks - t * kcols);
+                        if (!issue(n_blocks, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), idesc))
                             ok = false;
                     }
                     if (!ok)
@@ -762,10 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         // ------------------------------------------- TMA: codes, scales/zeros
         // Two producer threads, one per parity gp of the CTA's stage sequence:
         // stage g goes to slot g % kStagesW, so a parity owns every other
-        // slot, only its own dequant warps free them, and a parity whose
-        // warps run ahead is never held back by the other's slower ones.
-        // The parity-0 thread also issues each unit's scales and zeros
-        // before the unit's stages.
+        // slot and each thread waits only on its own slots' releases.  The
+        // parity-0 thread also issues each unit's scales and zeros before the
+        // unit's stages.
         if (lane == 0) {
             const int gp = warp == kWarpTmaW ? 0 : 1;
             const uint64_t pol = l2_policy_evict_first();
@@ -892,40 +871,41 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
     } else if (warp >= kFirstDqWarp && warp < kFirstDqWarp + kNumDqWarps) {
         // ---------------------------------------------------------- dequant
-        // Warp (q4, gp, h): for every stage whose global index has parity
-        // gp, expands sub-chunk h (codes 128 h .. 128 h + 127) for its 32
-        // rows into ring gp's next A buffer.  The other stages it skips (the
-        // other ring takes them), so each of its sub-chunks has two stages'
-        // time.  The stage count is even, so a warp touches only the stage
-        // slots of its parity, and every phase of them.  Both halves' warps
-        // count all of the ring's fills, so they agree on every buffer.
+        // Warp (q4, r): for every stage, expands slice r (codes 64 r ..
+        // 64 r + 63, block 4 kc + r of the unit) for its 32 rows into ring
+        // r's next A buffer.  A slice past K (a last stage of fewer than 256
+        // codes) is skipped, but the stage is still waited for and released,
+        // so the stage's arrival count is every dequant warp.
         const int q4 = warp & 3;
-        const int gp = (warp - kFirstDqWarp) >> 3, h = ((warp - kFirstDqWarp) >> 2) & 1;
+        const int r = (warp - kFirstDqWarp) >> 2;
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        const int n_blocks = p.n_blocks;
         uint32_t a_col0 = 0;    // the claimed buffer (this warp's lane quarter)
-        uint32_t fill = 0;      // fills of ring gp so far
+        uint32_t fill = 0;      // fills of ring r so far
         int szb = 0;
         uint32_t ph_sz = 0, n_unit = 0;
         const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
-        // this warp's half of a row: 16-byte chunks 4 h .. 4 h + 3, swizzled
+        // this warp's slice of a row: 16-byte chunks 2 r, 2 r + 1, swizzled
         const uint32_t row_off = static_cast<uint32_t>(row * 128);
         const uint32_t sw = static_cast<uint32_t>(row & 7);
-        // claim the buffer of the ring's fill f (the MMAs of fill f - 3 in it
-        // complete) and hand it over once written
-        auto claim = [&](uint32_t f) -> bool {
-            const int buf = gp * kRingBufs + static_cast<int>(f % kRingBufs);
-            if (!warp_all_wait(&bar.a_empty[buf], ((f / kRingBufs) & 1) ^ 1, wc))
+        const uint32_t chunk0 = ((2u * r) ^ sw) << 4, chunk1 = ((2u * r + 1) ^ sw) << 4;
+        // claim the ring's next buffer (the MMAs of fill - 2 in it complete)
+        // and hand it over once written
+        auto claim = [&]() -> bool {
+            const int buf = r * kRingBufs + static_cast<int>(fill % kRingBufs);
+            if (!warp_all_wait(&bar.a_empty[buf], ((fill / kRingBufs) & 1) ^ 1, wc))
                 return false;
             tc_fence_after();
-            a_col0 = tmem + lane_base + static_cast<uint32_t>(buf) * kSubCols;
+            a_col0 = tmem + lane_base + static_cast<uint32_t>(buf) * kFillCols;
             return true;
         };
-        auto hand_over = [&](uint32_t f) {
+        auto hand_over = [&]() {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            mbar_arrive_elect(&bar.a_full[gp * kRingBufs + static_cast<int>(f % kRingBufs)]);
+            mbar_arrive_elect(&bar.a_full[r * kRingBufs + static_cast<int>(fill % kRingBufs)]);
+            fill++;
         };
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
@@ -938,20 +918,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const float scale_s = exp2i(24 - c), scale_c = exp2i(-c);
             for (int kc = 0; kc < p.n_kchunks; kc++) {
                 const int g = gs0 + kc;
-                if ((g & 1) != gp)
-                    continue;
                 const int sa = g % kStagesW;
-                const int j = 2 * kc + h;                 // sub-chunk of the unit
-                const bool mine = j < n_sub;
-                // the ring's fill of this sub-chunk: the stage's half 0 first
-                const uint32_t my_fill = fill + (h && 2 * kc < n_sub ? 1u : 0u);
-                fill += (2 * kc < n_sub ? 1u : 0u) + (2 * kc + 1 < n_sub ? 1u : 0u);
-                const bool tail = mine && half_tail && j == n_sub - 1;   // 64 codes
-                // groups of the two 64-code halves (the same group for g128),
-                // their constants from the unit's scale stage before the codes
-                // arrive
-                const uint32_t g0 = static_cast<uint32_t>(j * kSubK) >> p.group_shift;
-                const uint32_t g1 = static_cast<uint32_t>(j * kSubK + 64) >> p.group_shift;
+                const int j = 4 * kc + r;                 // block of the unit
+                const bool mine = j < n_blocks;
+                // the block's group constants, from the unit's scale stage,
+                // before the codes arrive
+                const uint32_t g0 = static_cast<uint32_t>(j * kSliceK) >> p.group_shift;
                 GroupK k0{};
                 if (mine)
                     k0 = group_consts(lds_u16(s_addr + 2 * g0), lds_u16(z_addr + 2 * g0), scale_s,
@@ -961,14 +933,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     break;
                 }
                 const uint32_t rp = stage_w_s + sa * kStageWBytes + row_off;
-                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0, v3 = v0;
+                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
                 if (mine) {
-                    v0 = lds128(rp + (((4 * h + 0) ^ sw) << 4));
-                    v1 = lds128(rp + (((4 * h + 1) ^ sw) << 4));
-                    if (!tail) {
-                        v2 = lds128(rp + (((4 * h + 2) ^ sw) << 4));
-                        v3 = lds128(rp + (((4 * h + 3) ^ sw) << 4));
-                    }
+                    v0 = lds128(rp + chunk0);
+                    v1 = lds128(rp + chunk1);
                 }
                 __syncwarp();
                 mbar_arrive_elect(&bar.w_empty[sa]);
@@ -979,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 dequant_word(v0.y, k0.S, k0.S16, k0.C, &o[4]);
                 dequant_word(v0.z, k0.S, k0.S16, k0.C, &o[8]);
                 dequant_word(v0.w, k0.S, k0.S16, k0.C, &o[12]);
-                if (!claim(my_fill)) {
+                if (!claim()) {
                     ok = false;
                     break;
                 }
@@ -992,34 +960,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 dequant_word(v1.z, k0.S, k0.S16, k0.C, &o[8]);
                 dequant_word(v1.w, k0.S, k0.S16, k0.C, &o[12]);
                 tmem_st_32x32b_x16(a_col0 + 16, o);
-                if (!tail) {        // (a 64-code tail has no second half)
-                    const GroupK k1 = g1 == g0 ? k0
-                                               : group_consts(lds_u16(s_addr + 2 * g1),
-                                                              lds_u16(z_addr + 2 * g1), scale_s,
-                                                              scale_c);
-                    dequant_word(v2.x, k1.S, k1.S16, k1.C, &o[0]);
-                    dequant_word(v2.y, k1.S, k1.S16, k1.C, &o[4]);
-                    dequant_word(v2.z, k1.S, k1.S16, k1.C, &o[8]);
-                    dequant_word(v2.w, k1.S, k1.S16, k1.C, &o[12]);
-                    tmem_st_32x32b_x16(a_col0 + 32, o);
-                    dequant_word(v3.x, k1.S, k1.S16, k1.C, &o[0]);
-                    dequant_word(v3.y, k1.S, k1.S16, k1.C, &o[4]);
-                    dequant_word(v3.z, k1.S, k1.S16, k1.C, &o[8]);
-                    dequant_word(v3.w, k1.S, k1.S16, k1.C, &o[12]);
-                    tmem_st_32x32b_x16(a_col0 + 48, o);
-                }
-                hand_over(my_fill);
+                hand_over();
             }
             if (!ok)
                 break;
-            // the correction: a fill of its ring (counted by both halves'
-            // warps), made by the half-1 warps
-            const bool corr_here = gp == corr_ring(gs0 & 1, p.n_kchunks);
-            const uint32_t corr_fill = fill;
-            if (corr_here)
-                fill++;
-            if (corr_here && h == 1) {
-                // The correction sub-chunk: C = -s z 2^-c rounded to fp16 (the
+            // the correction: a fill of ring corr_ring, after its last block
+            if (r == corr_ring(static_cast<int>(n_unit), n_blocks)) {
+                // The correction fill: C = -s z 2^-c rounded to fp16 (the
                 // constant of every dequantised weight of the group) leaves
                 // the part C_lo = fp16(C_exact - C).  The activations carry
                 // one (xg) or four (h) sum columns per group, so contraction
@@ -1030,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 // down (four sum columns per group): both halves of words
                 // 2 i' and 2 i' + 1 of step t hold group 4 t + i'
                 constexpr int kRep = GATE_UP ? 1 : 4;
-                if (!claim(corr_fill))
+                if (!claim())
                     break;
 #pragma unroll
                 for (int t = 0; t < 4; t++) {
@@ -1065,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                     tmem_st_32x32b_x8(a_col0 + 8 * t, cw);
                 }
-                hand_over(corr_fill);
+                hand_over();
             }
             __syncwarp();
             mbar_arrive_elect(&bar.sz_empty[szb]);
@@ -1097,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tc_fence_after();
             // 2^c of this lane's weight row, published by the dequant warps
             const float factor = row_scale[(n_unit & (kRowScaleSets - 1)) * kTileRows + row];
-            const int mask = p.acc_mask[(n_unit * p.n_kchunks) & 1];
+            const int mask = p.acc_mask[n_unit & 3];
             uint16_t *hout = reinterpret_cast<uint16_t *>(p.out);
             float *yout = reinterpret_cast<float *>(p.out);
             const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);    // gate_up
@@ -1338,7 +1285,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.G = q.K / q.group;
     a.n_panels = q.gate_up ? (q.R / 2) / 64 : q.R / 128;
     a.n_kchunks = (q.K + kChunkK - 1) / kChunkK;
-    a.n_sub = (q.K + kSubK - 1) / kSubK;
+    a.n_blocks = q.K / kSliceK;     // K is a multiple of the group, 64 or 128
     a.n_sz = sz_stages(a.G);
     // the activation rows end in one 64-column block of group sums: xg one
     // per group of 128, h one per quarter (16 intermediates) of each group of 64
@@ -1349,12 +1296,12 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         return cudaErrorInvalidValue;
     }
     a.n_corr_mma = (a.G * corr_rep + 15) / 16;
-    // the accumulators (issuers) that receive MMAs in a unit, for either
-    // parity of its first stage's global index
-    for (int gp0 = 0; gp0 < 2; gp0++) {
-        a.acc_mask[gp0] = 1 << corr_ring(gp0, a.n_kchunks);
-        for (int j = 0; j < a.n_sub; j++)
-            a.acc_mask[gp0] |= 1 << unit_ring(gp0, j);
+    // the accumulators (issuers) that receive MMAs in the CTA's unit n, by
+    // n % 4
+    for (int n = 0; n < 4; n++) {
+        a.acc_mask[n] = 1 << corr_ring(n, a.n_blocks);
+        for (int j = 0; j < a.n_blocks; j++)
+            a.acc_mask[n] |= 1 << block_ring(j);
     }
     a.h_stride = q.gate_up ? q.R / 2 + 64 : 0;
     a.h_groups = q.gate_up ? (q.R / 2) / 64 : 0;
