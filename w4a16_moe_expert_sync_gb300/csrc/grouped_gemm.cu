@@ -311,33 +311,23 @@ __device__ __forceinline__ int row_exponent(uint32_t smax_bits)
 }
 
 // The largest |scale| bit pattern among the G scales of a row in shared
-// memory at s_addr: for even G two scales per 32-bit load and a packed
-// 16-bit max, else sixteen independent 16-bit loads at a time.
+// memory at s_addr: a 16-bit load up to the first 4-byte boundary, then two
+// scales per 32-bit load with a packed 16-bit max, then the odd last one.
 __device__ __forceinline__ uint32_t row_smax(uint32_t s_addr, int G)
 {
-    if ((G & 1) == 0) {
-        uint32_t m2 = 0;
-        for (int g0 = 0; g0 < G; g0 += 16) {
-            uint32_t v[8];
-#pragma unroll
-            for (int i = 0; i < 8; i++)
-                v[i] = g0 + 2 * i < G ? lds_u32(s_addr + 2 * (g0 + 2 * i)) : 0u;
-#pragma unroll
-            for (int i = 0; i < 8; i++)
-                m2 = __vmaxu2(m2, v[i] & 0x7FFF7FFFu);
-        }
-        return max(m2 & 0xFFFFu, m2 >> 16);
-    }
     uint32_t smax = 0;
-    for (int g0 = 0; g0 < G; g0 += 16) {
-        uint32_t v[16];
-#pragma unroll
-        for (int i = 0; i < 16; i++)
-            v[i] = g0 + i < G ? lds_u16(s_addr + 2 * (g0 + i)) : 0u;
-#pragma unroll
-        for (int i = 0; i < 16; i++)
-            smax = max(smax, v[i] & 0x7FFFu);
+    if (s_addr & 2u) {
+        smax = lds_u16(s_addr) & 0x7FFFu;
+        s_addr += 2;
+        G--;
     }
+    uint32_t m2 = 0;
+#pragma unroll 2
+    for (int i = 0; i < (G >> 1); i++)
+        m2 = __vmaxu2(m2, lds_u32(s_addr + 4 * i) & 0x7FFF7FFFu);
+    smax = max(smax, max(m2 & 0xFFFFu, m2 >> 16));
+    if (G & 1)
+        smax = max(smax, lds_u16(s_addr + 2 * (G - 1)) & 0x7FFFu);
     return smax;
 }
 

@@ -475,8 +475,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr)
     return d;
 }
 
-// 32 lanes x 32 columns of 32 bit: thread i of the warp writes lane
-// (warp quarter base + i), columns [col, col + 32).
 // 32 lanes x 8 columns of 32 bit (thread i: lane quarter base + i).
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8])
 {
@@ -499,6 +497,8 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         : "memory");
 }
 
+// 32 lanes x 32 columns of 32 bit: thread i of the warp writes lane
+// (warp quarter base + i), columns [col, col + 32).
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
