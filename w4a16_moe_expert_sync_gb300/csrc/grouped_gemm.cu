@@ -384,6 +384,12 @@ __device__ __forceinline__ bool warp_all_wait(uint64_t *bar, uint32_t parity, co
                           wc.limit_ns);
 }
 
+__device__ __forceinline__ bool warp_all_wait_a(uint32_t bar, uint32_t parity, const WaitCtx &wc)
+{
+    return mbar_wait_warp_a(bar, parity, wc.abort_flag, wc.status, kDevPipelineTimeout,
+                            wc.limit_ns);
+}
+
 __device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, const WaitCtx &wc)
 {
     return mbar_wait(bar, parity, wc.abort_flag, wc.status, kDevPipelineTimeout, wc.limit_ns);
@@ -871,67 +877,74 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int row = tile_row<GATE_UP>(q4, lane);
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
         const int n_blocks = p.n_blocks;
-        uint32_t a_col0 = 0;    // the claimed buffer (this warp's lane quarter)
-        uint32_t fill = 0;      // fills of ring r so far
         int szb = 0;
         uint32_t ph_sz = 0, n_unit = 0;
-        const uint32_t stage_w_s = smem_u32(stage_w), sz_base_s = smem_u32(sz_base);
+        const uint32_t sz_base_s = smem_u32(sz_base);
+        // The running state, in registers: the next code stage slot `sa`
+        // (its shared address, its barriers' addresses, its phase) and the
+        // ring's next buffer `fb` (its TMEM column, its barriers, its phase).
+        const uint32_t w_full0 = smem_u32(bar.w_full), w_empty0 = smem_u32(bar.w_empty);
+        const uint32_t a_full0 = smem_u32(bar.a_full + r * kRingBufs);
+        const uint32_t a_empty0 = smem_u32(bar.a_empty + r * kRingBufs);
+        const uint32_t a_col_ring = tmem + lane_base + static_cast<uint32_t>(r * kRingBufs * kFillCols);
+        int sa = 0;
+        uint32_t ph_w = 0, fb = 0, ph_a = 0;
         // this warp's slice of a row: 16-byte chunks 2 r, 2 r + 1, swizzled
-        const uint32_t row_off = static_cast<uint32_t>(row * 128);
         const uint32_t sw = static_cast<uint32_t>(row & 7);
-        const uint32_t chunk0 = ((2u * r) ^ sw) << 4, chunk1 = ((2u * r + 1) ^ sw) << 4;
-        // claim the ring's next buffer (the MMAs of fill - 2 in it complete)
-        // and hand it over once written
+        const uint32_t code0 = smem_u32(stage_w) + static_cast<uint32_t>(row * 128) +
+                               (((2u * r) ^ sw) << 4);
+        const uint32_t code1 = smem_u32(stage_w) + static_cast<uint32_t>(row * 128) +
+                               (((2u * r + 1) ^ sw) << 4);
+        // the group index advances by 256 codes per stage
+        const uint32_t g_step = 2u * (static_cast<uint32_t>(kChunkK) >> p.group_shift);
+        // claim the ring's next buffer (the MMAs of two fills ago in it
+        // complete); hand it over once written
         auto claim = [&]() -> bool {
-            const int buf = r * kRingBufs + static_cast<int>(fill % kRingBufs);
-            if (!warp_all_wait(&bar.a_empty[buf], ((fill / kRingBufs) & 1) ^ 1, wc))
+            if (!warp_all_wait_a(a_empty0 + 8 * fb, ph_a ^ 1, wc))
                 return false;
             tc_fence_after();
-            a_col0 = tmem + lane_base + static_cast<uint32_t>(buf) * kFillCols;
             return true;
         };
         auto hand_over = [&]() {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            mbar_arrive_elect(&bar.a_full[r * kRingBufs + static_cast<int>(fill % kRingBufs)]);
-            fill++;
+            mbar_arrive_elect_a(a_full0 + 8 * fb);
+            fb ^= 1;
+            ph_a ^= fb ^ 1;    // the phase turns after buffer 1
+        };
+        // wait for the stage in slot sa; release it after the loads
+        auto stage_wait = [&]() -> bool { return warp_all_wait_a(w_full0 + 8 * sa, ph_w, wc); };
+        auto stage_release = [&]() {
+            __syncwarp();
+            mbar_arrive_elect_a(w_empty0 + 8 * sa);
+            if (++sa == kStagesW) {
+                sa = 0;
+                ph_w ^= 1;
+            }
         };
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
             if (!warp_all_wait(&bar.sz_full[szb], ph_sz, wc))
                 break;
-            const int gs0 = static_cast<int>(n_unit) * p.n_kchunks;   // the unit's first stage
             const uint32_t s_addr = sz_base_s + szb * L.sz_stride + 2 * row * p.G;
             const uint32_t z_addr = s_addr + 2 * kTileRows * p.G;
             const int c = row_exponent(row_smax(s_addr, p.G));
             const float scale_s = exp2i(24 - c), scale_c = exp2i(-c);
-            for (int kc = 0; kc < p.n_kchunks; kc++) {
-                const int g = gs0 + kc;
-                const int sa = g % kStagesW;
-                const int j = 4 * kc + r;                 // block of the unit
-                const bool mine = j < n_blocks;
-                // the block's group constants, from the unit's scale stage,
-                // before the codes arrive
-                const uint32_t g0 = static_cast<uint32_t>(j * kSliceK) >> p.group_shift;
-                GroupK k0{};
-                if (mine)
-                    k0 = group_consts(lds_u16(s_addr + 2 * g0), lds_u16(z_addr + 2 * g0), scale_s,
-                                      scale_c);
-                if (!warp_all_wait(&bar.w_full[sa], (g / kStagesW) & 1, wc)) {
+            // stages 0 .. n_my - 1 hold a block of this ring (4 kc + r < n_blocks)
+            const int n_my = (n_blocks - r + 3) >> 2;
+            uint32_t g_off = 2u * ((static_cast<uint32_t>(r) * kSliceK) >> p.group_shift);
+            for (int kc = 0; kc < n_my; kc++, g_off += g_step) {
+                // the block's group constants before the codes arrive
+                const GroupK k0 = group_consts(lds_u16(s_addr + g_off), lds_u16(z_addr + g_off),
+                                               scale_s, scale_c);
+                if (!stage_wait()) {
                     ok = false;
                     break;
                 }
-                const uint32_t rp = stage_w_s + sa * kStageWBytes + row_off;
-                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-                if (mine) {
-                    v0 = lds128(rp + chunk0);
-                    v1 = lds128(rp + chunk1);
-                }
-                __syncwarp();
-                mbar_arrive_elect(&bar.w_empty[sa]);
-                if (!mine)
-                    continue;
+                const uint32_t so = static_cast<uint32_t>(sa * kStageWBytes);
+                const uint4 v0 = lds128(code0 + so), v1 = lds128(code1 + so);
+                stage_release();
                 uint32_t o[16];
                 dequant_word(v0.x, k0.S, k0.S16, k0.C, &o[0]);
                 dequant_word(v0.y, k0.S, k0.S16, k0.C, &o[4]);
@@ -941,8 +954,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     ok = false;
                     break;
                 }
-                if (j == 0)
+                if (kc == 0 && r == 0)   // block 0
                     row_scale[(n_unit & (kRowScaleSets - 1)) * kTileRows + row] = exp2i(c);
+                const uint32_t a_col0 = a_col_ring + fb * kFillCols;
                 // o is read by each store at issue and is free again after it
                 tmem_st_32x32b_x16(a_col0, o);
                 dequant_word(v1.x, k0.S, k0.S16, k0.C, &o[0]);
@@ -951,6 +965,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 dequant_word(v1.w, k0.S, k0.S16, k0.C, &o[12]);
                 tmem_st_32x32b_x16(a_col0 + 16, o);
                 hand_over();
+            }
+            // the unit's last stage when it holds no block of this ring
+            for (int kc = n_my; kc < p.n_kchunks && ok; kc++) {
+                if (!stage_wait()) {
+                    ok = false;
+                    break;
+                }
+                stage_release();
             }
             if (!ok)
                 break;
@@ -969,6 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 constexpr int kRep = GATE_UP ? 1 : 4;
                 if (!claim())
                     break;
+                const uint32_t a_col0 = a_col_ring + fb * kFillCols;
 #pragma unroll
                 for (int t = 0; t < 4; t++) {
                     if (t >= p.n_corr_mma)

@@ -56,7 +56,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+// The barrier helpers come in two forms: by pointer, and by 32-bit shared
+// address (suffix _a) for loops that keep their barriers' addresses in
+// registers.
+__device__ __forceinline__ bool mbar_try_wait_a(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
@@ -64,16 +67,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    return mbar_try_wait_a(smem_u32(bar), parity);
 }
 
 // try_wait with a suspend-time hint: the thread is suspended until the phase
 // completes or about `hint_ns` elapse, so a waiting warp does not spin on the
 // issue slots the working warps of its sub-partition need.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
-                                                    uint32_t hint_ns)
+__device__ __forceinline__ bool mbar_try_wait_sleep_a(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns)
 {
     uint32_t ok;
     asm volatile(
@@ -81,9 +89,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    return mbar_try_wait_sleep_a(smem_u32(bar), parity, hint_ns);
 }
 
 // A pipeline wait with a time limit.  Returns false (and raises the CTA's
@@ -134,16 +148,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // probes the phase (so every lane observes its completion) and one vote
 // decides each branch, so the loop needs no divergence handling.  Same time
 // limit and abort handling as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                               int32_t *dev_status, int32_t timeout_bit,
-                                               uint64_t limit_ns = 1000000000ull)
+__device__ __forceinline__ bool mbar_wait_warp_a(uint32_t bar, uint32_t parity,
+                                                 volatile int *abort_flag, int32_t *dev_status,
+                                                 int32_t timeout_bit,
+                                                 uint64_t limit_ns = 1000000000ull)
 {
     const unsigned full = 0xffffffffu;
-    if (__all_sync(full, mbar_try_wait(bar, parity)))
+    if (__all_sync(full, mbar_try_wait_a(bar, parity)))
         return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (__all_sync(full, mbar_try_wait_sleep(bar, parity, W4_WAIT_HINT_NS)))
+        if (__all_sync(full, mbar_try_wait_sleep_a(bar, parity, W4_WAIT_HINT_NS)))
             return true;
         if ((it & 15u) == 0) {
             if (__any_sync(full, *abort_flag != 0))
@@ -160,14 +175,26 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, v
     }
 }
 
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               int32_t *dev_status, int32_t timeout_bit,
+                                               uint64_t limit_ns = 1000000000ull)
+{
+    return mbar_wait_warp_a(smem_u32(bar), parity, abort_flag, dev_status, timeout_bit, limit_ns);
+}
+
 // One arrival per warp, made by an elected lane without a branch (call with
 // the warp converged, after whatever the arrival must publish).
-__device__ __forceinline__ void mbar_arrive_elect(uint64_t *bar)
+__device__ __forceinline__ void mbar_arrive_elect_a(uint32_t bar)
 {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_elect(uint64_t *bar)
+{
+    mbar_arrive_elect_a(smem_u32(bar));
 }
 
 // A pipeline wait for roles whose wake-up latency matters little (producers
