@@ -536,6 +536,17 @@ __global__ void __launch_bounds__(1024, 1)
             const int c8 = tid + r * nthr;
             ahead[tl][r] = tl < ntok && c8 < c8n ? __ldg(xr + tl * c8n + c8) : make_uint4(0, 0, 0, 0);
         }
+    // this thread's first kIdsAhead ids, loaded before the first barrier so
+    // that their latency overlaps it
+    constexpr int kIdsAhead = 4;
+    int ids_ahead[kIdsAhead];
+    if constexpr (!ROUTE) {
+#pragma unroll
+        for (int i = 0; i < kIdsAhead; i++) {
+            const int a = tid + i * nthr;
+            ids_ahead[i] = a < A ? __ldg(ids + a) : -1;
+        }
+    }
     for (int i = tid; i < E; i += nthr) {
         cnt[i] = 0;
         pre[i] = 0;
@@ -562,8 +573,7 @@ __global__ void __launch_bounds__(1024, 1)
 
     // counts: every valid id, and separately those before own0
     bool bad = false;
-    for (int a = tid; a < A; a += nthr) {
-        const int e = id_at(a);
+    auto count = [&](int a, int e) {
         if (e >= 0 && e < E) {
             atomicAdd(&cnt[e], 1);
             if (a < own0)
@@ -571,30 +581,43 @@ __global__ void __launch_bounds__(1024, 1)
         } else {
             bad = true;
         }
+    };
+    int a_next = tid;
+    if constexpr (!ROUTE) {
+#pragma unroll
+        for (int i = 0; i < kIdsAhead; i++, a_next += nthr)
+            if (a_next < A)
+                count(a_next, ids_ahead[i]);
     }
+    for (int a = a_next; a < A; a += nthr)
+        count(a, id_at(a));
     if (blockIdx.x == 0 && __any_sync(full, bad) && lane == 0 && dev_status)
         atomicOr(dev_status, kDevBadExpertId);
     __syncthreads();
 
-    // padded offsets: exclusive scan of ceil(count / bm) * bm (warp 0)
+    // padded offsets: exclusive scan of ceil(count / bm) * bm (warp 0; lane
+    // l takes the run of experts [l * per, (l + 1) * per): a sum of its run,
+    // one warp scan of the sums, then the run's offsets)
     if (warp == 0) {
-        int base = 0;
-        for (int e0 = 0; e0 < E; e0 += 32) {
-            const int e = e0 + lane;
-            const int padded = e < E ? (cnt[e] + bm - 1) / bm * bm : 0;
-            int inc = padded;
+        const int per = (E + 31) / 32;
+        const int e_lo = min(E, lane * per), e_hi = min(E, e_lo + per);
+        int run = 0;
+        for (int e = e_lo; e < e_hi; e++)
+            run += (cnt[e] + bm - 1) / bm * bm;
+        int inc = run;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(full, inc, o);
-                if (lane >= o)
-                    inc += v;
-            }
-            if (e < E)
-                offs[e] = base + inc - padded;
-            base += __shfl_sync(full, inc, 31);
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(full, inc, o);
+            if (lane >= o)
+                inc += v;
         }
-        if (lane == 0)
-            offs[E] = base;
+        int base = inc - run;
+        for (int e = e_lo; e < e_hi; e++) {
+            offs[e] = base;
+            base += (cnt[e] + bm - 1) / bm * bm;
+        }
+        if (lane == 31)
+            offs[E] = inc;
     }
     __syncthreads();
 
@@ -657,14 +680,16 @@ __global__ void __launch_bounds__(1024, 1)
     if (__any_sync(full, range) && lane == 0 && dev_status)
         atomicOr(dev_status, kDevFp16Range);
 
-    // padding slots and block owners, one expert per thread of the grid; the
-    // slots past the last expert; offsets and num_padded from CTA 0
+    // padding slots and block owners, one expert per warp of the grid (its
+    // lanes over the expert's slots and blocks); the slots past the last
+    // expert; offsets and num_padded from CTA 0
     const int gtid = blockIdx.x * nthr + tid, gstride = gridDim.x * nthr;
-    for (int e = gtid; e < E; e += gstride) {
-        for (int sl = offs[e] + cnt[e]; sl < offs[e + 1]; sl++)
+    const int nwarps = nthr >> 5;
+    for (int e = blockIdx.x + gridDim.x * warp; e < E; e += gridDim.x * nwarps) {
+        for (int sl = offs[e] + cnt[e] + lane; sl < offs[e + 1]; sl += 32)
             if (W4_IN_BOUNDS(sl < cap, dev_status))
                 sorted_ids[sl] = A;
-        for (int b = offs[e] / bm; b < offs[e + 1] / bm; b++)
+        for (int b = offs[e] / bm + lane; b < offs[e + 1] / bm; b += 32)
             if (W4_IN_BOUNDS(b < cap / bm, dev_status))
                 block_expert[b] = e;
     }
