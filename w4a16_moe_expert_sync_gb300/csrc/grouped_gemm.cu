@@ -1099,6 +1099,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     // GEMM's contraction; this warp holds 16 of them and also
                     // writes their sum (of the fp16 values) to sum column
                     // 4 pnl + q4 of the row, the down GEMM's correction input
+                    uint32_t pk[4];   // this lane's fp16 h of slot pairs 2 j, 2 j + 1
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
                         const float send = is_gate ? v[i + 1] : v[i];
@@ -1112,27 +1113,46 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         range |= real && !(fabsf(hv) <= 65504.0f);
                         const uint16_t hq = real ? static_cast<uint16_t>(f16x2_sat(hv, 0.0f)) : 0;
                         uint16_t *hrow = hout + (J.start + si) * static_cast<int64_t>(p.h_stride);
-                        const bool row_ok = W4_IN_BOUNDS(J.start + si < p.cap, status);
-                        if (row_ok && W4_IN_BOUNDS(pos < p.h_stride, status))
+                        if (W4_IN_BOUNDS(J.start + si < p.cap, status) &&
+                            W4_IN_BOUNDS(pos < p.h_stride, status))
                             hrow[pos] = hq;
-                        // lanes 0-15 sum slot i, lanes 16-31 slot i + 1 (fixed tree)
-                        float part = __half2float(__ushort_as_half(hq));
-                        part += __shfl_xor_sync(full, part, 8);
-                        part += __shfl_xor_sync(full, part, 4);
-                        part += __shfl_xor_sync(full, part, 2);
-                        part += __shfl_xor_sync(full, part, 1);
-                        if ((lane & 15) == 0 && row_ok) {
-                            range |= !(fabsf(part) <= 65504.0f);
-                            if (W4_IN_BOUNDS(p.out_cols + 4 * pnl + q4 < p.h_stride, status))
-                                hrow[p.out_cols + 4 * pnl + q4] =
-                                    static_cast<uint16_t>(f16x2_sat(part, 0.0f));
-                            if (pnl == 0)   // sum columns past the last group, read by
-                                            // the correction's last MMA step: zero
-                                for (int c = 4 * p.h_groups + q4;
-                                     c < 16 * ((p.h_groups + 3) / 4); c += 4)
-                                    if (W4_IN_BOUNDS(p.out_cols + c < p.h_stride, status))
-                                        hrow[p.out_cols + c] = 0;
-                        }
+                        if (i & 2)
+                            pk[i >> 2] |= static_cast<uint32_t>(hq) << 16;
+                        else
+                            pk[i >> 2] = hq;
+                    }
+                    // The eight slots' sums over the 16 lanes of each half of
+                    // the warp (lanes 0-15 the even slots, 16-31 the odd
+                    // ones): a butterfly that keeps half of the values at each
+                    // step, pairing lanes by xor 8, 4, 2, 1 (the same fixed
+                    // tree for every slot); lanes 2 m and 2 m + 1 of a half
+                    // end with the sum of its pair m.
+                    const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+                    float s4[4], s2[2];
+#pragma unroll
+                    for (int w2 = 0; w2 < 2; w2++) {
+                        const __half2 kh = u2h(b3 ? pk[w2 + 2] : pk[w2]);
+                        const __half2 rh = u2h(__shfl_xor_sync(full, b3 ? pk[w2] : pk[w2 + 2], 8));
+                        s4[2 * w2] = __low2float(kh) + __low2float(rh);
+                        s4[2 * w2 + 1] = __high2float(kh) + __high2float(rh);
+                    }
+#pragma unroll
+                    for (int m = 0; m < 2; m++)
+                        s2[m] = (b2 ? s4[m + 2] : s4[m]) +
+                                __shfl_xor_sync(full, b2 ? s4[m] : s4[m + 2], 4);
+                    float sum = (b1 ? s2[1] : s2[0]) + __shfl_xor_sync(full, b1 ? s2[0] : s2[1], 2);
+                    sum += __shfl_xor_sync(full, sum, 1);
+                    const int si = 16 * half + 2 * ((lane >> 1) & 7) + (is_gate ? 0 : 1);
+                    if ((lane & 1) == 0 && si < J.n && W4_IN_BOUNDS(J.start + si < p.cap, status)) {
+                        uint16_t *hrow = hout + (J.start + si) * static_cast<int64_t>(p.h_stride);
+                        range |= !(fabsf(sum) <= 65504.0f);
+                        if (W4_IN_BOUNDS(p.out_cols + 4 * pnl + q4 < p.h_stride, status))
+                            hrow[p.out_cols + 4 * pnl + q4] = static_cast<uint16_t>(f16x2_sat(sum, 0.0f));
+                        if (pnl == 0)   // sum columns past the last group, read by the
+                                        // correction's last MMA step: zero
+                            for (int c = 4 * p.h_groups + q4; c < 16 * ((p.h_groups + 3) / 4); c += 4)
+                                if (W4_IN_BOUNDS(p.out_cols + c < p.h_stride, status))
+                                    hrow[p.out_cols + c] = 0;
                     }
                 } else {
                     const int col = pnl * 128 + row;
