@@ -65,24 +65,27 @@ def b_kcols(n):
 
 
 class Grouped:
-    def __init__(self, K, units, rng, group=None):
+    def __init__(self, K, units, rng, group=None, big=False):
+        """big: the big-job mode (jobs of up to 64 slots, activations always
+        streamed, two issuers taking rings r and r + 2)."""
         self.K, self.units, self.rng = K, units, rng
+        self.n_iss = 2 if big else ISSUERS
         group = group or (128 if K % 128 == 0 and K > 704 else 64)
         self.G = K // group
         self.n_sz = sz_stages(self.G)
         self.n_kchunks = (K + CHUNK_K - 1) // CHUNK_K
         self.n_blocks = K // SLICE_K
-        self.resident = (K + 64) * 2 * MAX_N <= RES_BYTES
+        self.resident = not big and (K + 64) * 2 * MAX_N <= RES_BYTES
         self.stages_w = STAGES_W_RESIDENT if self.resident else STAGES_W_STREAMED
         B = lambda name, n, c: [Bar(f"{name}{i}", c) for i in range(n)]
         self.w_full = B("w_full", self.stages_w, 1)
         self.w_empty = B("w_empty", self.stages_w, DQ_WARPS)
         nb = 2 if self.resident else STAGES_B
-        self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, ISSUERS)
+        self.b_full, self.b_empty = B("b_full", nb, 1), B("b_empty", nb, self.n_iss)
         # ring r's buffer b is a_full / a_empty [r * RING_BUFS + b]
         self.a_full = B("a_full", RINGS * RING_BUFS, 4)
         self.a_empty = B("a_empty", RINGS * RING_BUFS, 1)
-        self.acc_full, self.acc_empty = B("acc_full", SETS, ISSUERS), B("acc_empty", SETS, EPI_WARPS)
+        self.acc_full, self.acc_empty = B("acc_full", SETS, self.n_iss), B("acc_empty", SETS, EPI_WARPS)
         self.sz_full = B("sz_full", self.n_sz, 1)
         self.sz_empty = B("sz_empty", self.n_sz, DQ_WARPS)
         # row-scale tables (dequant -> epilogue), one entry per lane quarter
@@ -136,17 +139,20 @@ class Grouped:
                     sb, ph_b = 0, ph_b ^ 1
 
     def issuer(self, me):
-        fill = 0
+        fill = {}               # per ring this issuer takes: its fills so far
         acc_use, b_use = [0] * SETS, [0] * (2 if self.resident else STAGES_B)
         cur_job, res_slot, b_seq = None, 0, 0
         nb = self.n_blocks
 
-        def issue():
-            nonlocal fill
-            buf = me * RING_BUFS + fill % RING_BUFS
-            yield ("wait", self.a_full[buf], (fill // RING_BUFS) & 1, fill // RING_BUFS)
-            fill += 1
+        def issue(ring):
+            f = fill.get(ring, 0)
+            buf = ring * RING_BUFS + f % RING_BUFS
+            yield ("wait", self.a_full[buf], (f // RING_BUFS) & 1, f // RING_BUFS)
+            fill[ring] = f + 1
             yield ("commit", me, self.a_empty[buf])
+
+        def mine(ring):
+            return ring % self.n_iss == me
 
         for n_unit, (job, n) in enumerate(self.units):
             st, acc_ph = n_unit & 1, (n_unit >> 1) & 1
@@ -161,10 +167,11 @@ class Grouped:
                     b_use[res_slot] += 1
                     b_seq += 1
                     cur_job = job
-                for j in range(me, nb, RINGS):
-                    yield from issue()
-                if me == corr:
-                    yield from issue()
+                for j in range(nb):
+                    if mine(block_ring(j)):
+                        yield from issue(block_ring(j))
+                if mine(corr):
+                    yield from issue(corr)
             else:
                 kcols = b_kcols(n)
                 n_bslots = nb // kcols + 1
@@ -173,10 +180,10 @@ class Grouped:
                     yield ("wait", self.b_full[sb], ((b_seq + t) // STAGES_B) & 1, b_use[sb])
                     b_use[sb] += 1
                     for j in range(t * kcols, min(nb, (t + 1) * kcols)):
-                        if block_ring(j) == me:
-                            yield from issue()
-                    if t == n_bslots - 1 and me == corr:
-                        yield from issue()
+                        if mine(block_ring(j)):
+                            yield from issue(block_ring(j))
+                    if t == n_bslots - 1 and mine(corr):
+                        yield from issue(corr)
                     yield ("commit", me, self.b_empty[sb])
                 b_seq += n_bslots
             yield ("commit", me, self.acc_full[st])
@@ -237,7 +244,7 @@ class Grouped:
 
     def run(self):
         roles = [self.tma_w(0), self.tma_w(1), self.tma_b()]
-        roles += [self.issuer(i) for i in range(ISSUERS)]
+        roles += [self.issuer(i) for i in range(self.n_iss)]
         roles += [self.dequant(w // 4, w % 4) for w in range(DQ_WARPS)]   # 4 lane quarters per ring
         roles += [self.epilogue(q) for q in range(EPI_WARPS)]
         nxt = [next(r, None) for r in roles]
@@ -292,12 +299,12 @@ class Grouped:
             nxt[i] = next(roles[i], None)
 
 
-def _units(rng, n_units):
+def _units(rng, n_units, big=False):
     """A CTA's unit list: panels of jobs in the kernel's round-robin order,
     consecutive units sometimes of the same job (short expert lists)."""
     units, job = [], 0
     while len(units) < n_units:
-        n = rng.choice((16, 32))
+        n = rng.choice((16, 32, 48, 64) if big else (16, 32))
         for _ in range(rng.randint(1, 3)):
             units.append((job, n))
         job += 1
@@ -309,6 +316,15 @@ def _units(rng, n_units):
 def test_grouped_pipeline_protocol(K, seed):
     rng = random.Random(seed * 104729 + K)
     Grouped(K, _units(rng, rng.randint(1, 7)), rng).run()
+
+
+@pytest.mark.parametrize("K", [2816, 704, 384, 192])
+@pytest.mark.parametrize("seed", range(8))
+def test_grouped_pipeline_protocol_big_jobs(K, seed):
+    """Big-job mode: jobs of 16 to 64 slots, streamed activations, two
+    issuers taking two rings each."""
+    rng = random.Random(seed * 7919 + K)
+    Grouped(K, _units(rng, rng.randint(1, 7), big=True), rng, big=True).run()
 
 
 def test_the_grouped_model_catches_a_broken_protocol():

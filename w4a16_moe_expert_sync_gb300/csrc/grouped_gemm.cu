@@ -39,7 +39,8 @@
 //
 // Design (one persistent CTA of 28 warps per SM, static round-robin schedule):
 //   * A work unit is (job, panel).  A job is at most 32 consecutive slots of
-//     one expert; a panel is 128 weight rows (gate_up: 64 gate rows and the
+//     one expert (64 in big-job mode, when the experts average 64 or more
+//     slots); a panel is 128 weight rows (gate_up: 64 gate rows and the
 //     matching 64 up rows; down: 128 output rows).
 //   * Swap-AB: the 128 weight rows are the M = 128 operand, in tensor memory
 //     (written with tcgen05.st), the job's tokens are N (16 or 32).  B, the
@@ -122,6 +123,15 @@ constexpr int kStageWBytes = kTileRows * kChunkK / 2;   // 16 KB
 constexpr int kStageBBytes = 32768;
 constexpr int kResSlotBytes = kStagesB * kStageBBytes / 2;   // resident mode: 2 x 48 KB
 constexpr int kMaxN = 32;                   // slots per job
+// Big-job mode (many tokens per expert): jobs of up to 64 slots, so each
+// weight panel is dequantised once per 64 tokens; its accumulators take
+// twice the columns, so two issuers take two rings each and keep two
+// chains.  Activations always stream in this mode.
+constexpr int kMaxNBig = 64;
+template <bool BIGN> struct JobShape {
+    static constexpr int kMaxN = BIGN ? kMaxNBig : ::w4::kMaxN;
+    static constexpr int kIssuers = BIGN ? 2 : 4;   // issuers with MMAs (= chains)
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = kRings * kRingBufs * kFillCols;  // 256
 // Accumulators: one per issuer ("chain" i of issuer i), at kAccCol + 128 set
@@ -139,11 +149,13 @@ constexpr int kRowScaleSets = 8;
 // (a longer list is combined as it overflows).
 constexpr int kCombListCap = 1024;
 static_assert(kAccCol + 2 * kChains * kMaxN <= kTmemCols, "tensor memory budget");
+static_assert(kAccCol + 2 * JobShape<true>::kIssuers * kMaxNBig <= kTmemCols,
+              "tensor memory budget (big jobs)");
 static_assert(kStagesW % 2 == 0, "a dequant warp must see every phase of its stage slots");
 
 struct GemmArgs {
     CUtensorMap tmap_w;       // packed codes u8 [E*R rows, K/2 B], box 128 B x 64 rows, SW128
-    CUtensorMap tmap_b[2];    // activations [cap, K] fp16 as {64, cap, K/64}, box {64, 16(i+1), kcols}
+    CUtensorMap tmap_b[4];    // activations [cap, K] fp16 as {64, cap, K/64}, box {64, 16(i+1), kcols}
     const uint16_t *sc;       // [E*R, G] fp16
     const uint16_t *zp;       // [E*R, G] fp16
     const int32_t *sorted_ids;
@@ -233,8 +245,9 @@ struct Job {
 };
 
 // Job j of the schedule: the expert whose job range holds j (jp = exclusive
-// prefix of jobs per expert) and its j - jp[e]-th block of kMaxN slots.
-__device__ __forceinline__ Job decode_job(const int *jp, const int *offs, int E, int j)
+// prefix of jobs per expert) and its j - jp[e]-th block of maxn slots.
+__device__ __forceinline__ Job decode_job(const int *jp, const int *offs, int E, int j,
+                                          int maxn = kMaxN)
 {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -246,8 +259,8 @@ __device__ __forceinline__ Job decode_job(const int *jp, const int *offs, int E,
     }
     Job J;
     J.e = lo;
-    J.start = offs[lo] + (j - jp[lo]) * kMaxN;
-    J.n = min(kMaxN, offs[lo + 1] - J.start);
+    J.start = offs[lo] + (j - jp[lo]) * maxn;
+    J.n = min(maxn, offs[lo + 1] - J.start);
     return J;
 }
 
@@ -517,9 +530,12 @@ __device__ __forceinline__ void combine_count(const GemmArgs &p, const Job &J, i
 
 // RESIDENT: each job's activations are loaded once into one of two 48 KB
 // slots (contraction dim <= 768); otherwise they stream through 32 KB slots.
-template <bool GATE_UP, bool RESIDENT>
+template <bool GATE_UP, bool RESIDENT, bool BIGN>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p)
 {
+    constexpr int kJobN = JobShape<BIGN>::kMaxN;         // slots per job
+    constexpr int kIss = JobShape<BIGN>::kIssuers;       // issuers with MMAs, chains
+    static_assert(!(BIGN && RESIDENT), "big jobs stream their activations");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -551,14 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int i = 0; i < kStagesB; i++) {
             mbar_init(&bar.b_full[i], 1);
-            mbar_init(&bar.b_empty[i], kNumIssuers);   // every issuer's commit
+            mbar_init(&bar.b_empty[i], kIss);   // every active issuer's commit
         }
         for (int i = 0; i < kRings * kRingBufs; i++) {
             mbar_init(&bar.a_full[i], 4);            // the ring's four lane quarters
             mbar_init(&bar.a_empty[i], 1);           // the ring's issuer's commit
         }
         for (int i = 0; i < 2; i++) {
-            mbar_init(&bar.acc_full[i], kNumIssuers);
+            mbar_init(&bar.acc_full[i], kIss);
             mbar_init(&bar.acc_empty[i], kNumEpiWarps);
         }
         for (int i = 0; i < kMaxStagesSZ; i++) {
@@ -577,8 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
     if (warp == kWarpTmaW && lane == 0) {
         prefetch_tmap(&p.tmap_w);
-        prefetch_tmap(&p.tmap_b[0]);
-        prefetch_tmap(&p.tmap_b[1]);
+        for (int i = 0; i < kJobN / 16; i++)
+            prefetch_tmap(&p.tmap_b[i]);
     }
     // everything above touched only this CTA; from here on the inputs of the
     // preceding kernels are read (the schedule possibly early, see GemmArgs)
@@ -592,12 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
 
-    // jobs per expert (ceil(slots / kMaxN)), exclusive prefix in jp[0..E]
+    // jobs per expert (ceil(slots / kJobN)), exclusive prefix in jp[0..E]
     if (warp == kFirstEpiWarp) {
         int base = 0;
         for (int e0 = 0; e0 < p.E; e0 += 32) {
             const int e = e0 + lane;
-            const int nj = e < p.E ? (offs[e + 1] - offs[e] + kMaxN - 1) / kMaxN : 0;
+            const int nj = e < p.E ? (offs[e + 1] - offs[e] + kJobN - 1) / kJobN : 0;
             int inc = nj;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -619,19 +635,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int K = p.K;
     const int n_blocks = p.n_blocks;     // 64-code blocks along K
 
-    if (warp < kNumIssuers) {
+    if (warp < kIss) {
         // ------------------------------------------------------ MMA issuers
         // Issuer r takes the fills of ring r in order: the unit's blocks j
         // with block_ring(j) == r, four K = 16 MMAs and the commit that frees
         // the buffer as one issue block each, then the correction when r is
         // the unit's correction ring, into its own accumulator.  Four issuers,
-        // one per SM sub-partition.  The warp runs this loop converged (every
-        // value in it is warp-uniform, kept in registers) and one elected
-        // lane issues each tcgen05 instruction.
+        // one per SM sub-partition.  (Big jobs: issuer r takes rings r and
+        // r + 2, blocks with j % 2 == r, into its one chain.)  The warp runs
+        // this loop converged (every value in it is warp-uniform, kept in
+        // registers) and one elected lane issues each tcgen05 instruction.
         const int me = warp;
         const uint32_t b_base = smem_u32(stage_b);
         uint32_t b_seq = 0, n_unit = 0;
-        uint32_t fill = 0;      // fills of this ring so far: buffer fill % kRingBufs
+        // fills so far of ring me (low half) and, big jobs, ring me + 2 (high
+        // half): buffer fill % kRingBufs
+        uint32_t fills = 0;
         int cur_job = -1;       // resident mode: the job whose activations are held
         uint32_t res_slot = 0;
         bool ok = true;
@@ -640,13 +659,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         // buffer, issue its MMAs (four; n_corr_mma for the correction) with B
         // at the descriptor bdesc of the block's 64-code column block, and
         // release the buffer.
-        auto issue = [&](int j, uint32_t d_tmem, uint64_t bdesc, uint32_t idesc) -> bool {
+        auto issue = [&](int j, int ring, uint32_t d_tmem, uint64_t bdesc, uint32_t idesc) -> bool {
             const int n_mma = j == n_blocks ? p.n_corr_mma : 4;
-            const int buf = me * kRingBufs + static_cast<int>(fill % kRingBufs);
+            const int sh = ring == me ? 0 : 16;
+            const uint32_t fill = (fills >> sh) & 0xFFFFu;
+            const int buf = ring * kRingBufs + static_cast<int>(fill % kRingBufs);
             const uint32_t a_tmem = tmem + static_cast<uint32_t>(buf) * kFillCols;
             if (!warp_all_wait(&bar.a_full[buf], (fill / kRingBufs) & 1, wc))
                 return false;
-            fill++;
+            fills = (fills & ~(0xFFFFu << sh)) | (((fill + 1) & 0xFFFFu) << sh);
             tc_fence_after();
             // K steps of 16: +32 B in the swizzled row (+2 in the descriptor's
             // address field), +8 columns of A
@@ -657,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         };
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
             const int job = u / p.n_panels;
-            const Job J = decode_job(jp, offs, p.E, job);
+            const Job J = decode_job(jp, offs, p.E, job, kJobN);
             const uint32_t idesc = idesc_f16_f32(kTileRows, J.n);
             const uint32_t col_bytes = static_cast<uint32_t>(J.n) * 128;
             const int set = n_unit & 1;
@@ -668,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + kAccCol + set * (kChains * kMaxN) + me * kMaxN;
+            const uint32_t d_tmem = tmem + kAccCol + set * (kIss * kJobN) + me * kJobN;
             started = false;
             if constexpr (RESIDENT) {
                 // the job's activations stay in one slot for all its units
@@ -686,12 +707,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 const uint32_t b_slot = b_base + res_slot * kResSlotBytes;
                 for (int j = me; j < n_blocks && ok; j += kRings)
-                    if (!issue(j, d_tmem, sdesc_sw128(b_slot + static_cast<uint32_t>(j) * col_bytes),
-                               idesc))
+                    if (!issue(j, j & (kRings - 1), d_tmem,
+                               sdesc_sw128(b_slot + static_cast<uint32_t>(j) * col_bytes), idesc))
                         ok = false;
                 // the correction reads block n_blocks (the group sums)
                 if (ok && me == corr &&
-                    !issue(n_blocks, d_tmem,
+                    !issue(n_blocks, corr, d_tmem,
                            sdesc_sw128(b_slot + static_cast<uint32_t>(n_blocks) * col_bytes),
                            idesc))
                     ok = false;
@@ -710,14 +731,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const int j0 = t * kcols;
                     const int j1 = min(n_blocks, j0 + kcols);
                     for (int j = j0; j < j1 && ok; j++)
-                        if (block_ring(j) == me &&
-                            !issue(j, d_tmem,
+                        if (block_ring(j) % kIss == me &&
+                            !issue(j, block_ring(j), d_tmem,
                                    sdesc_sw128(b_slot + static_cast<uint32_t>(j - j0) * col_bytes),
                                    idesc))
                             ok = false;
-                    if (ok && t == n_bslots - 1 && me == corr) {
+                    if (ok && t == n_bslots - 1 && corr % kIss == me) {
                         const uint32_t blk = static_cast<uint32_t>(n_blocks - t * kcols);
-                        if (!issue(n_blocks, d_tmem, sdesc_sw128(b_slot + blk * col_bytes), idesc))
+                        if (!issue(n_blocks, corr, d_tmem, sdesc_sw128(b_slot + blk * col_bytes),
+                                   idesc))
                             ok = false;
                     }
                     if (!ok)
@@ -734,6 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tc_commit_elect(&bar.drain[me]);
         drain_wait(&bar.drain[me], 0);
         __syncwarp();
+    } else if (warp < kNumIssuers) {
+        // big jobs: issuers 2-3 idle
     } else if (warp == kWarpTmaW || warp == kWarpTmaW1) {
         // ------------------------------------------- TMA: codes, scales/zeros
         // Two producer threads, one per parity gp of the CTA's stage sequence:
@@ -749,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             bool ok = true;
             int n_unit = 0;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, n_unit++) {
-                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                const Job J = decode_job(jp, offs, p.E, u / p.n_panels, kJobN);
                 const int pnl = u % p.n_panels;
                 const int row0 = J.e * p.R + pnl * (GATE_UP ? 64 : 128);
                 const int row1 = GATE_UP ? row0 + p.m_up : row0 + 64;
@@ -820,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     if (job == cur_job)
                         continue;
                     cur_job = job;
-                    const Job J = decode_job(jp, offs, p.E, job);
+                    const Job J = decode_job(jp, offs, p.E, job, kJobN);
                     const int s = b_seq & 1;
                     const uint32_t ph = (b_seq >> 1) & 1;
                     if (!lane_wait(&bar.b_empty[s], ph ^ 1, wc)) {
@@ -837,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
             } else {
                 for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                    const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                    const Job J = decode_job(jp, offs, p.E, u / p.n_panels, kJobN);
                     const CUtensorMap *map = &p.tmap_b[J.n / 16 - 1];
                     const int kcols = b_kcols(J.n);
                     const uint32_t bytes = static_cast<uint32_t>(J.n) * 128 * kcols;
@@ -1045,13 +1069,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int il = 16 * q4 + (lane & 15);     // intermediate index in the panel
         uint32_t n_unit = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, n_unit++) {
-            const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+            const Job J = decode_job(jp, offs, p.E, u / p.n_panels, kJobN);
             const int pnl = u % p.n_panels;
             const int set = n_unit & 1;
             const uint32_t acc_ph = (n_unit >> 1) & 1;
             // the assignment of every slot of the job, fetched early (gate_up:
             // padding slots get zero rows; down: rows go to y by assignment)
             const int my_a = lane < J.n ? __ldg(p.sorted_ids + J.start + lane) : -1;
+            // big jobs: slots 32 .. 63
+            const int my_a2 =
+                BIGN && lane + 32 < J.n ? __ldg(p.sorted_ids + J.start + 32 + lane) : -1;
             if (!warp_all_wait(&bar.acc_full[set], acc_ph, wc))
                 break;
             tc_fence_after();
@@ -1062,9 +1089,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             float *yout = reinterpret_cast<float *>(p.out);
             const int pos = pnl * 64 + (il & ~7) + korder_pos(il & 7);    // gate_up
             bool range = false;
-            // two passes of 16 slots (one for a 16-slot job)
+            // passes of 16 slots (one for a 16-slot job)
 #pragma unroll 1
-            for (int half = 0; half < 2; half++) {
+            for (int half = 0; half < kJobN / 16; half++) {
                 if (half * 16 >= J.n)
                     break;
                 float v[16];
@@ -1074,12 +1101,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     for (int i = 0; i < 16; i++)
                         v[i] = 0.0f;
 #pragma unroll
-                    for (int c = 0; c < kChains; c++) {
+                    for (int c = 0; c < kIss; c++) {
                         if (!(mask >> c & 1))
                             continue;
                         uint32_t rr[16];
-                        tmem_ld_32x32b_x16(tmem + lane_base + kAccCol + set * (kChains * kMaxN) +
-                                               c * kMaxN + 16 * half,
+                        tmem_ld_32x32b_x16(tmem + lane_base + kAccCol + set * (kIss * kJobN) +
+                                               c * kJobN + 16 * half,
                                            rr);
 #pragma unroll
                         for (int i = 0; i < 16; i++)
@@ -1107,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         const float gv = is_gate ? v[i] : recv;
                         const float uv = is_gate ? recv : v[i + 1];
                         const int si = 16 * half + i + (is_gate ? 0 : 1);
-                        const int a = __shfl_sync(full, my_a, si);
+                        const int a = __shfl_sync(full, half < 2 ? my_a : my_a2, si & 31);
                         const bool real = static_cast<unsigned>(a) < static_cast<unsigned>(p.A);
                         const float hv = gelu_tanh(gv) * uv;
                         range |= real && !(fabsf(hv) <= 65504.0f);
@@ -1158,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const int col = pnl * 128 + row;
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
-                        const int a = __shfl_sync(full, my_a, 16 * half + i);
+                        const int a = __shfl_sync(full, half < 2 ? my_a : my_a2, (16 * half + i) & 31);
                         if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A) &&
                             W4_IN_BOUNDS(col < p.out_cols, status))
                             yout[static_cast<int64_t>(a) * p.out_cols + col] = v[i];
@@ -1201,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int n = warp; n * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x) < n_units;
                  n += kNumWarps) {
                 const int u = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
-                const Job J = decode_job(jp, offs, p.E, u / p.n_panels);
+                const Job J = decode_job(jp, offs, p.E, u / p.n_panels, kJobN);
                 combine_count(p, J, u % p.n_panels, lane, comb_list, comb_count);
             }
             __syncthreads();
@@ -1234,7 +1261,7 @@ EncodeTiledFn get_encode_fn()
 
 struct DeviceInfo {
     int sms = 0, smem_optin = 0;
-    bool attr_set[3] = {false, false, false};
+    bool attr_set[5] = {false, false, false, false, false};
 };
 
 DeviceInfo &device_info(int dev)
@@ -1329,12 +1356,17 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         return cudaErrorInvalidValue;
     }
     a.n_corr_mma = (a.G * corr_rep + 15) / 16;
+    // Big jobs when the batch gives the experts 64 or more slots on average
+    // (not with the folded combine, which counts a job's slots with one warp).
+    const bool bign =
+        q.comb_cnt == nullptr && static_cast<int64_t>(q.M) * q.k >= static_cast<int64_t>(kMaxNBig) * q.E;
+    const int n_iss = bign ? JobShape<true>::kIssuers : JobShape<false>::kIssuers;
     // the accumulators (issuers) that receive MMAs in the CTA's unit n, by
     // n % 4
     for (int n = 0; n < 4; n++) {
-        a.acc_mask[n] = 1 << corr_ring(n, a.n_blocks);
+        a.acc_mask[n] = 1 << (corr_ring(n, a.n_blocks) % n_iss);
         for (int j = 0; j < a.n_blocks; j++)
-            a.acc_mask[n] |= 1 << block_ring(j);
+            a.acc_mask[n] |= 1 << (block_ring(j) % n_iss);
     }
     a.h_stride = q.gate_up ? q.R / 2 + 64 : 0;
     a.h_groups = q.gate_up ? (q.R / 2) / 64 : 0;
@@ -1349,7 +1381,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
     a.cap = q.cap;
     a.wait_ns = q.wait_ns;
     a.test_withhold_sz = q.test_withhold_sz ? 1 : 0;
-    const bool resident = !q.gate_up && b_fits_resident(q.K);
+    const bool resident = !q.gate_up && !bign && b_fits_resident(q.K);
 
     const SmemLayout L = smem_layout(a.G, a.E, q.gate_up);
     const size_t smem = static_cast<size_t>(L.total) + 1024;
@@ -1374,7 +1406,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         *why = "cuTensorMapEncodeTiled rejected the packed weight tensor";
         return cudaErrorInvalidValue;
     }
-    for (int i = 0; i < 2; i++) {
+    for (int i = 0; i < (bign ? kMaxNBig : kMaxN) / 16; i++) {
         const int rows = 16 * (i + 1);
         const int kcols = resident ? q.K / 64 + 1 : b_kcols(rows);
         if (!encode_act(encode, &a.tmap_b[i], q.act, q.cap, q.K + 64, rows, kcols)) {
@@ -1383,10 +1415,12 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         }
     }
 
-    auto kern = q.gate_up ? grouped_gemm_kernel<true, false>
-                : resident ? grouped_gemm_kernel<false, true>
-                           : grouped_gemm_kernel<false, false>;
-    const int which = q.gate_up ? 2 : (resident ? 1 : 0);
+    auto kern = q.gate_up ? (bign ? grouped_gemm_kernel<true, false, true>
+                                  : grouped_gemm_kernel<true, false, false>)
+                : resident ? grouped_gemm_kernel<false, true, false>
+                : bign     ? grouped_gemm_kernel<false, false, true>
+                           : grouped_gemm_kernel<false, false, false>;
+    const int which = q.gate_up ? (bign ? 4 : 2) : resident ? 1 : bign ? 3 : 0;
     if (!di.attr_set[which]) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    di.smem_optin);
