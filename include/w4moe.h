@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W4MOE_ABI_VERSION 8
+#define W4MOE_ABI_VERSION 9
 
 /* Opaque CUDA stream; ABI-identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *w4_stream_t;
@@ -354,6 +354,31 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
                  const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
                  void *workspace, size_t workspace_bytes, uint16_t *out,
                  int32_t *dev_status, w4_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * w4_moe_layer_host -- w4_moe_layer with the step's activations, routing
+ * and output in host memory: on `stream` it copies x [M, d] bf16, topk_ids
+ * [M, k] and topk_weights [M, k] from the host into staging buffers in the
+ * workspace (one cudaMemcpyAsync each), runs the layer's four launches and
+ * copies out [M, d] bf16 back to out_host.  Everything is enqueued
+ * asynchronously: with page-locked host buffers the copies overlap other
+ * streams' work, and the call returns before they finish, so synchronise
+ * the stream before reading out_host or changing the host inputs.  Calls on
+ * different streams with different workspaces may run concurrently.
+ *
+ * workspace: device buffer of at least w4_moe_layer_host_workspace_size(...)
+ * bytes, 256-byte aligned: the layer's workspace followed by the staging
+ * buffers.  Weights, dev_status and the shape rules as w4_moe_layer; a host
+ * pointer that is NULL while M > 0 is W4_ERR_INVALID_ARG; M = 0 does nothing.
+ * ------------------------------------------------------------------------ */
+size_t w4_moe_layer_host_workspace_size(int M, int d, int m, int E, int k, int block_m);
+int w4_moe_layer_host(const uint16_t *x_host, const int32_t *topk_ids_host,
+                      const float *topk_weights_host, int M, int d, int m, int E, int k,
+                      int block_m,
+                      const uint8_t *gu_q, const uint16_t *gu_s, const uint16_t *gu_z, int gu_group,
+                      const uint8_t *dn_q, const uint16_t *dn_s, const uint16_t *dn_z, int dn_group,
+                      void *workspace, size_t workspace_bytes, uint16_t *out_host,
+                      int32_t *dev_status, w4_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * w4_moe_layer_from_logits -- w4_moe_layer with the router in its first

@@ -39,7 +39,7 @@ def test_header_compiles_as_plain_c():
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4_abi_version() == 8
+    assert clib.w4_abi_version() == 9
     assert clib.w4_status_string(0) == b"W4_OK"
     assert clib.w4_status_string(2) == b"W4_ERR_UNSUPPORTED_SHAPE"
     assert clib.w4_status_string(99) == b"W4_ERR_UNKNOWN"
@@ -97,6 +97,19 @@ def test_argument_validation_without_launching(clib):
     # workspace too small
     assert clib.w4_moe_layer(fake, fake, fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128,
                              fake, fake, fake, 64, fake, 16, fake, None, None) == 6
+    # the host-buffer layer: NULL host buffer, workspace too small, misaligned
+    # workspace (all before any copy or launch); the staging follows the layer
+    hargs = [fake, fake, fake, 16, 256, 128, 8, 2, 16, fake, fake, fake, 128, fake, fake, fake,
+             64, fake, 1 << 30, None, None, None]
+    assert clib.w4_moe_layer_host(*hargs) == 1
+    need = clib.w4_moe_layer_host_workspace_size(16, 256, 128, 8, 2, 16)
+    assert need > clib.w4_moe_layer_workspace_size(16, 256, 128, 8, 2, 16) + 2 * 2 * 16 * 256
+    hargs[19] = fake
+    hargs[18] = need - 1
+    assert clib.w4_moe_layer_host(*hargs) == 6
+    hargs[18] = need
+    hargs[17] = P(0x10040)
+    assert clib.w4_moe_layer_host(*hargs) == 3
 
 
 def test_binding_raises_on_cpu_tensors():

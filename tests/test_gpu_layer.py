@@ -232,3 +232,33 @@ def test_layer_rejects_shapes_beyond_shared_memory_before_launching(lib):
     assert e.value.status == 2 and "shared memory" in str(e.value)
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "layer256", "canvas2048"])
+def test_layer_from_host_buffers_equals_the_device_call(lib, name):
+    """w4_moe_layer_host (x, ids, weights and out in page-locked host memory,
+    copied on the stream) gives out bit-identical to w4_moe_layer on the same
+    inputs, also with two calls in flight on two streams with their own
+    workspaces; M = 0 does nothing."""
+    import torch
+    cfg, x, lg, _, _ = gpu_inputs(name)
+    gu, dn = gpu_weights(name)
+    ids, w = lib.w4_moe_route(lg, cfg.k)
+    ref = lib.w4_moe_layer(x, ids, w, gu, dn)
+    x_h, ids_h, w_h = (t.cpu().pin_memory() for t in (x, ids, w))
+    need = lib.w4_moe_layer_host_workspace_size(cfg.M, cfg.d, cfg.m, cfg.E, cfg.k)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty((cfg.M, cfg.d), dtype=torch.bfloat16).pin_memory() for _ in streams]
+    wss = [torch.full((need,), 255, dtype=torch.uint8, device="cuda") for _ in streams]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for s, o, ws in zip(streams, outs, wss):
+            lib.w4_moe_layer_host(x_h, ids_h, w_h, gu, dn, o, ws, stream=s)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), ref.cpu().view(torch.int16))
+    empty = torch.zeros((0, cfg.d), dtype=torch.bfloat16).pin_memory()
+    lib.w4_moe_layer_host(empty, torch.zeros((0, cfg.k), dtype=torch.int32).pin_memory(),
+                          torch.zeros((0, cfg.k), dtype=torch.float32).pin_memory(), gu, dn,
+                          empty, wss[0])
+    torch.cuda.synchronize()

@@ -17,7 +17,8 @@ from ._lib import (W4_DEV_BAD_EXPERT_ID, W4_DEV_FP16_RANGE, W4_DEV_OUT_OF_BOUNDS
                    w4_grouped_gemm_gate_up, w4_moe_align, w4_moe_align_capacity,
                    w4_moe_combine_fixed_order, w4_moe_combine_prepare,
                    w4_grouped_gemm_down_combine, w4_moe_layer, w4_moe_layer_static_scratch,
-                   w4_moe_layer_workspace_size, w4_moe_layer_from_logits,
+                   w4_moe_layer_workspace_size, w4_moe_layer_from_logits, w4_moe_layer_host,
+                   w4_moe_layer_host_workspace_size,
                    w4_moe_route, w4_moe_route_align_gather, w4_quantize, w4_rmsnorm,
                    w4_sample_logits, w4_sample_logits_workspace_size, w4_fused_entropy,
                    w4_gumbel_argmax_sample, w4_w4a16_linear, w4_w4a16_linear_workspace_size)
@@ -29,6 +30,7 @@ __all__ = [
     "w4_grouped_gemm_gate_up", "w4_grouped_gemm_down", "w4_moe_combine_fixed_order",
     "w4_moe_combine_prepare", "w4_grouped_gemm_down_combine",
     "w4_moe_layer", "w4_moe_layer_workspace_size", "w4_moe_layer_static_scratch",
+    "w4_moe_layer_host", "w4_moe_layer_host_workspace_size",
     "w4_moe_route_align_gather", "w4_moe_layer_from_logits", "w4_rmsnorm", "w4_sample_logits",
     "w4_sample_logits_workspace_size", "w4_fused_entropy", "w4_gumbel_argmax_sample",
     "w4_w4a16_linear", "w4_w4a16_linear_workspace_size",

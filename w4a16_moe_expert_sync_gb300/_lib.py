@@ -82,6 +82,9 @@ def load_library(path: str | None = None):
             "w4_moe_layer_workspace_size": ([I, I, I, I, I, I], SZ),
             "w4_moe_layer": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V, SZ, V, V,
                               V], I),
+            "w4_moe_layer_host_workspace_size": ([I, I, I, I, I, I], SZ),
+            "w4_moe_layer_host": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V, SZ, V,
+                                   V, V], I),
             "w4_moe_layer_static_scratch": ([V, V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I,
                                              V, V, V], I),
             "w4_moe_layer_from_logits": ([V, V, I, I, I, I, I, I, V, V, V, I, V, V, V, I, V,
@@ -367,6 +370,36 @@ def w4_moe_layer(x, topk_ids, topk_weights, gu, dn, block_m: int = 16, gu_group:
         _ptr(workspace), workspace.numel(), _ptr(out), _ptr(dev_status), _stream(stream)),
         "w4_moe_layer")
     return out
+
+
+def w4_moe_layer_host_workspace_size(M, d, m, E, k, block_m=16) -> int:
+    return int(load_library().w4_moe_layer_host_workspace_size(M, d, m, E, k, block_m))
+
+
+def w4_moe_layer_host(x_host, topk_ids_host, topk_weights_host, gu, dn, out_host, workspace,
+                      block_m: int = 16, gu_group: int = 128, dn_group: int = 64,
+                      dev_status=None, stream=None):
+    """w4_moe_layer from host memory: x [M, d] bf16, topk_ids [M, k] int32
+    and topk_weights [M, k] fp32 (page-locked CPU tensors) are copied in and
+    out [M, d] bf16 is copied back to out_host, all enqueued on the stream;
+    synchronise before reading out_host.  workspace: a device uint8 tensor of
+    w4_moe_layer_host_workspace_size(...) bytes."""
+    gu_q, gu_s, gu_z = gu
+    dn_q, dn_s, dn_z = dn
+    _require_cuda(gu_q, gu_s, gu_z, dn_q, dn_s, dn_z, workspace, dev_status)
+    for t in (x_host, topk_ids_host, topk_weights_host, out_host):
+        if t.is_cuda:
+            raise ValueError("w4_moe_layer_host takes host tensors for x, ids, weights and out")
+    M, d = x_host.shape
+    E, two_m, _ = gu_q.shape
+    m = two_m // 2
+    k = topk_ids_host.shape[1]
+    _check(load_library().w4_moe_layer_host(
+        _ptr(x_host), _ptr(topk_ids_host), _ptr(topk_weights_host), M, d, m, E, k, block_m,
+        _ptr(gu_q), _ptr(gu_s), _ptr(gu_z), gu_group, _ptr(dn_q), _ptr(dn_s), _ptr(dn_z),
+        dn_group, _ptr(workspace), workspace.numel(), _ptr(out_host), _ptr(dev_status),
+        _stream(stream)), "w4_moe_layer_host")
+    return out_host
 
 
 def w4_moe_route_align_gather(logits, x, k: int, block_m: int = 16, dev_status=None, out=None,

@@ -629,6 +629,76 @@ int w4_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w
                        gu_group, dn_q, dn_s, dn_z, dn_group, ws, L, out, dev_status, stream);
 }
 
+// Staging buffers of w4_moe_layer_host after the layer's workspace.
+struct HostStaging {
+    size_t x, ids, w, out, total;
+};
+
+static HostStaging host_staging(size_t base, int M, int d, int k)
+{
+    auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    HostStaging h;
+    h.x = up(base);
+    h.ids = up(h.x + 2 * static_cast<size_t>(M) * d);
+    h.w = up(h.ids + 4 * static_cast<size_t>(M) * k);
+    h.out = up(h.w + 4 * static_cast<size_t>(M) * k);
+    h.total = up(h.out + 2 * static_cast<size_t>(M) * d);
+    return h;
+}
+
+size_t w4_moe_layer_host_workspace_size(int M, int d, int m, int E, int k, int block_m)
+{
+    if (M < 0 || d <= 0 || m <= 0 || E <= 0 || k <= 0 || !valid_block_m(block_m))
+        return 0;
+    return host_staging(layer_ws(M, d, m, E, k, block_m).total, M, d, k).total;
+}
+
+int w4_moe_layer_host(const uint16_t *x_host, const int32_t *topk_ids_host,
+                      const float *topk_weights_host, int M, int d, int m, int E, int k,
+                      int block_m, const uint8_t *gu_q, const uint16_t *gu_s,
+                      const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
+                      const uint16_t *dn_s, const uint16_t *dn_z, int dn_group, void *workspace,
+                      size_t workspace_bytes, uint16_t *out_host, int32_t *dev_status,
+                      w4_stream_t stream)
+{
+    if (!valid_block_m(block_m))
+        return fail(W4_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256 (got %d)", block_m);
+    if (M < 0 || d <= 0 || m <= 0 || E <= 0 || k <= 0)
+        return fail(W4_ERR_INVALID_ARG, "bad sizes");
+    if (M > 0 && (!x_host || !topk_ids_host || !topk_weights_host || !out_host))
+        return fail(W4_ERR_INVALID_ARG, "NULL host buffer");
+    const LayerWs L = layer_ws(M, d, m, E, k, block_m);
+    const HostStaging H = host_staging(L.total, M, d, k);
+    if (!workspace || workspace_bytes < H.total)
+        return fail(W4_ERR_WORKSPACE, "workspace needs %zu bytes", H.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(W4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    if (M == 0)   // no rows to copy or compute
+        return W4_OK;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint16_t *x_d = reinterpret_cast<uint16_t *>(ws + H.x);
+    int32_t *ids_d = reinterpret_cast<int32_t *>(ws + H.ids);
+    float *w_d = reinterpret_cast<float *>(ws + H.w);
+    uint16_t *out_d = reinterpret_cast<uint16_t *>(ws + H.out);
+    const cudaStream_t s = as_stream(stream);
+    const size_t nx = 2 * static_cast<size_t>(M) * d, nk = 4 * static_cast<size_t>(M) * k;
+    cudaError_t err = cudaMemcpyAsync(x_d, x_host, nx, cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(ids_d, topk_ids_host, nk, cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(w_d, topk_weights_host, nk, cudaMemcpyHostToDevice, s);
+    if (err != cudaSuccess)
+        return fail(W4_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(err));
+    if (int rc = w4_moe_layer(x_d, ids_d, w_d, M, d, m, E, k, block_m, gu_q, gu_s, gu_z, gu_group,
+                              dn_q, dn_s, dn_z, dn_group, workspace, L.total, out_d, dev_status,
+                              stream))
+        return rc;
+    err = cudaMemcpyAsync(out_host, out_d, nx, cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess)
+        return fail(W4_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(err));
+    return W4_OK;
+}
+
 int w4_moe_layer_from_logits(const uint16_t *x, const float *logits, int M, int d, int m, int E,
                              int k, int block_m, const uint8_t *gu_q, const uint16_t *gu_s,
                              const uint16_t *gu_z, int gu_group, const uint8_t *dn_q,
