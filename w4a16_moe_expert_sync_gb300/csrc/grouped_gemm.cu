@@ -43,7 +43,8 @@
 //     slots); a panel is 128 weight rows (gate_up: 64 gate rows and the
 //     matching 64 up rows; down: 128 output rows).
 //   * Swap-AB: the 128 weight rows are the M = 128 operand, in tensor memory
-//     (written with tcgen05.st), the job's tokens are N (16 or 32).  B, the
+//     (written with tcgen05.st), the job's tokens are N (16 or 32; up to 64
+//     in big-job mode).  B, the
 //     activations, is read by the tensor core from shared memory in the
 //     128-byte-swizzled K-major layout; 3-D TMA copies fill its slots (or, for
 //     down, one copy per job fills a resident slot).
@@ -57,7 +58,9 @@
 //     into its own fp32 accumulator ("chain").  The epilogue adds the chains
 //     in a fixed order.  Two accumulator sets alternate per unit, so a
 //     unit's epilogue overlaps the next unit's MMAs.  The unit's correction
-//     goes to ring (blocks + unit) % 4, after that ring's last block.
+//     goes to ring (blocks + unit) % 4, after that ring's last block.  In
+//     big-job mode issuers 0 and 1 take rings r and r + 2 each, into two
+//     chains of 64 columns, and issuers 2-3 idle.
 //   * Warp roles
 //       warps 0-3   tcgen05.mma issuers (converged, one elected lane issues);
 //                   warp 0 also allocates tensor memory
@@ -72,7 +75,7 @@
 //                   every warp of the CTA counts the CTA's y panels and
 //                   combines the (token, panel) pairs it completed
 //   * Tensor memory (512 columns): A buffers at 32 (2 r + b), accumulators
-//     at 256 + 128 set + 32 chain.
+//     at 256 + 128 set + 32 chain (big jobs: + 64 chain).
 //   * Every barrier has one producer group and one consumer group that take
 //     its phases in order, so a waiter is never two phases ahead and parity
 //     waits are exact (tests/test_grouped_pipeline_protocol.py models it).
