@@ -78,7 +78,7 @@ def _compare(cfg, sorted_ids, npad, h, y, h_ref, y_ref, rows=None):
 
 
 @pytest.mark.parametrize("block_m", [16, 32, 64])
-@pytest.mark.parametrize("name", ["tiny", "ragged"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "bigjobs"])
 def test_gemm_steps_match_oracle(lib, name, block_m):
     cfg = wl.CONFIGS[name]
     gu, dn = gpu_weights(name)
@@ -94,8 +94,9 @@ def test_gemm_steps_match_oracle(lib, name, block_m):
 
 
 def test_gemm_expert_with_more_than_256_tokens(lib):
-    """One expert receives 300 tokens: its range splits into jobs of 32 slots
-    and a 16-slot tail."""
+    """One expert receives 300 tokens (600 assignments over 4 experts: the
+    big-job mode): its range splits into jobs of 64 slots and a 48-slot
+    tail."""
     import torch
     cfg = wl.LayerShape("hot", 300, 256, 128, 4, 2, seed=21)
     rng = np.random.default_rng(21)

@@ -25,7 +25,7 @@ def _layer(lib, name, block_m=16, status=None):
 
 
 @pytest.mark.parametrize("block_m", [16, 32])
-@pytest.mark.parametrize("name", ["tiny", "ragged"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "bigjobs"])
 def test_layer_matches_oracle(lib, name, block_m):
     import torch
     status = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -57,6 +57,8 @@ CONFIGS = {
     "tiny": LayerShape("tiny", 16, 256, 128, 8, 2, seed=0),
     # several tiles in every dimension and a ragged contraction tail
     "ragged": LayerShape("ragged", 37, 384, 192, 12, 3, seed=6),
+    # experts averaging 75 slots: the GEMMs' big-job mode (jobs of 16 to 64 slots)
+    "bigjobs": LayerShape("bigjobs", 200, 384, 192, 8, 3, seed=7),
     # one 256-token canvas at the pages' layer shape
     "layer256": LayerShape("layer256", 256, 2816, 704, 128, 8, seed=1),
     # skewed routing: a few experts with >100 rows, many with none
