@@ -239,6 +239,10 @@ int w4_moe_route_align_gather(const float *logits, const uint16_t *x, int M, int
  * fp32), multiplied on the tensor cores (tcgen05, fp16 x fp16 -> fp32), and
  * the part of -z * s lost to its fp16 rounding is added back through the
  * group sums; h is rounded to fp16 with saturation at +-65504.
+ * The work runs as units of (job, 128 weight rows), a job being up to 32
+ * consecutive slots of one expert, or up to 64 when M * k >= 64 * E; the
+ * fp32 summation order follows from the shape alone, so results are
+ * bit-identical from run to run.
  * Requires d % 128 == 0, d <= 8192, m % 64 == 0, m <= 1024, group == 128,
  * and that a unit's scales and zeros fit shared memory beside the code and
  * activation stages: d up to about 3584 at E = 128 (2688 at E = 1024);
