@@ -35,7 +35,7 @@ def _reference(lib, cfg, x, ids_d, w_d, gu, dn):
     return al, h, y, lib.w4_moe_combine_fixed_order(y, ids_d, w_d, cfg.E)
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "layer256", "zipf256"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "bigjobs", "layer256", "zipf256", "canvas2048"])
 def test_down_combine_equals_down_then_combine(lib, name):
     import torch
     cfg, x, ids, w = _ids_with_invalid(name)

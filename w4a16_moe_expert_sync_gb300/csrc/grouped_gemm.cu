@@ -500,34 +500,37 @@ __device__ __forceinline__ void combine_count(const GemmArgs &p, const Job &J, i
                                               int *list, int *count)
 {
     const unsigned full = 0xffffffffu;
-    int t = -1;
-    bool last = false;
-    if (lane < J.n) {
-        const int a = __ldg(p.sorted_ids + J.start + lane);
-        if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A)) {
-            t = a / p.k;
-            last = atomicAdd(p.comb_cnt + fold_counter_index(t, p.n_panels, pnl), 1) == p.k - 1;
+    for (int base = 0; base < J.n; base += 32) {   // the job's slots, 32 at a time
+        int t = -1;
+        bool last = false;
+        if (base + lane < J.n) {
+            const int a = __ldg(p.sorted_ids + J.start + base + lane);
+            if (static_cast<unsigned>(a) < static_cast<unsigned>(p.A)) {
+                t = a / p.k;
+                last = atomicAdd(p.comb_cnt + fold_counter_index(t, p.n_panels, pnl), 1) ==
+                       p.k - 1;
+            }
         }
-    }
-    unsigned done = __ballot_sync(full, last);
-    if (!done)
-        return;
-    fence_acq_rel_gpu();
-    int slot = 0;
-    if (lane == 0)
-        slot = atomicAdd(count, __popc(done));
-    slot = __shfl_sync(full, slot, 0);
-    while (done) {
-        const int src = __ffs(done) - 1;
-        done &= done - 1;
-        const int tt = __shfl_sync(full, t, src);
-        if (slot < kCombListCap) {
-            if (lane == 0)
-                list[slot] = tt * p.n_panels + pnl;
-        } else {
-            combine_panel(p, tt, pnl, lane);
+        unsigned done = __ballot_sync(full, last);
+        if (!done)
+            continue;
+        fence_acq_rel_gpu();
+        int slot = 0;
+        if (lane == 0)
+            slot = atomicAdd(count, __popc(done));
+        slot = __shfl_sync(full, slot, 0);
+        while (done) {
+            const int src = __ffs(done) - 1;
+            done &= done - 1;
+            const int tt = __shfl_sync(full, t, src);
+            if (slot < kCombListCap) {
+                if (lane == 0)
+                    list[slot] = tt * p.n_panels + pnl;
+            } else {
+                combine_panel(p, tt, pnl, lane);
+            }
+            slot++;
         }
-        slot++;
     }
 }
 
@@ -1359,10 +1362,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem &q, cudaStream_t stream
         return cudaErrorInvalidValue;
     }
     a.n_corr_mma = (a.G * corr_rep + 15) / 16;
-    // Big jobs when the batch gives the experts 64 or more slots on average
-    // (not with the folded combine, which counts a job's slots with one warp).
-    const bool bign =
-        q.comb_cnt == nullptr && static_cast<int64_t>(q.M) * q.k >= static_cast<int64_t>(kMaxNBig) * q.E;
+    // Big jobs when the batch gives the experts 64 or more slots on average.
+    const bool bign = static_cast<int64_t>(q.M) * q.k >= static_cast<int64_t>(kMaxNBig) * q.E;
     const int n_iss = bign ? JobShape<true>::kIssuers : JobShape<false>::kIssuers;
     // the accumulators (issuers) that receive MMAs in the CTA's unit n, by
     // n % 4
