@@ -11,8 +11,9 @@ issuers (issuer r takes ring r: two A buffers in tensor memory that take the
 ring's fills in turn, and its own accumulator in each of two sets; each
 issuer's commits complete asynchronously in its issue order), sixteen
 dequantisation warps (lane quarter x ring; ring r takes 64-code slice r of
-every stage, i.e. the unit's blocks j with j % 4 == r, and ring
-(blocks + unit) % 4 also takes the unit's group-constant correction) and
+every stage, i.e. the unit's blocks j with j % 4 == r, and ring blocks % 4
+(ring unit % 4 when blocks % 4 == 0) also takes the unit's group-constant
+correction) and
 four epilogue warps (which also read the row scales the ring-0 dequant
 warps publish per unit).  Every wait is checked against the exact
 condition: the phase it stands for, counted from per-stage uses kept apart
@@ -45,7 +46,8 @@ def block_ring(j):
 
 
 def corr_ring(n_unit, n_blocks):
-    return (n_blocks + n_unit) & (RINGS - 1)
+    rest = n_blocks & (RINGS - 1)
+    return rest if rest else n_unit & (RINGS - 1)
 
 
 class Bar:

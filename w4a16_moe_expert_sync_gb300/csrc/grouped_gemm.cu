@@ -58,7 +58,8 @@
 //     into its own fp32 accumulator ("chain").  The epilogue adds the chains
 //     in a fixed order.  Two accumulator sets alternate per unit, so a
 //     unit's epilogue overlaps the next unit's MMAs.  The unit's correction
-//     goes to ring (blocks + unit) % 4, after that ring's last block.  In
+//     goes, after that ring's last block, to the ring with one block fewer
+//     (blocks % 4), or to ring unit % 4 when the rings have as many.  In
 //     big-job mode issuers 0 and 1 take rings r and r + 2 each, into two
 //     chains of 64 columns, and issuers 2-3 idle.
 //   * Warp roles
@@ -170,7 +171,7 @@ struct GemmArgs {
     int h_stride;             // gate_up: row length of h (m + 64: values, then group sums)
     int h_groups;             // gate_up: groups of 64 along m (the down GEMM's groups)
     int acc_mask[4];          // issuers (accumulators) with MMAs in the CTA's unit n,
-                              // by n % 4 (the correction's ring rotates)
+                              // by n % 4 (the correction's ring may rotate)
     int early_schedule;       // the schedule may be read before the grid-dependency wait
     // The layer's combine, folded into the down GEMM (comb_cnt non-null):
     // counters [M][d/128 panels][4 lane quarters], set by the gate_up launch
@@ -424,11 +425,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 __host__ __device__ __forceinline__ int block_ring(int j) { return j & (kRings - 1); }
 
 // The ring that carries the correction fill of the CTA's unit n (after the
-// ring's last block of the unit): the ring the next block would go to,
-// turned by one per unit, so that over four units every ring takes one.
+// ring's last block of the unit).  When the block count is not a multiple of
+// four, the ring the next block would go to: it has one block fewer than
+// ring 0, so the correction evens the rings' fills out (down at m = 704: 11
+// blocks, rings 3/3/3/2).  Otherwise every ring has as many blocks, and the
+// correction turns by one per unit, so that over four units every ring takes
+// one.
 __host__ __device__ __forceinline__ int corr_ring(int n_unit, int n_blocks)
 {
-    return (n_blocks + n_unit) & (kRings - 1);
+    const int rest = n_blocks & (kRings - 1);
+    return rest ? rest : (n_unit & (kRings - 1));
 }
 
 // Tile row (0..127 of the stage) held by lane `lane` of a warp of TMEM lane
